@@ -1,0 +1,236 @@
+/*
+ * mx8q -- microscaling quantization (MXFP8, per-token NVFP4) and the
+ * block-scaled tensor-core GEMM it feeds, for GB300 (sm_103a).
+ *
+ * Plain C ABI: device pointers, sizes and a CUDA stream; no framework types.
+ *
+ * Sources (page title -- section):
+ *   [MRL] "Miles Blackwell RL Cambia la Uniformidad BF16 por MXFP8 y NVFP4
+ *         Nativos" -- "La Compatibilidad de Miles Blackwell Ahora Abarca Todo
+ *         el Ciclo de RL" (MXFP8 = 32 E4M3 values sharing one E8M0 scale,
+ *         used by rollout, Fprop, Wgrad and Dgrad; NVFP4 = E2M1 with an E4M3
+ *         scale per 16 values plus an FP32 scale computed per token; the
+ *         dequantized-backward mode), and "Un Cuantizador Compartido Es el
+ *         Mecanismo Real" (rowwise and columnwise copies made from the
+ *         high-precision input; scale blocks along the reduction dimension;
+ *         the FP32 token scale fused into the activation quantizer; gate and
+ *         up projections quantized together).
+ *   [NV4] "NVIDIA presenta una metodologia de preentrenamiento de 4 bits
+ *         utilizando NVFP4" -- "Que es realmente NVFP4" (E2M1 grid, E4M3
+ *         block scales, FP32 second-level scale), "La metodologia de
+ *         formacion de cuatro partes" (1x16 blocks, round-to-nearest-even).
+ *   [REC] "Miles Blackwell MXFP8 / NVFP4 RL recipes" (aib.vote) -- MXFP8
+ *         row/column copies, NVFP4 on MoE routed experts with a tensor- or
+ *         token-scope FP32 scale, the bit-exact quantizer contract.
+ *
+ * Numerical convention (bit-exact; the pages leave these points open):
+ *   MXFP8 block exponent e = smallest integer with amax <= 448 * 2^e,
+ *   clamped to [-127, 127]; scale byte = e + 127; element = RNE_E4M3(x*2^-e)
+ *   saturating, signed zero kept.
+ *   NVFP4 with scope amax A:  S_enc = min(RN(2688/A), FLT_MAX);
+ *   S_dec = RN(A/2688) (stored); per 16-block: sb = RNE_E4M3(RN(RN(amax_b/6)
+ *   * S_enc)); r = sb ? min(RN(S_enc/sb), FLT_MAX) : 0;
+ *   element = RNE_E2M1(RN(x*r)) saturating.  All FP32, IEEE round-to-nearest
+ *   (no approximate division, as the FP4 quantizer contract in [MRL] asks).
+ *
+ * Data layouts (all row-major, every buffer allocated and owned by the
+ * caller; the library never allocates device memory):
+ *   bf16 input x          : [rows, cols] with row stride ld elements.
+ *   MXFP8 data            : uint8 E4M3 [rows, cols].
+ *   MXFP8 columnwise data : uint8 E4M3 [cols, rows] -- stored transposed, so
+ *                           its 1x32 blocks run along its contiguous axis.
+ *   NVFP4 data            : uint8 [rows, cols/2]; element 2j in the low
+ *                           nibble of byte j, element 2j+1 in the high nibble.
+ *   Scale factors         : the tensor-core tile layout.  For a logical
+ *                           [R, S] scale matrix (S = cols/32 or cols/16),
+ *                           scale (r, k) lives at byte
+ *                             ((r/128)*ceil(S/4) + k/4)*512
+ *                             + (r%32)*16 + ((r%128)/32)*4 + k%4
+ *                           of a buffer of ceil(R/128)*128 * ceil(S/4)*4
+ *                           bytes; padding bytes are written as zero.
+ *                           With group offsets, group g's rows start at
+ *                           padded row P_g = sum_{h<g} ceil(n_h/128)*128.
+ *
+ * Errors: arguments are validated on the host before any launch
+ * (MX8_ERR_INVALID_ARG / MX8_ERR_ALIGNMENT / MX8_ERR_UNSUPPORTED); a failed
+ * launch returns MX8_ERR_CUDA.  Every device-side wait is bounded (about one
+ * second); a wait that runs out sets an error word in the caller's
+ * workspace, and mx8_check_device_error() reports it as MX8_ERR_TIMEOUT.
+ *
+ * Workspace: a caller-owned device buffer of at least
+ * mx8_workspace_bytes(num_groups) bytes, zero-filled once before first use.
+ * Its first 16 bytes hold the error word; the rest is scratch for the call.
+ * Calls are asynchronous on the given stream; two calls that share one
+ * workspace must be ordered (same stream or synchronised).
+ */
+#ifndef MX8Q_H
+#define MX8Q_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *mx8_stream_t; /* the same type as cudaStream_t */
+
+typedef enum {
+    MX8_OK = 0,
+    MX8_ERR_INVALID_ARG = 1,  /* null pointer, bad size or mode           */
+    MX8_ERR_ALIGNMENT = 2,    /* pointer or stride not 16-byte aligned     */
+    MX8_ERR_UNSUPPORTED = 3,  /* valid request this build does not handle  */
+    MX8_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed         */
+    MX8_ERR_TIMEOUT = 5,      /* a bounded device wait ran out             */
+    MX8_ERR_WORKSPACE = 6     /* workspace missing or too small            */
+} mx8_status;
+
+enum { MX8_ROWWISE = 1, MX8_COLWISE = 2 };
+enum { NVFP4_SCOPE_TOKEN = 0, NVFP4_SCOPE_GROUP = 1, NVFP4_SCOPE_TENSOR = 2 };
+enum { MX8_FMT_MXFP8 = 0, MX8_FMT_NVFP4 = 1 };
+enum { MX8_OUT_F32 = 0, MX8_OUT_BF16 = 1 };
+/* How an FP32 decode scale vector applies to the rows of a matrix. */
+enum { MX8_S32_NONE = 0, MX8_S32_ROW = 1, MX8_S32_TENSOR = 2, MX8_S32_GROUP = 3 };
+
+/* Bytes of the tensor-core scale buffer for a [rows, cols] matrix in format
+ * fmt (block 32 for MXFP8, 16 for NVFP4). */
+size_t mx8_scale_bytes(int fmt, int64_t rows, int64_t cols);
+
+/* Upper bound of the grouped scale buffer (every group padded to whole
+ * 128-row tiles) for total_rows rows split into num_groups groups. */
+size_t mx8_scale_bytes_grouped(int fmt, int64_t total_rows, int num_groups, int64_t cols);
+
+/* Workspace bytes needed by any call below with up to num_groups groups. */
+size_t mx8_workspace_bytes(int num_groups);
+
+/* Number of streaming multiprocessors the kernels size their grids for. */
+int mx8_device_sm_count(void);
+
+/*
+ * MXFP8 quantization of a bf16 matrix, rowwise and/or columnwise in one pass
+ * over the input ([MRL] "La Compatibilidad...": 32 E4M3 values share one E8M0
+ * scale; [MRL] "Un Cuantizador Compartido...": both copies come from the
+ * high-precision input; [REC] MXFP8 paragraph).
+ *   x        : bf16 [rows, cols], row stride ld >= cols elements
+ *   flags    : MX8_ROWWISE | MX8_COLWISE
+ *   q_row    : E4M3 [rows, cols]                 (ROWWISE)
+ *   s_row    : mx8_scale_bytes(MXFP8, rows, cols) (ROWWISE)
+ *   q_col    : E4M3 [cols, rows], transposed     (COLWISE)
+ *   s_col    : mx8_scale_bytes(MXFP8, cols, rows) (COLWISE)
+ * Requires cols % 32 == 0, and rows % 32 == 0 for COLWISE; ld % 8 == 0;
+ * x, q_*, s_* 16-byte aligned.  rows == 0 or cols == 0 is a no-op.
+ */
+mx8_status mx8_quantize(const void *x, int64_t rows, int64_t cols, int64_t ld, int flags,
+                        uint8_t *q_row, uint8_t *s_row, uint8_t *q_col, uint8_t *s_col,
+                        void *workspace, size_t workspace_bytes, mx8_stream_t stream);
+
+/*
+ * Two-level NVFP4 quantization of a bf16 matrix with the FP32 scale computed
+ * online per token ([MRL] "La Compatibilidad..." and "Un Cuantizador
+ * Compartido...": one FP32 activation scale per token, fused into the
+ * activation quantizer that also emits the packed FP4 values and the block
+ * scales; [NV4] "Que es realmente NVFP4"; [REC] NVFP4 paragraphs).
+ *   x      : bf16 [rows, cols], row stride ld
+ *   scope  : NVFP4_SCOPE_TOKEN  -> s32[rows], one decode scale per row
+ *            NVFP4_SCOPE_GROUP  -> s32[num_groups] (e.g. one per expert
+ *                                  weight, gate|up stored jointly)
+ *            NVFP4_SCOPE_TENSOR -> s32[1]
+ *   group_offsets : device int64 [num_groups+1], non-decreasing, 0..rows;
+ *            when given, the scale buffer uses the grouped (per-group
+ *            padded) tile layout; NULL means one group.  Required for
+ *            NVFP4_SCOPE_GROUP.
+ *   q      : uint8 [rows, cols/2]
+ *   s_blk  : E4M3 scales, mx8_scale_bytes(NVFP4, rows, cols), or
+ *            mx8_scale_bytes_grouped(...) with group_offsets
+ * Requires cols % 16 == 0, ld % 8 == 0, 16-byte aligned x/q/s_blk.
+ */
+mx8_status nvfp4_quantize_per_token(const void *x, int64_t rows, int64_t cols, int64_t ld,
+                                    int scope, const int64_t *group_offsets, int num_groups,
+                                    uint8_t *q, uint8_t *s_blk, float *s32,
+                                    void *workspace, size_t workspace_bytes,
+                                    mx8_stream_t stream);
+
+/*
+ * Dequantization back to f32 or bf16 (the dequantized-backward mode of [MRL]
+ * "La Compatibilidad..." and [REC]: rebuild high-precision operands from the
+ * exact low-precision forward values).
+ *   MXFP8: out = e4m3 * 2^(scale-127)            (exact; may overflow to inf)
+ *   NVFP4: out = RN((e2m1 * sb) * S_dec)
+ *   q, s   : as produced by the quantizers (any rowwise-blocked matrix,
+ *            including a transposed columnwise copy)
+ *   s32, s32_mode : MX8_S32_NONE / ROW ([rows]) / TENSOR ([1]) / GROUP
+ *            ([num_groups], needs group_offsets)
+ *   group_offsets : grouped scale layout (as in nvfp4_quantize_per_token)
+ *   out    : [rows, cols] f32 or bf16 (out_dtype); bf16 = RNE of the f32 value
+ */
+mx8_status dequantize(int fmt, const uint8_t *q, const uint8_t *s, const float *s32, int s32_mode,
+                      const int64_t *group_offsets, int num_groups,
+                      int64_t rows, int64_t cols, int out_dtype, void *out,
+                      mx8_stream_t stream);
+
+/*
+ * Block-scaled GEMM on the tcgen05 tensor cores:
+ *     C[m, n] (+)= A32[m] * B32[n] * sum_k A^[m, k] * B^[n, k]
+ * where A^ and B^ are the block-scaled decodes (MXFP8: E4M3 * E8M0 per 32
+ * along K; NVFP4: E2M1 * E4M3 per 16 along K).  Both operands store K
+ * contiguously, so Fprop (A = X rowwise, B = W rowwise), Dgrad (A = dY
+ * rowwise, B = W columnwise copy) and Wgrad (A = dY columnwise copy,
+ * B = X columnwise copy) are all this call ([MRL] "La Compatibilidad...":
+ * MXFP8 in forward, weight-gradient and data-gradient GEMMs; [MRL] "Un
+ * Cuantizador Compartido...": scale blocks follow the reduction dimension).
+ *   A, SA : [M, K] data (K/2 bytes per row for NVFP4) + tensor-core scales
+ *   B, SB : [N, K] data + scales
+ *   A32 / a32_mode : MX8_S32_NONE, MX8_S32_ROW ([M], per-token scale),
+ *                    MX8_S32_TENSOR ([1])
+ *   B32 / b32_mode : MX8_S32_NONE, MX8_S32_ROW ([N]), MX8_S32_TENSOR ([1])
+ *   C     : [M, N] with row stride ldc, f32 or bf16; accumulate=1 adds to C
+ *           (f32 only)
+ * Requires K % 32 == 0, ldc % 8 == 0, 16-byte aligned pointers.
+ * Accumulation is FP32 in tensor memory.
+ */
+mx8_status bs_gemm(int fmt, int64_t M, int64_t N, int64_t K,
+                   const uint8_t *A, const uint8_t *SA, const float *A32, int a32_mode,
+                   const uint8_t *B, const uint8_t *SB, const float *B32, int b32_mode,
+                   int out_dtype, void *C, int64_t ldc, int accumulate,
+                   void *workspace, size_t workspace_bytes, mx8_stream_t stream);
+
+/*
+ * Grouped block-scaled GEMM for MoE routed experts ([REC] NVFP4 on MoE
+ * experts; [MRL] "NVFP4 por token..."): rows [off[g], off[g+1]) of A are the
+ * tokens routed to expert g and multiply that expert's weight B[g]:
+ *     C[m, n] = A32[m] * B32[g] * sum_k A^[m, k] * B^_g[n, k]
+ * The per-expert tile schedule is built on the device from group_offsets:
+ * no host synchronisation on the routing.
+ *   group_offsets : device int64 [num_groups+1]; total_rows = off[G]
+ *   A, SA  : [total_rows, K] data + grouped scale layout (per-group padded)
+ *   A32    : [total_rows] per-token FP32 decode scale, or NULL
+ *   B, SB  : [G, N, K] data + scales ([G*N, K] tile layout, N % 128 == 0
+ *            keeps groups on whole tiles; any N works since each group's
+ *            scale block is laid out on its own)
+ *   B32    : [G] per-expert FP32 decode scale, or NULL
+ *   C      : [total_rows, N] with row stride ldc, f32 or bf16
+ */
+mx8_status bs_grouped_gemm(int fmt, int num_groups, const int64_t *group_offsets,
+                           int64_t total_rows, int64_t N, int64_t K,
+                           const uint8_t *A, const uint8_t *SA, const float *A32,
+                           const uint8_t *B, const uint8_t *SB, const float *B32,
+                           int out_dtype, void *C, int64_t ldc,
+                           void *workspace, size_t workspace_bytes, mx8_stream_t stream);
+
+/* Synchronises the stream, reads and clears the workspace error word:
+ * MX8_OK, or MX8_ERR_TIMEOUT if a bounded device wait ran out. */
+mx8_status mx8_check_device_error(void *workspace, mx8_stream_t stream);
+
+/* Self-test of the bounded wait: launches one block that waits on a barrier
+ * nothing will complete, with the given limit in nanoseconds; the wait gives
+ * up, records the error and the kernel returns.  Follow with
+ * mx8_check_device_error(), which then reports MX8_ERR_TIMEOUT. */
+mx8_status mx8_selftest_bounded_wait(void *workspace, uint64_t limit_ns, mx8_stream_t stream);
+
+const char *mx8_status_string(mx8_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MX8Q_H */

@@ -1,0 +1,288 @@
+"""GB300-native microscaling quantization (MXFP8, per-token NVFP4) and the
+block-scaled tcgen05 GEMM it feeds.
+
+This package is a thin ctypes binding over the C ABI of ``_build/libmx8q.so``
+(declared in ``include/mx8q.h``): it marshals torch tensors into device
+pointers, sizes and the current CUDA stream.  Every step of the computation
+runs in the library's CUDA kernels; there is no CPU fallback.  Importing the
+package does not load the library; the first call does, and raises if the
+library has not been built (``python -m moe_mx8_quantize_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libmx8q.so")
+
+# ---------------------------------------------------------------- constants
+OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = range(7)
+ROWWISE, COLWISE = 1, 2
+SCOPE_TOKEN, SCOPE_GROUP, SCOPE_TENSOR = 0, 1, 2
+FMT_MXFP8, FMT_NVFP4 = 0, 1
+OUT_F32, OUT_BF16 = 0, 1
+S32_NONE, S32_ROW, S32_TENSOR, S32_GROUP = 0, 1, 2, 3
+
+# every C symbol the header declares
+EXPORTS = ("mx8_scale_bytes", "mx8_scale_bytes_grouped", "mx8_workspace_bytes",
+           "mx8_device_sm_count", "mx8_quantize", "nvfp4_quantize_per_token", "dequantize",
+           "bs_gemm", "bs_grouped_gemm", "mx8_check_device_error", "mx8_selftest_bounded_wait",
+           "mx8_status_string")
+
+
+class Mx8Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+_lib = None
+_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_i = ctypes.c_int
+_sz = ctypes.c_size_t
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads the CUDA library (once).  Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"mx8q CUDA library not built: {path} is missing "
+                           "(run python -m moe_mx8_quantize_gb300.build)")
+    lib = ctypes.CDLL(path)
+    lib.mx8_scale_bytes.restype = _sz
+    lib.mx8_scale_bytes.argtypes = [_i, _i64, _i64]
+    lib.mx8_scale_bytes_grouped.restype = _sz
+    lib.mx8_scale_bytes_grouped.argtypes = [_i, _i64, _i, _i64]
+    lib.mx8_workspace_bytes.restype = _sz
+    lib.mx8_workspace_bytes.argtypes = [_i]
+    lib.mx8_device_sm_count.restype = _i
+    lib.mx8_device_sm_count.argtypes = []
+    lib.mx8_quantize.restype = _i
+    lib.mx8_quantize.argtypes = [_p, _i64, _i64, _i64, _i, _p, _p, _p, _p, _p, _sz, _p]
+    lib.nvfp4_quantize_per_token.restype = _i
+    lib.nvfp4_quantize_per_token.argtypes = [_p, _i64, _i64, _i64, _i, _p, _i, _p, _p, _p, _p, _sz, _p]
+    lib.dequantize.restype = _i
+    lib.dequantize.argtypes = [_i, _p, _p, _p, _i, _p, _i, _i64, _i64, _i, _p, _p]
+    lib.bs_gemm.restype = _i
+    lib.bs_gemm.argtypes = [_i, _i64, _i64, _i64, _p, _p, _p, _i, _p, _p, _p, _i, _i, _p, _i64, _i,
+                            _p, _sz, _p]
+    lib.bs_grouped_gemm.restype = _i
+    lib.bs_grouped_gemm.argtypes = [_i, _i, _p, _i64, _i64, _i64, _p, _p, _p, _p, _p, _p, _i, _p,
+                                    _i64, _p, _sz, _p]
+    lib.mx8_check_device_error.restype = _i
+    lib.mx8_check_device_error.argtypes = [_p, _p]
+    lib.mx8_selftest_bounded_wait.restype = _i
+    lib.mx8_selftest_bounded_wait.argtypes = [_p, ctypes.c_uint64, _p]
+    lib.mx8_status_string.restype = ctypes.c_char_p
+    lib.mx8_status_string.argtypes = [_i]
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().mx8_status_string(status).decode()
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise Mx8Error(status, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+# ---------------------------------------------------------------- sizes
+def scale_bytes(fmt: int, rows: int, cols: int) -> int:
+    return int(load().mx8_scale_bytes(fmt, rows, cols))
+
+
+def scale_bytes_grouped(fmt: int, total_rows: int, num_groups: int, cols: int) -> int:
+    return int(load().mx8_scale_bytes_grouped(fmt, total_rows, num_groups, cols))
+
+
+def workspace_bytes(num_groups: int = 1) -> int:
+    return int(load().mx8_workspace_bytes(num_groups))
+
+
+def new_workspace(num_groups: int = 1, device=None) -> torch.Tensor:
+    """Zero-filled workspace (error word + scratch) for calls with up to
+    num_groups groups."""
+    return torch.zeros(workspace_bytes(num_groups), dtype=torch.uint8, device=device or "cuda")
+
+
+_default_ws = {}
+
+
+def _ws(ws, num_groups, device):
+    if ws is not None:
+        return ws
+    key = (device, num_groups)
+    w = _default_ws.get(key)
+    if w is None or w.numel() < workspace_bytes(num_groups):
+        w = new_workspace(num_groups, device)
+        _default_ws[key] = w
+    return w
+
+
+def _u8(n, device):
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
+# ---------------------------------------------------------------- MXFP8
+def mx8_quantize_into(x, q_row, s_row, q_col, s_col, flags=ROWWISE | COLWISE, ws=None, stream=None):
+    """In-place form of :func:`mx8_quantize` (outputs pre-allocated)."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    R, C = x.shape
+    ws = _ws(ws, 1, x.device)
+    _check(load().mx8_quantize(_ptr(x), R, C, x.stride(0), flags, _ptr(q_row), _ptr(s_row),
+                               _ptr(q_col), _ptr(s_col), _ptr(ws), ws.numel(), _stream(stream)),
+           "mx8_quantize")
+
+
+def mx8_quantize(x: torch.Tensor, flags: int = ROWWISE | COLWISE, ws=None, stream=None):
+    """MXFP8 rowwise and/or columnwise quantization of a bf16 [R, C] matrix.
+
+    Returns (q_row [R,C] u8, s_row u8 tiles, q_col [C,R] u8, s_col u8 tiles);
+    the copies not requested are None.
+    """
+    R, C = x.shape
+    dev = x.device
+    q_row = s_row = q_col = s_col = None
+    if flags & ROWWISE:
+        q_row = torch.empty((R, C), dtype=torch.uint8, device=dev)
+        s_row = _u8(scale_bytes(FMT_MXFP8, R, C), dev)
+    if flags & COLWISE:
+        q_col = torch.empty((C, R), dtype=torch.uint8, device=dev)
+        s_col = _u8(scale_bytes(FMT_MXFP8, C, R), dev)
+    mx8_quantize_into(x, q_row, s_row, q_col, s_col, flags, ws, stream)
+    return q_row, s_row, q_col, s_col
+
+
+# ---------------------------------------------------------------- NVFP4
+def nvfp4_quantize_into(x, q, s_blk, s32, scope=SCOPE_TOKEN, group_offsets=None, ws=None,
+                        stream=None):
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    R, C = x.shape
+    G = 0 if group_offsets is None else group_offsets.numel() - 1
+    ws = _ws(ws, max(G, 1), x.device)
+    _check(load().nvfp4_quantize_per_token(_ptr(x), R, C, x.stride(0), scope, _ptr(group_offsets), G,
+                                           _ptr(q), _ptr(s_blk), _ptr(s32), _ptr(ws), ws.numel(),
+                                           _stream(stream)),
+           "nvfp4_quantize_per_token")
+
+
+def nvfp4_quantize_per_token(x: torch.Tensor, scope: int = SCOPE_TOKEN, group_offsets=None,
+                             ws=None, stream=None):
+    """Two-level NVFP4 quantization with an FP32 scale per token (or group /
+    tensor).  Returns (q [R, C/2] u8, s_blk u8 tiles, s32 f32 decode scales).
+    group_offsets (device int64 [G+1]) selects the grouped scale layout."""
+    R, C = x.shape
+    dev = x.device
+    G = 0 if group_offsets is None else group_offsets.numel() - 1
+    q = torch.empty((R, C // 2), dtype=torch.uint8, device=dev)
+    if group_offsets is None:
+        s_blk = _u8(scale_bytes(FMT_NVFP4, R, C), dev)
+    else:
+        s_blk = _u8(scale_bytes_grouped(FMT_NVFP4, R, G, C), dev)
+    n32 = R if scope == SCOPE_TOKEN else (G if scope == SCOPE_GROUP else 1)
+    s32 = torch.empty(max(n32, 1), dtype=torch.float32, device=dev)
+    nvfp4_quantize_into(x, q, s_blk, s32, scope, group_offsets, ws, stream)
+    return q, s_blk, s32[:n32]
+
+
+# ---------------------------------------------------------------- dequantize
+def dequantize_into(fmt, q, s, out, s32=None, s32_mode=S32_NONE, group_offsets=None, stream=None):
+    R = q.shape[0]
+    C = q.shape[1] if fmt == FMT_MXFP8 else q.shape[1] * 2
+    G = 0 if group_offsets is None else group_offsets.numel() - 1
+    od = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
+    _check(load().dequantize(fmt, _ptr(q), _ptr(s), _ptr(s32), s32_mode, _ptr(group_offsets), G, R, C,
+                             od, _ptr(out), _stream(stream)), "dequantize")
+
+
+def dequantize(fmt, q, s, s32=None, s32_mode=None, group_offsets=None, out_dtype=torch.float32,
+               stream=None):
+    R = q.shape[0]
+    C = q.shape[1] if fmt == FMT_MXFP8 else q.shape[1] * 2
+    if s32_mode is None:
+        if s32 is None:
+            s32_mode = S32_NONE
+        elif s32.numel() == R and R != 1:
+            s32_mode = S32_ROW
+        else:
+            s32_mode = S32_TENSOR
+    out = torch.empty((R, C), dtype=out_dtype, device=q.device)
+    dequantize_into(fmt, q, s, out, s32, s32_mode, group_offsets, stream)
+    return out
+
+
+# ---------------------------------------------------------------- GEMM
+def _mode(v, n):
+    if v is None:
+        return S32_NONE
+    return S32_TENSOR if (v.numel() == 1 and n != 1) else S32_ROW
+
+
+def bs_gemm_into(fmt, A, SA, B, SB, K, out, A32=None, B32=None, accumulate=False, ws=None,
+                 stream=None, a32_mode=None, b32_mode=None):
+    M, N = A.shape[0], B.shape[0]
+    ws = _ws(ws, 1, A.device)
+    od = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
+    am = _mode(A32, M) if a32_mode is None else a32_mode
+    bm = _mode(B32, N) if b32_mode is None else b32_mode
+    _check(load().bs_gemm(fmt, M, N, K, _ptr(A), _ptr(SA), _ptr(A32), am, _ptr(B), _ptr(SB), _ptr(B32),
+                          bm, od, _ptr(out), out.stride(0), int(accumulate), _ptr(ws), ws.numel(),
+                          _stream(stream)), "bs_gemm")
+
+
+def bs_gemm(fmt, A, SA, B, SB, K, A32=None, B32=None, out_dtype=torch.float32, ws=None, stream=None):
+    """C[M, N] = A32[m] * B32[n] * sum_k A^[m,k] B^[n,k] on the tensor cores.
+    A: [M, K] (MXFP8) or [M, K/2] (NVFP4) u8 with K contiguous; SA/SB the
+    scale tiles; A32/B32 optional FP32 decode scales (per row or [1])."""
+    out = torch.empty((A.shape[0], B.shape[0]), dtype=out_dtype, device=A.device)
+    bs_gemm_into(fmt, A, SA, B, SB, K, out, A32, B32, False, ws, stream)
+    return out
+
+
+def bs_grouped_gemm_into(fmt, group_offsets, A, SA, B, SB, K, out, A32=None, B32=None, ws=None,
+                         stream=None):
+    G = group_offsets.numel() - 1
+    rows = A.shape[0]
+    N = B.shape[1]
+    ws = _ws(ws, G, A.device)
+    od = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
+    _check(load().bs_grouped_gemm(fmt, G, _ptr(group_offsets), rows, N, K, _ptr(A), _ptr(SA), _ptr(A32),
+                                  _ptr(B), _ptr(SB), _ptr(B32), od, _ptr(out), out.stride(0), _ptr(ws),
+                                  ws.numel(), _stream(stream)), "bs_grouped_gemm")
+
+
+def bs_grouped_gemm(fmt, group_offsets, A, SA, B, SB, K, A32=None, B32=None,
+                    out_dtype=torch.bfloat16, ws=None, stream=None):
+    """MoE routed-expert GEMM: rows [off[g], off[g+1]) of A times B[g]^T.
+    B: [G, N, K] (or [G, N, K/2]) u8; SB the [G*N, K/bs] scale tiles."""
+    out = torch.empty((A.shape[0], B.shape[1]), dtype=out_dtype, device=A.device)
+    bs_grouped_gemm_into(fmt, group_offsets, A, SA, B, SB, K, out, A32, B32, ws, stream)
+    return out
+
+
+# ---------------------------------------------------------------- errors
+def check_device_error(ws, stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device error
+    status of the workspace: OK or ERR_TIMEOUT."""
+    return int(load().mx8_check_device_error(_ptr(ws), _stream(stream)))
+
+
+def selftest_bounded_wait(ws, limit_ns: int, stream=None):
+    _check(load().mx8_selftest_bounded_wait(_ptr(ws), limit_ns, _stream(stream)), "selftest")

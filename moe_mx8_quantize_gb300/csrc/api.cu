@@ -1,0 +1,323 @@
+// C-ABI entry points: argument validation, TMA descriptor encoding and kernel
+// launches on the caller's stream.  The library never allocates device
+// memory; all buffers, including the workspace, belong to the caller.
+#include <cudaTypedefs.h>
+#include <stdio.h>
+
+#include <mutex>
+
+#include "../../include/mx8q.h"
+#include "device.cuh"
+#include "kernels.h"
+
+using namespace mx8q;
+
+namespace {
+
+constexpr size_t kErrWordBytes = 256;   // error word + padding; scratch starts here
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------- device info
+int sm_count_current() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+// ------------------------------------------------------------- TMA encode
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D or 3-D tiled map; dims/strides innermost first, strides in bytes for
+// dimensions 1.. (dimension 0 is contiguous).
+bool encode_map(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
+                const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+                CUtensorMapSwizzle swz) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  uint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, dt, rank, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int* err_word(void* ws) { return static_cast<int*>(ws); }
+
+mx8_status check_ws(void* ws, size_t bytes, int groups) {
+  if (ws == nullptr || !aligned16(ws)) return MX8_ERR_WORKSPACE;
+  if (bytes < mx8_workspace_bytes(groups)) return MX8_ERR_WORKSPACE;
+  return MX8_OK;
+}
+
+mx8_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MX8_OK : MX8_ERR_CUDA; }
+
+}  // namespace
+
+// ===================================================================== sizes
+extern "C" size_t mx8_scale_bytes(int fmt, int64_t rows, int64_t cols) {
+  if (rows < 0 || cols < 0) return 0;
+  const int64_t bs = fmt == MX8_FMT_MXFP8 ? 32 : 16;
+  return static_cast<size_t>(cdiv(rows, 128) * 128 * cdiv(cols / bs, 4) * 4);
+}
+
+extern "C" size_t mx8_scale_bytes_grouped(int fmt, int64_t total_rows, int num_groups, int64_t cols) {
+  if (total_rows < 0 || cols < 0 || num_groups < 0) return 0;
+  const int64_t bs = fmt == MX8_FMT_MXFP8 ? 32 : 16;
+  const int64_t tiles = cdiv(total_rows, 128) + num_groups;
+  return static_cast<size_t>(tiles * 128 * cdiv(cols / bs, 4) * 4);
+}
+
+extern "C" size_t mx8_workspace_bytes(int num_groups) {
+  const int64_t g = num_groups > 1 ? num_groups : 1;
+  return kErrWordBytes + static_cast<size_t>(cdiv(g * 4, 256) * 256);
+}
+
+extern "C" int mx8_device_sm_count(void) { return sm_count_current(); }
+
+extern "C" const char* mx8_status_string(mx8_status s) {
+  switch (s) {
+    case MX8_OK: return "ok";
+    case MX8_ERR_INVALID_ARG: return "invalid argument";
+    case MX8_ERR_ALIGNMENT: return "pointer or stride not 16-byte aligned";
+    case MX8_ERR_UNSUPPORTED: return "unsupported request";
+    case MX8_ERR_CUDA: return "CUDA error";
+    case MX8_ERR_TIMEOUT: return "a bounded device wait ran out";
+    case MX8_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+// ===================================================================== MXFP8
+extern "C" mx8_status mx8_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int flags,
+                                   uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                                   void* workspace, size_t workspace_bytes, mx8_stream_t stream) {
+  const bool row = flags & MX8_ROWWISE, col = flags & MX8_COLWISE;
+  if ((flags & ~(MX8_ROWWISE | MX8_COLWISE)) || !(row || col)) return MX8_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0 || ld < cols || cols % 32 != 0) return MX8_ERR_INVALID_ARG;
+  if (col && rows % 32 != 0) return MX8_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return MX8_OK;
+  if (x == nullptr || (row && (q_row == nullptr || s_row == nullptr)) ||
+      (col && (q_col == nullptr || s_col == nullptr)))
+    return MX8_ERR_INVALID_ARG;
+  if (!aligned16(x) || ld % 8 != 0 || (row && (!aligned16(q_row) || !aligned16(s_row))) ||
+      (col && (!aligned16(q_col) || !aligned16(s_col))))
+    return MX8_ERR_ALIGNMENT;
+  if (rows > INT32_MAX || cols > INT32_MAX) return MX8_ERR_UNSUPPORTED;
+  mx8_status st = check_ws(workspace, workspace_bytes, 1);
+  if (st != MX8_OK) return st;
+
+  CUtensorMap map;
+  const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)};
+  const uint64_t strides[1] = {static_cast<uint64_t>(ld) * 2};
+  const uint32_t box[2] = {128, 128};
+  if (!encode_map(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, dims, strides, box,
+                  CU_TENSOR_MAP_SWIZZLE_NONE))
+    return MX8_ERR_CUDA;
+  return from_cuda(launch_mxfp8_quant(map, rows, cols, row, col, q_row, s_row, q_col, s_col,
+                                      err_word(workspace), sm_count_current(),
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// ===================================================================== NVFP4
+extern "C" mx8_status nvfp4_quantize_per_token(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                               int scope, const int64_t* group_offsets,
+                                               int num_groups, uint8_t* q, uint8_t* s_blk,
+                                               float* s32, void* workspace, size_t workspace_bytes,
+                                               mx8_stream_t stream) {
+  if (scope < NVFP4_SCOPE_TOKEN || scope > NVFP4_SCOPE_TENSOR) return MX8_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0 || ld < cols || cols % 16 != 0) return MX8_ERR_INVALID_ARG;
+  if (scope == NVFP4_SCOPE_GROUP && group_offsets == nullptr) return MX8_ERR_INVALID_ARG;
+  if (group_offsets != nullptr && (num_groups < 1 || num_groups > kMaxGroups)) return MX8_ERR_INVALID_ARG;
+  const int G = group_offsets ? num_groups : 1;
+  if (cols == 0) return MX8_OK;
+  if (rows > 0 && (x == nullptr || q == nullptr)) return MX8_ERR_INVALID_ARG;
+  if (s_blk == nullptr || s32 == nullptr) return MX8_ERR_INVALID_ARG;
+  if ((rows > 0 && (!aligned16(x) || !aligned16(q))) || !aligned16(s_blk) || ld % 8 != 0)
+    return MX8_ERR_ALIGNMENT;
+  mx8_status st = check_ws(workspace, workspace_bytes, G);
+  if (st != MX8_OK) return st;
+  float* amax_ws = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kErrWordBytes);
+  return from_cuda(launch_nvfp4_quant(static_cast<const uint16_t*>(x), rows, cols, ld, scope,
+                                      group_offsets, G, q, s_blk, s32, amax_ws, sm_count_current(),
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// ===================================================================== dequantize
+extern "C" mx8_status dequantize(int fmt, const uint8_t* q, const uint8_t* s, const float* s32,
+                                 int s32_mode, const int64_t* group_offsets, int num_groups,
+                                 int64_t rows, int64_t cols, int out_dtype, void* out,
+                                 mx8_stream_t stream) {
+  if (fmt != MX8_FMT_MXFP8 && fmt != MX8_FMT_NVFP4) return MX8_ERR_INVALID_ARG;
+  if (out_dtype != MX8_OUT_F32 && out_dtype != MX8_OUT_BF16) return MX8_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0 || cols % (fmt == MX8_FMT_MXFP8 ? 32 : 16) != 0) return MX8_ERR_INVALID_ARG;
+  if (s32_mode < MX8_S32_NONE || s32_mode > MX8_S32_GROUP) return MX8_ERR_INVALID_ARG;
+  if (fmt == MX8_FMT_MXFP8 && s32_mode != MX8_S32_NONE) return MX8_ERR_INVALID_ARG;
+  if (s32_mode != MX8_S32_NONE && s32 == nullptr) return MX8_ERR_INVALID_ARG;
+  if ((s32_mode == MX8_S32_GROUP || group_offsets != nullptr) &&
+      (group_offsets == nullptr || num_groups < 1 || num_groups > kMaxGroups))
+    return MX8_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return MX8_OK;
+  if (q == nullptr || s == nullptr || out == nullptr) return MX8_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out)) return MX8_ERR_ALIGNMENT;
+  return from_cuda(launch_dequant(fmt, q, s, s32, s32_mode, group_offsets, num_groups, rows, cols,
+                                  out_dtype == MX8_OUT_BF16, out, sm_count_current(),
+                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// ===================================================================== GEMM
+namespace {
+
+mx8_status gemm_common_checks(int fmt, int64_t N, int64_t K, const uint8_t* A, const uint8_t* SA,
+                              const uint8_t* B, const uint8_t* SB, int out_dtype, void* C,
+                              int64_t ldc) {
+  if (fmt != MX8_FMT_MXFP8 && fmt != MX8_FMT_NVFP4) return MX8_ERR_INVALID_ARG;
+  if (out_dtype != MX8_OUT_F32 && out_dtype != MX8_OUT_BF16) return MX8_ERR_INVALID_ARG;
+  if (N < 0 || K < 0 || K % 32 != 0 || ldc < N) return MX8_ERR_INVALID_ARG;
+  if (A == nullptr || SA == nullptr || B == nullptr || SB == nullptr || C == nullptr)
+    return MX8_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(SA) || !aligned16(B) || !aligned16(SB) || !aligned16(C) ||
+      ldc % 8 != 0)
+    return MX8_ERR_ALIGNMENT;
+  return MX8_OK;
+}
+
+cudaError_t zero_output(void* C, int64_t ldc, int64_t rows, int64_t N, int out_dtype, cudaStream_t s) {
+  const size_t es = out_dtype == MX8_OUT_BF16 ? 2 : 4;
+  return cudaMemset2DAsync(C, ldc * es, 0, N * es, rows, s);
+}
+
+}  // namespace
+
+extern "C" mx8_status bs_gemm(int fmt, int64_t M, int64_t N, int64_t K, const uint8_t* A,
+                              const uint8_t* SA, const float* A32, int a32_mode, const uint8_t* B,
+                              const uint8_t* SB, const float* B32, int b32_mode, int out_dtype,
+                              void* C, int64_t ldc, int accumulate, void* workspace,
+                              size_t workspace_bytes, mx8_stream_t stream) {
+  if (M < 0) return MX8_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return MX8_OK;
+  mx8_status st = gemm_common_checks(fmt, N, K, A, SA, B, SB, out_dtype, C, ldc);
+  if (st != MX8_OK) return st;
+  if (a32_mode < 0 || a32_mode > MX8_S32_TENSOR || b32_mode < 0 || b32_mode > MX8_S32_TENSOR)
+    return MX8_ERR_INVALID_ARG;
+  if ((a32_mode != MX8_S32_NONE && A32 == nullptr) || (b32_mode != MX8_S32_NONE && B32 == nullptr))
+    return MX8_ERR_INVALID_ARG;
+  if (accumulate && out_dtype != MX8_OUT_F32) return MX8_ERR_UNSUPPORTED;
+  if (M > INT32_MAX || N > INT32_MAX) return MX8_ERR_UNSUPPORTED;
+  st = check_ws(workspace, workspace_bytes, 1);
+  if (st != MX8_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) return accumulate ? MX8_OK : from_cuda(zero_output(C, ldc, M, N, out_dtype, s));
+
+  const uint64_t kbytes = fmt == MX8_FMT_MXFP8 ? K : K / 2;
+  CUtensorMap ma, mb;
+  const uint32_t box[2] = {128, 128};
+  const uint64_t da[2] = {kbytes, static_cast<uint64_t>(M)}, sa[1] = {kbytes};
+  const uint64_t db[2] = {kbytes, static_cast<uint64_t>(N)}, sb[1] = {kbytes};
+  if (!encode_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, A, da, sa, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, B, db, sb, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    return MX8_ERR_CUDA;
+  GemmArgs a{};
+  a.fmt = fmt; a.M = M; a.N = N; a.K = K;
+  a.SA = SA; a.SB = SB; a.A32 = A32; a.a32_mode = a32_mode; a.B32 = B32; a.b32_mode = b32_mode;
+  a.C = C; a.ldc = ldc; a.out_bf16 = out_dtype == MX8_OUT_BF16; a.accumulate = accumulate;
+  a.grouped = 0; a.G = 1; a.offs = nullptr; a.err = err_word(workspace);
+  return from_cuda(launch_bs_gemm(a, ma, mb, sm_count_current(), s));
+}
+
+extern "C" mx8_status bs_grouped_gemm(int fmt, int num_groups, const int64_t* group_offsets,
+                                      int64_t total_rows, int64_t N, int64_t K, const uint8_t* A,
+                                      const uint8_t* SA, const float* A32, const uint8_t* B,
+                                      const uint8_t* SB, const float* B32, int out_dtype, void* C,
+                                      int64_t ldc, void* workspace, size_t workspace_bytes,
+                                      mx8_stream_t stream) {
+  if (num_groups < 1 || num_groups > kMaxGroups || group_offsets == nullptr || total_rows < 0)
+    return MX8_ERR_INVALID_ARG;
+  if (total_rows == 0 || N == 0) return MX8_OK;
+  mx8_status st = gemm_common_checks(fmt, N, K, A, SA, B, SB, out_dtype, C, ldc);
+  if (st != MX8_OK) return st;
+  if (total_rows > INT32_MAX || N > INT32_MAX) return MX8_ERR_UNSUPPORTED;
+  st = check_ws(workspace, workspace_bytes, num_groups);
+  if (st != MX8_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) return from_cuda(zero_output(C, ldc, total_rows, N, out_dtype, s));
+
+  const uint64_t kbytes = fmt == MX8_FMT_MXFP8 ? K : K / 2;
+  CUtensorMap ma, mb;
+  const uint32_t box2[2] = {128, 128};
+  const uint64_t da[2] = {kbytes, static_cast<uint64_t>(total_rows)}, sa[1] = {kbytes};
+  const uint32_t box3[3] = {128, 128, 1};
+  const uint64_t db[3] = {kbytes, static_cast<uint64_t>(N), static_cast<uint64_t>(num_groups)};
+  const uint64_t sb[2] = {kbytes, kbytes * static_cast<uint64_t>(N)};
+  if (!encode_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, A, da, sa, box2, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, B, db, sb, box3, CU_TENSOR_MAP_SWIZZLE_128B))
+    return MX8_ERR_CUDA;
+  GemmArgs a{};
+  a.fmt = fmt; a.M = total_rows; a.N = N; a.K = K;
+  a.SA = SA; a.SB = SB; a.A32 = A32; a.a32_mode = A32 ? MX8_S32_ROW : MX8_S32_NONE;
+  a.B32 = B32; a.b32_mode = B32 ? MX8_S32_GROUP : MX8_S32_NONE;
+  a.C = C; a.ldc = ldc; a.out_bf16 = out_dtype == MX8_OUT_BF16; a.accumulate = 0;
+  a.grouped = 1; a.G = num_groups; a.offs = group_offsets; a.err = err_word(workspace);
+  return from_cuda(launch_bs_gemm(a, ma, mb, sm_count_current(), s));
+}
+
+// ===================================================================== errors
+extern "C" mx8_status mx8_check_device_error(void* workspace, mx8_stream_t stream) {
+  if (workspace == nullptr) return MX8_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MX8_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MX8_ERR_CUDA;
+  if (word == 0) return MX8_OK;
+  if (cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return MX8_ERR_CUDA;
+  return MX8_ERR_TIMEOUT;
+}
+
+namespace mx8q {
+namespace {
+// One block waits on a barrier that no thread will ever complete.
+__global__ void selftest_wait_kernel(int* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, err, kErrWaitSelftest, &abort, limit_ns);
+}
+}  // namespace
+
+cudaError_t launch_selftest_wait(int* err, uint64_t limit_ns, cudaStream_t stream) {
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(err, limit_ns);
+  return cudaGetLastError();
+}
+}  // namespace mx8q
+
+extern "C" mx8_status mx8_selftest_bounded_wait(void* workspace, uint64_t limit_ns, mx8_stream_t stream) {
+  if (workspace == nullptr || !aligned16(workspace)) return MX8_ERR_WORKSPACE;
+  if (limit_ns == 0 || limit_ns > 2000000000ull) return MX8_ERR_INVALID_ARG;
+  return from_cuda(launch_selftest_wait(err_word(workspace), limit_ns,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}

@@ -1,0 +1,153 @@
+// Dequantization of MXFP8 / NVFP4 matrices back to f32 or bf16: the
+// "dequantized backward" mode of "Miles Blackwell RL Cambia la Uniformidad
+// BF16 por MXFP8 y NVFP4 Nativos" (section "La Compatibilidad...") rebuilds
+// high-precision operands from the exact low-precision values of the forward
+// pass.
+//   MXFP8: out = e4m3 * 2^(s - 127)          (exact in f32 unless it overflows)
+//   NVFP4: out = RN((e2m1 * sb) * S_dec)     (the inner product is exact)
+// bf16 output is the round-to-nearest-even of the f32 value.
+//
+// Elementwise and bandwidth-bound: each thread turns 16 elements (one NVFP4
+// block or half an MXFP8 block) into 64 bytes of f32 or 32 bytes of bf16 with
+// 16-byte stores; the block scale is read from the tensor-core tile layout.
+#include <cuda_bf16.h>
+
+#include "device.cuh"
+#include "groups.cuh"
+#include "kernels.h"
+
+namespace mx8q {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ float e8m0_to_f32(uint32_t c) {
+  if (c == 255u) return __uint_as_float(0x7FC00000u);
+  if (c == 0u) return __uint_as_float(0x00400000u);   // 2^-127
+  return __uint_as_float(c << 23);
+}
+
+// E2M1 nibble: exponent field e (2 bits), mantissa m (1 bit), sign bit 3.
+__device__ __forceinline__ float e2m1_to_f32(uint32_t c) {
+  const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+  const uint32_t mag = (e == 0u) ? (m ? 0x3F000000u : 0u) : (((e + 126u) << 23) | (m << 22));
+  return __uint_as_float(mag | ((c & 8u) << 28));
+}
+
+__device__ __forceinline__ void e4m3x2_to_f32(uint32_t two, float& lo, float& hi) {
+  uint32_t h2;
+  const uint16_t in = static_cast<uint16_t>(two & 0xFFFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+  __half_raw a, b;
+  a.x = static_cast<unsigned short>(h2 & 0xFFFFu);
+  b.x = static_cast<unsigned short>(h2 >> 16);
+  lo = __half2float(__half(a));
+  hi = __half2float(__half(b));
+}
+
+__device__ __forceinline__ int64_t sf_byte(int64_t sr, int64_t k, int64_t kt) {
+  return ((sr >> 7) * kt + (k >> 2)) * 512 + (sr & 31) * 16 + ((sr >> 5) & 3) * 4 + (k & 3);
+}
+
+template <int kFmt, bool kGrouped>
+__global__ void __launch_bounds__(kThreads) dequant_kernel(
+    const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, const float* __restrict__ s32,
+    int s32_mode, const int64_t* __restrict__ offs, int G, int64_t R, int64_t C, int out_bf16,
+    void* __restrict__ out) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  GroupSmem& gs = *reinterpret_cast<GroupSmem*>(smem_raw);
+  if (kGrouped || s32_mode == MX8Q_S32_GROUP_MODE) load_group_prefix(gs, offs, G);
+
+  const int64_t bs = (kFmt == 0) ? 32 : 16;
+  const int64_t kt = (C / bs + 3) / 4;
+  const int64_t chunks = C / 16;
+  const int64_t total = R * chunks;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const int64_t r = i / chunks, c = (i % chunks) * 16;
+    int64_t sr = r;
+    int g = 0;
+    if (kGrouped || s32_mode == MX8Q_S32_GROUP_MODE) {
+      g = upper_group(gs.offs, G, r);
+      if (kGrouped) sr = gs.pref[g] + (r - gs.offs[g]);
+    }
+    const float sc = (kFmt == 0) ? e8m0_to_f32(s[sf_byte(sr, c / 32, kt)])
+                                 : e4m3_to_f32(s[sf_byte(sr, c / 16, kt)]);
+    float v[16];
+    if (kFmt == 0) {
+      const uint4 w = *reinterpret_cast<const uint4*>(q + r * C + c);
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        e4m3x2_to_f32(ws[j] & 0xFFFFu, v[4 * j], v[4 * j + 1]);
+        e4m3x2_to_f32(ws[j] >> 16, v[4 * j + 2], v[4 * j + 3]);
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], sc);
+    } else {
+      const uint2 w = *reinterpret_cast<const uint2*>(q + r * (C / 2) + c / 2);
+      float sd = 1.f;
+      if (s32_mode == 1) sd = s32[r];
+      else if (s32_mode == 2) sd = s32[0];
+      else if (s32_mode == 3) sd = s32[g];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t byte = ((j < 4 ? w.x : w.y) >> (8 * (j & 3))) & 0xFFu;
+        v[2 * j] = __fmul_rn(__fmul_rn(e2m1_to_f32(byte & 15u), sc), sd);
+        v[2 * j + 1] = __fmul_rn(__fmul_rn(e2m1_to_f32(byte >> 4), sc), sd);
+      }
+    }
+    if (out_bf16) {
+      uint32_t p[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const __nv_bfloat16 a = __float2bfloat16_rn(v[2 * j]);
+        const __nv_bfloat16 b = __float2bfloat16_rn(v[2 * j + 1]);
+        p[j] = static_cast<uint32_t>(__bfloat16_as_ushort(a)) |
+               (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + r * C + c);
+      dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
+      dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+    } else {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + r * C + c);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dequant(int fmt, const uint8_t* q, const uint8_t* s, const float* s32,
+                           int s32_mode, const int64_t* offs, int G, int64_t R, int64_t C,
+                           int out_bf16, void* out, int sm_count, cudaStream_t stream) {
+  const int64_t total = R * (C / 16);
+  if (total == 0) return cudaSuccess;
+  const bool grouped = offs != nullptr;
+  const bool need_groups = grouped || s32_mode == MX8Q_S32_GROUP_MODE;
+  const size_t smem = need_groups ? sizeof(GroupSmem) : 0;
+  const int64_t want = (total + kThreads - 1) / kThreads;
+  const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+  const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
+#define MX8Q_DQ_LAUNCH(F, GRP)                                                                  \
+  do {                                                                                           \
+    auto k = dequant_kernel<F, GRP>;                                                            \
+    if (smem > 0) {                                                                              \
+      cudaError_t ea = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,     \
+                                            static_cast<int>(smem));                           \
+      if (ea != cudaSuccess) return ea;                                                          \
+    }                                                                                            \
+    k<<<grid, kThreads, smem, stream>>>(q, s, s32, s32_mode, offs, G, R, C, out_bf16, out);     \
+  } while (0)
+  if (fmt == 0) {
+    if (grouped) MX8Q_DQ_LAUNCH(0, true); else MX8Q_DQ_LAUNCH(0, false);
+  } else {
+    if (grouped) MX8Q_DQ_LAUNCH(1, true); else MX8Q_DQ_LAUNCH(1, false);
+  }
+#undef MX8Q_DQ_LAUNCH
+  return cudaGetLastError();
+}
+
+}  // namespace mx8q

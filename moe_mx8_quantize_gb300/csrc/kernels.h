@@ -1,0 +1,52 @@
+// Host-side launch interface of the CUDA kernels (internal to the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mx8q {
+
+constexpr int kMaxGroups = 1024;   // groups (experts) per grouped call
+#define MX8Q_S32_GROUP_MODE 3          // FP32 scale per group (same value as MX8_S32_GROUP)
+
+size_t mxfp8_quant_smem_bytes();
+cudaError_t launch_mxfp8_quant(const CUtensorMap& tmap_x, int64_t R, int64_t C, bool row, bool col,
+                               uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                               int* err, int sm_count, cudaStream_t stream);
+
+cudaError_t launch_nvfp4_quant(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int scope,
+                               const int64_t* offs, int G, uint8_t* q, uint8_t* sblk, float* s32,
+                               float* amax_ws, int sm_count, cudaStream_t stream);
+
+cudaError_t launch_dequant(int fmt, const uint8_t* q, const uint8_t* s, const float* s32,
+                           int s32_mode, const int64_t* offs, int G, int64_t R, int64_t C,
+                           int out_bf16, void* out, int sm_count, cudaStream_t stream);
+
+struct GemmArgs {
+  int fmt;                 // 0 MXFP8, 1 NVFP4
+  int64_t M, N, K;         // K in elements
+  const uint8_t* SA;       // tensor-core scale tiles of A
+  const uint8_t* SB;
+  const float* A32;        // per-row (or per-tensor) FP32 decode scales
+  int a32_mode;
+  const float* B32;
+  int b32_mode;            // grouped: per group
+  void* C;
+  int64_t ldc;
+  int out_bf16;
+  int accumulate;
+  // grouped GEMM
+  int grouped;
+  int G;
+  const int64_t* offs;
+  int* err;
+};
+
+size_t gemm_smem_bytes(int fmt);
+cudaError_t launch_bs_gemm(const GemmArgs& a, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                           int sm_count, cudaStream_t stream);
+
+cudaError_t launch_selftest_wait(int* err, uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace mx8q

@@ -1,0 +1,215 @@
+"""GPU parity of the quantizers and the dequantizer against the CPU oracle:
+bit-exact codes, scales (every byte of the tensor-core tile buffers, padding
+included) and FP32 decode scales, on the workloads' shapes, ragged tails and
+edge-case inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import moe_mx8_quantize_gb300 as mx
+from moe_mx8_quantize_gb300 import inputs
+from tests._lib import dev, ensure_built, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+def _mx8_check(xb, flags=mx.ROWWISE | mx.COLWISE):
+    x = dev(xb)
+    q_row, s_row, q_col, s_col = mx.mx8_quantize(x, flags)
+    torch.cuda.synchronize()
+    R, C = xb.shape
+    if flags & mx.ROWWISE:
+        q, s = oracle.mxfp8_quantize_rowwise(xb)
+        assert np.array_equal(host(q_row), q), "rowwise codes"
+        sw = oracle.swizzle_scales(s)
+        assert np.array_equal(host(s_row)[: sw.size], sw), "rowwise scales"
+    if flags & mx.COLWISE:
+        qT, sT = oracle.mxfp8_quantize_colwise(xb)
+        assert np.array_equal(host(q_col), qT), "colwise codes"
+        sw = oracle.swizzle_scales(sT)
+        assert np.array_equal(host(s_col)[: sw.size], sw), "colwise scales"
+
+
+def test_mxfp8_pr1():
+    d = inputs.pr1()
+    _mx8_check(inputs.bits(d["X"]))
+    _mx8_check(inputs.bits(d["W"]))
+
+
+@pytest.mark.parametrize("shape,flags", [
+    ((96, 160), mx.ROWWISE | mx.COLWISE),     # ragged rows and columns of the 128x128 tile
+    ((32, 32), mx.ROWWISE | mx.COLWISE),
+    ((1, 32), mx.ROWWISE),
+    ((200, 96), mx.ROWWISE),
+    ((33, 4096), mx.ROWWISE),
+    ((256, 544), mx.COLWISE),
+    ((640, 384), mx.ROWWISE | mx.COLWISE),
+])
+def test_mxfp8_ragged_and_sweep_mix(shape, flags):
+    _mx8_check(inputs.bits(inputs.sweep(*shape, seed=11 + shape[0])), flags)
+
+
+def test_mxfp8_edge_values():
+    xb = np.zeros((64, 64), np.uint16)
+    xb[0, 0] = 0x7F7F           # +bf16 max
+    xb[1, 5] = 0xFF7F           # -bf16 max
+    xb[2, :] = 0x0001           # smallest subnormal
+    xb[3, 7] = 0x8000           # -0
+    xb[4, 3] = 0x8001           # negative subnormal
+    xb[5, :32] = 0x3F80         # all equal blocks (1.0)
+    xb[6, 32:] = 0xC3E0         # -448
+    _mx8_check(xb)
+
+
+def test_mxfp8_linear_full_size():
+    d = inputs.linear(device="cuda")
+    for name in ("X", "W", "dY"):
+        _mx8_check(inputs.bits(d[name]))
+
+
+def test_mxfp8_strided_input():
+    xb = inputs.bits(inputs.sweep(128, 256, seed=3))
+    big = torch.zeros((128, 320), dtype=torch.bfloat16, device="cuda")
+    big[:, :256] = dev(xb)
+    view = big[:, :256]
+    q_row, s_row, q_col, s_col = mx.mx8_quantize(view)
+    q, s = oracle.mxfp8_quantize_rowwise(xb)
+    assert np.array_equal(host(q_row), q)
+    qT, _ = oracle.mxfp8_quantize_colwise(xb)
+    assert np.array_equal(host(q_col), qT)
+
+
+def test_mxfp8_empty():
+    x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    mx.mx8_quantize(x, mx.ROWWISE)
+    torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------ NVFP4
+def _nv_check(xb, scope=mx.SCOPE_TOKEN, offs=None):
+    x = dev(xb)
+    go = None if offs is None else torch.tensor(offs, dtype=torch.int64, device="cuda")
+    q, s, s32 = mx.nvfp4_quantize_per_token(x, scope, go)
+    torch.cuda.synchronize()
+    oq, os_, o32 = oracle.nvfp4_quantize(xb, scope, offs)
+    assert np.array_equal(host(q), oq), "codes"
+    assert np.array_equal(host(s32).view(np.uint32), o32.view(np.uint32)), "fp32 scales"
+    sw = oracle.swizzle_scales(os_, offs)
+    assert np.array_equal(host(s)[: sw.size], sw), "block scales"
+    return q, s, s32
+
+
+def test_nvfp4_pr1():
+    d = inputs.pr1()
+    _nv_check(inputs.bits(d["X"]))
+    _nv_check(inputs.bits(d["W"]), mx.SCOPE_TENSOR)
+
+
+@pytest.mark.parametrize("shape", [(5, 16), (7, 48), (130, 80), (64, 208), (300, 768), (33, 7168)])
+def test_nvfp4_ragged(shape):
+    rows, cols = shape
+    wide = inputs.sweep(rows, (cols + 31) // 32 * 32, seed=rows)
+    _nv_check(inputs.bits(wide[:, :cols]))
+
+
+def test_nvfp4_edge_values():
+    xb = np.zeros((8, 64), np.uint16)
+    xb[1, 3] = 0x0001
+    xb[1, 9] = 0x8001
+    xb[2, :] = 0x7F7F
+    xb[3, ::2] = 0xFF7F
+    xb[4, 5] = 0x8000
+    xb[5, :] = 0x3F80
+    xb[6, 0] = 0x4528           # 2688
+    xb[6, 1:16] = 0x4100        # 8
+    xb[7, :16] = 0x0080         # smallest normal bf16 (2^-126)
+    _nv_check(xb)
+    _nv_check(xb, mx.SCOPE_TENSOR)
+
+
+def test_nvfp4_qwen_activation_full_size():
+    d = inputs.qwen_moe(device="cuda", with_weights=False)
+    _nv_check(inputs.bits(d["X"]))
+
+
+def test_nvfp4_group_scope_and_grouped_layout():
+    xb = inputs.bits(inputs.sweep(700, 256, seed=21))
+    offs = [0, 130, 130, 131, 400, 700]
+    _nv_check(xb, mx.SCOPE_GROUP, offs)
+    _nv_check(xb, mx.SCOPE_TOKEN, offs)
+    _nv_check(xb, mx.SCOPE_TENSOR, offs)
+
+
+def test_nvfp4_expert_weights_group_scope():
+    # gate|up of 4 experts stored jointly [E*2F, H], one FP32 scale per expert
+    d = inputs.qwen_moe(with_weights=True, tokens=8, hidden=256, experts=4, ffn=96)
+    W = inputs.bits(d["W_gu"]).reshape(4 * 192, 256)
+    _nv_check(W, mx.SCOPE_GROUP, [0, 192, 384, 576, 768])
+
+
+def test_nvfp4_per_token_batch_invariance_on_gpu():
+    xb = inputs.bits(inputs.qwen_moe(with_weights=False, tokens=256, hidden=512)["X"])
+    qa, sa, s32a = mx.nvfp4_quantize_per_token(dev(xb))
+    perm = np.random.default_rng(1).permutation(256)[:100]
+    qb, sb, s32b = mx.nvfp4_quantize_per_token(dev(xb[perm]))
+    assert np.array_equal(host(qa)[perm], host(qb))
+    assert np.array_equal(host(s32a)[perm], host(s32b))
+
+
+# ------------------------------------------------------------------ dequantize
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_dequant_mxfp8(out_dtype):
+    xb = inputs.bits(inputs.sweep(160, 320, seed=31))
+    q, s = oracle.mxfp8_quantize_rowwise(xb)
+    ref = oracle.dequant_mxfp8(q, s)
+    out = mx.dequantize(mx.FMT_MXFP8, dev(q), dev(oracle.swizzle_scales(s)), out_dtype=out_dtype)
+    got = host(out)
+    if out_dtype == torch.float32:
+        assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+    else:
+        assert np.array_equal(got, oracle.f32_to_bf16(ref))
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_dequant_nvfp4(out_dtype):
+    xb = inputs.bits(inputs.pr1()["X"])
+    q, s, s32 = oracle.nvfp4_quantize(xb)
+    ref = oracle.dequant_nvfp4(q, s, s32, oracle.S32_ROW)
+    out = mx.dequantize(mx.FMT_NVFP4, dev(q), dev(oracle.swizzle_scales(s)), dev(s32), out_dtype=out_dtype)
+    got = host(out)
+    if out_dtype == torch.float32:
+        assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+    else:
+        assert np.array_equal(got, oracle.f32_to_bf16(ref))
+
+
+def test_dequant_nvfp4_grouped_group_scale():
+    xb = inputs.bits(inputs.sweep(300, 128, seed=41))
+    offs = [0, 100, 100, 300]
+    q, s, s32 = oracle.nvfp4_quantize(xb, oracle.SCOPE_GROUP, offs)
+    ref = oracle.dequant_nvfp4(q, s, s32, oracle.S32_GROUP, offs)
+    go = torch.tensor(offs, dtype=torch.int64, device="cuda")
+    out = mx.dequantize(mx.FMT_NVFP4, dev(q), dev(oracle.swizzle_scales(s, offs)), dev(s32),
+                        s32_mode=mx.S32_GROUP, group_offsets=go)
+    assert np.array_equal(host(out).view(np.uint32), ref.view(np.uint32))
+
+
+# ------------------------------------------------------------------ bounded waits
+def test_bounded_wait_times_out_and_reports():
+    ws = mx.new_workspace()
+    assert mx.check_device_error(ws) == mx.OK
+    mx.selftest_bounded_wait(ws, 5_000_000)        # 5 ms
+    assert mx.check_device_error(ws) == mx.ERR_TIMEOUT
+    assert mx.check_device_error(ws) == mx.OK      # cleared
+    # the context is still usable
+    x = torch.ones((32, 32), dtype=torch.bfloat16, device="cuda")
+    q, s, _, _ = mx.mx8_quantize(x, mx.ROWWISE, ws=ws)
+    oq, _ = oracle.mxfp8_quantize_rowwise(host(x))
+    assert np.array_equal(host(q), oq)
+    assert mx.check_device_error(ws) == mx.OK

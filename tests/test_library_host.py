@@ -1,0 +1,86 @@
+"""Host-side checks of the C-ABI library that need no GPU: it builds for
+sm_103a, loads, exports every symbol the header declares, sizes its buffers
+as documented, and rejects bad arguments before any device work."""
+import ctypes
+import re
+
+import pytest
+
+from tests._lib import ROOT, ensure_built
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ensure_built()
+    import moe_mx8_quantize_gb300 as m
+    return m.load()
+
+
+def _header_functions():
+    src = open(f"{ROOT}/include/mx8q.h").read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return set(re.findall(r"\b([a-z_0-9]+)\s*\(", src)) - {"sizeof"}
+
+
+def test_exports_every_declared_symbol(lib):
+    import moe_mx8_quantize_gb300 as m
+    declared = _header_functions()
+    assert declared == set(m.EXPORTS), declared ^ set(m.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_scale_and_workspace_sizes(lib):
+    import moe_mx8_quantize_gb300 as m
+    # [R, C/32] padded to 128 x 4
+    assert m.scale_bytes(m.FMT_MXFP8, 2048, 2048) == 2048 * 64
+    assert m.scale_bytes(m.FMT_MXFP8, 130, 160) == 256 * 8
+    assert m.scale_bytes(m.FMT_NVFP4, 1, 16) == 128 * 4
+    assert m.scale_bytes(m.FMT_NVFP4, 4096, 2048) == 4096 * 128
+    assert m.scale_bytes_grouped(m.FMT_NVFP4, 300, 4, 256) == (3 + 4) * 128 * 16
+    assert m.workspace_bytes(1) >= 16 and m.workspace_bytes(256) >= 256 + 1024
+
+
+def test_invalid_arguments_rejected_on_host(lib):
+    import moe_mx8_quantize_gb300 as m
+    p = ctypes.c_void_p(16)      # never dereferenced: validation fails first
+    # cols not a multiple of 32
+    assert lib.mx8_quantize(p, 64, 48, 48, m.ROWWISE, p, p, None, None, p, 4096, None) == m.ERR_INVALID_ARG
+    # colwise needs rows % 32 == 0
+    assert lib.mx8_quantize(p, 40, 64, 64, m.COLWISE, None, None, p, p, p, 4096, None) == m.ERR_INVALID_ARG
+    # no copy requested / unknown flag
+    assert lib.mx8_quantize(p, 64, 64, 64, 0, p, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
+    assert lib.mx8_quantize(p, 64, 64, 64, 8, p, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
+    # ld < cols
+    assert lib.mx8_quantize(p, 64, 64, 32, m.ROWWISE, p, p, None, None, p, 4096, None) == m.ERR_INVALID_ARG
+    # misaligned input pointer
+    q = ctypes.c_void_p(24)
+    assert lib.mx8_quantize(q, 64, 64, 64, m.ROWWISE, p, p, None, None, p, 4096, None) == m.ERR_ALIGNMENT
+    # NVFP4: cols % 16, group scope without offsets, bad scope
+    assert lib.nvfp4_quantize_per_token(p, 4, 24, 24, 0, None, 0, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
+    assert lib.nvfp4_quantize_per_token(p, 4, 32, 32, 1, None, 0, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
+    assert lib.nvfp4_quantize_per_token(p, 4, 32, 32, 7, None, 0, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
+    # workspace missing or too small
+    assert lib.nvfp4_quantize_per_token(p, 4, 32, 32, 0, None, 0, p, p, p, None, 0, None) == m.ERR_WORKSPACE
+    # GEMM: K % 32, ldc < N, accumulate into bf16, bad scale modes
+    assert lib.bs_gemm(0, 8, 8, 48, p, p, None, 0, p, p, None, 0, 0, p, 8, 0, p, 4096, None) == m.ERR_INVALID_ARG
+    assert lib.bs_gemm(0, 8, 16, 64, p, p, None, 0, p, p, None, 0, 0, p, 8, 0, p, 4096, None) == m.ERR_INVALID_ARG
+    assert lib.bs_gemm(0, 8, 8, 64, p, p, None, 0, p, p, None, 0, 1, p, 8, 1, p, 4096, None) == m.ERR_UNSUPPORTED
+    assert lib.bs_gemm(1, 8, 8, 64, p, p, None, 1, p, p, None, 0, 0, p, 8, 0, p, 4096, None) == m.ERR_INVALID_ARG
+    assert lib.bs_gemm(0, 8, 8, 64, p, p, None, 0, p, p, None, 0, 0, p, 12, 0, p, 4096, None) == m.ERR_ALIGNMENT
+    # grouped: group count out of range
+    assert lib.bs_grouped_gemm(1, 0, p, 8, 8, 64, p, p, None, p, p, None, 0, p, 8, p, 4096, None) == m.ERR_INVALID_ARG
+    assert lib.bs_grouped_gemm(1, 5000, p, 8, 8, 64, p, p, None, p, p, None, 0, p, 8, p, 1 << 20, None) == m.ERR_INVALID_ARG
+    # dequantize: MXFP8 takes no FP32 scale, bad dtype
+    assert lib.dequantize(0, p, p, p, 1, None, 0, 4, 32, 0, p, None) == m.ERR_INVALID_ARG
+    assert lib.dequantize(1, p, p, None, 0, None, 0, 4, 32, 5, p, None) == m.ERR_INVALID_ARG
+    # empty problems are no-ops
+    assert lib.mx8_quantize(None, 0, 64, 64, m.ROWWISE, None, None, None, None, None, 0, None) == m.OK
+    assert lib.bs_gemm(0, 0, 8, 64, None, None, None, 0, None, None, None, 0, 0, None, 8, 0, None, 0, None) == m.OK
+
+
+def test_status_strings(lib):
+    import moe_mx8_quantize_gb300 as m
+    for s in range(7):
+        assert m.status_string(s)
+    assert m.status_string(m.ERR_TIMEOUT) == "a bounded device wait ran out"
