@@ -217,6 +217,20 @@ mx8_status bs_grouped_gemm(int fmt, int num_groups, const int64_t *group_offsets
                            int out_dtype, void *C, int64_t ldc,
                            void *workspace, size_t workspace_bytes, mx8_stream_t stream);
 
+/*
+ * SwiGLU between the joint gate|up GEMM and the down GEMM of a MoE expert
+ * ([MRL] "Un Cuantizador Compartido...": SwiGLU experts compute gate and up
+ * in one fused GEMM):
+ *     h[r, j] = RN_bf16( silu(g) * u ),  g = gate_up[r, j], u = gate_up[r, ffn + j]
+ * with silu(g) = g / (1 + exp(-g)) in FP32 (exp from the CUDA math library,
+ * so h can differ from a correctly rounded result by one bf16 unit).
+ *   gate_up : bf16 [rows, 2*ffn], row stride ld_gate_up
+ *   h       : bf16 [rows, ffn], row stride ld_h
+ * Requires ffn % 8 == 0, 16-byte aligned pointers and strides % 8 == 0.
+ */
+mx8_status mx8_swiglu(const void *gate_up, int64_t rows, int64_t ffn, int64_t ld_gate_up,
+                      void *h, int64_t ld_h, mx8_stream_t stream);
+
 /* Synchronises the stream, reads and clears the workspace error word:
  * MX8_OK, or MX8_ERR_TIMEOUT if a bounded device wait ran out. */
 mx8_status mx8_check_device_error(void *workspace, mx8_stream_t stream);

@@ -29,7 +29,7 @@ S32_NONE, S32_ROW, S32_TENSOR, S32_GROUP = 0, 1, 2, 3
 # every C symbol the header declares
 EXPORTS = ("mx8_scale_bytes", "mx8_scale_bytes_grouped", "mx8_workspace_bytes",
            "mx8_device_sm_count", "mx8_quantize", "nvfp4_quantize_per_token", "dequantize",
-           "bs_gemm", "bs_grouped_gemm", "mx8_check_device_error", "mx8_selftest_bounded_wait",
+           "bs_gemm", "bs_grouped_gemm", "mx8_swiglu", "mx8_check_device_error", "mx8_selftest_bounded_wait",
            "mx8_status_string")
 
 
@@ -75,6 +75,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bs_grouped_gemm.restype = _i
     lib.bs_grouped_gemm.argtypes = [_i, _i, _p, _i64, _i64, _i64, _p, _p, _p, _p, _p, _p, _i, _p,
                                     _i64, _p, _sz, _p]
+    lib.mx8_swiglu.restype = _i
+    lib.mx8_swiglu.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p]
     lib.mx8_check_device_error.restype = _i
     lib.mx8_check_device_error.argtypes = [_p, _p]
     lib.mx8_selftest_bounded_wait.restype = _i
@@ -275,6 +277,21 @@ def bs_grouped_gemm(fmt, group_offsets, A, SA, B, SB, K, A32=None, B32=None,
     out = torch.empty((A.shape[0], B.shape[1]), dtype=out_dtype, device=A.device)
     bs_grouped_gemm_into(fmt, group_offsets, A, SA, B, SB, K, out, A32, B32, ws, stream)
     return out
+
+
+# ---------------------------------------------------------------- SwiGLU
+def swiglu_into(gate_up, h, stream=None):
+    R, F2 = gate_up.shape
+    _check(load().mx8_swiglu(_ptr(gate_up), R, F2 // 2, gate_up.stride(0), _ptr(h), h.stride(0),
+                             _stream(stream)), "mx8_swiglu")
+
+
+def swiglu(gate_up, stream=None):
+    """h = silu(gate) * up for a bf16 [R, 2F] gate|up matrix -> bf16 [R, F]."""
+    R, F2 = gate_up.shape
+    h = torch.empty((R, F2 // 2), dtype=torch.bfloat16, device=gate_up.device)
+    swiglu_into(gate_up, h, stream)
+    return h
 
 
 # ---------------------------------------------------------------- errors

@@ -185,6 +185,18 @@ extern "C" mx8_status dequantize(int fmt, const uint8_t* q, const uint8_t* s, co
                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// ===================================================================== SwiGLU
+extern "C" mx8_status mx8_swiglu(const void* gate_up, int64_t rows, int64_t ffn, int64_t ld_gate_up,
+                                 void* h, int64_t ld_h, mx8_stream_t stream) {
+  if (rows < 0 || ffn < 0 || ffn % 8 != 0 || ld_gate_up < 2 * ffn || ld_h < ffn) return MX8_ERR_INVALID_ARG;
+  if (rows == 0 || ffn == 0) return MX8_OK;
+  if (gate_up == nullptr || h == nullptr) return MX8_ERR_INVALID_ARG;
+  if (!aligned16(gate_up) || !aligned16(h) || ld_gate_up % 8 != 0 || ld_h % 8 != 0) return MX8_ERR_ALIGNMENT;
+  return from_cuda(launch_swiglu(static_cast<const uint16_t*>(gate_up), rows, ffn, ld_gate_up,
+                                 static_cast<uint16_t*>(h), ld_h, sm_count_current(),
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
 // ===================================================================== GEMM
 namespace {
 
@@ -232,10 +244,11 @@ extern "C" mx8_status bs_gemm(int fmt, int64_t M, int64_t N, int64_t K, const ui
   const uint64_t kbytes = fmt == MX8_FMT_MXFP8 ? K : K / 2;
   CUtensorMap ma, mb;
   const uint32_t box[2] = {128, 128};
+  const uint32_t box_b[2] = {128, static_cast<uint32_t>(gemm_tile_n())};
   const uint64_t da[2] = {kbytes, static_cast<uint64_t>(M)}, sa[1] = {kbytes};
   const uint64_t db[2] = {kbytes, static_cast<uint64_t>(N)}, sb[1] = {kbytes};
   if (!encode_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, A, da, sa, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, B, db, sb, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      !encode_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, B, db, sb, box_b, CU_TENSOR_MAP_SWIZZLE_128B))
     return MX8_ERR_CUDA;
   GemmArgs a{};
   a.fmt = fmt; a.M = M; a.N = N; a.K = K;
@@ -266,7 +279,7 @@ extern "C" mx8_status bs_grouped_gemm(int fmt, int num_groups, const int64_t* gr
   CUtensorMap ma, mb;
   const uint32_t box2[2] = {128, 128};
   const uint64_t da[2] = {kbytes, static_cast<uint64_t>(total_rows)}, sa[1] = {kbytes};
-  const uint32_t box3[3] = {128, 128, 1};
+  const uint32_t box3[3] = {128, static_cast<uint32_t>(gemm_tile_n()), 1};
   const uint64_t db[3] = {kbytes, static_cast<uint64_t>(N), static_cast<uint64_t>(num_groups)};
   const uint64_t sb[2] = {kbytes, kbytes * static_cast<uint64_t>(N)};
   if (!encode_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, A, da, sa, box2, CU_TENSOR_MAP_SWIZZLE_128B) ||

@@ -15,18 +15,24 @@
 //
 //   C[m, n] (+)= A32[m] * B32[n or group] * sum_k A^[m, k] B^[n, k]
 //
-// Structure (one CTA per SM, persistent over 128x128 output tiles):
-//   warp 0      : TMA producer -- A and B tiles (128 rows x 128 bytes of K,
-//                 128-byte swizzle) and the matching 512-byte scale tiles,
-//                 into a ring of shared-memory stages guarded by mbarriers;
+// Structure (one CTA per SM, persistent over 128 x BN output tiles):
+//   warp 0      : TMA producer -- A (128 rows) and B (BN rows) tiles of 128
+//                 bytes of K with the 128-byte swizzle, plus the matching
+//                 512-byte scale tiles, into a ring of shared-memory stages
+//                 guarded by mbarriers;
 //   warp 1      : allocates tensor memory; one thread copies each stage's
 //                 scale tiles into tensor memory (tcgen05.cp) and issues the
-//                 block-scaled MMAs, accumulating in one of two 128-column
-//                 FP32 accumulators, then commits the stage back to the
-//                 producer and the finished accumulator to the epilogue;
-//   warps 2..5  : epilogue -- tcgen05.ld of their 32-lane quarter, FP32
-//                 scales, convert, store; the accumulator is released as soon
-//                 as it has been read, so the next tile's MMAs overlap.
+//                 block-scaled MMAs (M = 128, N = BN) into an FP32 accumulator
+//                 in tensor memory, commits each stage back to the producer
+//                 and each finished accumulator to the epilogue;
+//   epilogue    : BN/32 warps, two per 32-lane quarter of tensor memory when
+//                 BN = 256; each pulls its 32 rows x 128 columns into
+//                 registers, releases the accumulator at once (so the next
+//                 tile's MMAs start), then applies the FP32 scales, converts
+//                 and stores.
+// BN = 128 keeps two accumulators (epilogue fully overlapped); BN = 256 moves
+// half the operand bytes per FLOP of BN = 128 and keeps one accumulator (the
+// 512 tensor-memory columns hold 256 accumulator columns plus the scales).
 // Every mbarrier wait is bounded (about a second) and reports through the
 // workspace error word.
 #include <cuda_bf16.h>
@@ -35,17 +41,19 @@
 #include "groups.cuh"
 #include "kernels.h"
 
+#ifndef MX8Q_GEMM_BN
+#define MX8Q_GEMM_BN 256
+#endif
+
 namespace mx8q {
 
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 128;
 constexpr int kKBytes = 128;               // bytes of K per stage and row (one swizzle atom)
-constexpr int kThreads = 192;
-constexpr int kTileBytes = BM * kKBytes;   // 16 KB for A (and for B, since BN == BM)
+constexpr int kTileABytes = BM * kKBytes;  // 16 KB
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCols = BN;          // f32 accumulator: one column per output column
+constexpr int kSmemBudget = 227 * 1024 - 1024;
 
 template <int kFmt>
 struct Cfg;
@@ -53,7 +61,7 @@ template <>
 struct Cfg<0> {                 // MXFP8: K = 128 elements per stage, 32 per MMA
   static constexpr int kElemsPerStage = 128;
   static constexpr int kElemsPerMma = 32;
-  static constexpr int kSfTiles = 1;     // 128x4 scale tiles per operand per stage
+  static constexpr int kSfTiles = 1;     // 128x4 scale tiles per 128 rows per stage
   static constexpr int kBlock = 32;
 };
 template <>
@@ -64,20 +72,34 @@ struct Cfg<1> {                 // NVFP4: K = 256 elements per stage, 64 per MMA
   static constexpr int kBlock = 16;
 };
 
-template <int kFmt, bool kGrouped>
+template <int kFmt, bool kGrouped, int kBN>
 struct Layout {
-  static constexpr int kStages = (kFmt == 1 && kGrouped) ? 5 : 6;
-  static constexpr int kSfBytes = Cfg<kFmt>::kSfTiles * 512;
-  static constexpr uint32_t kSfCols = 4 * Cfg<kFmt>::kSfTiles;   // tmem columns per operand
+  static constexpr int kBRow128 = kBN / 128;                         // 128-row blocks of B
+  static constexpr int kTileBBytes = kBN * kKBytes;
+  static constexpr int kSfaBytes = Cfg<kFmt>::kSfTiles * 512;
+  static constexpr int kSfbBytes = Cfg<kFmt>::kSfTiles * 512 * kBRow128;
+  static constexpr int kStageBytes = kTileABytes + kTileBBytes + kSfaBytes + kSfbBytes;
+  static constexpr int kFixed = 256 + (kGrouped ? static_cast<int>(sizeof(GroupSmem)) : 0);
+  static constexpr int kStagesFit = (kSmemBudget - kFixed) / kStageBytes;
+  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+  static constexpr int kAccBufs = kBN == 128 ? 2 : 1;
+  static constexpr uint32_t kSfaCols = 4 * Cfg<kFmt>::kSfTiles;      // tensor-memory columns
+  static constexpr uint32_t kSfbCols = 4 * Cfg<kFmt>::kSfTiles * kBRow128;
+  static constexpr uint32_t kSfColsPerStage = kSfaCols + kSfbCols;
+  static constexpr uint32_t kAccCols = kAccBufs * kBN;
+  static constexpr int kEpiWarps = kBN / 32;                         // 128 columns per warp
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static_assert(kStages >= 3, "pipeline too shallow");
+  static_assert(kAccCols + kStages * kSfColsPerStage <= kTmemCols, "tensor memory overflow");
 };
 
-template <int kFmt, bool kGrouped>
+template <int kFmt, bool kGrouped, int kBN>
 struct __align__(1024) GemmSmem {
-  using L = Layout<kFmt, kGrouped>;
-  uint8_t a[L::kStages][kTileBytes];
-  uint8_t b[L::kStages][kTileBytes];
-  uint8_t sfa[L::kStages][L::kSfBytes];
-  uint8_t sfb[L::kStages][L::kSfBytes];
+  using L = Layout<kFmt, kGrouped, kBN>;
+  uint8_t a[L::kStages][kTileABytes];
+  uint8_t b[L::kStages][L::kTileBBytes];
+  uint8_t sfa[L::kStages][L::kSfaBytes];
+  uint8_t sfb[L::kStages][L::kSfbBytes];
   uint64_t full[L::kStages];
   uint64_t empty[L::kStages];
   uint64_t acc_full[2];
@@ -87,17 +109,17 @@ struct __align__(1024) GemmSmem {
   int abort;
 };
 
-// Instruction descriptor of the block-scaled MMA (M = 128, N = BN, both
-// operands K-major): B scale id bits 4-5, A/B element type bits 7-9 / 10-12,
-// N >> 3 bits 17-22, scale type bit 23 (1 = UE8M0, 0 = UE4M3), M >> 4 bits
-// 24-28, A scale id bits 29-30.
-__device__ __forceinline__ uint32_t make_idesc(int fmt, uint32_t sf_id) {
+// Instruction descriptor of the block-scaled MMA (M = 128, both operands
+// K-major): B scale id bits 4-5, A/B element type bits 7-9 / 10-12, N >> 3
+// bits 17-22, scale type bit 23 (1 = UE8M0, 0 = UE4M3), M >> 4 bits 24-28,
+// A scale id bits 29-30.
+__device__ __forceinline__ uint32_t make_idesc(int fmt, int n, uint32_t sf_id) {
   const uint32_t etype = fmt == 0 ? 0u /* E4M3 */ : 1u /* E2M1 */;
   uint32_t d = 0;
   d |= (sf_id & 3u) << 4;
   d |= etype << 7;
   d |= etype << 10;
-  d |= static_cast<uint32_t>(BN >> 3) << 17;
+  d |= static_cast<uint32_t>(n >> 3) << 17;
   d |= (fmt == 0 ? 1u : 0u) << 23;
   d |= static_cast<uint32_t>(BM >> 4) << 24;
   d |= (sf_id & 3u) << 29;
@@ -113,7 +135,7 @@ struct TileCoord {
   int64_t n0;
 };
 
-template <bool kGrouped>
+template <bool kGrouped, int kBN>
 __device__ __forceinline__ TileCoord decode_tile(int64_t t, int64_t tiles_n, int64_t M,
                                                  const GroupSmem* gs, int G) {
   TileCoord c;
@@ -124,7 +146,7 @@ __device__ __forceinline__ TileCoord decode_tile(int64_t t, int64_t tiles_n, int
     c.a_row0 = mt * BM;
     c.rows = M - c.a_row0 < BM ? M - c.a_row0 : BM;
     c.sfa_tile = mt;
-    c.n0 = nt * BN;
+    c.n0 = nt * kBN;
     return c;
   }
   const int64_t gmt = t / tiles_n;                   // global m-tile band
@@ -138,17 +160,17 @@ __device__ __forceinline__ TileCoord decode_tile(int64_t t, int64_t tiles_n, int
   c.a_row0 = gs->offs[g] + mt * BM;
   c.rows = ng - mt * BM < BM ? ng - mt * BM : BM;
   c.sfa_tile = mt0 + mt;
-  c.n0 = nt * BN;
+  c.n0 = nt * kBN;
   return c;
 }
 
-template <int kFmt, bool kGrouped>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int kFmt, bool kGrouped, int kBN>
+__global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
     bs_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b, const GemmArgs args) {
-  using L = Layout<kFmt, kGrouped>;
+  using L = Layout<kFmt, kGrouped, kBN>;
   using F = Cfg<kFmt>;
-  using Smem = GemmSmem<kFmt, kGrouped>;
+  using Smem = GemmSmem<kFmt, kGrouped, kBN>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   Smem& sm = *reinterpret_cast<Smem*>(base);
@@ -156,6 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int* err = args.err;
+  constexpr int kEpiThreads = 32 * L::kEpiWarps;
 
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmap_a);
@@ -166,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sm.acc_full[i]), 1);
-      mbar_init(smem_u32(&sm.acc_empty[i]), 128);
+      mbar_init(smem_u32(&sm.acc_empty[i]), kEpiThreads);
     }
     mbar_init(smem_u32(&sm.drain), 1);
     sm.abort = 0;
@@ -183,7 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = sm.tmem_base;
 
   const int64_t M = args.M, N = args.N, K = args.K;
-  const int64_t tiles_n = (N + BN - 1) / BN;
+  const int64_t tiles_n = (N + kBN - 1) / kBN;
+  const int64_t n_rt = (N + 127) / 128;                   // 128-row scale tiles of B (per group)
   const int64_t tiles_m = kGrouped ? gs->pref[args.G] / BM : (M + BM - 1) / BM;
   const int64_t ntiles = tiles_m * tiles_n;
   const int64_t kbytes = kFmt == 0 ? K : K / 2;
@@ -197,11 +221,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       bool ok = true;
       for (int64_t t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
-        const TileCoord tc = decode_tile<kGrouped>(t, tiles_n, M, gs, G);
-        const int64_t nt = tc.n0 / BN;
+        const TileCoord tc = decode_tile<kGrouped, kBN>(t, tiles_n, M, gs, G);
         const uint8_t* sfa_src = args.SA + tc.sfa_tile * sf_kt * 512;
-        const uint8_t* sfb_src =
-            args.SB + ((kGrouped ? static_cast<int64_t>(tc.g) * tiles_n : 0) + nt) * sf_kt * 512;
+        const int64_t brt0 = (kGrouped ? static_cast<int64_t>(tc.g) * n_rt : 0) + tc.n0 / 128;
+        const uint8_t* sfb_src[L::kBRow128];
+#pragma unroll
+        for (int h = 0; h < L::kBRow128; ++h) {
+          // a 128-row block of B past N has zero data; reuse a valid scale tile for it
+          const int64_t rt = (tc.n0 / 128 + h < n_rt) ? brt0 + h : brt0;
+          sfb_src[h] = args.SB + rt * sf_kt * 512;
+        }
         for (int kt = 0; kt < ktiles; ++kt, ++it) {
           const int s = it % L::kStages;
           const uint32_t ph = (it / L::kStages) & 1;
@@ -212,14 +241,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int64_t sf0 = static_cast<int64_t>(kt) * F::kSfTiles;
           const int nsf = static_cast<int>(sf_kt - sf0 < F::kSfTiles ? sf_kt - sf0 : F::kSfTiles);
           const uint32_t full = smem_u32(&sm.full[s]);
-          mbar_arrive_expect_tx(full, 2 * kTileBytes + 2 * nsf * 512);
+          mbar_arrive_expect_tx(full, kTileABytes + L::kTileBBytes + (1 + L::kBRow128) * nsf * 512);
           tma_load_2d(smem_u32(sm.a[s]), &tmap_a, kt * kKBytes, static_cast<int32_t>(tc.a_row0), full);
           if (kGrouped)
             tma_load_3d(smem_u32(sm.b[s]), &tmap_b, kt * kKBytes, static_cast<int32_t>(tc.n0), tc.g, full);
           else
             tma_load_2d(smem_u32(sm.b[s]), &tmap_b, kt * kKBytes, static_cast<int32_t>(tc.n0), full);
           bulk_load(smem_u32(sm.sfa[s]), sfa_src + sf0 * 512, nsf * 512, full);
-          bulk_load(smem_u32(sm.sfb[s]), sfb_src + sf0 * 512, nsf * 512, full);
+#pragma unroll
+          for (int h = 0; h < L::kBRow128; ++h)
+            bulk_load(smem_u32(sm.sfb[s]) + h * F::kSfTiles * 512, sfb_src[h] + sf0 * 512, nsf * 512, full);
         }
       }
       if (!ok) {
@@ -234,16 +265,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int it = 0, tcount = 0;
       bool ok = true;
-      const uint32_t sf_base = tmem + 2 * kAccCols;
+      const uint32_t sf_base = tmem + L::kAccCols;
       for (int64_t t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++tcount) {
-        const int as = tcount & 1;
-        const uint32_t aph = (tcount >> 1) & 1;
+        const int as = tcount % L::kAccBufs;
+        const uint32_t aph = (tcount / L::kAccBufs) & 1;
         if (!mbar_wait(smem_u32(&sm.acc_empty[as]), aph ^ 1, err, kErrWaitAccum, &sm.abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + as * kAccCols;
+        const uint32_t d_tmem = tmem + as * kBN;
         for (int kt = 0; kt < ktiles; ++kt, ++it) {
           const int s = it % L::kStages;
           const uint32_t ph = (it / L::kStages) & 1;
@@ -254,11 +285,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const int64_t sf0 = static_cast<int64_t>(kt) * F::kSfTiles;
           const int nsf = static_cast<int>(sf_kt - sf0 < F::kSfTiles ? sf_kt - sf0 : F::kSfTiles);
-          const uint32_t tsfa = sf_base + s * 2 * L::kSfCols;
-          const uint32_t tsfb = tsfa + L::kSfCols;
+          // tensor-memory scale layout per stage: A -> 4 columns per K sub-tile;
+          // B -> (4 columns x kBRow128) per K sub-tile, the 128-row blocks adjacent
+          const uint32_t tsfa = sf_base + s * L::kSfColsPerStage;
+          const uint32_t tsfb = tsfa + L::kSfaCols;
           for (int j = 0; j < nsf; ++j) {
             tc_cp_32x128b_x4(tsfa + 4 * j, smem_desc(smem_u32(sm.sfa[s]) + 512 * j, 128, 128, kSwizzleNone));
-            tc_cp_32x128b_x4(tsfb + 4 * j, smem_desc(smem_u32(sm.sfb[s]) + 512 * j, 128, 128, kSwizzleNone));
+#pragma unroll
+            for (int h = 0; h < L::kBRow128; ++h)
+              tc_cp_32x128b_x4(tsfb + (j * L::kBRow128 + h) * 4,
+                               smem_desc(smem_u32(sm.sfb[s]) + (h * F::kSfTiles + j) * 512, 128, 128,
+                                         kSwizzleNone));
           }
           const int64_t krem = K - static_cast<int64_t>(kt) * F::kElemsPerStage;
           const int nmma = static_cast<int>(krem >= F::kElemsPerStage
@@ -270,9 +307,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bd = smem_desc(b0 + kk * 32, 16, 1024, kSwizzle128B);
             const uint32_t acc = (kt > 0 || kk > 0) ? 1u : 0u;
             if (kFmt == 0)
-              tc_mma_mxf8(d_tmem, ad, bd, make_idesc(0, kk), tsfa, tsfb, acc);
+              tc_mma_mxf8(d_tmem, ad, bd, make_idesc(0, kBN, kk), tsfa, tsfb, acc);
             else
-              tc_mma_nvf4(d_tmem, ad, bd, make_idesc(1, 0), tsfa + 4 * kk, tsfb + 4 * kk, acc);
+              tc_mma_nvf4(d_tmem, ad, bd, make_idesc(1, kBN, 0), tsfa + 4 * kk,
+                          tsfb + 4 * L::kBRow128 * kk, acc);
           }
           tc_commit(smem_u32(&sm.empty[s]));   // stage free once these MMAs finish
         }
@@ -285,16 +323,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;
     const int quarter = warp & 3;              // tcgen05.ld lane quarter of this warp
+    const int col0 = (ew / 4) * 128;           // this warp's 128 accumulator columns
     const int r_in_tile = quarter * 32 + lane;
     int tcount = 0;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++tcount) {
-      const int as = tcount & 1;
-      const uint32_t aph = (tcount >> 1) & 1;
+      const int as = tcount % L::kAccBufs;
+      const uint32_t aph = (tcount / L::kAccBufs) & 1;
       const bool ok = mbar_wait(smem_u32(&sm.acc_full[as]), aph, err, kErrWaitEpilogue, &sm.abort);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const TileCoord tc = decode_tile<kGrouped>(t, tiles_n, M, gs, G);
+      uint32_t r[4][32];
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + as * kBN + col0;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) tmem_ld_32x32b_x32(taddr + ch * 32, r[ch]);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.acc_empty[as]));   // accumulator drained into registers
+
+      const TileCoord tc = decode_tile<kGrouped, kBN>(t, tiles_n, M, gs, G);
       const bool row_ok = r_in_tile < tc.rows;
       const int64_t m = tc.a_row0 + r_in_tile;
       float sa = 1.f;
@@ -306,24 +354,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kGrouped && args.B32 != nullptr) sg = args.B32[tc.g];
       else if (!kGrouped && args.b32_mode == 2) sg = args.B32[0];
       const bool b_row = !kGrouped && args.b32_mode == 1;
-#pragma unroll 1
-      for (int ch = 0; ch < BN / 32; ++ch) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + as * kAccCols + ch * 32, r);
-        tmem_wait_ld();
-        if (ch == BN / 32 - 1) {
-          tc_fence_before();
-          mbar_arrive(smem_u32(&sm.acc_empty[as]));
-        }
-        const int64_t n0 = tc.n0 + ch * 32;
-        if (!row_ok || n0 >= N) continue;
+      // the two FP32 decode scales are combined first: acc * A32 alone can
+      // overflow for tokens whose amax is near the bf16 maximum
+      const float s_ab = __fmul_rn(sa, sg);
+      if (!row_ok) continue;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        const int64_t n0 = tc.n0 + col0 + ch * 32;
+        if (n0 >= N) break;
         float v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          float y = __fmul_rn(__uint_as_float(r[j]), sa);
-          float sbn = sg;
-          if (b_row) sbn = (n0 + j < N) ? args.B32[n0 + j] : 0.f;
-          v[j] = __fmul_rn(y, sbn);
+          float sc = s_ab;
+          if (b_row) sc = (n0 + j < N) ? __fmul_rn(sa, args.B32[n0 + j]) : 0.f;
+          v[j] = __fmul_rn(__uint_as_float(r[ch][j]), sc);
         }
         const bool full_chunk = n0 + 32 <= N;
         if (args.out_bf16) {
@@ -367,41 +411,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int kFmt, bool kGrouped>
-size_t smem_bytes_for() {
-  return sizeof(GemmSmem<kFmt, kGrouped>) + (kGrouped ? sizeof(GroupSmem) : 0) + 1024;
+template <int kFmt, bool kGrouped, int kBN>
+cudaError_t launch_variant(const GemmArgs& a, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                           int sm_count, cudaStream_t stream) {
+  using L = Layout<kFmt, kGrouped, kBN>;
+  const int64_t tiles_n = (a.N + kBN - 1) / kBN;
+  int64_t tiles_m = (a.M + BM - 1) / BM;
+  if (a.grouped) tiles_m += a.G;                  // upper bound: every group pads a tile
+  const int64_t ntiles = tiles_m * tiles_n;
+  const unsigned grid = static_cast<unsigned>(ntiles < sm_count ? ntiles : sm_count);
+  if (grid == 0) return cudaSuccess;
+  auto k = bs_gemm_kernel<kFmt, kGrouped, kBN>;
+  constexpr size_t smem = sizeof(GemmSmem<kFmt, kGrouped, kBN>) + (kGrouped ? sizeof(GroupSmem) : 0) + 1024;
+  static_assert(smem <= 227 * 1024, "shared memory over the per-block limit");
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  k<<<grid, L::kThreads, smem, stream>>>(tmap_a, tmap_b, a);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t gemm_smem_bytes(int fmt) {
-  return fmt == 0 ? smem_bytes_for<0, true>() : smem_bytes_for<1, true>();
-}
+int gemm_tile_n() { return MX8Q_GEMM_BN; }
 
 cudaError_t launch_bs_gemm(const GemmArgs& a, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                            int sm_count, cudaStream_t stream) {
-  const int64_t tiles_n = (a.N + BN - 1) / BN;
-  int64_t tiles_m = (a.M + BM - 1) / BM;
-  if (a.grouped) tiles_m = (a.M + BM - 1) / BM + a.G;   // upper bound: every group pads a tile
-  const int64_t ntiles = tiles_m * tiles_n;
-  const unsigned grid = static_cast<unsigned>(ntiles < sm_count ? ntiles : sm_count);
-  if (grid == 0) return cudaSuccess;
-#define MX8Q_GEMM_LAUNCH(F, GRP)                                                               \
-  do {                                                                                          \
-    auto k = bs_gemm_kernel<F, GRP>;                                                           \
-    const size_t smem = smem_bytes_for<F, GRP>();                                              \
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,       \
-                                         static_cast<int>(smem));                             \
-    if (e != cudaSuccess) return e;                                                             \
-    k<<<grid, kThreads, smem, stream>>>(tmap_a, tmap_b, a);                                    \
-  } while (0)
+  constexpr int BN = MX8Q_GEMM_BN;
   if (a.fmt == 0) {
-    if (a.grouped) MX8Q_GEMM_LAUNCH(0, true); else MX8Q_GEMM_LAUNCH(0, false);
-  } else {
-    if (a.grouped) MX8Q_GEMM_LAUNCH(1, true); else MX8Q_GEMM_LAUNCH(1, false);
+    return a.grouped ? launch_variant<0, true, BN>(a, tmap_a, tmap_b, sm_count, stream)
+                     : launch_variant<0, false, BN>(a, tmap_a, tmap_b, sm_count, stream);
   }
-#undef MX8Q_GEMM_LAUNCH
-  return cudaGetLastError();
+  return a.grouped ? launch_variant<1, true, BN>(a, tmap_a, tmap_b, sm_count, stream)
+                   : launch_variant<1, false, BN>(a, tmap_a, tmap_b, sm_count, stream);
 }
 
 }  // namespace mx8q

@@ -150,4 +150,56 @@ cudaError_t launch_dequant(int fmt, const uint8_t* q, const uint8_t* s, const fl
   return cudaGetLastError();
 }
 
+// SwiGLU between the gate|up and down GEMMs of a MoE expert: gate and up are
+// the two halves of one fused GEMM output ("Un Cuantizador Compartido Es el
+// Mecanismo Real": SwiGLU experts compute gate and up in one fused GEMM).
+//   h[r, j] = RN_bf16( silu(g) * u ),  silu(g) = g / (1 + exp(-g)),
+//   g = gu[r, j], u = gu[r, F + j]; f32 arithmetic, exp from CUDA's expf,
+//   evaluated as g*e^-|g|/(1+e^-|g|) for negative g so nothing overflows.
+namespace {
+__global__ void __launch_bounds__(kThreads) swiglu_kernel(const uint16_t* __restrict__ gu, int64_t R,
+                                                          int64_t F, int64_t ld_gu,
+                                                          uint16_t* __restrict__ h, int64_t ld_h) {
+  const int64_t chunks = F / 8;
+  const int64_t total = R * chunks;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const int64_t r = i / chunks, c = (i % chunks) * 8;
+    const uint4 g = *reinterpret_cast<const uint4*>(gu + r * ld_gu + c);
+    const uint4 u = *reinterpret_cast<const uint4*>(gu + r * ld_gu + F + c);
+    const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float v[2];
+      const float gv[2] = {bf16_lo(gw[j]), bf16_hi(gw[j])};
+      const float uv[2] = {bf16_lo(uw[j]), bf16_hi(uw[j])};
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        // silu(g) = g * sigmoid(g); the exponent is taken of -|g| so it never
+        // overflows: sigmoid(g) = 1/(1+e^-g) for g >= 0, e^g/(1+e^g) for g < 0
+        const float t = expf(-fabsf(gv[k]));
+        const float num = gv[k] >= 0.f ? gv[k] : __fmul_rn(gv[k], t);
+        const float silu = __fdiv_rn(num, __fadd_rn(1.0f, t));
+        v[k] = __fmul_rn(silu, uv[k]);
+      }
+      o[j] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[0]))) |
+             (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[1]))) << 16);
+    }
+    *reinterpret_cast<uint4*>(h + r * ld_h + c) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+}  // namespace
+
+cudaError_t launch_swiglu(const uint16_t* gu, int64_t R, int64_t F, int64_t ld_gu, uint16_t* h,
+                          int64_t ld_h, int sm_count, cudaStream_t stream) {
+  const int64_t total = R * (F / 8);
+  if (total == 0) return cudaSuccess;
+  const int64_t want = (total + kThreads - 1) / kThreads;
+  const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+  swiglu_kernel<<<static_cast<unsigned>(want < cap ? want : cap), kThreads, 0, stream>>>(gu, R, F, ld_gu,
+                                                                                        h, ld_h);
+  return cudaGetLastError();
+}
+
 }  // namespace mx8q

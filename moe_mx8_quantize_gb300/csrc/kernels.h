@@ -23,6 +23,9 @@ cudaError_t launch_dequant(int fmt, const uint8_t* q, const uint8_t* s, const fl
                            int s32_mode, const int64_t* offs, int G, int64_t R, int64_t C,
                            int out_bf16, void* out, int sm_count, cudaStream_t stream);
 
+cudaError_t launch_swiglu(const uint16_t* gu, int64_t R, int64_t F, int64_t ld_gu, uint16_t* h,
+                          int64_t ld_h, int sm_count, cudaStream_t stream);
+
 struct GemmArgs {
   int fmt;                 // 0 MXFP8, 1 NVFP4
   int64_t M, N, K;         // K in elements
@@ -43,7 +46,7 @@ struct GemmArgs {
   int* err;
 };
 
-size_t gemm_smem_bytes(int fmt);
+int gemm_tile_n();   // N extent of the GEMM output tile (rows of B per TMA box)
 cudaError_t launch_bs_gemm(const GemmArgs& a, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                            int sm_count, cudaStream_t stream);
 

@@ -22,12 +22,14 @@
 //   sb    = RNE_E4M3_sat((amax_b / 6) * S_enc)
 //   r     = sb ? min(S_enc / sb, FLT_MAX) : 0,   code = RNE_E2M1_sat(x * r)
 //
-// Design: one warp per scale row, 8 elements (16 bytes) per lane per step so
-// loads and stores are fully coalesced; a 16-element block is a lane pair, a
-// 4-block scale group (one aligned 32-bit word of the tensor-core tile) is 8
-// lanes.  Per-token scope reads the row twice (amax, then encode); the second
-// read is served from L1/L2, so HBM sees one read.  Rows of the padded scale
-// tile that hold no token are written as zero by the same warps.
+// Design: one warp per scale row.  Lane l owns elements [256*i + 8*l, +8) of
+// the row for every 256-element chunk i, so loads and stores are fully
+// coalesced; a 16-element block is a lane pair and a 4-block scale group (one
+// aligned 32-bit word of the tensor-core tile) is 8 lanes.  Rows of up to
+// 256*kCh elements are loaded into registers with all loads issued up front
+// (many bytes in flight per warp, one HBM read per element); longer rows are
+// streamed twice (the second read comes from L1/L2).  Rows of the padded
+// scale tile that hold no token are written as zero by the same warps.
 #include <float.h>
 
 #include "device.cuh"
@@ -54,14 +56,29 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-__device__ __forceinline__ float row_amax(const uint16_t* __restrict__ xr, int64_t C, int lane) {
+__device__ __forceinline__ float amax8(const uint4& w) {
+  return fmaxf(fmaxf(fmaxf(fabsf(bf16_lo(w.x)), fabsf(bf16_hi(w.x))),
+                     fmaxf(fabsf(bf16_lo(w.y)), fabsf(bf16_hi(w.y)))),
+               fmaxf(fmaxf(fabsf(bf16_lo(w.z)), fabsf(bf16_hi(w.z))),
+                     fmaxf(fabsf(bf16_lo(w.w)), fabsf(bf16_hi(w.w)))));
+}
+
+__device__ __forceinline__ uint4 ld_nc(const uint16_t* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+// Streaming row amax, 8 chunks of 256 elements in flight per lane.
+__device__ __forceinline__ float row_amax_stream(const uint16_t* __restrict__ xr, int64_t C, int lane) {
   float a = 0.f;
-  for (int64_t c = lane * 8; c < C; c += 256) {
-    const uint4 w = *reinterpret_cast<const uint4*>(xr + c);
-    a = fmaxf(a, fmaxf(fmaxf(fabsf(bf16_lo(w.x)), fabsf(bf16_hi(w.x))),
-                       fmaxf(fabsf(bf16_lo(w.y)), fabsf(bf16_hi(w.y)))));
-    a = fmaxf(a, fmaxf(fmaxf(fabsf(bf16_lo(w.z)), fabsf(bf16_hi(w.z))),
-                       fmaxf(fabsf(bf16_lo(w.w)), fabsf(bf16_hi(w.w)))));
+  for (int64_t base = 0; base < C; base += 256 * 8) {
+    uint4 w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int64_t c = base + i * 256 + lane * 8;
+      w[i] = c < C ? ld_nc(xr + c) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a = fmaxf(a, amax8(w[i]));
   }
   return warp_max(a);
 }
@@ -71,36 +88,67 @@ __device__ __forceinline__ int64_t sf_word(int64_t sr, int64_t k4, int64_t kt) {
   return ((sr >> 7) * kt + k4) * 512 + (sr & 31) * 16 + ((sr >> 5) & 3) * 4;
 }
 
-// scope: 0 token, 1 group, 2 tensor.  grouped: scale layout padded per group.
-template <int kScope, bool kGrouped>
+// Encodes one 256-element chunk (8 elements per lane) starting at column
+// `base`: packed nibbles to qr, the chunk's 16 block scales to the tile.
+__device__ __forceinline__ void encode_chunk(const uint4& w, int64_t base, int64_t C, int lane, float senc,
+                                             uint8_t* __restrict__ qr, uint8_t* __restrict__ sblk,
+                                             int64_t sr, int64_t kt) {
+  const int64_t c = base + lane * 8;
+  const bool valid = c < C;
+  float v[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+  float bmax = amax8(w);
+  bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 1));   // lane pair = one 16-block
+  const float t = __fmul_rn(__fdiv_rn(bmax, 6.0f), senc);
+  const uint32_t sb = cvt_e4m3x2(t, 0.0f) & 0xFFu;
+  float r = 0.f;
+  if (sb != 0) r = fminf(__fdiv_rn(senc, e4m3_to_f32(sb)), FLT_MAX);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(v[i], r);
+  const uint32_t packed = cvt_e2m1x8(v);
+  if (valid) *reinterpret_cast<uint32_t*>(qr + c / 2) = packed;
+  const int l0 = lane & ~7;                    // gather the 8-lane group's 4 scales
+  const uint32_t s0 = __shfl_sync(0xffffffffu, sb, l0);
+  const uint32_t s1 = __shfl_sync(0xffffffffu, sb, l0 + 2);
+  const uint32_t s2 = __shfl_sync(0xffffffffu, sb, l0 + 4);
+  const uint32_t s3 = __shfl_sync(0xffffffffu, sb, l0 + 6);
+  const int64_t k4 = (base >> 6) + (lane >> 3);
+  if ((lane & 7) == 0 && k4 < kt)
+    *reinterpret_cast<uint32_t*>(sblk + sf_word(sr, k4, kt)) = s0 | (s1 << 8) | (s2 << 16) | (s3 << 24);
+}
+
+// scope: 0 token, 1 group, 2 tensor.  kCh: 256-element chunks held in
+// registers (0 = stream the row twice).
+template <int kCh>
 __global__ void __launch_bounds__(kThreads) nvfp4_quant_kernel(
-    const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ld,
-    const int64_t* __restrict__ offs, int G, int64_t tp_bound, uint8_t* __restrict__ q,
-    uint8_t* __restrict__ sblk, float* __restrict__ s32, const float* __restrict__ amax_ws) {
+    const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ld, int scope,
+    const int64_t* __restrict__ offs, int G, uint8_t* __restrict__ q, uint8_t* __restrict__ sblk,
+    float* __restrict__ s32, const float* __restrict__ amax_ws) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   GroupSmem& gs = *reinterpret_cast<GroupSmem*>(smem_raw);
+  const bool grouped = offs != nullptr;
   int64_t TP;
-  if (kGrouped) {
+  if (grouped) {
     load_group_prefix(gs, offs, G);
     TP = gs.pref[G];
   } else {
     TP = (R + 127) / 128 * 128;
   }
-  (void)tp_bound;
-  if (kScope != 0 && blockIdx.x == 0) {
-    const int ng = (kScope == 1) ? G : 1;
+  if (scope != 0 && blockIdx.x == 0) {
+    const int ng = (scope == 1) ? G : 1;
     for (int g = threadIdx.x; g < ng; g += blockDim.x) s32[g] = __fdiv_rn(amax_ws[g], 2688.0f);
   }
 
   const int lane = threadIdx.x & 31;
   const int64_t kt = (C / 16 + 3) / 4;           // scale-tile columns (4 scales each)
+  const int nch = static_cast<int>((C + 255) / 256);
   const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
 
   for (int64_t sr = warp0; sr < TP; sr += nwarps) {
     int64_t row;
     int g = 0;
-    if (kGrouped) {
+    if (grouped) {
       g = upper_group(gs.pref, G, sr);
       const int64_t local = sr - gs.pref[g];
       row = (local < gs.offs[g + 1] - gs.offs[g]) ? gs.offs[g] + local : -1;
@@ -113,66 +161,84 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quant_kernel(
       continue;
     }
     const uint16_t* xr = x + row * ld;
-    float amax;
-    if (kScope == 0) amax = row_amax(xr, C, lane);
-    else amax = amax_ws[kScope == 1 ? g : 0];
-    float senc, sdec;
-    nvfp4_scales(amax, senc, sdec);
-    if (kScope == 0 && lane == 0) s32[row] = sdec;
-
     uint8_t* qr = q + row * (C / 2);
-    for (int64_t base = 0; base < C; base += 256) {
-      const int64_t c = base + lane * 8;
-      const bool valid = c < C;
-      uint4 w = make_uint4(0, 0, 0, 0);
-      if (valid) w = *reinterpret_cast<const uint4*>(xr + c);
-      float v[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
-                    bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
-      float bmax = 0.f;
+    if (kCh > 0) {
+      uint4 w[kCh > 0 ? kCh : 1];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
-      bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 1));   // lane pair = block
-      const float t = __fmul_rn(__fdiv_rn(bmax, 6.0f), senc);
-      const uint32_t sb = cvt_e4m3x2(t, 0.0f) & 0xFFu;
-      float r = 0.f;
-      if (sb != 0) r = fminf(__fdiv_rn(senc, e4m3_to_f32(sb)), FLT_MAX);
+      for (int i = 0; i < kCh; ++i) {
+        const int64_t c = static_cast<int64_t>(i) * 256 + lane * 8;
+        w[i] = (i < nch && c < C) ? ld_nc(xr + c) : make_uint4(0, 0, 0, 0);
+      }
+      float amax;
+      if (scope == 0) {
+        float a = 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(v[i], r);
-      const uint32_t packed = cvt_e2m1x8(v);
-      if (valid) *reinterpret_cast<uint32_t*>(qr + c / 2) = packed;
-
-      // gather the 4 block scales of this lane's 8-lane group
-      const int l0 = lane & ~7;
-      const uint32_t s0 = __shfl_sync(0xffffffffu, sb, l0);
-      const uint32_t s1 = __shfl_sync(0xffffffffu, sb, l0 + 2);
-      const uint32_t s2 = __shfl_sync(0xffffffffu, sb, l0 + 4);
-      const uint32_t s3 = __shfl_sync(0xffffffffu, sb, l0 + 6);
-      const int64_t k4 = (base >> 6) + (lane >> 3);
-      if ((lane & 7) == 0 && k4 < kt)
-        *reinterpret_cast<uint32_t*>(sblk + sf_word(sr, k4, kt)) = s0 | (s1 << 8) | (s2 << 16) | (s3 << 24);
+        for (int i = 0; i < kCh; ++i) a = fmaxf(a, amax8(w[i]));
+        amax = warp_max(a);
+      } else {
+        amax = amax_ws[scope == 1 ? g : 0];
+      }
+      float senc, sdec;
+      nvfp4_scales(amax, senc, sdec);
+      if (scope == 0 && lane == 0) s32[row] = sdec;
+#pragma unroll
+      for (int i = 0; i < kCh; ++i)
+        if (i < nch) encode_chunk(w[i], static_cast<int64_t>(i) * 256, C, lane, senc, qr, sblk, sr, kt);
+    } else {
+      const float amax = scope == 0 ? row_amax_stream(xr, C, lane) : amax_ws[scope == 1 ? g : 0];
+      float senc, sdec;
+      nvfp4_scales(amax, senc, sdec);
+      if (scope == 0 && lane == 0) s32[row] = sdec;
+      for (int64_t base = 0; base < C; base += 256) {
+        const int64_t c = base + lane * 8;
+        const uint4 w = c < C ? ld_nc(xr + c) : make_uint4(0, 0, 0, 0);
+        encode_chunk(w, base, C, lane, senc, qr, sblk, sr, kt);
+      }
     }
   }
 }
 
-// Per-row amax folded into the scope amax (group or tensor) with atomicMax on
-// the bit pattern (non-negative floats order like their bits).
-template <bool kGroupScope>
+// Scope amax (group or tensor): each warp owns a contiguous range of rows,
+// keeps a running maximum while the group stays the same and folds it into
+// the group's word with one atomicMax on the bit pattern (non-negative floats
+// order like their bits) when the group changes or the range ends -- a few
+// atomics per warp instead of one per row on a handful of addresses.
 __global__ void __launch_bounds__(kThreads) nvfp4_amax_kernel(
     const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ld,
-    const int64_t* __restrict__ offs, int G, float* __restrict__ amax_ws) {
+    const int64_t* __restrict__ offs, int G, bool group_scope, float* __restrict__ amax_ws) {
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
-  for (int64_t row = warp0; row < R; row += nwarps) {
-    const float a = row_amax(x + row * ld, C, lane);
-    if (lane == 0) {
-      int g = 0;
-      if (kGroupScope) {
-        g = upper_group(offs, G, row);        // group with offs[g] <= row < offs[g+1]
-      }
-      atomicMax(reinterpret_cast<unsigned int*>(amax_ws + g), __float_as_uint(a));
+  const int64_t per = (R + nwarps - 1) / nwarps;
+  const int64_t r0 = warp0 * per;
+  const int64_t r1 = r0 + per < R ? r0 + per : R;
+  if (r0 >= r1) return;
+  int g = group_scope ? upper_group(offs, G, r0) : 0;      // offs[g] <= r0 < offs[g+1]
+  int64_t gend = group_scope ? offs[g + 1] : R;
+  float run = 0.f;
+  for (int64_t row = r0; row < r1; ++row) {
+    if (row >= gend) {                                      // entering the next group
+      if (lane == 0) atomicMax(reinterpret_cast<unsigned int*>(amax_ws + g), __float_as_uint(run));
+      run = 0.f;
+      g = upper_group(offs, G, row);
+      gend = offs[g + 1];
     }
+    run = fmaxf(run, row_amax_stream(x + row * ld, C, lane));
   }
+  if (lane == 0) atomicMax(reinterpret_cast<unsigned int*>(amax_ws + g), __float_as_uint(run));
+}
+
+template <int kCh>
+cudaError_t launch_quant(unsigned grid, size_t smem, cudaStream_t stream, const uint16_t* x, int64_t R,
+                         int64_t C, int64_t ld, int scope, const int64_t* offs, int G, uint8_t* q,
+                         uint8_t* sblk, float* s32, const float* amax_ws) {
+  auto k = nvfp4_quant_kernel<kCh>;
+  if (smem > 0) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  k<<<grid, kThreads, smem, stream>>>(x, R, C, ld, scope, offs, G, q, sblk, s32, amax_ws);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -188,8 +254,7 @@ cudaError_t launch_nvfp4_quant(const uint16_t* x, int64_t R, int64_t C, int64_t 
       const int64_t want = (R + kWarps - 1) / kWarps;
       const int64_t cap = static_cast<int64_t>(sm_count) * 8;
       const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
-      if (scope == 1) nvfp4_amax_kernel<true><<<grid, kThreads, 0, stream>>>(x, R, C, ld, offs, G, amax_ws);
-      else nvfp4_amax_kernel<false><<<grid, kThreads, 0, stream>>>(x, R, C, ld, offs, G, amax_ws);
+      nvfp4_amax_kernel<<<grid, kThreads, 0, stream>>>(x, R, C, ld, offs, G, scope == 1, amax_ws);
       e = cudaGetLastError();
       if (e != cudaSuccess) return e;
     }
@@ -201,26 +266,11 @@ cudaError_t launch_nvfp4_quant(const uint16_t* x, int64_t R, int64_t C, int64_t 
   unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
   if (grid == 0) grid = 1;
   const size_t smem = grouped ? sizeof(GroupSmem) : 0;
-#define MX8Q_NV_LAUNCH(S, GRP)                                                                 \
-  do {                                                                                          \
-    auto k = nvfp4_quant_kernel<S, GRP>;                                                       \
-    if (smem > 0) {                                                                             \
-      cudaError_t ea = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,    \
-                                            static_cast<int>(smem));                          \
-      if (ea != cudaSuccess) return ea;                                                         \
-    }                                                                                           \
-    k<<<grid, kThreads, smem, stream>>>(x, R, C, ld, offs, G, tp_bound, q, sblk, s32, amax_ws); \
-  } while (0)
-  if (grouped) {
-    if (scope == 0) MX8Q_NV_LAUNCH(0, true);
-    else if (scope == 1) MX8Q_NV_LAUNCH(1, true);
-    else MX8Q_NV_LAUNCH(2, true);
-  } else {
-    if (scope == 0) MX8Q_NV_LAUNCH(0, false);
-    else MX8Q_NV_LAUNCH(2, false);
-  }
-#undef MX8Q_NV_LAUNCH
-  return cudaGetLastError();
+  if (C <= 1024) return launch_quant<4>(grid, smem, stream, x, R, C, ld, scope, offs, G, q, sblk, s32, amax_ws);
+  if (C <= 2048) return launch_quant<8>(grid, smem, stream, x, R, C, ld, scope, offs, G, q, sblk, s32, amax_ws);
+  if (C <= 4096) return launch_quant<16>(grid, smem, stream, x, R, C, ld, scope, offs, G, q, sblk, s32, amax_ws);
+  if (C <= 8192) return launch_quant<32>(grid, smem, stream, x, R, C, ld, scope, offs, G, q, sblk, s32, amax_ws);
+  return launch_quant<0>(grid, smem, stream, x, R, C, ld, scope, offs, G, q, sblk, s32, amax_ws);
 }
 
 }  // namespace mx8q

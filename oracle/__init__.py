@@ -81,6 +81,7 @@ def _L():
         lib.or_grouped_gemm_ref.argtypes = [ctypes.c_int, ctypes.c_int, _p, _i64, _i64,
                                             _p, _p, _p, _p, _p, _p,
                                             _p, _i64, _p, _p, _p]
+        lib.or_swiglu.argtypes = [_p, _i64, _i64, _p]
         _lib = lib
     return _lib
 
@@ -283,3 +284,13 @@ def grouped_gemm_ref(fmt, offs, A, SA, B, SB, K, a32=None, b32=None, pairs=None)
                              _ptr(B), _ptr(SB), _ptr(b), _ptr(pr), pr.shape[0],
                              _ptr(ref), _ptr(absref), _ptr(scratch))
     return ref, absref
+
+
+# ----------------------------------------------------------------- SwiGLU
+def swiglu(gu_bits):
+    """h = RN_bf16(silu(g) * u) for a bf16 [R, 2F] gate|up matrix (bit patterns)."""
+    gu = _c(gu_bits, np.uint16)
+    R, F2 = gu.shape
+    h = np.empty((R, F2 // 2), np.uint16)
+    _L().or_swiglu(_ptr(gu), R, F2 // 2, _ptr(h))
+    return h

@@ -495,3 +495,21 @@ void or_grouped_gemm_ref(int fmt, int G, const i64 *offs, i64 N, i64 K,
         absref[p] = aacc;
     }
 }
+
+/* ------------------------------------------------------------------ */
+/* SwiGLU between the MoE gate|up and down GEMMs                        */
+/* ------------------------------------------------------------------ */
+
+/* h[r, j] = RN_bf16( silu(g) * u ), silu(g) = g / (1 + e^-g), evaluated in
+ * double ("Un Cuantizador Compartido Es el Mecanismo Real": gate and up of a
+ * SwiGLU expert are one fused GEMM output).  gu: bf16 [R, 2F]; h: bf16 [R, F]. */
+void or_swiglu(const uint16_t *gu, i64 R, i64 F, uint16_t *h)
+{
+    for (i64 r = 0; r < R; r++)
+        for (i64 j = 0; j < F; j++) {
+            double g = (double)or_bf16_to_f32(gu[r * 2 * F + j]);
+            double u = (double)or_bf16_to_f32(gu[r * 2 * F + F + j]);
+            double v = g / (1.0 + exp(-g)) * u;
+            h[r * F + j] = or_f32_to_bf16((float)v);
+        }
+}

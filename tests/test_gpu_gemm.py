@@ -25,8 +25,9 @@ def _mx8_operand(xb):
     return q, s
 
 
-def _check(y, ref, absref, bf16=False):
-    ok, bad = gemm_tolerance_ok(y, ref, absref, bf16)
+def _check(y, ref, absref, bf16=False, K=None):
+    assert K is not None
+    ok, bad = gemm_tolerance_ok(y, ref, absref, bf16, K)
     if not ok:
         yf = np.asarray(y, np.float64).ravel()
         i = bad[:5]
@@ -50,7 +51,7 @@ def test_mxfp8_one_nonzero():
     y = host(_run_mx8(A, SA, B, SB, K))
     ref, absref = oracle.gemm_ref(0, A, SA, B, SB, K)
     assert np.count_nonzero(ref) == 1
-    _check(y, ref, absref)
+    _check(y, ref, absref, K=K)
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 512), (200, 72, 96), (1, 8, 32), (257, 384, 1056),
@@ -63,9 +64,9 @@ def test_mxfp8_gemm_shapes(M, N, K):
     B, SB = _mx8_operand(xb)
     y = host(_run_mx8(A, SA, B, SB, K))
     ref, absref = oracle.gemm_ref(0, A, SA, B, SB, K)
-    _check(y, ref, absref)
+    _check(y, ref, absref, K=K)
     yb = host(_run_mx8(A, SA, B, SB, K, torch.bfloat16))
-    _check(oracle.bf16_to_f32(yb), ref, absref, bf16=True)
+    _check(oracle.bf16_to_f32(yb), ref, absref, bf16=True, K=K)
     del rng
 
 
@@ -75,7 +76,7 @@ def test_mxfp8_pr1_fprop():
     B, SB = _mx8_operand(inputs.bits(d["W"]))
     y = host(_run_mx8(A, SA, B, SB, 512))
     ref, absref = oracle.gemm_ref(0, A, SA, B, SB, 512)
-    _check(y, ref, absref)
+    _check(y, ref, absref, K=512)
 
 
 def _sample_pairs(M, N, n, seed):
@@ -107,7 +108,7 @@ def test_mxfp8_linear_fprop_dgrad_wgrad_full_size():
         y = host(_run_mx8(A, SA, B, SB, K))
         pairs = _sample_pairs(A.shape[0], B.shape[0], 3000, 100 + seed)
         ref, absref = oracle.gemm_ref(0, A, SA, B, SB, K, pairs=pairs)
-        _check(y[pairs[:, 0], pairs[:, 1]], ref, absref)
+        _check(y[pairs[:, 0], pairs[:, 1]], ref, absref, K=K)
 
 
 # ------------------------------------------------------------------ NVFP4
@@ -128,7 +129,7 @@ def test_nvfp4_one_nonzero():
                         dev(oracle.swizzle_scales(SB)), K, dev(a32), dev(b32)))
     ref, absref = oracle.gemm_ref(1, A, SA, B, SB, K, a32, b32)
     assert np.count_nonzero(ref) == 1
-    _check(y, ref, absref)
+    _check(y, ref, absref, K=K)
 
 
 def test_nvfp4_pr1_per_token_x_per_tensor_w():
@@ -138,7 +139,7 @@ def test_nvfp4_pr1_per_token_x_per_tensor_w():
     y = host(mx.bs_gemm(mx.FMT_NVFP4, dev(A), dev(oracle.swizzle_scales(SA)), dev(B),
                         dev(oracle.swizzle_scales(SB)), 512, dev(a32), dev(b32)))
     ref, absref = oracle.gemm_ref(1, A, SA, B, SB, 512, a32, b32)
-    _check(y, ref, absref)
+    _check(y, ref, absref, K=512)
 
 
 @pytest.mark.parametrize("M,N,K", [(200, 136, 96), (128, 256, 1024), (3, 8, 32), (130, 128, 544)])
@@ -150,7 +151,7 @@ def test_nvfp4_gemm_shapes_per_row_scales(M, N, K):
     y = host(mx.bs_gemm(mx.FMT_NVFP4, dev(A), dev(oracle.swizzle_scales(SA)), dev(B),
                         dev(oracle.swizzle_scales(SB)), K, dev(a32), dev(b32)))
     ref, absref = oracle.gemm_ref(1, A, SA, B, SB, K, a32, b32)
-    _check(y, ref, absref)
+    _check(y, ref, absref, K=K)
 
 
 # ------------------------------------------------------------------ grouped
@@ -177,7 +178,7 @@ def test_nvfp4_grouped_small(T, H, E, N, topk, zipf):
     rows = A.shape[0]
     pairs = np.array([(m, n) for m in range(rows) for n in range(N)])
     ref, absref = oracle.grouped_gemm_ref(1, offs, A, SA, B, SB, H, a32, b32, pairs)
-    _check(y.ravel(), ref, absref)
+    _check(y.ravel(), ref, absref, K=H)
 
 
 def test_nvfp4_grouped_empty_and_single_row_groups():
@@ -195,7 +196,7 @@ def test_nvfp4_grouped_empty_and_single_row_groups():
                                 out_dtype=torch.float32))
     pairs = np.array([(m, n) for m in range(260) for n in range(N)])
     ref, absref = oracle.grouped_gemm_ref(1, offs, A, SA, B, SB, H, a32, b32, pairs)
-    _check(y.ravel(), ref, absref)
+    _check(y.ravel(), ref, absref, K=H)
     del rng
 
 
@@ -210,4 +211,4 @@ def test_nvfp4_grouped_qwen_gate_up_sampled():
                                 out_dtype=torch.bfloat16))
     pairs = _sample_pairs(A.shape[0], N, 3000, 7)
     ref, absref = oracle.grouped_gemm_ref(1, offs, A, SA, B, SB, H, a32, b32, pairs)
-    _check(oracle.bf16_to_f32(y[pairs[:, 0], pairs[:, 1]]), ref, absref, bf16=True)
+    _check(oracle.bf16_to_f32(y[pairs[:, 0], pairs[:, 1]]), ref, absref, bf16=True, K=H)

@@ -111,7 +111,7 @@ def test_nvfp4_pr1():
     _nv_check(inputs.bits(d["W"]), mx.SCOPE_TENSOR)
 
 
-@pytest.mark.parametrize("shape", [(5, 16), (7, 48), (130, 80), (64, 208), (300, 768), (33, 7168)])
+@pytest.mark.parametrize("shape", [(5, 16), (7, 48), (130, 80), (64, 208), (300, 768), (9, 4096), (33, 7168), (5, 8448)])
 def test_nvfp4_ragged(shape):
     rows, cols = shape
     wide = inputs.sweep(rows, (cols + 31) // 32 * 32, seed=rows)
@@ -213,3 +213,24 @@ def test_bounded_wait_times_out_and_reports():
     oq, _ = oracle.mxfp8_quantize_rowwise(host(x))
     assert np.array_equal(host(q), oq)
     assert mx.check_device_error(ws) == mx.OK
+
+
+# ------------------------------------------------------------------ SwiGLU
+def _bf16_ulps(a, b):
+    def ordered(x):
+        x = x.astype(np.int64)
+        return np.where(x & 0x8000, -(x & 0x7FFF), x)
+    return np.abs(ordered(a) - ordered(b))
+
+
+def test_swiglu_within_one_bf16_unit_of_oracle():
+    """silu uses CUDA's expf in FP32; the oracle evaluates in double.  Both
+    round to bf16 once, so results agree to one bf16 unit and almost always
+    exactly."""
+    g = torch.Generator().manual_seed(5)
+    gu = inputs.bits(inputs.normal_bf16((512, 2 * 768), 2.0, g, "cpu", 0.01, 20.0))
+    got = host(mx.swiglu(dev(gu)))
+    ref = oracle.swiglu(gu)
+    ulps = _bf16_ulps(got, ref)
+    assert ulps.max() <= 1
+    assert (ulps == 0).mean() >= 0.999
