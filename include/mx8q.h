@@ -151,6 +151,24 @@ mx8_status nvfp4_quantize_per_token(const void *x, int64_t rows, int64_t cols, i
                                     mx8_stream_t stream);
 
 /*
+ * nvfp4_quantize_per_token() for callers that cannot allocate device memory
+ * and so cannot provide a workspace (for instance a plugin whose host
+ * application owns every allocation).  Same arguments and results, minus the
+ * workspace: the per-group / per-tensor amax scratch is a fixed 4 KB array
+ * inside the library (at most 1024 groups; more return MX8_ERR_INVALID_ARG),
+ * resident on each GPU that loads the library until the process exits.
+ * No allocation of any kind happens in this call.  The first call on a device
+ * looks up that array's device address; make it before any stream capture.
+ * All calls share the array (cleared at the start of each call), so calls
+ * that could run at the same time on the GPU race and must be serialised.
+ * The pages describe no such variant; it exists for this library's callers.
+ */
+mx8_status nvfp4_quantize_per_token_noalloc(const void *x, int64_t rows, int64_t cols, int64_t ld,
+                                            int scope, const int64_t *group_offsets, int num_groups,
+                                            uint8_t *q, uint8_t *s_blk, float *s32,
+                                            mx8_stream_t stream);
+
+/*
  * Dequantization back to f32 or bf16 (the dequantized-backward mode of [MRL]
  * "La Compatibilidad..." and [REC]: rebuild high-precision operands from the
  * exact low-precision forward values).

@@ -28,7 +28,8 @@ S32_NONE, S32_ROW, S32_TENSOR, S32_GROUP = 0, 1, 2, 3
 
 # every C symbol the header declares
 EXPORTS = ("mx8_scale_bytes", "mx8_scale_bytes_grouped", "mx8_workspace_bytes",
-           "mx8_device_sm_count", "mx8_quantize", "nvfp4_quantize_per_token", "dequantize",
+           "mx8_device_sm_count", "mx8_quantize", "nvfp4_quantize_per_token",
+           "nvfp4_quantize_per_token_noalloc", "dequantize",
            "bs_gemm", "bs_grouped_gemm", "mx8_swiglu", "mx8_check_device_error", "mx8_selftest_bounded_wait",
            "mx8_status_string")
 
@@ -67,6 +68,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mx8_quantize.argtypes = [_p, _i64, _i64, _i64, _i, _p, _p, _p, _p, _p, _sz, _p]
     lib.nvfp4_quantize_per_token.restype = _i
     lib.nvfp4_quantize_per_token.argtypes = [_p, _i64, _i64, _i64, _i, _p, _i, _p, _p, _p, _p, _sz, _p]
+    lib.nvfp4_quantize_per_token_noalloc.restype = _i
+    lib.nvfp4_quantize_per_token_noalloc.argtypes = [_p, _i64, _i64, _i64, _i, _p, _i, _p, _p, _p, _p]
     lib.dequantize.restype = _i
     lib.dequantize.argtypes = [_i, _p, _p, _p, _i, _p, _i, _i64, _i64, _i, _p, _p]
     lib.bs_gemm.restype = _i

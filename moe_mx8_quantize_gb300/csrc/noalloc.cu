@@ -1,0 +1,81 @@
+// Allocation-free variant of the NVFP4 quantizer entry point.
+//
+// Some callers cannot allocate device memory at all: code that runs inside a
+// host that owns every allocation (a plugin or a serving runtime with its own
+// arena), or code called where an allocation would be unsafe or forbidden.
+// They cannot pass the workspace that nvfp4_quantize_per_token() needs for the
+// per-group / per-tensor amax of its first pass.  This entry point instead
+// keeps that scratch in a fixed array inside the library itself.
+//
+// The array lives in device memory for as long as the library is loaded, on
+// every GPU that loads it: kNoAllocMaxGroups FP32 words (4 KB).  Its device
+// address is looked up once per device, on the first call made with that
+// device current; make that first call before capturing any stream.  Every
+// call shares the one array: the amax words are cleared at the start of each
+// call, and calls that overlap on the GPU (different streams, or different
+// host threads without ordering) race on it and must be serialised.
+#include <mutex>
+
+#include "../../include/mx8q.h"
+#include "kernels.h"
+
+namespace {
+
+constexpr int kNoAllocMaxGroups = 1024;   // FP32 amax words held by the library
+
+static __device__ __align__(256) float g_noalloc_amax[kNoAllocMaxGroups];
+
+std::mutex g_lock;
+float* g_amax_addr[64] = {nullptr};       // device address of the array, per device
+
+// Device address of the array on the current device (looked up once).
+cudaError_t scratch_address(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> guard(g_lock);
+  if (g_amax_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_amax);
+    if (e != cudaSuccess) return e;
+    g_amax_addr[dev] = static_cast<float*>(p);
+  }
+  *out = g_amax_addr[dev];
+  return cudaSuccess;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+}  // namespace
+
+extern "C" mx8_status nvfp4_quantize_per_token_noalloc(const void* x, int64_t rows, int64_t cols,
+                                                       int64_t ld, int scope,
+                                                       const int64_t* group_offsets, int num_groups,
+                                                       uint8_t* q, uint8_t* s_blk, float* s32,
+                                                       mx8_stream_t stream) {
+  if (scope < NVFP4_SCOPE_TOKEN || scope > NVFP4_SCOPE_TENSOR) return MX8_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0 || ld < cols || cols % 16 != 0) return MX8_ERR_INVALID_ARG;
+  if (scope == NVFP4_SCOPE_GROUP && group_offsets == nullptr) return MX8_ERR_INVALID_ARG;
+  // the library's scratch holds kNoAllocMaxGroups amax words: more groups are refused
+  if (group_offsets != nullptr && (num_groups < 1 || num_groups > kNoAllocMaxGroups))
+    return MX8_ERR_INVALID_ARG;
+  const int G = group_offsets ? num_groups : 1;
+  if (cols == 0) return MX8_OK;
+  if (rows > 0 && (x == nullptr || q == nullptr)) return MX8_ERR_INVALID_ARG;
+  if (s_blk == nullptr || s32 == nullptr) return MX8_ERR_INVALID_ARG;
+  auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+  if ((rows > 0 && (misaligned(x) || misaligned(q))) || misaligned(s_blk) || ld % 8 != 0)
+    return MX8_ERR_ALIGNMENT;
+  float* amax = nullptr;
+  if (scratch_address(&amax) != cudaSuccess) return MX8_ERR_CUDA;
+  const cudaError_t e = mx8q::launch_nvfp4_quant(static_cast<const uint16_t*>(x), rows, cols, ld, scope,
+                                                 group_offsets, G, q, s_blk, s32, amax, sm_count(),
+                                                 reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MX8_OK : MX8_ERR_CUDA;
+}
