@@ -154,7 +154,7 @@ mx8_status nvfp4_quantize_per_token(const void *x, int64_t rows, int64_t cols, i
  * nvfp4_quantize_per_token() for callers that cannot allocate device memory
  * and so cannot provide a workspace (for instance a plugin whose host
  * application owns every allocation).  Same arguments and results, minus the
- * workspace: the per-group / per-tensor amax scratch is a fixed 4 KB array
+ * workspace: the per-group / per-tensor scratch is a fixed ~8 KB array
  * inside the library (at most 1024 groups; more return MX8_ERR_INVALID_ARG),
  * resident on each GPU that loads the library until the process exits.
  * No allocation of any kind happens in this call.  The first call on a device

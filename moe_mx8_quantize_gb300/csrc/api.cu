@@ -90,7 +90,7 @@ extern "C" size_t mx8_scale_bytes_grouped(int fmt, int64_t total_rows, int num_g
 
 extern "C" size_t mx8_workspace_bytes(int num_groups) {
   const int64_t g = num_groups > 1 ? num_groups : 1;
-  return kErrWordBytes + static_cast<size_t>(cdiv(g * 4, 256) * 256);
+  return kErrWordBytes + static_cast<size_t>(cdiv(static_cast<int64_t>(nvfp4_scratch_bytes(static_cast<int>(g))), 256) * 256);
 }
 
 extern "C" int mx8_device_sm_count(void) { return sm_count_current(); }
@@ -157,10 +157,10 @@ extern "C" mx8_status nvfp4_quantize_per_token(const void* x, int64_t rows, int6
     return MX8_ERR_ALIGNMENT;
   mx8_status st = check_ws(workspace, workspace_bytes, G);
   if (st != MX8_OK) return st;
-  float* amax_ws = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kErrWordBytes);
+  void* scratch = static_cast<uint8_t*>(workspace) + kErrWordBytes;
   return from_cuda(launch_nvfp4_quant(static_cast<const uint16_t*>(x), rows, cols, ld, scope,
-                                      group_offsets, G, q, s_blk, s32, amax_ws, sm_count_current(),
-                                      reinterpret_cast<cudaStream_t>(stream)));
+                                      group_offsets, G, q, s_blk, s32, scratch, err_word(workspace),
+                                      sm_count_current(), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 // ===================================================================== dequantize

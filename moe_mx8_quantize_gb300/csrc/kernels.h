@@ -15,9 +15,13 @@ cudaError_t launch_mxfp8_quant(const CUtensorMap& tmap_x, int64_t R, int64_t C, 
                                uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
                                int* err, int sm_count, cudaStream_t stream);
 
+// Scratch bytes of the group / tensor scope path (amax, done counts, ticket).
+size_t nvfp4_scratch_bytes(int groups);
+// scratch: nvfp4_scratch_bytes(groups) bytes, 16-byte aligned (zeroed here on
+// the stream); err: the error word a timed-out wait writes.
 cudaError_t launch_nvfp4_quant(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int scope,
                                const int64_t* offs, int G, uint8_t* q, uint8_t* sblk, float* s32,
-                               float* amax_ws, int sm_count, cudaStream_t stream);
+                               void* scratch, int* err, int sm_count, cudaStream_t stream);
 
 cudaError_t launch_dequant(int fmt, const uint8_t* q, const uint8_t* s, const float* s32,
                            int s32_mode, const int64_t* offs, int G, int64_t R, int64_t C,

@@ -8,12 +8,13 @@
 // keeps that scratch in a fixed array inside the library itself.
 //
 // The array lives in device memory for as long as the library is loaded, on
-// every GPU that loads it: kNoAllocMaxGroups FP32 words (4 KB).  Its device
+// every GPU that loads it: two words per group for up to kNoAllocMaxGroups
+// groups plus a counter and an error word (about 8 KB).  Its device
 // address is looked up once per device, on the first call made with that
 // device current; make that first call before capturing any stream.  Every
-// call shares the one array: the amax words are cleared at the start of each
-// call, and calls that overlap on the GPU (different streams, or different
-// host threads without ordering) race on it and must be serialised.
+// call shares the one array: its words are cleared at the start of each call,
+// and calls that overlap on the GPU (different streams, or different host
+// threads without ordering) race on it and must be serialised.
 #include <mutex>
 
 #include "../../include/mx8q.h"
@@ -21,27 +22,28 @@
 
 namespace {
 
-constexpr int kNoAllocMaxGroups = 1024;   // FP32 amax words held by the library
+constexpr int kNoAllocMaxGroups = 1024;   // groups the library's scratch can serve
+constexpr int kNoAllocWords = 2 * kNoAllocMaxGroups + 8;   // amax, counts, ticket, error word
 
-static __device__ __align__(256) float g_noalloc_amax[kNoAllocMaxGroups];
+static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocWords];
 
 std::mutex g_lock;
-float* g_amax_addr[64] = {nullptr};       // device address of the array, per device
+uint32_t* g_scratch_addr[64] = {nullptr};   // device address of the array, per device
 
 // Device address of the array on the current device (looked up once).
-cudaError_t scratch_address(float** out) {
+cudaError_t scratch_address(uint32_t** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> guard(g_lock);
-  if (g_amax_addr[dev] == nullptr) {
+  if (g_scratch_addr[dev] == nullptr) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_amax);
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    g_amax_addr[dev] = static_cast<float*>(p);
+    g_scratch_addr[dev] = static_cast<uint32_t*>(p);
   }
-  *out = g_amax_addr[dev];
+  *out = g_scratch_addr[dev];
   return cudaSuccess;
 }
 
@@ -72,10 +74,13 @@ extern "C" mx8_status nvfp4_quantize_per_token_noalloc(const void* x, int64_t ro
   auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
   if ((rows > 0 && (misaligned(x) || misaligned(q))) || misaligned(s_blk) || ld % 8 != 0)
     return MX8_ERR_ALIGNMENT;
-  float* amax = nullptr;
-  if (scratch_address(&amax) != cudaSuccess) return MX8_ERR_CUDA;
+  uint32_t* scratch = nullptr;
+  if (scratch_address(&scratch) != cudaSuccess) return MX8_ERR_CUDA;
+  // words 0 .. 2*groups+1 are the quantizer scratch; the error word sits after them
+  static_assert(kNoAllocWords - 4 >= 2 * kNoAllocMaxGroups + 2, "scratch too small");
+  int* err = reinterpret_cast<int*>(scratch + kNoAllocWords - 4);
   const cudaError_t e = mx8q::launch_nvfp4_quant(static_cast<const uint16_t*>(x), rows, cols, ld, scope,
-                                                 group_offsets, G, q, s_blk, s32, amax, sm_count(),
+                                                 group_offsets, G, q, s_blk, s32, scratch, err, sm_count(),
                                                  reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MX8_OK : MX8_ERR_CUDA;
 }

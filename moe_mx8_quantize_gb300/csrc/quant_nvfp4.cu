@@ -10,26 +10,39 @@
 // Compartido Es el Mecanismo Real": the per-token FP32 scale is computed
 // online inside the activation quantizer, which emits packed FP4, block
 // scales and token scales in one operation; the FP4 quantizer runs without
-// approximate math.  Section "Las Curvas de Recompensa...": running the
-// per-token scale as a separate framework op is what slowed NVFP4 training.
-// "NVIDIA presenta una metodologia de preentrenamiento de 4 bits utilizando
-// NVFP4", section "Que es realmente NVFP4": E4M3 block scales under an FP32
-// scale that keeps them in range; section "La metodologia...": 1x16 blocks,
-// round-to-nearest-even.
+// approximate math; gate and up weights share one FP32 scale.  Section "Las
+// Curvas de Recompensa...": running the per-token scale as a separate
+// framework op is what slowed NVFP4 training.  "NVIDIA presenta una
+// metodologia de preentrenamiento de 4 bits utilizando NVFP4", section "Que es
+// realmente NVFP4": E4M3 block scales under an FP32 scale that keeps them in
+// range; section "La metodologia...": 1x16 blocks, round-to-nearest-even.
 //
 // Arithmetic (all FP32, one IEEE round-to-nearest step each):
 //   S_enc = min(2688 / A, FLT_MAX), S_dec = A / 2688      (A = scope amax)
 //   sb    = RNE_E4M3_sat((amax_b / 6) * S_enc)
 //   r     = sb ? min(S_enc / sb, FLT_MAX) : 0,   code = RNE_E2M1_sat(x * r)
 //
-// Design: one warp per scale row.  Lane l owns elements [256*i + 8*l, +8) of
-// the row for every 256-element chunk i, so loads and stores are fully
-// coalesced; a 16-element block is a lane pair and a 4-block scale group (one
-// aligned 32-bit word of the tensor-core tile) is 8 lanes.  Rows of up to
-// 256*kCh elements are loaded into registers with all loads issued up front
-// (many bytes in flight per warp, one HBM read per element); longer rows are
-// streamed twice (the second read comes from L1/L2).  Rows of the padded
-// scale tile that hold no token are written as zero by the same warps.
+// Layout of the work: one warp per row; lane l owns the 16-element block
+// [512*i + 16*l, +16) of every 512-element chunk i, so each lane computes its
+// block's scale once (no duplicated divisions), loads are 32 contiguous bytes
+// per lane and the 8-byte code stores of a warp are contiguous.  |x| maxima are
+// taken as unsigned maxima of the bf16 bit patterns with the sign cleared
+// (they order like the values), two per instruction.  Four lanes hold one
+// 4-scale group of the tensor-core tile and write it as one 32-bit word.
+//
+// Token scope: rows of up to 512*kCh elements are held in registers, all loads
+// issued up front, so the amax and the encode read HBM once.
+//
+// Group / tensor scope (one FP32 scale per expert weight or per tensor) needs
+// the scope amax before any element is encoded.  A single kernel takes work
+// items from an ordered ticket counter: "amax" items (32 rows: fold their
+// maximum into the group's word, then count themselves done) and "encode"
+// items (32 scale rows of the group: wait until all of the group's amax items
+// are done, then encode).  Tickets hand out the amax items of a group about
+// L2-capacity/2 bytes of input ahead of the group's encode items, so the
+// second read of a group is served from L2.  An encode item only waits on
+// items with smaller tickets, which are already held by running blocks that
+// never wait, so the order cannot deadlock; the wait is bounded anyway.
 #include <float.h>
 
 #include "device.cuh"
@@ -42,6 +55,8 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kItemRows = 32;                 // rows (or scale rows) per work item
+constexpr int64_t kL2LeadBytes = 32ll << 20;  // input bytes between a group's amax and encode items
 
 __device__ __forceinline__ void nvfp4_scales(float amax, float& senc, float& sdec) {
   float e = __fdiv_rn(2688.0f, amax);          // 2688 = 6 (E2M1 max) * 448 (E4M3 max)
@@ -50,80 +65,172 @@ __device__ __forceinline__ void nvfp4_scales(float amax, float& senc, float& sde
   sdec = __fdiv_rn(amax, 2688.0f);
 }
 
+__device__ __forceinline__ uint32_t umax2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Packed |x| maxima of 16 bf16 values (two u16 halves).
+__device__ __forceinline__ uint32_t absmax16(const uint4& a, const uint4& b) {
+  const uint32_t m = 0x7FFF7FFFu;
+  return umax2(umax2(umax2(a.x & m, a.y & m), umax2(a.z & m, a.w & m)),
+               umax2(umax2(b.x & m, b.y & m), umax2(b.z & m, b.w & m)));
+}
+
+__device__ __forceinline__ float halves_max(uint32_t w) { return fmaxf(bf16_lo(w), bf16_hi(w)); }
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int d = 16; d >= 1; d >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, d));
   return v;
 }
 
-__device__ __forceinline__ float amax8(const uint4& w) {
-  return fmaxf(fmaxf(fmaxf(fabsf(bf16_lo(w.x)), fabsf(bf16_hi(w.x))),
-                     fmaxf(fabsf(bf16_lo(w.y)), fabsf(bf16_hi(w.y)))),
-               fmaxf(fmaxf(fabsf(bf16_lo(w.z)), fabsf(bf16_hi(w.z))),
-                     fmaxf(fabsf(bf16_lo(w.w)), fabsf(bf16_hi(w.w)))));
-}
-
 __device__ __forceinline__ uint4 ld_nc(const uint16_t* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
-// Streaming row amax, 8 chunks of 256 elements in flight per lane.
-__device__ __forceinline__ float row_amax_stream(const uint16_t* __restrict__ xr, int64_t C, int lane) {
-  float a = 0.f;
-  for (int64_t base = 0; base < C; base += 256 * 8) {
-    uint4 w[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int64_t c = base + i * 256 + lane * 8;
-      w[i] = c < C ? ld_nc(xr + c) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) a = fmaxf(a, amax8(w[i]));
-  }
-  return warp_max(a);
+// L2 eviction-priority policies: a first read whose data is read again soon
+// keeps its lines (evict_last); the last read of data marks them evict_first.
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint4 ld_hint(const uint16_t* p, uint64_t pol) {
+  uint4 r;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p), "l"(pol));
+  return r;
 }
 
-// Scale-tile byte offset of the 4-scale word (row sr, scale columns k4*4..+3).
+// Scale-tile byte offset of the 4-scale word (scale row sr, scale columns k4*4..+3).
 __device__ __forceinline__ int64_t sf_word(int64_t sr, int64_t k4, int64_t kt) {
   return ((sr >> 7) * kt + k4) * 512 + (sr & 31) * 16 + ((sr >> 5) & 3) * 4;
 }
 
-// Encodes one 256-element chunk (8 elements per lane) starting at column
-// `base`: packed nibbles to qr, the chunk's 16 block scales to the tile.
-__device__ __forceinline__ void encode_chunk(const uint4& w, int64_t base, int64_t C, int lane, float senc,
-                                             uint8_t* __restrict__ qr, uint8_t* __restrict__ sblk,
-                                             int64_t sr, int64_t kt) {
-  const int64_t c = base + lane * 8;
-  const bool valid = c < C;
-  float v[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
-                bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
-  float bmax = amax8(w);
-  bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 1));   // lane pair = one 16-block
+// Streaming row amax (each lane: 16 elements per 512-element chunk, 4 chunks
+// in flight); with kHint the loads carry the L2 policy `pol`.
+template <bool kHint = false>
+__device__ __forceinline__ float row_amax_stream(const uint16_t* __restrict__ xr, int64_t C, int lane,
+                                                 uint64_t pol = 0) {
+  uint32_t m = 0;
+  for (int64_t base = 0; base < C; base += 512 * 4) {
+    uint4 w[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t c = base + i * 512 + lane * 16;
+      const bool ok = c < C;
+      w[2 * i] = ok ? (kHint ? ld_hint(xr + c, pol) : ld_nc(xr + c)) : make_uint4(0, 0, 0, 0);
+      w[2 * i + 1] = ok ? (kHint ? ld_hint(xr + c + 8, pol) : ld_nc(xr + c + 8)) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m = umax2(m, absmax16(w[2 * i], w[2 * i + 1]));
+  }
+  return warp_max(halves_max(m));
+}
+
+// Encodes one 512-element chunk starting at column `base`: lane l encodes the
+// 16-element block [base + 16 l, +16) held in (a, b).
+__device__ __forceinline__ void encode_chunk(const uint4& a, const uint4& b, int64_t base, int64_t C,
+                                             int lane, float senc, uint8_t* __restrict__ qr,
+                                             uint8_t* __restrict__ sblk, int64_t sr, int64_t kt) {
+  const int64_t c = base + lane * 16;
+  const float bmax = halves_max(absmax16(a, b));
   const float t = __fmul_rn(__fdiv_rn(bmax, 6.0f), senc);
   const uint32_t sb = cvt_e4m3x2(t, 0.0f) & 0xFFu;
   float r = 0.f;
   if (sb != 0) r = fminf(__fdiv_rn(senc, e4m3_to_f32(sb)), FLT_MAX);
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  float v0[8], v1[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(v[i], r);
-  const uint32_t packed = cvt_e2m1x8(v);
-  if (valid) *reinterpret_cast<uint32_t*>(qr + c / 2) = packed;
-  const int l0 = lane & ~7;                    // gather the 8-lane group's 4 scales
-  const uint32_t s0 = __shfl_sync(0xffffffffu, sb, l0);
-  const uint32_t s1 = __shfl_sync(0xffffffffu, sb, l0 + 2);
-  const uint32_t s2 = __shfl_sync(0xffffffffu, sb, l0 + 4);
-  const uint32_t s3 = __shfl_sync(0xffffffffu, sb, l0 + 6);
-  const int64_t k4 = (base >> 6) + (lane >> 3);
-  if ((lane & 7) == 0 && k4 < kt)
-    *reinterpret_cast<uint32_t*>(sblk + sf_word(sr, k4, kt)) = s0 | (s1 << 8) | (s2 << 16) | (s3 << 24);
+  for (int i = 0; i < 4; ++i) {
+    v0[2 * i] = __fmul_rn(bf16_lo(w[i]), r);
+    v0[2 * i + 1] = __fmul_rn(bf16_hi(w[i]), r);
+    v1[2 * i] = __fmul_rn(bf16_lo(w[4 + i]), r);
+    v1[2 * i + 1] = __fmul_rn(bf16_hi(w[4 + i]), r);
+  }
+  const uint32_t p0 = cvt_e2m1x8(v0), p1 = cvt_e2m1x8(v1);
+  if (c < C) *reinterpret_cast<uint2*>(qr + c / 2) = make_uint2(p0, p1);
+  const uint32_t s1 = __shfl_down_sync(0xffffffffu, sb, 1);
+  const uint32_t s2 = __shfl_down_sync(0xffffffffu, sb, 2);
+  const uint32_t s3 = __shfl_down_sync(0xffffffffu, sb, 3);
+  const int64_t k4 = (base >> 6) + (lane >> 2);
+  if ((lane & 3) == 0 && k4 < kt)
+    *reinterpret_cast<uint32_t*>(sblk + sf_word(sr, k4, kt)) = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
 }
 
-// scope: 0 token, 1 group, 2 tensor.  kCh: 256-element chunks held in
-// registers (0 = stream the row twice).
+// Encodes data row `row` (or zeros scale row sr when row < 0) with scale S_enc;
+// for scope_token the amax and S_dec come from the row itself.
+template <int kCh, bool kHint = false>
+__device__ __forceinline__ void process_row(const uint16_t* __restrict__ x, int64_t row, int64_t C, int64_t ld,
+                                            bool scope_token, float senc_given, uint8_t* __restrict__ q,
+                                            uint8_t* __restrict__ sblk, float* __restrict__ s32, int64_t sr,
+                                            int64_t kt, int lane, uint64_t pol = 0) {
+  if (row < 0) {  // padding row of the scale tile
+    for (int64_t k4 = lane; k4 < kt; k4 += 32) *reinterpret_cast<uint32_t*>(sblk + sf_word(sr, k4, kt)) = 0u;
+    return;
+  }
+  const uint16_t* xr = x + row * ld;
+  uint8_t* qr = q + row * (C / 2);
+  if (kCh > 0) {
+    const int nch = static_cast<int>((C + 511) / 512);
+    uint4 w[2 * (kCh > 0 ? kCh : 1)];
+#pragma unroll
+    for (int i = 0; i < kCh; ++i) {
+      const int64_t c = static_cast<int64_t>(i) * 512 + lane * 16;
+      const bool ok = i < nch && c < C;
+      w[2 * i] = ok ? (kHint ? ld_hint(xr + c, pol) : ld_nc(xr + c)) : make_uint4(0, 0, 0, 0);
+      w[2 * i + 1] = ok ? (kHint ? ld_hint(xr + c + 8, pol) : ld_nc(xr + c + 8)) : make_uint4(0, 0, 0, 0);
+    }
+    float senc = senc_given;
+    if (scope_token) {
+      uint32_t m = 0;
+#pragma unroll
+      for (int i = 0; i < kCh; ++i) m = umax2(m, absmax16(w[2 * i], w[2 * i + 1]));
+      float sdec;
+      nvfp4_scales(warp_max(halves_max(m)), senc, sdec);
+      if (lane == 0) s32[row] = sdec;
+    }
+#pragma unroll
+    for (int i = 0; i < kCh; ++i)
+      if (i < nch) encode_chunk(w[2 * i], w[2 * i + 1], static_cast<int64_t>(i) * 512, C, lane, senc, qr, sblk, sr, kt);
+  } else {
+    float senc = senc_given;
+    if (scope_token) {
+      float sdec;
+      nvfp4_scales(row_amax_stream(xr, C, lane), senc, sdec);
+      if (lane == 0) s32[row] = sdec;
+    }
+    for (int64_t base = 0; base < C; base += 512) {
+      const int64_t c = base + lane * 16;
+      const bool ok = c < C;
+      const uint4 a = ok ? (kHint ? ld_hint(xr + c, pol) : ld_nc(xr + c)) : make_uint4(0, 0, 0, 0);
+      const uint4 b = ok ? (kHint ? ld_hint(xr + c + 8, pol) : ld_nc(xr + c + 8)) : make_uint4(0, 0, 0, 0);
+      encode_chunk(a, b, base, C, lane, senc, qr, sblk, sr, kt);
+    }
+  }
+}
+
+// Data row behind scale row sr (-1 for padding).
+__device__ __forceinline__ int64_t data_row(const GroupSmem& gs, bool grouped, int G, int64_t R, int64_t sr) {
+  if (!grouped) return sr < R ? sr : -1;
+  const int g = upper_group(gs.pref, G, sr);
+  const int64_t local = sr - gs.pref[g];
+  return local < gs.offs[g + 1] - gs.offs[g] ? gs.offs[g] + local : -1;
+}
+
+// ------------------------------------------------------------------ token scope
 template <int kCh>
-__global__ void __launch_bounds__(kThreads) nvfp4_quant_kernel(
-    const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ld, int scope,
-    const int64_t* __restrict__ offs, int G, uint8_t* __restrict__ q, uint8_t* __restrict__ sblk,
-    float* __restrict__ s32, const float* __restrict__ amax_ws) {
+__global__ void __launch_bounds__(kThreads) nvfp4_token_kernel(
+    const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ld, const int64_t* __restrict__ offs, int G,
+    uint8_t* __restrict__ q, uint8_t* __restrict__ sblk, float* __restrict__ s32) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   GroupSmem& gs = *reinterpret_cast<GroupSmem*>(smem_raw);
   const bool grouped = offs != nullptr;
@@ -134,130 +241,199 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quant_kernel(
   } else {
     TP = (R + 127) / 128 * 128;
   }
-  if (scope != 0 && blockIdx.x == 0) {
-    const int ng = (scope == 1) ? G : 1;
-    for (int g = threadIdx.x; g < ng; g += blockDim.x) s32[g] = __fdiv_rn(amax_ws[g], 2688.0f);
-  }
-
   const int lane = threadIdx.x & 31;
-  const int64_t kt = (C / 16 + 3) / 4;           // scale-tile columns (4 scales each)
-  const int nch = static_cast<int>((C + 255) / 256);
-  const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  const int64_t kt = (C / 16 + 3) / 4;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
-
-  for (int64_t sr = warp0; sr < TP; sr += nwarps) {
-    int64_t row;
-    int g = 0;
-    if (grouped) {
-      g = upper_group(gs.pref, G, sr);
-      const int64_t local = sr - gs.pref[g];
-      row = (local < gs.offs[g + 1] - gs.offs[g]) ? gs.offs[g] + local : -1;
-    } else {
-      row = sr < R ? sr : -1;
-    }
-    if (row < 0) {  // padding row of the scale tile
-      for (int64_t k4 = lane; k4 < kt; k4 += 32)
-        *reinterpret_cast<uint32_t*>(sblk + sf_word(sr, k4, kt)) = 0u;
-      continue;
-    }
-    const uint16_t* xr = x + row * ld;
-    uint8_t* qr = q + row * (C / 2);
-    if (kCh > 0) {
-      uint4 w[kCh > 0 ? kCh : 1];
-#pragma unroll
-      for (int i = 0; i < kCh; ++i) {
-        const int64_t c = static_cast<int64_t>(i) * 256 + lane * 8;
-        w[i] = (i < nch && c < C) ? ld_nc(xr + c) : make_uint4(0, 0, 0, 0);
-      }
-      float amax;
-      if (scope == 0) {
-        float a = 0.f;
-#pragma unroll
-        for (int i = 0; i < kCh; ++i) a = fmaxf(a, amax8(w[i]));
-        amax = warp_max(a);
-      } else {
-        amax = amax_ws[scope == 1 ? g : 0];
-      }
-      float senc, sdec;
-      nvfp4_scales(amax, senc, sdec);
-      if (scope == 0 && lane == 0) s32[row] = sdec;
-#pragma unroll
-      for (int i = 0; i < kCh; ++i)
-        if (i < nch) encode_chunk(w[i], static_cast<int64_t>(i) * 256, C, lane, senc, qr, sblk, sr, kt);
-    } else {
-      const float amax = scope == 0 ? row_amax_stream(xr, C, lane) : amax_ws[scope == 1 ? g : 0];
-      float senc, sdec;
-      nvfp4_scales(amax, senc, sdec);
-      if (scope == 0 && lane == 0) s32[row] = sdec;
-      for (int64_t base = 0; base < C; base += 256) {
-        const int64_t c = base + lane * 8;
-        const uint4 w = c < C ? ld_nc(xr + c) : make_uint4(0, 0, 0, 0);
-        encode_chunk(w, base, C, lane, senc, qr, sblk, sr, kt);
-      }
-    }
-  }
+  for (int64_t sr = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); sr < TP; sr += nwarps)
+    process_row<kCh>(x, data_row(gs, grouped, G, R, sr), C, ld, true, 0.f, q, sblk, s32, sr, kt, lane);
 }
 
-// Scope amax (group or tensor): each warp owns a contiguous range of rows,
-// keeps a running maximum while the group stays the same and folds it into
-// the group's word with one atomicMax on the bit pattern (non-negative floats
-// order like their bits) when the group changes or the range ends -- a few
-// atomics per warp instead of one per row on a handful of addresses.
-__global__ void __launch_bounds__(kThreads) nvfp4_amax_kernel(
-    const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ld,
-    const int64_t* __restrict__ offs, int G, bool group_scope, float* __restrict__ amax_ws) {
-  const int lane = threadIdx.x & 31;
-  const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
-  const int64_t per = (R + nwarps - 1) / nwarps;
-  const int64_t r0 = warp0 * per;
-  const int64_t r1 = r0 + per < R ? r0 + per : R;
-  if (r0 >= r1) return;
-  int g = group_scope ? upper_group(offs, G, r0) : 0;      // offs[g] <= r0 < offs[g+1]
-  int64_t gend = group_scope ? offs[g + 1] : R;
-  float run = 0.f;
-  for (int64_t row = r0; row < r1; ++row) {
-    if (row >= gend) {                                      // entering the next group
-      if (lane == 0) atomicMax(reinterpret_cast<unsigned int*>(amax_ws + g), __float_as_uint(run));
-      run = 0.f;
-      g = upper_group(offs, G, row);
-      gend = offs[g + 1];
+// ------------------------------------------------------------------ group / tensor scope
+// Scratch words (zeroed before launch): amax bits [Gp], done counts [Gp],
+// then a 64-bit ticket counter; Gp = scope groups rounded up to even.
+__host__ __device__ __forceinline__ int scratch_gp(int groups) { return (groups + 1) / 2 * 2; }
+
+struct ScopedSmem {
+  GroupSmem gs;                       // scale-layout groups (or one group)
+  int64_t aoffs[kMaxGroups + 1];      // scope groups: data row offsets
+  int64_t apref[kMaxGroups + 1];      // scope groups: scale-row offsets (padded)
+  int32_t seg_start[2 * kMaxGroups + 1];
+  int32_t seg_info[2 * kMaxGroups];   // (group << 1) | is_encode
+  int32_t nseg;
+  int64_t ticket;
+  float amax;
+  float red[kWarps];
+};
+
+template <int kCh>
+__global__ void __launch_bounds__(kThreads) nvfp4_scoped_kernel(
+    const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ld, int scope,
+    const int64_t* __restrict__ offs, int G, uint8_t* __restrict__ q, uint8_t* __restrict__ sblk,
+    float* __restrict__ s32, uint32_t* __restrict__ scratch, int* err) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  ScopedSmem& sm = *reinterpret_cast<ScopedSmem*>(smem_raw);
+  const bool grouped = offs != nullptr;
+  const int Gs = scope == 1 ? G : 1;                       // scope groups
+  uint32_t* amax_bits = scratch;
+  uint32_t* done = scratch + scratch_gp(Gs);
+  unsigned long long* ticket = reinterpret_cast<unsigned long long*>(scratch + 2 * scratch_gp(Gs));
+
+  if (grouped) load_group_prefix(sm.gs, offs, G);
+  __syncthreads();
+  int64_t TP = grouped ? sm.gs.pref[G] : (R + 127) / 128 * 128;
+  if (threadIdx.x == 0) {
+    // scope groups: data rows and padded scale rows
+    if (scope == 1) {
+      for (int g = 0; g <= G; ++g) { sm.aoffs[g] = sm.gs.offs[g]; sm.apref[g] = sm.gs.pref[g]; }
+    } else {
+      sm.aoffs[0] = 0; sm.aoffs[1] = R; sm.apref[0] = 0; sm.apref[1] = TP;
     }
-    run = fmaxf(run, row_amax_stream(x + row * ld, C, lane));
+    // segment order: amax(0..L-1), then encode(g), amax(g+L) for g = 0..Gs-1
+    const int64_t per_group_bytes = Gs > 0 ? (R * C * 2) / Gs : 0;
+    int lead = per_group_bytes > 0 ? static_cast<int>(kL2LeadBytes / per_group_bytes) : Gs;
+    if (lead < 1) lead = 1;
+    if (lead > Gs) lead = Gs;
+    int nseg = 0;
+    int32_t pos = 0;
+    auto push = [&](int g, int enc) {
+      const int64_t n = enc ? (sm.apref[g + 1] - sm.apref[g]) / kItemRows
+                            : (sm.aoffs[g + 1] - sm.aoffs[g] + kItemRows - 1) / kItemRows;
+      sm.seg_start[nseg] = pos;
+      sm.seg_info[nseg] = (g << 1) | enc;
+      pos += static_cast<int32_t>(n);
+      ++nseg;
+    };
+    for (int g = 0; g < lead; ++g) push(g, 0);
+    for (int g = 0; g < Gs; ++g) {
+      push(g, 1);
+      if (g + lead < Gs) push(g + lead, 0);
+    }
+    sm.seg_start[nseg] = pos;
+    sm.nseg = nseg;
   }
-  if (lane == 0) atomicMax(reinterpret_cast<unsigned int*>(amax_ws + g), __float_as_uint(run));
+  __syncthreads();
+  const int nseg = sm.nseg;
+  const int64_t total = sm.seg_start[nseg];
+  // groups with no rows still get their (zero) decode scale
+  if (blockIdx.x == 0)
+    for (int g = threadIdx.x; g < Gs; g += blockDim.x)
+      if (sm.aoffs[g + 1] == sm.aoffs[g]) s32[g] = 0.f;
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t kt = (C / 16 + 3) / 4;
+  const uint64_t keep = policy_evict_last();    // first read: to be read again
+  const uint64_t drop = policy_evict_first();   // second read: last use
+
+  while (true) {
+    __syncthreads();
+    if (threadIdx.x == 0) sm.ticket = static_cast<int64_t>(atomicAdd(ticket, 1ull));
+    __syncthreads();
+    const int64_t t = sm.ticket;
+    if (t >= total) break;
+    int lo = 0, hi = nseg - 1;                   // segment holding ticket t
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (sm.seg_start[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    const int g = sm.seg_info[lo] >> 1;
+    const bool enc = sm.seg_info[lo] & 1;
+    const int64_t item = t - sm.seg_start[lo];
+    if (!enc) {
+      // ---- amax item: rows [aoffs[g] + 32 item, +32) of scope group g
+      const int64_t r0 = sm.aoffs[g] + item * kItemRows;
+      const int64_t r1 = r0 + kItemRows < sm.aoffs[g + 1] ? r0 + kItemRows : sm.aoffs[g + 1];
+      float m = 0.f;
+      for (int64_t row = r0 + warp; row < r1; row += kWarps)
+        m = fmaxf(m, row_amax_stream<true>(x + row * ld, C, lane, keep));
+      if (lane == 0) sm.red[warp] = m;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        float bm = sm.red[0];
+        for (int i = 1; i < kWarps; ++i) bm = fmaxf(bm, sm.red[i]);
+        atomicMax(amax_bits + g, __float_as_uint(bm));
+        __threadfence();                          // the maximum is visible before the count
+        atomicAdd(done + g, 1u);
+      }
+    } else {
+      // ---- encode item: scale rows [apref[g] + 32 item, +32) of scope group g
+      if (threadIdx.x == 0) {
+        const uint32_t need = static_cast<uint32_t>((sm.aoffs[g + 1] - sm.aoffs[g] + kItemRows - 1) / kItemRows);
+        const volatile uint32_t* dv = done + g;
+        if (*dv < need) {
+          const uint64_t t0 = globaltimer();
+          while (*dv < need) {
+            if (globaltimer() - t0 > kWaitLimitNs) {
+              atomicCAS(err, 0, kErrWaitConsumer);
+              break;
+            }
+            __nanosleep(64);
+          }
+        }
+        __threadfence();
+        sm.amax = __uint_as_float(*reinterpret_cast<volatile uint32_t*>(amax_bits + g));
+      }
+      __syncthreads();
+      float senc, sdec;
+      nvfp4_scales(sm.amax, senc, sdec);
+      if (item == 0 && threadIdx.x == 0) s32[g] = sdec;
+      const int64_t s0 = sm.apref[g] + item * kItemRows;
+      for (int64_t sr = s0 + warp; sr < s0 + kItemRows; sr += kWarps)
+        process_row<kCh, true>(x, data_row(sm.gs, grouped, G, R, sr), C, ld, false, senc, q, sblk, s32, sr, kt,
+                               lane, drop);
+    }
+  }
 }
 
 template <int kCh>
-cudaError_t launch_quant(unsigned grid, size_t smem, cudaStream_t stream, const uint16_t* x, int64_t R,
-                         int64_t C, int64_t ld, int scope, const int64_t* offs, int G, uint8_t* q,
-                         uint8_t* sblk, float* s32, const float* amax_ws) {
-  auto k = nvfp4_quant_kernel<kCh>;
+cudaError_t launch_token(unsigned grid, size_t smem, cudaStream_t stream, const uint16_t* x, int64_t R,
+                         int64_t C, int64_t ld, const int64_t* offs, int G, uint8_t* q, uint8_t* sblk,
+                         float* s32) {
+  auto k = nvfp4_token_kernel<kCh>;
   if (smem > 0) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  k<<<grid, kThreads, smem, stream>>>(x, R, C, ld, scope, offs, G, q, sblk, s32, amax_ws);
+  k<<<grid, kThreads, smem, stream>>>(x, R, C, ld, offs, G, q, sblk, s32);
+  return cudaGetLastError();
+}
+
+template <int kCh>
+cudaError_t launch_scoped(int sm_count, cudaStream_t stream, const uint16_t* x, int64_t R, int64_t C,
+                          int64_t ld, int scope, const int64_t* offs, int G, uint8_t* q, uint8_t* sblk,
+                          float* s32, uint32_t* scratch, int* err) {
+  auto k = nvfp4_scoped_kernel<kCh>;
+  const size_t smem = sizeof(ScopedSmem);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  k<<<static_cast<unsigned>(sm_count * per_sm), kThreads, smem, stream>>>(x, R, C, ld, scope, offs, G, q, sblk,
+                                                                         s32, scratch, err);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+size_t nvfp4_scratch_bytes(int groups) {
+  return (2 * static_cast<size_t>(scratch_gp(groups > 1 ? groups : 1)) + 2) * sizeof(uint32_t);
+}
+
 cudaError_t launch_nvfp4_quant(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int scope,
                                const int64_t* offs, int G, uint8_t* q, uint8_t* sblk, float* s32,
-                               float* amax_ws, int sm_count, cudaStream_t stream) {
+                               void* scratch, int* err, int sm_count, cudaStream_t stream) {
   const bool grouped = offs != nullptr;
   if (scope != 0) {
-    cudaError_t e = cudaMemsetAsync(amax_ws, 0, sizeof(float) * (scope == 1 ? G : 1), stream);
+    const int Gs = scope == 1 ? G : 1;
+    cudaError_t e = cudaMemsetAsync(scratch, 0, nvfp4_scratch_bytes(Gs), stream);
     if (e != cudaSuccess) return e;
-    if (R > 0) {
-      const int64_t want = (R + kWarps - 1) / kWarps;
-      const int64_t cap = static_cast<int64_t>(sm_count) * 8;
-      const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
-      nvfp4_amax_kernel<<<grid, kThreads, 0, stream>>>(x, R, C, ld, offs, G, scope == 1, amax_ws);
-      e = cudaGetLastError();
-      if (e != cudaSuccess) return e;
-    }
+    uint32_t* sc = static_cast<uint32_t*>(scratch);
+    if (C <= 1024) return launch_scoped<2>(sm_count, stream, x, R, C, ld, scope, offs, G, q, sblk, s32, sc, err);
+    if (C <= 2048) return launch_scoped<4>(sm_count, stream, x, R, C, ld, scope, offs, G, q, sblk, s32, sc, err);
+    if (C <= 4096) return launch_scoped<8>(sm_count, stream, x, R, C, ld, scope, offs, G, q, sblk, s32, sc, err);
+    if (C <= 8192) return launch_scoped<16>(sm_count, stream, x, R, C, ld, scope, offs, G, q, sblk, s32, sc, err);
+    return launch_scoped<0>(sm_count, stream, x, R, C, ld, scope, offs, G, q, sblk, s32, sc, err);
   }
   const int64_t tp_bound = grouped ? (R + 127 * static_cast<int64_t>(G) + 127) / 128 * 128
                                    : (R + 127) / 128 * 128;
@@ -266,11 +442,11 @@ cudaError_t launch_nvfp4_quant(const uint16_t* x, int64_t R, int64_t C, int64_t 
   unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
   if (grid == 0) grid = 1;
   const size_t smem = grouped ? sizeof(GroupSmem) : 0;
-  if (C <= 1024) return launch_quant<4>(grid, smem, stream, x, R, C, ld, scope, offs, G, q, sblk, s32, amax_ws);
-  if (C <= 2048) return launch_quant<8>(grid, smem, stream, x, R, C, ld, scope, offs, G, q, sblk, s32, amax_ws);
-  if (C <= 4096) return launch_quant<16>(grid, smem, stream, x, R, C, ld, scope, offs, G, q, sblk, s32, amax_ws);
-  if (C <= 8192) return launch_quant<32>(grid, smem, stream, x, R, C, ld, scope, offs, G, q, sblk, s32, amax_ws);
-  return launch_quant<0>(grid, smem, stream, x, R, C, ld, scope, offs, G, q, sblk, s32, amax_ws);
+  if (C <= 1024) return launch_token<2>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32);
+  if (C <= 2048) return launch_token<4>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32);
+  if (C <= 4096) return launch_token<8>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32);
+  if (C <= 8192) return launch_token<16>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32);
+  return launch_token<0>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32);
 }
 
 }  // namespace mx8q

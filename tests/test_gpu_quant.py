@@ -153,6 +153,21 @@ def test_nvfp4_expert_weights_group_scope():
     _nv_check(W, mx.SCOPE_GROUP, [0, 192, 384, 576, 768])
 
 
+def test_nvfp4_group_scope_interleaved_work_order():
+    """24 experts of Qwen3-30B-A3B gate|up shape ([1536, 2048] bf16, 6 MB each):
+    enough data that the fused group-scope kernel interleaves the amax work of
+    later experts with the encode work of earlier ones."""
+    g = torch.Generator(device="cuda").manual_seed(17)
+    W = inputs.normal_bf16((24 * 1536, 2048), 0.02, g, "cuda", 0.001, 30.0)
+    _nv_check(inputs.bits(W), mx.SCOPE_GROUP, list(range(0, 24 * 1536 + 1, 1536)))
+
+
+def test_nvfp4_tensor_scope_large():
+    g = torch.Generator(device="cuda").manual_seed(18)
+    W = inputs.normal_bf16((8192, 2048), 0.02, g, "cuda")
+    _nv_check(inputs.bits(W), mx.SCOPE_TENSOR)
+
+
 def test_nvfp4_per_token_batch_invariance_on_gpu():
     xb = inputs.bits(inputs.qwen_moe(with_weights=False, tokens=256, hidden=512)["X"])
     qa, sa, s32a = mx.nvfp4_quantize_per_token(dev(xb))
