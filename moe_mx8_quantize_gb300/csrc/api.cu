@@ -6,7 +6,7 @@
 
 #include <mutex>
 
-#include "../../include/mx8q.h"
+#include "mx8q.h"
 #include "device.cuh"
 #include "kernels.h"
 
@@ -214,6 +214,18 @@ mx8_status gemm_common_checks(int fmt, int64_t N, int64_t K, const uint8_t* A, c
   return MX8_OK;
 }
 
+// Output map for the GEMM epilogue's bulk stores: [rows, N] with row stride
+// ldc, box 64 bytes x 32 rows.
+bool encode_output_map(CUtensorMap* map, void* C, int64_t rows, int64_t N, int64_t ldc, int out_dtype) {
+  const bool bf = out_dtype == MX8_OUT_BF16;
+  const uint64_t es = bf ? 2 : 4;
+  const uint64_t dims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(rows)};
+  const uint64_t strides[1] = {static_cast<uint64_t>(ldc) * es};
+  const uint32_t box[2] = {static_cast<uint32_t>(64 / es), 32};
+  return encode_map(map, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, C, dims,
+                    strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 cudaError_t zero_output(void* C, int64_t ldc, int64_t rows, int64_t N, int out_dtype, cudaStream_t s) {
   const size_t es = out_dtype == MX8_OUT_BF16 ? 2 : 4;
   return cudaMemset2DAsync(C, ldc * es, 0, N * es, rows, s);
@@ -244,18 +256,20 @@ extern "C" mx8_status bs_gemm(int fmt, int64_t M, int64_t N, int64_t K, const ui
   const uint64_t kbytes = fmt == MX8_FMT_MXFP8 ? K : K / 2;
   CUtensorMap ma, mb;
   const uint32_t box[2] = {128, 128};
-  const uint32_t box_b[2] = {128, static_cast<uint32_t>(gemm_tile_n())};
+  const uint32_t box_b[2] = {128, 128};   // B is loaded in 128-row boxes
   const uint64_t da[2] = {kbytes, static_cast<uint64_t>(M)}, sa[1] = {kbytes};
   const uint64_t db[2] = {kbytes, static_cast<uint64_t>(N)}, sb[1] = {kbytes};
   if (!encode_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, A, da, sa, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, B, db, sb, box_b, CU_TENSOR_MAP_SWIZZLE_128B))
     return MX8_ERR_CUDA;
+  CUtensorMap mc;
+  if (!encode_output_map(&mc, C, M, N, ldc, out_dtype)) return MX8_ERR_CUDA;
   GemmArgs a{};
   a.fmt = fmt; a.M = M; a.N = N; a.K = K;
   a.SA = SA; a.SB = SB; a.A32 = A32; a.a32_mode = a32_mode; a.B32 = B32; a.b32_mode = b32_mode;
   a.C = C; a.ldc = ldc; a.out_bf16 = out_dtype == MX8_OUT_BF16; a.accumulate = accumulate;
   a.grouped = 0; a.G = 1; a.offs = nullptr; a.err = err_word(workspace);
-  return from_cuda(launch_bs_gemm(a, ma, mb, sm_count_current(), s));
+  return from_cuda(launch_bs_gemm(a, ma, mb, mc, sm_count_current(), s));
 }
 
 extern "C" mx8_status bs_grouped_gemm(int fmt, int num_groups, const int64_t* group_offsets,
@@ -279,19 +293,21 @@ extern "C" mx8_status bs_grouped_gemm(int fmt, int num_groups, const int64_t* gr
   CUtensorMap ma, mb;
   const uint32_t box2[2] = {128, 128};
   const uint64_t da[2] = {kbytes, static_cast<uint64_t>(total_rows)}, sa[1] = {kbytes};
-  const uint32_t box3[3] = {128, static_cast<uint32_t>(gemm_tile_n()), 1};
+  const uint32_t box3[3] = {128, 128, 1};
   const uint64_t db[3] = {kbytes, static_cast<uint64_t>(N), static_cast<uint64_t>(num_groups)};
   const uint64_t sb[2] = {kbytes, kbytes * static_cast<uint64_t>(N)};
   if (!encode_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, A, da, sa, box2, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, B, db, sb, box3, CU_TENSOR_MAP_SWIZZLE_128B))
     return MX8_ERR_CUDA;
+  CUtensorMap mc;
+  if (!encode_output_map(&mc, C, total_rows, N, ldc, out_dtype)) return MX8_ERR_CUDA;
   GemmArgs a{};
   a.fmt = fmt; a.M = total_rows; a.N = N; a.K = K;
   a.SA = SA; a.SB = SB; a.A32 = A32; a.a32_mode = A32 ? MX8_S32_ROW : MX8_S32_NONE;
   a.B32 = B32; a.b32_mode = B32 ? MX8_S32_GROUP : MX8_S32_NONE;
   a.C = C; a.ldc = ldc; a.out_bf16 = out_dtype == MX8_OUT_BF16; a.accumulate = 0;
   a.grouped = 1; a.G = num_groups; a.offs = group_offsets; a.err = err_word(workspace);
-  return from_cuda(launch_bs_gemm(a, ma, mb, sm_count_current(), s));
+  return from_cuda(launch_bs_gemm(a, ma, mb, mc, sm_count_current(), s));
 }
 
 // ===================================================================== errors

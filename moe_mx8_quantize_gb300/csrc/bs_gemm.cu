@@ -79,7 +79,9 @@ struct Layout {
   static constexpr int kSfaBytes = Cfg<kFmt>::kSfTiles * 512;
   static constexpr int kSfbBytes = Cfg<kFmt>::kSfTiles * 512 * kBRow128;
   static constexpr int kStageBytes = kTileABytes + kTileBBytes + kSfaBytes + kSfbBytes;
-  static constexpr int kFixed = 256 + (kGrouped ? static_cast<int>(sizeof(GroupSmem)) : 0);
+  static constexpr int kEpiStageBytes = 2048;                         // 32 rows x 64 B per epilogue warp
+  static constexpr int kFixed = 256 + (kBN / 32) * kEpiStageBytes +
+                                (kGrouped ? static_cast<int>(sizeof(GroupSmem)) : 0);
   static constexpr int kStagesFit = (kSmemBudget - kFixed) / kStageBytes;
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
   static constexpr int kAccBufs = kBN == 128 ? 2 : 1;
@@ -100,6 +102,7 @@ struct __align__(1024) GemmSmem {
   uint8_t b[L::kStages][L::kTileBBytes];
   uint8_t sfa[L::kStages][L::kSfaBytes];
   uint8_t sfb[L::kStages][L::kSfbBytes];
+  uint8_t cstage[L::kEpiWarps][L::kEpiStageBytes];   // epilogue staging for bulk stores
   uint64_t full[L::kStages];
   uint64_t empty[L::kStages];
   uint64_t acc_full[2];
@@ -167,7 +170,8 @@ __device__ __forceinline__ TileCoord decode_tile(int64_t t, int64_t tiles_n, int
 template <int kFmt, bool kGrouped, int kBN>
 __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
     bs_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                   const __grid_constant__ CUtensorMap tmap_b, const GemmArgs args) {
+                   const __grid_constant__ CUtensorMap tmap_b,
+                   const __grid_constant__ CUtensorMap tmap_c, const GemmArgs args) {
   using L = Layout<kFmt, kGrouped, kBN>;
   using F = Cfg<kFmt>;
   using Smem = GemmSmem<kFmt, kGrouped, kBN>;
@@ -183,6 +187,7 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmap_a);
     prefetch_tmap(&tmap_b);
+    prefetch_tmap(&tmap_c);
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(smem_u32(&sm.full[s]), 1);
       mbar_init(smem_u32(&sm.empty[s]), 1);
@@ -209,7 +214,9 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
   const int64_t tiles_n = (N + kBN - 1) / kBN;
   const int64_t n_rt = (N + 127) / 128;                   // 128-row scale tiles of B (per group)
   const int64_t tiles_m = kGrouped ? gs->pref[args.G] / BM : (M + BM - 1) / BM;
-  const int64_t ntiles = tiles_m * tiles_n;
+  const int64_t nunits = tiles_m * tiles_n;          // output tiles, strided over the CTAs
+  const int64_t unit0 = blockIdx.x, ustep = gridDim.x;
+  auto tile_of = [&](int64_t u) { return decode_tile<kGrouped, kBN>(u, tiles_n, M, gs, args.G); };
   const int64_t kbytes = kFmt == 0 ? K : K / 2;
   const int ktiles = static_cast<int>((kbytes + kKBytes - 1) / kKBytes);
   const int64_t sf_kt = (K / F::kBlock + 3) / 4;          // scale tiles along K
@@ -220,8 +227,8 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
     if (lane == 0) {
       int it = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
-        const TileCoord tc = decode_tile<kGrouped, kBN>(t, tiles_n, M, gs, G);
+      for (int64_t u = unit0; ok && u < nunits; u += ustep) {
+        const TileCoord tc = tile_of(u);
         const uint8_t* sfa_src = args.SA + tc.sfa_tile * sf_kt * 512;
         const int64_t brt0 = (kGrouped ? static_cast<int64_t>(tc.g) * n_rt : 0) + tc.n0 / 128;
         const uint8_t* sfb_src[L::kBRow128];
@@ -243,14 +250,18 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
           const uint32_t full = smem_u32(&sm.full[s]);
           mbar_arrive_expect_tx(full, kTileABytes + L::kTileBBytes + (1 + L::kBRow128) * nsf * 512);
           tma_load_2d(smem_u32(sm.a[s]), &tmap_a, kt * kKBytes, static_cast<int32_t>(tc.a_row0), full);
-          if (kGrouped)
-            tma_load_3d(smem_u32(sm.b[s]), &tmap_b, kt * kKBytes, static_cast<int32_t>(tc.n0), tc.g, full);
-          else
-            tma_load_2d(smem_u32(sm.b[s]), &tmap_b, kt * kKBytes, static_cast<int32_t>(tc.n0), full);
           bulk_load(smem_u32(sm.sfa[s]), sfa_src + sf0 * 512, nsf * 512, full);
+          // B in 128-row boxes (a 128-row box is 16 KB; boxes stack in shared memory)
 #pragma unroll
-          for (int h = 0; h < L::kBRow128; ++h)
+          for (int h = 0; h < L::kBRow128; ++h) {
+            if (kGrouped)
+              tma_load_3d(smem_u32(sm.b[s]) + h * 16384, &tmap_b, kt * kKBytes,
+                          static_cast<int32_t>(tc.n0 + h * 128), tc.g, full);
+            else
+              tma_load_2d(smem_u32(sm.b[s]) + h * 16384, &tmap_b, kt * kKBytes,
+                          static_cast<int32_t>(tc.n0 + h * 128), full);
             bulk_load(smem_u32(sm.sfb[s]) + h * F::kSfTiles * 512, sfb_src[h] + sf0 * 512, nsf * 512, full);
+          }
         }
       }
       if (!ok) {
@@ -266,7 +277,7 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
       int it = 0, tcount = 0;
       bool ok = true;
       const uint32_t sf_base = tmem + L::kAccCols;
-      for (int64_t t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++tcount) {
+      for (int64_t u = unit0; ok && u < nunits; u += ustep, ++tcount) {
         const int as = tcount % L::kAccBufs;
         const uint32_t aph = (tcount / L::kAccBufs) & 1;
         if (!mbar_wait(smem_u32(&sm.acc_empty[as]), aph ^ 1, err, kErrWaitAccum, &sm.abort)) {
@@ -328,7 +339,7 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
     const int col0 = (ew / 4) * 128;           // this warp's 128 accumulator columns
     const int r_in_tile = quarter * 32 + lane;
     int tcount = 0;
-    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++tcount) {
+    for (int64_t u = unit0; u < nunits; u += ustep, ++tcount) {
       const int as = tcount % L::kAccBufs;
       const uint32_t aph = (tcount / L::kAccBufs) & 1;
       const bool ok = mbar_wait(smem_u32(&sm.acc_full[as]), aph, err, kErrWaitEpilogue, &sm.abort);
@@ -342,7 +353,7 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.acc_empty[as]));   // accumulator drained into registers
 
-      const TileCoord tc = decode_tile<kGrouped, kBN>(t, tiles_n, M, gs, G);
+      const TileCoord tc = tile_of(u);
       const bool row_ok = r_in_tile < tc.rows;
       const int64_t m = tc.a_row0 + r_in_tile;
       float sa = 1.f;
@@ -357,6 +368,54 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
       // the two FP32 decode scales are combined first: acc * A32 alone can
       // overflow for tokens whose amax is near the bf16 maximum
       const float s_ab = __fmul_rn(sa, sg);
+      // Whole 32-row slabs leave through shared memory and bulk tensor stores
+      // (full lines, asynchronous); a slab that crosses the end of its group
+      // or that accumulates into C is stored directly, row by row.
+      if (quarter * 32 + 32 <= tc.rows && !args.accumulate) {
+        const uint32_t stage = smem_u32(sm.cstage[ew]);
+        const int32_t y = static_cast<int32_t>(tc.a_row0 + quarter * 32);
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          const int64_t n0 = tc.n0 + col0 + ch * 32;
+          if (n0 >= N) break;
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            float sc = s_ab;
+            if (b_row) sc = (n0 + j < N) ? __fmul_rn(sa, args.B32[n0 + j]) : 0.f;
+            v[j] = __fmul_rn(__uint_as_float(r[ch][j]), sc);
+          }
+#pragma unroll
+          for (int half = 0; half < (args.out_bf16 ? 1 : 2); ++half) {
+            if (lane == 0) bulk_wait_read_all();      // staging buffer free again
+            __syncwarp();
+            uint4* dst = reinterpret_cast<uint4*>(sm.cstage[ew] + lane * 64);
+            if (args.out_bf16) {
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t p[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  p[j] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[8 * q4 + 2 * j]))) |
+                         (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[8 * q4 + 2 * j + 1]))) << 16);
+                dst[q4] = make_uint4(p[0], p[1], p[2], p[3]);
+              }
+            } else {
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4)
+                dst[q4] = make_uint4(__float_as_uint(v[16 * half + 4 * q4]), __float_as_uint(v[16 * half + 4 * q4 + 1]),
+                                     __float_as_uint(v[16 * half + 4 * q4 + 2]), __float_as_uint(v[16 * half + 4 * q4 + 3]));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmap_c, static_cast<int32_t>(n0 + 16 * half), y, stage);
+              bulk_commit_group();
+            }
+          }
+        }
+        continue;
+      }
       if (!row_ok) continue;
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
@@ -405,6 +464,7 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
     }
   }
 
+  if (warp >= 2 && lane == 0) bulk_wait_all();   // every bulk store has landed
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -413,7 +473,7 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
 
 template <int kFmt, bool kGrouped, int kBN>
 cudaError_t launch_variant(const GemmArgs& a, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
-                           int sm_count, cudaStream_t stream) {
+                           const CUtensorMap& tmap_c, int sm_count, cudaStream_t stream) {
   using L = Layout<kFmt, kGrouped, kBN>;
   const int64_t tiles_n = (a.N + kBN - 1) / kBN;
   int64_t tiles_m = (a.M + BM - 1) / BM;
@@ -426,23 +486,21 @@ cudaError_t launch_variant(const GemmArgs& a, const CUtensorMap& tmap_a, const C
   static_assert(smem <= 227 * 1024, "shared memory over the per-block limit");
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  k<<<grid, L::kThreads, smem, stream>>>(tmap_a, tmap_b, a);
+  k<<<grid, L::kThreads, smem, stream>>>(tmap_a, tmap_b, tmap_c, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-int gemm_tile_n() { return MX8Q_GEMM_BN; }
-
 cudaError_t launch_bs_gemm(const GemmArgs& a, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
-                           int sm_count, cudaStream_t stream) {
+                           const CUtensorMap& tmap_c, int sm_count, cudaStream_t stream) {
   constexpr int BN = MX8Q_GEMM_BN;
   if (a.fmt == 0) {
-    return a.grouped ? launch_variant<0, true, BN>(a, tmap_a, tmap_b, sm_count, stream)
-                     : launch_variant<0, false, BN>(a, tmap_a, tmap_b, sm_count, stream);
+    return a.grouped ? launch_variant<0, true, BN>(a, tmap_a, tmap_b, tmap_c, sm_count, stream)
+                     : launch_variant<0, false, BN>(a, tmap_a, tmap_b, tmap_c, sm_count, stream);
   }
-  return a.grouped ? launch_variant<1, true, BN>(a, tmap_a, tmap_b, sm_count, stream)
-                   : launch_variant<1, false, BN>(a, tmap_a, tmap_b, sm_count, stream);
+  return a.grouped ? launch_variant<1, true, BN>(a, tmap_a, tmap_b, tmap_c, sm_count, stream)
+                   : launch_variant<1, false, BN>(a, tmap_a, tmap_b, tmap_c, sm_count, stream);
 }
 
 }  // namespace mx8q

@@ -50,9 +50,10 @@ struct GemmArgs {
   int* err;
 };
 
-int gemm_tile_n();   // N extent of the GEMM output tile (rows of B per TMA box)
+// tmap_c: the output [rows, N] as a 2-D map with a box of 64 bytes x 32 rows
+// (element type of the output), used for the epilogue's bulk stores.
 cudaError_t launch_bs_gemm(const GemmArgs& a, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
-                           int sm_count, cudaStream_t stream);
+                           const CUtensorMap& tmap_c, int sm_count, cudaStream_t stream);
 
 cudaError_t launch_selftest_wait(int* err, uint64_t limit_ns, cudaStream_t stream);
 

@@ -17,7 +17,7 @@
 // threads without ordering) race on it and must be serialised.
 #include <mutex>
 
-#include "../../include/mx8q.h"
+#include "mx8q.h"
 #include "kernels.h"
 
 namespace {
