@@ -41,3 +41,27 @@ def gemm_tolerance_ok(y, ref, absref, bf16=False, K=0):
         tol = tol + 2.0 ** -8 * np.abs(ref)
     bad = np.abs(y - ref) > tol
     return (~bad).all(), np.nonzero(bad.ravel())[0]
+
+
+def scale_offsets(rows_idx, scols, padded_row_of=None):
+    """Byte offsets, in a tensor-core scale buffer with scols logical scale
+    columns, of the scales of the given rows (rows x scols array).
+    padded_row_of maps a data row to its row in the (grouped) padded layout."""
+    rows_idx = np.asarray(rows_idx, np.int64)
+    pr = rows_idx if padded_row_of is None else padded_row_of(rows_idx)
+    kt = -(-scols // 4)
+    k = np.arange(scols, dtype=np.int64)
+    r = pr[:, None]
+    return ((r // 128) * kt + k[None, :] // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + k[None, :] % 4
+
+
+def grouped_padded_row(offs):
+    """Data row -> row of the per-group padded scale layout."""
+    offs = np.asarray(offs, np.int64)
+    n = np.diff(offs)
+    pref = np.concatenate([[0], np.cumsum(-(-n // 128) * 128)])
+
+    def f(rows):
+        g = np.searchsorted(offs, rows, side="right") - 1
+        return pref[g] + (rows - offs[g])
+    return f
