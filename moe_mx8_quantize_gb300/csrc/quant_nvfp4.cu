@@ -24,11 +24,23 @@
 //
 // Layout of the work: one warp per row; lane l owns the 16-element block
 // [512*i + 16*l, +16) of every 512-element chunk i, so each lane computes its
-// block's scale once (no duplicated divisions), loads are 32 contiguous bytes
-// per lane and the 8-byte code stores of a warp are contiguous.  |x| maxima are
-// taken as unsigned maxima of the bf16 bit patterns with the sign cleared
-// (they order like the values), two per instruction.  Four lanes hold one
-// 4-scale group of the tensor-core tile and write it as one 32-bit word.
+// block's scale once, loads are 32 contiguous bytes per lane and the 8-byte
+// code stores of a warp are contiguous.  |x| maxima are taken two bf16 values
+// per instruction (max of magnitudes), the products x * r two per instruction
+// (packed binary32 multiply).  Four lanes hold one 4-scale group of the
+// tensor-core tile and write it as one 32-bit word.
+//
+// The two divisions of a block, amax_b / 6 and S_enc / sb, are computed as
+// Markstein's FMA-corrected quotients (P. Markstein, "IA-64 and Elementary
+// Functions", 2000; J.-M. Muller et al., "Handbook of Floating-Point
+// Arithmetic", the theorem on correcting a quotient with one FMA): with
+// y = RN(1/b) and q = RN(a y), the remainder a - b q is exact in one FMA and
+// RN(q + (a - b q) y) = RN(a / b).  Both dividends come from bf16 maxima
+// (amax_b, and S_enc = min(2688 / A, FLT_MAX) for a bf16 A), so the result
+// was checked bit for bit against IEEE division over every finite bf16 value
+// and every positive E4M3 divisor, the overflow cases included (they
+// saturate to FLT_MAX through the min).  1/sb comes from a 128-entry table of
+// {E4M3 value, RN(1/value)} per block.
 //
 // Token scope: rows of up to 512*kCh elements are held in registers, all loads
 // issued up front, so the amax and the encode read HBM once.
@@ -65,20 +77,40 @@ __device__ __forceinline__ void nvfp4_scales(float amax, float& senc, float& sde
   sdec = __fdiv_rn(amax, 2688.0f);
 }
 
-__device__ __forceinline__ uint32_t umax2(uint32_t a, uint32_t b) {
+// Per bf16 half: the larger magnitude of a and b (its sign bit is not
+// meaningful; abs_halves_max clears it).
+__device__ __forceinline__ uint32_t amax2(uint32_t a, uint32_t b) {
   uint32_t d;
-  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
 
-// Packed |x| maxima of 16 bf16 values (two u16 halves).
+// Packed |x| maxima of 16 bf16 values (two halves, sign bits not meaningful).
 __device__ __forceinline__ uint32_t absmax16(const uint4& a, const uint4& b) {
-  const uint32_t m = 0x7FFF7FFFu;
-  return umax2(umax2(umax2(a.x & m, a.y & m), umax2(a.z & m, a.w & m)),
-               umax2(umax2(b.x & m, b.y & m), umax2(b.z & m, b.w & m)));
+  return amax2(amax2(amax2(a.x, a.y), amax2(a.z, a.w)), amax2(amax2(b.x, b.y), amax2(b.z, b.w)));
 }
 
-__device__ __forceinline__ float halves_max(uint32_t w) { return fmaxf(bf16_lo(w), bf16_hi(w)); }
+__device__ __forceinline__ float abs_halves_max(uint32_t w) {
+  return fmaxf(__uint_as_float((w << 16) & 0x7FFFFFFFu), __uint_as_float(w & 0x7FFF0000u));
+}
+
+// {E4M3 value, RN(1 / value)} per E4M3 code; {0, 0} for code 0.
+__device__ __forceinline__ void init_scale_table(float2* tab) {
+  for (int c = threadIdx.x; c < 128; c += blockDim.x) {
+    const float b = e4m3_to_f32(static_cast<uint32_t>(c));
+    tab[c] = make_float2(b, c == 0 ? 0.f : __frcp_rn(b));
+  }
+}
+
+// x * r (IEEE binary32) for the two bf16 values of w.
+__device__ __forceinline__ void mul_bf16x2(uint32_t w, uint64_t rr, float& lo, float& hi) {
+  asm("{\n\t.reg .b64 p, q;\n\t"
+      "mov.b64 p, {%2, %3};\n\t"
+      "mul.rn.f32x2 q, p, %4;\n\t"
+      "mov.b64 {%0, %1}, q;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(w << 16), "r"(w & 0xFFFF0000u), "l"(rr));
+}
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -131,30 +163,33 @@ __device__ __forceinline__ float row_amax_stream(const uint16_t* __restrict__ xr
       w[2 * i + 1] = ok ? (kHint ? ld_hint(xr + c + 8, pol) : ld_nc(xr + c + 8)) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) m = umax2(m, absmax16(w[2 * i], w[2 * i + 1]));
+    for (int i = 0; i < 4; ++i) m = amax2(m, absmax16(w[2 * i], w[2 * i + 1]));
   }
-  return warp_max(halves_max(m));
+  return warp_max(abs_halves_max(m));
 }
 
 // Encodes one 512-element chunk starting at column `base`: lane l encodes the
 // 16-element block [base + 16 l, +16) held in (a, b).
 __device__ __forceinline__ void encode_chunk(const uint4& a, const uint4& b, int64_t base, int64_t C,
-                                             int lane, float senc, uint8_t* __restrict__ qr,
-                                             uint8_t* __restrict__ sblk, int64_t sr, int64_t kt) {
+                                             int lane, float senc, const float2* __restrict__ tab,
+                                             uint8_t* __restrict__ qr, uint8_t* __restrict__ sblk, int64_t sr,
+                                             int64_t kt) {
   const int64_t c = base + lane * 16;
-  const float bmax = halves_max(absmax16(a, b));
-  const float t = __fmul_rn(__fdiv_rn(bmax, 6.0f), senc);
-  const uint32_t sb = cvt_e4m3x2(t, 0.0f) & 0xFFu;
-  float r = 0.f;
-  if (sb != 0) r = fminf(__fdiv_rn(senc, e4m3_to_f32(sb)), FLT_MAX);
+  const float bmax = abs_halves_max(absmax16(a, b));
+  constexpr float kInv6 = 1.0f / 6.0f;                     // RN(1/6)
+  float q = __fmul_rn(bmax, kInv6);
+  q = __fmaf_rn(__fmaf_rn(-q, 6.0f, bmax), kInv6, q);      // RN(bmax / 6)
+  const uint32_t sb = cvt_e4m3x2(__fmul_rn(q, senc), 0.0f) & 0xFFu;
+  const float2 by = tab[sb & 127u];
+  const float q0 = __fmul_rn(senc, by.y);
+  const float r = fminf(__fmaf_rn(__fmaf_rn(-q0, by.x, senc), by.y, q0), FLT_MAX);   // min(RN(senc / sb), FLT_MAX); 0 for sb = 0
+  const uint64_t rr = (static_cast<uint64_t>(__float_as_uint(r)) << 32) | __float_as_uint(r);
   const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
   float v0[8], v1[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    v0[2 * i] = __fmul_rn(bf16_lo(w[i]), r);
-    v0[2 * i + 1] = __fmul_rn(bf16_hi(w[i]), r);
-    v1[2 * i] = __fmul_rn(bf16_lo(w[4 + i]), r);
-    v1[2 * i + 1] = __fmul_rn(bf16_hi(w[4 + i]), r);
+    mul_bf16x2(w[i], rr, v0[2 * i], v0[2 * i + 1]);
+    mul_bf16x2(w[4 + i], rr, v1[2 * i], v1[2 * i + 1]);
   }
   const uint32_t p0 = cvt_e2m1x8(v0), p1 = cvt_e2m1x8(v1);
   if (c < C) *reinterpret_cast<uint2*>(qr + c / 2) = make_uint2(p0, p1);
@@ -170,9 +205,10 @@ __device__ __forceinline__ void encode_chunk(const uint4& a, const uint4& b, int
 // for scope_token the amax and S_dec come from the row itself.
 template <int kCh, bool kHint = false>
 __device__ __forceinline__ void process_row(const uint16_t* __restrict__ x, int64_t row, int64_t C, int64_t ld,
-                                            bool scope_token, float senc_given, uint8_t* __restrict__ q,
-                                            uint8_t* __restrict__ sblk, float* __restrict__ s32, int64_t sr,
-                                            int64_t kt, int lane, uint64_t pol = 0) {
+                                            bool scope_token, float senc_given, const float2* __restrict__ tab,
+                                            uint8_t* __restrict__ q, uint8_t* __restrict__ sblk,
+                                            float* __restrict__ s32, int64_t sr, int64_t kt, int lane,
+                                            uint64_t pol = 0) {
   if (row < 0) {  // padding row of the scale tile
     for (int64_t k4 = lane; k4 < kt; k4 += 32) *reinterpret_cast<uint32_t*>(sblk + sf_word(sr, k4, kt)) = 0u;
     return;
@@ -193,14 +229,15 @@ __device__ __forceinline__ void process_row(const uint16_t* __restrict__ x, int6
     if (scope_token) {
       uint32_t m = 0;
 #pragma unroll
-      for (int i = 0; i < kCh; ++i) m = umax2(m, absmax16(w[2 * i], w[2 * i + 1]));
+      for (int i = 0; i < kCh; ++i) m = amax2(m, absmax16(w[2 * i], w[2 * i + 1]));
       float sdec;
-      nvfp4_scales(warp_max(halves_max(m)), senc, sdec);
+      nvfp4_scales(warp_max(abs_halves_max(m)), senc, sdec);
       if (lane == 0) s32[row] = sdec;
     }
 #pragma unroll
     for (int i = 0; i < kCh; ++i)
-      if (i < nch) encode_chunk(w[2 * i], w[2 * i + 1], static_cast<int64_t>(i) * 512, C, lane, senc, qr, sblk, sr, kt);
+      if (i < nch)
+        encode_chunk(w[2 * i], w[2 * i + 1], static_cast<int64_t>(i) * 512, C, lane, senc, tab, qr, sblk, sr, kt);
   } else {
     float senc = senc_given;
     if (scope_token) {
@@ -213,7 +250,7 @@ __device__ __forceinline__ void process_row(const uint16_t* __restrict__ x, int6
       const bool ok = c < C;
       const uint4 a = ok ? (kHint ? ld_hint(xr + c, pol) : ld_nc(xr + c)) : make_uint4(0, 0, 0, 0);
       const uint4 b = ok ? (kHint ? ld_hint(xr + c + 8, pol) : ld_nc(xr + c + 8)) : make_uint4(0, 0, 0, 0);
-      encode_chunk(a, b, base, C, lane, senc, qr, sblk, sr, kt);
+      encode_chunk(a, b, base, C, lane, senc, tab, qr, sblk, sr, kt);
     }
   }
 }
@@ -233,6 +270,9 @@ __global__ void __launch_bounds__(kThreads) nvfp4_token_kernel(
     uint8_t* __restrict__ q, uint8_t* __restrict__ sblk, float* __restrict__ s32) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   GroupSmem& gs = *reinterpret_cast<GroupSmem*>(smem_raw);
+  __shared__ float2 tab[128];
+  init_scale_table(tab);
+  __syncthreads();
   const bool grouped = offs != nullptr;
   int64_t TP;
   if (grouped) {
@@ -245,7 +285,7 @@ __global__ void __launch_bounds__(kThreads) nvfp4_token_kernel(
   const int64_t kt = (C / 16 + 3) / 4;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
   for (int64_t sr = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); sr < TP; sr += nwarps)
-    process_row<kCh>(x, data_row(gs, grouped, G, R, sr), C, ld, true, 0.f, q, sblk, s32, sr, kt, lane);
+    process_row<kCh>(x, data_row(gs, grouped, G, R, sr), C, ld, true, 0.f, tab, q, sblk, s32, sr, kt, lane);
 }
 
 // ------------------------------------------------------------------ group / tensor scope
@@ -260,6 +300,7 @@ struct ScopedSmem {
   int32_t seg_start[2 * kMaxGroups + 1];
   int32_t seg_info[2 * kMaxGroups];   // (group << 1) | is_encode
   int32_t nseg;
+  float2 tab[128];
   int64_t ticket;
   float amax;
   float red[kWarps];
@@ -278,6 +319,7 @@ __global__ void __launch_bounds__(kThreads) nvfp4_scoped_kernel(
   uint32_t* done = scratch + scratch_gp(Gs);
   unsigned long long* ticket = reinterpret_cast<unsigned long long*>(scratch + 2 * scratch_gp(Gs));
 
+  init_scale_table(sm.tab);
   if (grouped) load_group_prefix(sm.gs, offs, G);
   __syncthreads();
   int64_t TP = grouped ? sm.gs.pref[G] : (R + 127) / 128 * 128;
@@ -378,8 +420,8 @@ __global__ void __launch_bounds__(kThreads) nvfp4_scoped_kernel(
       if (item == 0 && threadIdx.x == 0) s32[g] = sdec;
       const int64_t s0 = sm.apref[g] + item * kItemRows;
       for (int64_t sr = s0 + warp; sr < s0 + kItemRows; sr += kWarps)
-        process_row<kCh, true>(x, data_row(sm.gs, grouped, G, R, sr), C, ld, false, senc, q, sblk, s32, sr, kt,
-                               lane, drop);
+        process_row<kCh, true>(x, data_row(sm.gs, grouped, G, R, sr), C, ld, false, senc, sm.tab, q, sblk, s32, sr,
+                               kt, lane, drop);
     }
   }
 }
