@@ -142,7 +142,8 @@ mx8_status mx8_quantize(const void *x, int64_t rows, int64_t cols, int64_t ld, i
  *   q      : uint8 [rows, cols/2]
  *   s_blk  : E4M3 scales, mx8_scale_bytes(NVFP4, rows, cols), or
  *            mx8_scale_bytes_grouped(...) with group_offsets
- * Requires cols % 16 == 0, ld % 8 == 0, 16-byte aligned x/q/s_blk.
+ * Requires cols % 16 == 0, ld % 8 == 0, 16-byte aligned x/q/s_blk;
+ * cols > 2^30 returns MX8_ERR_UNSUPPORTED.
  */
 mx8_status nvfp4_quantize_per_token(const void *x, int64_t rows, int64_t cols, int64_t ld,
                                     int scope, const int64_t *group_offsets, int num_groups,

@@ -147,6 +147,7 @@ extern "C" mx8_status nvfp4_quantize_per_token(const void* x, int64_t rows, int6
                                                mx8_stream_t stream) {
   if (scope < NVFP4_SCOPE_TOKEN || scope > NVFP4_SCOPE_TENSOR) return MX8_ERR_INVALID_ARG;
   if (rows < 0 || cols < 0 || ld < cols || cols % 16 != 0) return MX8_ERR_INVALID_ARG;
+  if (cols > (int64_t{1} << 30)) return MX8_ERR_UNSUPPORTED;   // columns are 32-bit in the kernels
   if (scope == NVFP4_SCOPE_GROUP && group_offsets == nullptr) return MX8_ERR_INVALID_ARG;
   if (group_offsets != nullptr && (num_groups < 1 || num_groups > kMaxGroups)) return MX8_ERR_INVALID_ARG;
   const int G = group_offsets ? num_groups : 1;

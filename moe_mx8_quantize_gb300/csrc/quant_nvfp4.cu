@@ -142,39 +142,49 @@ __device__ __forceinline__ uint4 ld_hint(const uint16_t* p, uint64_t pol) {
   return r;
 }
 
-// Scale-tile byte offset of the 4-scale word (scale row sr, scale columns k4*4..+3).
-__device__ __forceinline__ int64_t sf_word(int64_t sr, int64_t k4, int64_t kt) {
-  return ((sr >> 7) * kt + k4) * 512 + (sr & 31) * 16 + ((sr >> 5) & 3) * 4;
+// Scale-tile byte offset of scale row sr's first 4-scale word; the word of
+// scale columns k4*4..+3 is 512 * k4 bytes further.
+__device__ __forceinline__ int64_t sf_row_base(int64_t sr, int64_t kt) {
+  return (sr >> 7) * kt * 512 + (sr & 31) * 16 + ((sr >> 5) & 3) * 4;
 }
 
-// Streaming row amax (each lane: 16 elements per 512-element chunk, 4 chunks
-// in flight); with kHint the loads carry the L2 policy `pol`.
-template <bool kHint = false>
-__device__ __forceinline__ float row_amax_stream(const uint16_t* __restrict__ xr, int64_t C, int lane,
-                                                 uint64_t pol = 0) {
+template <bool kHint>
+__device__ __forceinline__ uint4 ld_row16(const uint16_t* p, uint64_t pol) {
+  return kHint ? ld_hint(p, pol) : ld_nc(p);
+}
+
+// This lane's packed |x| maximum over its blocks of a row (sign bits not
+// meaningful).  kCh > 0: the row has at most kCh 512-value chunks, all loads
+// issued at once; kCh = 0: any length, 4 chunks in flight.  With kHint the
+// loads carry the L2 policy `pol`.
+template <int kCh, bool kHint = false>
+__device__ __forceinline__ uint32_t row_absmax_lane(const uint16_t* __restrict__ xr, int C, int lane,
+                                                    uint64_t pol = 0) {
+  constexpr int kN = kCh > 0 ? kCh : 4;
   uint32_t m = 0;
-  for (int64_t base = 0; base < C; base += 512 * 4) {
-    uint4 w[8];
+  for (int base = 0; base < C; base += 512 * kN) {
+    uint4 w[2 * kN];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int64_t c = base + i * 512 + lane * 16;
+    for (int i = 0; i < kN; ++i) {
+      const int c = base + i * 512 + lane * 16;
       const bool ok = c < C;
-      w[2 * i] = ok ? (kHint ? ld_hint(xr + c, pol) : ld_nc(xr + c)) : make_uint4(0, 0, 0, 0);
-      w[2 * i + 1] = ok ? (kHint ? ld_hint(xr + c + 8, pol) : ld_nc(xr + c + 8)) : make_uint4(0, 0, 0, 0);
+      w[2 * i] = ok ? ld_row16<kHint>(xr + c, pol) : make_uint4(0, 0, 0, 0);
+      w[2 * i + 1] = ok ? ld_row16<kHint>(xr + c + 8, pol) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) m = amax2(m, absmax16(w[2 * i], w[2 * i + 1]));
+    for (int i = 0; i < kN; ++i) m = amax2(m, absmax16(w[2 * i], w[2 * i + 1]));
+    if (kCh > 0) break;
   }
-  return warp_max(abs_halves_max(m));
+  return m;
 }
 
-// Encodes one 512-element chunk starting at column `base`: lane l encodes the
-// 16-element block [base + 16 l, +16) held in (a, b).
-__device__ __forceinline__ void encode_chunk(const uint4& a, const uint4& b, int64_t base, int64_t C,
-                                             int lane, float senc, const float2* __restrict__ tab,
-                                             uint8_t* __restrict__ qr, uint8_t* __restrict__ sblk, int64_t sr,
-                                             int64_t kt) {
-  const int64_t c = base + lane * 16;
+// Encodes 512-element chunk j of a row: lane l encodes the 16-element block
+// [512 j + 16 l, +16) held in (a, b); qr is the row's codes, swr its first
+// scale word in the tensor-core tile layout.
+__device__ __forceinline__ void encode_chunk(const uint4& a, const uint4& b, int j, int C, int lane, float senc,
+                                             const float2* __restrict__ tab, uint8_t* __restrict__ qr,
+                                             uint8_t* __restrict__ swr, int kt) {
+  const int c = j * 512 + lane * 16;
   const float bmax = abs_halves_max(absmax16(a, b));
   constexpr float kInv6 = 1.0f / 6.0f;                     // RN(1/6)
   float q = __fmul_rn(bmax, kInv6);
@@ -192,38 +202,39 @@ __device__ __forceinline__ void encode_chunk(const uint4& a, const uint4& b, int
     mul_bf16x2(w[4 + i], rr, v1[2 * i], v1[2 * i + 1]);
   }
   const uint32_t p0 = cvt_e2m1x8(v0), p1 = cvt_e2m1x8(v1);
-  if (c < C) *reinterpret_cast<uint2*>(qr + c / 2) = make_uint2(p0, p1);
+  if (c < C) *reinterpret_cast<uint2*>(qr + (c >> 1)) = make_uint2(p0, p1);
   const uint32_t s1 = __shfl_down_sync(0xffffffffu, sb, 1);
   const uint32_t s2 = __shfl_down_sync(0xffffffffu, sb, 2);
   const uint32_t s3 = __shfl_down_sync(0xffffffffu, sb, 3);
-  const int64_t k4 = (base >> 6) + (lane >> 2);
+  const int k4 = j * 8 + (lane >> 2);
   if ((lane & 3) == 0 && k4 < kt)
-    *reinterpret_cast<uint32_t*>(sblk + sf_word(sr, k4, kt)) = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+    *reinterpret_cast<uint32_t*>(swr + k4 * 512) = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
 }
 
 // Encodes data row `row` (or zeros scale row sr when row < 0) with scale S_enc;
 // for scope_token the amax and S_dec come from the row itself.
 template <int kCh, bool kHint = false>
-__device__ __forceinline__ void process_row(const uint16_t* __restrict__ x, int64_t row, int64_t C, int64_t ld,
+__device__ __forceinline__ void process_row(const uint16_t* __restrict__ x, int64_t row, int C, int64_t ld,
                                             bool scope_token, float senc_given, const float2* __restrict__ tab,
                                             uint8_t* __restrict__ q, uint8_t* __restrict__ sblk,
-                                            float* __restrict__ s32, int64_t sr, int64_t kt, int lane,
+                                            float* __restrict__ s32, int64_t sr, int kt, int lane,
                                             uint64_t pol = 0) {
+  uint8_t* swr = sblk + sf_row_base(sr, kt);
   if (row < 0) {  // padding row of the scale tile
-    for (int64_t k4 = lane; k4 < kt; k4 += 32) *reinterpret_cast<uint32_t*>(sblk + sf_word(sr, k4, kt)) = 0u;
+    for (int k4 = lane; k4 < kt; k4 += 32) *reinterpret_cast<uint32_t*>(swr + k4 * 512) = 0u;
     return;
   }
   const uint16_t* xr = x + row * ld;
   uint8_t* qr = q + row * (C / 2);
   if (kCh > 0) {
-    const int nch = static_cast<int>((C + 511) / 512);
+    const int nch = (C + 511) / 512;
     uint4 w[2 * (kCh > 0 ? kCh : 1)];
 #pragma unroll
     for (int i = 0; i < kCh; ++i) {
-      const int64_t c = static_cast<int64_t>(i) * 512 + lane * 16;
+      const int c = i * 512 + lane * 16;
       const bool ok = i < nch && c < C;
-      w[2 * i] = ok ? (kHint ? ld_hint(xr + c, pol) : ld_nc(xr + c)) : make_uint4(0, 0, 0, 0);
-      w[2 * i + 1] = ok ? (kHint ? ld_hint(xr + c + 8, pol) : ld_nc(xr + c + 8)) : make_uint4(0, 0, 0, 0);
+      w[2 * i] = ok ? ld_row16<kHint>(xr + c, pol) : make_uint4(0, 0, 0, 0);
+      w[2 * i + 1] = ok ? ld_row16<kHint>(xr + c + 8, pol) : make_uint4(0, 0, 0, 0);
     }
     float senc = senc_given;
     if (scope_token) {
@@ -236,21 +247,20 @@ __device__ __forceinline__ void process_row(const uint16_t* __restrict__ x, int6
     }
 #pragma unroll
     for (int i = 0; i < kCh; ++i)
-      if (i < nch)
-        encode_chunk(w[2 * i], w[2 * i + 1], static_cast<int64_t>(i) * 512, C, lane, senc, tab, qr, sblk, sr, kt);
+      if (i < nch) encode_chunk(w[2 * i], w[2 * i + 1], i, C, lane, senc, tab, qr, swr, kt);
   } else {
     float senc = senc_given;
     if (scope_token) {
       float sdec;
-      nvfp4_scales(row_amax_stream(xr, C, lane), senc, sdec);
+      nvfp4_scales(warp_max(abs_halves_max(row_absmax_lane<0, kHint>(xr, C, lane, pol))), senc, sdec);
       if (lane == 0) s32[row] = sdec;
     }
-    for (int64_t base = 0; base < C; base += 512) {
-      const int64_t c = base + lane * 16;
+    for (int j = 0; j * 512 < C; ++j) {
+      const int c = j * 512 + lane * 16;
       const bool ok = c < C;
-      const uint4 a = ok ? (kHint ? ld_hint(xr + c, pol) : ld_nc(xr + c)) : make_uint4(0, 0, 0, 0);
-      const uint4 b = ok ? (kHint ? ld_hint(xr + c + 8, pol) : ld_nc(xr + c + 8)) : make_uint4(0, 0, 0, 0);
-      encode_chunk(a, b, base, C, lane, senc, tab, qr, sblk, sr, kt);
+      const uint4 a = ok ? ld_row16<kHint>(xr + c, pol) : make_uint4(0, 0, 0, 0);
+      const uint4 b = ok ? ld_row16<kHint>(xr + c + 8, pol) : make_uint4(0, 0, 0, 0);
+      encode_chunk(a, b, j, C, lane, senc, tab, qr, swr, kt);
     }
   }
 }
@@ -265,7 +275,7 @@ __device__ __forceinline__ int64_t data_row(const GroupSmem& gs, bool grouped, i
 
 // ------------------------------------------------------------------ token scope
 template <int kCh>
-__global__ void __launch_bounds__(kThreads) nvfp4_token_kernel(
+__global__ void __launch_bounds__(kThreads, kCh >= 8 || kCh == 0 ? 1 : 4) nvfp4_token_kernel(
     const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ld, const int64_t* __restrict__ offs, int G,
     uint8_t* __restrict__ q, uint8_t* __restrict__ sblk, float* __restrict__ s32) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -282,10 +292,11 @@ __global__ void __launch_bounds__(kThreads) nvfp4_token_kernel(
     TP = (R + 127) / 128 * 128;
   }
   const int lane = threadIdx.x & 31;
-  const int64_t kt = (C / 16 + 3) / 4;
+  const int C32 = static_cast<int>(C);
+  const int kt = (C32 / 16 + 3) / 4;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
   for (int64_t sr = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); sr < TP; sr += nwarps)
-    process_row<kCh>(x, data_row(gs, grouped, G, R, sr), C, ld, true, 0.f, tab, q, sblk, s32, sr, kt, lane);
+    process_row<kCh>(x, data_row(gs, grouped, G, R, sr), C32, ld, true, 0.f, tab, q, sblk, s32, sr, kt, lane);
 }
 
 // ------------------------------------------------------------------ group / tensor scope
@@ -293,21 +304,54 @@ __global__ void __launch_bounds__(kThreads) nvfp4_token_kernel(
 // then a 64-bit ticket counter; Gp = scope groups rounded up to even.
 __host__ __device__ __forceinline__ int scratch_gp(int groups) { return (groups + 1) / 2 * 2; }
 
+// Block of the scoped kernel: warp 0 is the control warp (tickets, the amax
+// hand-off between blocks, dependency checks), warps 1..kDataWarps move data.
+// The control warp's latencies (the ticket atomic, the release of an amax
+// item's maximum, the check that a group's amax is complete) overlap the
+// data warps' work on the current item instead of stalling the block.
+constexpr int kDataWarps = 8;
+constexpr int kScopedThreads = 32 * (kDataWarps + 1);
+
 struct ScopedSmem {
   GroupSmem gs;                       // scale-layout groups (or one group)
-  int64_t aoffs[kMaxGroups + 1];      // scope groups: data row offsets
-  int64_t apref[kMaxGroups + 1];      // scope groups: scale-row offsets (padded)
+  int64_t toffs[2];                   // tensor scope: data rows [0, R) ...
+  int64_t tpref[2];                   // ... and scale rows [0, TP)
   int32_t seg_start[2 * kMaxGroups + 1];
   int32_t seg_info[2 * kMaxGroups];   // (group << 1) | is_encode
   int32_t nseg;
   float2 tab[128];
-  int64_t ticket;
-  float amax;
-  float red[kWarps];
+  // Two ticket slots, used by alternate work items: the control warp fills
+  // the next item's slot while the data warps run the current one.
+  int64_t tk[2];
+  int64_t titem[2];                   // item index within its segment
+  int32_t tg[2];                      // scope group
+  int32_t tenc[2];                    // 1 = encode item
+  int32_t tready[2];                  // encode item whose group amax is known
+  float tsenc[2];                     // ... and its S_enc
+  float red[2][kDataWarps];           // amax items: per-warp maxima
 };
 
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Ordering of the work items and the deadlock argument.  Tickets are taken in
+// order from one counter.  The amax items of a group all precede the group's
+// encode items in ticket order.  A data warp never waits.  The control warp
+// releases the amax of the block's previous item before anything else in an
+// iteration, and it only blocks (the rare case of an encode item whose group
+// was not complete when its ticket was taken) after that release, so every
+// amax item taken is released once its block finishes it, whatever the other
+// blocks wait for.  The wait is bounded anyway (error word on timeout).
 template <int kCh>
-__global__ void __launch_bounds__(kThreads) nvfp4_scoped_kernel(
+__global__ void __launch_bounds__(kScopedThreads, kCh >= 8 || kCh == 0 ? 1 : 4) nvfp4_scoped_kernel(
     const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ld, int scope,
     const int64_t* __restrict__ offs, int G, uint8_t* __restrict__ q, uint8_t* __restrict__ sblk,
     float* __restrict__ s32, uint32_t* __restrict__ scratch, int* err) {
@@ -322,14 +366,12 @@ __global__ void __launch_bounds__(kThreads) nvfp4_scoped_kernel(
   init_scale_table(sm.tab);
   if (grouped) load_group_prefix(sm.gs, offs, G);
   __syncthreads();
-  int64_t TP = grouped ? sm.gs.pref[G] : (R + 127) / 128 * 128;
+  const int64_t TP = grouped ? sm.gs.pref[G] : (R + 127) / 128 * 128;
+  // scope groups: data rows and padded scale rows
+  const int64_t* aoffs = scope == 1 ? sm.gs.offs : sm.toffs;
+  const int64_t* apref = scope == 1 ? sm.gs.pref : sm.tpref;
   if (threadIdx.x == 0) {
-    // scope groups: data rows and padded scale rows
-    if (scope == 1) {
-      for (int g = 0; g <= G; ++g) { sm.aoffs[g] = sm.gs.offs[g]; sm.apref[g] = sm.gs.pref[g]; }
-    } else {
-      sm.aoffs[0] = 0; sm.aoffs[1] = R; sm.apref[0] = 0; sm.apref[1] = TP;
-    }
+    sm.toffs[0] = 0; sm.toffs[1] = R; sm.tpref[0] = 0; sm.tpref[1] = TP;
     // segment order: amax(0..L-1), then encode(g), amax(g+L) for g = 0..Gs-1
     const int64_t per_group_bytes = Gs > 0 ? (R * C * 2) / Gs : 0;
     int lead = per_group_bytes > 0 ? static_cast<int>(kL2LeadBytes / per_group_bytes) : Gs;
@@ -338,8 +380,8 @@ __global__ void __launch_bounds__(kThreads) nvfp4_scoped_kernel(
     int nseg = 0;
     int32_t pos = 0;
     auto push = [&](int g, int enc) {
-      const int64_t n = enc ? (sm.apref[g + 1] - sm.apref[g]) / kItemRows
-                            : (sm.aoffs[g + 1] - sm.aoffs[g] + kItemRows - 1) / kItemRows;
+      const int64_t n = enc ? (apref[g + 1] - apref[g]) / kItemRows
+                            : (aoffs[g + 1] - aoffs[g] + kItemRows - 1) / kItemRows;
       sm.seg_start[nseg] = pos;
       sm.seg_info[nseg] = (g << 1) | enc;
       pos += static_cast<int32_t>(n);
@@ -359,51 +401,79 @@ __global__ void __launch_bounds__(kThreads) nvfp4_scoped_kernel(
   // groups with no rows still get their (zero) decode scale
   if (blockIdx.x == 0)
     for (int g = threadIdx.x; g < Gs; g += blockDim.x)
-      if (sm.aoffs[g + 1] == sm.aoffs[g]) s32[g] = 0.f;
+      if (aoffs[g + 1] == aoffs[g]) s32[g] = 0.f;
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t kt = (C / 16 + 3) / 4;
-  const uint64_t keep = policy_evict_last();    // first read: to be read again
-  const uint64_t drop = policy_evict_first();   // second read: last use
+  const int C32 = static_cast<int>(C);
+  const int kt = (C32 / 16 + 3) / 4;
 
-  while (true) {
-    __syncthreads();
-    if (threadIdx.x == 0) sm.ticket = static_cast<int64_t>(atomicAdd(ticket, 1ull));
-    __syncthreads();
-    const int64_t t = sm.ticket;
-    if (t >= total) break;
-    int lo = 0, hi = nseg - 1;                   // segment holding ticket t
+  // ---- control-lane helpers (thread 0 only)
+  auto amax_items = [&](int g) {
+    return static_cast<uint32_t>((aoffs[g + 1] - aoffs[g] + kItemRows - 1) / kItemRows);
+  };
+  auto publish = [&](int slot, int g, int64_t item, float amax) {
+    float senc, sdec;
+    nvfp4_scales(amax, senc, sdec);
+    sm.tsenc[slot] = senc;
+    if (item == 0) s32[g] = sdec;
+  };
+  // Takes the next ticket into `slot`; for an encode item whose group amax is
+  // already complete, also its S_enc (no waiting here).
+  auto take = [&](int slot) {
+    const int64_t t = static_cast<int64_t>(atomicAdd(ticket, 1ull));
+    sm.tk[slot] = t;
+    if (t >= total) return;
+    int lo = 0, hi = nseg - 1;                 // segment holding ticket t
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (sm.seg_start[mid] <= t) lo = mid; else hi = mid - 1;
     }
     const int g = sm.seg_info[lo] >> 1;
-    const bool enc = sm.seg_info[lo] & 1;
+    const int enc = sm.seg_info[lo] & 1;
     const int64_t item = t - sm.seg_start[lo];
-    if (!enc) {
-      // ---- amax item: rows [aoffs[g] + 32 item, +32) of scope group g
-      const int64_t r0 = sm.aoffs[g] + item * kItemRows;
-      const int64_t r1 = r0 + kItemRows < sm.aoffs[g + 1] ? r0 + kItemRows : sm.aoffs[g + 1];
-      float m = 0.f;
-      for (int64_t row = r0 + warp; row < r1; row += kWarps)
-        m = fmaxf(m, row_amax_stream<true>(x + row * ld, C, lane, keep));
-      if (lane == 0) sm.red[warp] = m;
-      __syncthreads();
+    sm.tg[slot] = g;
+    sm.tenc[slot] = enc;
+    sm.titem[slot] = item;
+    sm.tready[slot] = 0;
+    if (enc && ld_acquire_u32(done + g) >= amax_items(g)) {
+      publish(slot, g, item, __uint_as_float(ld_relaxed_u32(amax_bits + g)));
+      sm.tready[slot] = 1;
+    }
+  };
+  // Folds a finished amax item's maximum into its group, then counts it done
+  // (the fence orders the two for the encode side's acquire load).
+  auto release = [&](int g, int rslot) {
+    float m = sm.red[rslot][0];
+#pragma unroll
+    for (int i = 1; i < kDataWarps; ++i) m = fmaxf(m, sm.red[rslot][i]);
+    atomicMax(amax_bits + g, __float_as_uint(m));
+    __threadfence();
+    atomicAdd(done + g, 1u);
+  };
+
+  const uint64_t keep = policy_evict_last();    // first read: to be read again
+  const uint64_t drop = policy_evict_first();   // second read: last use
+  int pend_g = -1, pend_slot = 0;               // thread 0: amax item not yet released
+
+  if (threadIdx.x == 0) take(0);
+  __syncthreads();
+  for (int it = 0;; ++it) {
+    const int slot = it & 1;
+    if (sm.tk[slot] >= total) break;
+    const int g = sm.tg[slot];
+    const bool enc = sm.tenc[slot] != 0;
+    const int64_t item = sm.titem[slot];
+    if (enc && !sm.tready[slot]) {
+      // rare: the group's amax was not complete when the ticket was taken
       if (threadIdx.x == 0) {
-        float bm = sm.red[0];
-        for (int i = 1; i < kWarps; ++i) bm = fmaxf(bm, sm.red[i]);
-        atomicMax(amax_bits + g, __float_as_uint(bm));
-        __threadfence();                          // the maximum is visible before the count
-        atomicAdd(done + g, 1u);
-      }
-    } else {
-      // ---- encode item: scale rows [apref[g] + 32 item, +32) of scope group g
-      if (threadIdx.x == 0) {
-        const uint32_t need = static_cast<uint32_t>((sm.aoffs[g + 1] - sm.aoffs[g] + kItemRows - 1) / kItemRows);
-        const volatile uint32_t* dv = done + g;
-        if (*dv < need) {
+        if (pend_g >= 0) {
+          release(pend_g, pend_slot);
+          pend_g = -1;
+        }
+        const uint32_t need = amax_items(g);
+        if (ld_acquire_u32(done + g) < need) {
           const uint64_t t0 = globaltimer();
-          while (*dv < need) {
+          while (ld_acquire_u32(done + g) < need) {
             if (globaltimer() - t0 > kWaitLimitNs) {
               atomicCAS(err, 0, kErrWaitConsumer);
               break;
@@ -411,19 +481,48 @@ __global__ void __launch_bounds__(kThreads) nvfp4_scoped_kernel(
             __nanosleep(64);
           }
         }
-        __threadfence();
-        sm.amax = __uint_as_float(*reinterpret_cast<volatile uint32_t*>(amax_bits + g));
+        publish(slot, g, item, __uint_as_float(ld_relaxed_u32(amax_bits + g)));
       }
       __syncthreads();
-      float senc, sdec;
-      nvfp4_scales(sm.amax, senc, sdec);
-      if (item == 0 && threadIdx.x == 0) s32[g] = sdec;
-      const int64_t s0 = sm.apref[g] + item * kItemRows;
-      for (int64_t sr = s0 + warp; sr < s0 + kItemRows; sr += kWarps)
-        process_row<kCh, true>(x, data_row(sm.gs, grouped, G, R, sr), C, ld, false, senc, sm.tab, q, sblk, s32, sr,
-                               kt, lane, drop);
     }
+    if (warp == 0) {
+      if (lane == 0) {
+        if (pend_g >= 0) {
+          release(pend_g, pend_slot);
+          pend_g = -1;
+        }
+        take(slot ^ 1);
+        if (!enc) {
+          pend_g = g;
+          pend_slot = slot;
+        }
+      }
+    } else if (!enc) {
+      // ---- amax item: rows [aoffs[g] + 32 item, +32) of scope group g
+      const int dw = warp - 1;
+      const int64_t r0 = aoffs[g] + item * kItemRows;
+      const int64_t r1 = r0 + kItemRows < aoffs[g + 1] ? r0 + kItemRows : aoffs[g + 1];
+      uint32_t m = 0;
+      for (int64_t row = r0 + dw; row < r1; row += kDataWarps)
+        m = amax2(m, row_absmax_lane<kCh, true>(x + row * ld, C32, lane, keep));
+      const float wm = warp_max(abs_halves_max(m));
+      if (lane == 0) sm.red[slot][dw] = wm;
+    } else {
+      // ---- encode item: scale rows [apref[g] + 32 item, +32) of scope group g
+      const int dw = warp - 1;
+      const float senc = sm.tsenc[slot];
+      const int64_t s0 = apref[g] + item * kItemRows;
+      const int64_t grows = aoffs[g + 1] - aoffs[g];
+      for (int64_t sr = s0 + dw; sr < s0 + kItemRows; sr += kDataWarps) {
+        // scope groups are the layout groups: the data row follows directly
+        const int64_t local = sr - apref[g];
+        const int64_t row = scope == 1 ? (local < grows ? aoffs[g] + local : -1) : data_row(sm.gs, grouped, G, R, sr);
+        process_row<kCh, true>(x, row, C32, ld, false, senc, sm.tab, q, sblk, s32, sr, kt, lane, drop);
+      }
+    }
+    __syncthreads();
   }
+  if (threadIdx.x == 0 && pend_g >= 0) release(pend_g, pend_slot);
 }
 
 template <int kCh>
@@ -448,11 +547,11 @@ cudaError_t launch_scoped(int sm_count, cudaStream_t stream, const uint16_t* x, 
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kScopedThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
-  k<<<static_cast<unsigned>(sm_count * per_sm), kThreads, smem, stream>>>(x, R, C, ld, scope, offs, G, q, sblk,
-                                                                         s32, scratch, err);
+  k<<<static_cast<unsigned>(sm_count * per_sm), kScopedThreads, smem, stream>>>(x, R, C, ld, scope, offs, G, q,
+                                                                               sblk, s32, scratch, err);
   return cudaGetLastError();
 }
 
