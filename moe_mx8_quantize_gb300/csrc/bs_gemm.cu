@@ -16,10 +16,15 @@
 //   C[m, n] (+)= A32[m] * B32[n or group] * sum_k A^[m, k] B^[n, k]
 //
 // Structure (one CTA per SM, persistent over 128 x BN output tiles):
-//   warp 0      : TMA producer -- A (128 rows) and B (BN rows) tiles of 128
+//   producers   : TMA loads of A (128 rows) and B (BN rows) tiles of 128
 //                 bytes of K with the 128-byte swizzle, plus the matching
 //                 512-byte scale tiles, into a ring of shared-memory stages
-//                 guarded by mbarriers;
+//                 guarded by mbarriers.  One thread of warp 0 issues A and the
+//                 scale tiles, one thread in each of BN/128 further warps one
+//                 128-row box of B: a single issuing thread moves at most
+//                 about 50 GB/s per SM on this GPU, several in separate warps
+//                 move several times that, so the operand stream of a stage
+//                 is split over 1 + BN/128 issuers;
 //   warp 1      : allocates tensor memory; one thread copies each stage's
 //                 scale tiles into tensor memory (tcgen05.cp) and issues the
 //                 block-scaled MMAs (M = 128, N = BN) into an FP32 accumulator
@@ -90,7 +95,9 @@ struct Layout {
   static constexpr uint32_t kSfColsPerStage = kSfaCols + kSfbCols;
   static constexpr uint32_t kAccCols = kAccBufs * kBN;
   static constexpr int kEpiWarps = kBN / 32;                         // 128 columns per warp
-  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int kProducers = 1 + kBRow128;                    // warp 0 + one warp per B box
+  // warp 0 producer, warp 1 MMA, warps 2 .. 1 + kEpiWarps epilogue, then the B producers
+  static constexpr int kThreads = 64 + 32 * kEpiWarps + 32 * kBRow128;
   static_assert(kStages >= 3, "pipeline too shallow");
   static_assert(kAccCols + kStages * kSfColsPerStage <= kTmemCols, "tensor memory overflow");
 };
@@ -189,7 +196,7 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
     prefetch_tmap(&tmap_b);
     prefetch_tmap(&tmap_c);
     for (int s = 0; s < L::kStages; ++s) {
-      mbar_init(smem_u32(&sm.full[s]), 1);
+      mbar_init(smem_u32(&sm.full[s]), L::kProducers);
       mbar_init(smem_u32(&sm.empty[s]), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -222,8 +229,10 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
   const int64_t sf_kt = (K / F::kBlock + 3) / 4;          // scale tiles along K
   const int G = args.G;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  // producer index: 0 = warp 0 (A and the scale tiles), 1 + h = B box h
+  const int prod = warp == 0 ? 0 : (warp >= 2 + L::kEpiWarps ? warp - 1 - L::kEpiWarps : -1);
+  if (prod >= 0) {
+    // ------------------------------------------------------------ producers
     if (lane == 0) {
       int it = 0;
       bool ok = true;
@@ -245,22 +254,26 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
             ok = false;
             break;
           }
-          const int64_t sf0 = static_cast<int64_t>(kt) * F::kSfTiles;
-          const int nsf = static_cast<int>(sf_kt - sf0 < F::kSfTiles ? sf_kt - sf0 : F::kSfTiles);
           const uint32_t full = smem_u32(&sm.full[s]);
-          mbar_arrive_expect_tx(full, kTileABytes + L::kTileBBytes + (1 + L::kBRow128) * nsf * 512);
-          tma_load_2d(smem_u32(sm.a[s]), &tmap_a, kt * kKBytes, static_cast<int32_t>(tc.a_row0), full);
-          bulk_load(smem_u32(sm.sfa[s]), sfa_src + sf0 * 512, nsf * 512, full);
-          // B in 128-row boxes (a 128-row box is 16 KB; boxes stack in shared memory)
+          if (prod == 0) {
+            const int64_t sf0 = static_cast<int64_t>(kt) * F::kSfTiles;
+            const int nsf = static_cast<int>(sf_kt - sf0 < F::kSfTiles ? sf_kt - sf0 : F::kSfTiles);
+            mbar_arrive_expect_tx(full, kTileABytes + (1 + L::kBRow128) * nsf * 512);
+            tma_load_2d(smem_u32(sm.a[s]), &tmap_a, kt * kKBytes, static_cast<int32_t>(tc.a_row0), full);
+            bulk_load(smem_u32(sm.sfa[s]), sfa_src + sf0 * 512, nsf * 512, full);
 #pragma unroll
-          for (int h = 0; h < L::kBRow128; ++h) {
+            for (int h = 0; h < L::kBRow128; ++h)
+              bulk_load(smem_u32(sm.sfb[s]) + h * F::kSfTiles * 512, sfb_src[h] + sf0 * 512, nsf * 512, full);
+          } else {
+            // B in 128-row boxes (a 128-row box is 16 KB; boxes stack in shared memory)
+            const int h = prod - 1;
+            mbar_arrive_expect_tx(full, 16384);
             if (kGrouped)
               tma_load_3d(smem_u32(sm.b[s]) + h * 16384, &tmap_b, kt * kKBytes,
                           static_cast<int32_t>(tc.n0 + h * 128), tc.g, full);
             else
               tma_load_2d(smem_u32(sm.b[s]) + h * 16384, &tmap_b, kt * kKBytes,
                           static_cast<int32_t>(tc.n0 + h * 128), full);
-            bulk_load(smem_u32(sm.sfb[s]) + h * F::kSfTiles * 512, sfb_src[h] + sf0 * 512, nsf * 512, full);
           }
         }
       }
@@ -333,7 +346,7 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
       mbar_wait(smem_u32(&sm.drain), 0, err, kErrWaitTeardown, nullptr, 100000000ull);
     }
   } else {
-    // ------------------------------------------------------------ epilogue
+    // ------------------------------------------------------------ epilogue (warps 2 .. 1 + kEpiWarps)
     const int ew = warp - 2;
     const int quarter = warp & 3;              // tcgen05.ld lane quarter of this warp
     const int col0 = (ew / 4) * 128;           // this warp's 128 accumulator columns
