@@ -329,6 +329,8 @@ struct ScopedSmem {
   int32_t tready[2];                  // encode item whose group amax is known
   float tsenc[2];                     // ... and its S_enc
   float red[2][kDataWarps];           // amax items: per-warp maxima
+  uint64_t filled[2];                 // slot holds a new item (control lane arrives)
+  uint64_t consumed[2];               // every data warp finished the slot's item
 };
 
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
@@ -344,12 +346,14 @@ __device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
 
 // Ordering of the work items and the deadlock argument.  Tickets are taken in
 // order from one counter.  The amax items of a group all precede the group's
-// encode items in ticket order.  A data warp never waits.  The control warp
-// releases the amax of the block's previous item before anything else in an
-// iteration, and it only blocks (the rare case of an encode item whose group
-// was not complete when its ticket was taken) after that release, so every
-// amax item taken is released once its block finishes it, whatever the other
-// blocks wait for.  The wait is bounded anyway (error word on timeout).
+// encode items in ticket order.  A data warp waits only for its own control
+// lane to fill the next slot.  The control lane releases a slot's amax item
+// as soon as the data warps have finished it.  It only blocks on other blocks
+// in the rare case of an encode item whose group amax was not complete when
+// its ticket was taken, and before that it releases the one amax item the
+// block may still hold.  So every amax item taken is released once its block
+// finishes it, whatever the other blocks wait for.  Every wait is bounded
+// anyway (error word on timeout).
 template <int kCh>
 __global__ void __launch_bounds__(kScopedThreads, kCh >= 8 || kCh == 0 ? 1 : 4) nvfp4_scoped_kernel(
     const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ld, int scope,
@@ -364,6 +368,13 @@ __global__ void __launch_bounds__(kScopedThreads, kCh >= 8 || kCh == 0 ? 1 : 4) 
   unsigned long long* ticket = reinterpret_cast<unsigned long long*>(scratch + 2 * scratch_gp(Gs));
 
   init_scale_table(sm.tab);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&sm.filled[i]), 1);
+      mbar_init(smem_u32(&sm.consumed[i]), kDataWarps);
+    }
+    fence_barrier_init();
+  }
   if (grouped) load_group_prefix(sm.gs, offs, G);
   __syncthreads();
   const int64_t TP = grouped ? sm.gs.pref[G] : (R + 127) / 128 * 128;
@@ -453,23 +464,26 @@ __global__ void __launch_bounds__(kScopedThreads, kCh >= 8 || kCh == 0 ? 1 : 4) 
 
   const uint64_t keep = policy_evict_last();    // first read: to be read again
   const uint64_t drop = policy_evict_first();   // second read: last use
-  int pend_g = -1, pend_slot = 0;               // thread 0: amax item not yet released
 
-  if (threadIdx.x == 0) take(0);
-  __syncthreads();
-  for (int it = 0;; ++it) {
-    const int slot = it & 1;
-    if (sm.tk[slot] >= total) break;
-    const int g = sm.tg[slot];
-    const bool enc = sm.tenc[slot] != 0;
-    const int64_t item = sm.titem[slot];
-    if (enc && !sm.tready[slot]) {
-      // rare: the group's amax was not complete when the ticket was taken
-      if (threadIdx.x == 0) {
-        if (pend_g >= 0) {
-          release(pend_g, pend_slot);
-          pend_g = -1;
+  // Items alternate between two slots.  The control lane fills a slot
+  // (filled[slot]); the data warps each take their share and report
+  // (consumed[slot]); the control lane then releases the slot's amax item, if
+  // it was one, and refills the slot two items ahead.  No block-wide barrier:
+  // a data warp moves on to the next item as soon as its own share is done.
+  if (warp == 0) {
+    if (lane == 0) {
+      bool rel[2] = {false, false};   // slot's amax item already released
+      // For an encode item whose group amax was not complete when its ticket
+      // was taken: release the other slot's amax item first (it is being worked
+      // on, and the data warps never wait on other blocks), then wait.
+      auto resolve = [&](int slot, int other_it) {
+        const int other = slot ^ 1;
+        if (other_it >= 0 && sm.tk[other] < total && !sm.tenc[other] && !rel[other]) {
+          mbar_wait(smem_u32(&sm.consumed[other]), (other_it >> 1) & 1, err, kErrWaitConsumer, nullptr);
+          release(sm.tg[other], other);
+          rel[other] = true;
         }
+        const int g = sm.tg[slot];
         const uint32_t need = amax_items(g);
         if (ld_acquire_u32(done + g) < need) {
           const uint64_t t0 = globaltimer();
@@ -481,48 +495,57 @@ __global__ void __launch_bounds__(kScopedThreads, kCh >= 8 || kCh == 0 ? 1 : 4) 
             __nanosleep(64);
           }
         }
-        publish(slot, g, item, __uint_as_float(ld_relaxed_u32(amax_bits + g)));
-      }
-      __syncthreads();
-    }
-    if (warp == 0) {
-      if (lane == 0) {
-        if (pend_g >= 0) {
-          release(pend_g, pend_slot);
-          pend_g = -1;
-        }
-        take(slot ^ 1);
-        if (!enc) {
-          pend_g = g;
-          pend_slot = slot;
-        }
-      }
-    } else if (!enc) {
-      // ---- amax item: rows [aoffs[g] + 32 item, +32) of scope group g
-      const int dw = warp - 1;
-      const int64_t r0 = aoffs[g] + item * kItemRows;
-      const int64_t r1 = r0 + kItemRows < aoffs[g + 1] ? r0 + kItemRows : aoffs[g + 1];
-      uint32_t m = 0;
-      for (int64_t row = r0 + dw; row < r1; row += kDataWarps)
-        m = amax2(m, row_absmax_lane<kCh, true>(x + row * ld, C32, lane, keep));
-      const float wm = warp_max(abs_halves_max(m));
-      if (lane == 0) sm.red[slot][dw] = wm;
-    } else {
-      // ---- encode item: scale rows [apref[g] + 32 item, +32) of scope group g
-      const int dw = warp - 1;
-      const float senc = sm.tsenc[slot];
-      const int64_t s0 = apref[g] + item * kItemRows;
-      const int64_t grows = aoffs[g + 1] - aoffs[g];
-      for (int64_t sr = s0 + dw; sr < s0 + kItemRows; sr += kDataWarps) {
-        // scope groups are the layout groups: the data row follows directly
-        const int64_t local = sr - apref[g];
-        const int64_t row = scope == 1 ? (local < grows ? aoffs[g] + local : -1) : data_row(sm.gs, grouped, G, R, sr);
-        process_row<kCh, true>(x, row, C32, ld, false, senc, sm.tab, q, sblk, s32, sr, kt, lane, drop);
+        publish(slot, g, sm.titem[slot], __uint_as_float(ld_relaxed_u32(amax_bits + g)));
+      };
+      auto fill = [&](int slot, int other_it) {
+        take(slot);
+        if (sm.tk[slot] < total && sm.tenc[slot] && !sm.tready[slot]) resolve(slot, other_it);
+        mbar_arrive(smem_u32(&sm.filled[slot]));
+      };
+      fill(0, -1);
+      fill(1, 0);
+      for (int it = 0;; ++it) {
+        const int slot = it & 1;
+        if (sm.tk[slot] >= total) break;
+        mbar_wait(smem_u32(&sm.consumed[slot]), (it >> 1) & 1, err, kErrWaitConsumer, nullptr);
+        if (!sm.tenc[slot] && !rel[slot]) release(sm.tg[slot], slot);
+        rel[slot] = false;
+        fill(slot, it + 1);
       }
     }
-    __syncthreads();
+  } else {
+    const int dw = warp - 1;
+    for (int it = 0;; ++it) {
+      const int slot = it & 1;
+      if (!mbar_wait(smem_u32(&sm.filled[slot]), (it >> 1) & 1, err, kErrWaitConsumer, nullptr)) break;
+      if (sm.tk[slot] >= total) break;
+      const int g = sm.tg[slot];
+      const int64_t item = sm.titem[slot];
+      if (!sm.tenc[slot]) {
+        // ---- amax item: rows [aoffs[g] + 32 item, +32) of scope group g
+        const int64_t r0 = aoffs[g] + item * kItemRows;
+        const int64_t r1 = r0 + kItemRows < aoffs[g + 1] ? r0 + kItemRows : aoffs[g + 1];
+        uint32_t m = 0;
+        for (int64_t row = r0 + dw; row < r1; row += kDataWarps)
+          m = amax2(m, row_absmax_lane<kCh, true>(x + row * ld, C32, lane, keep));
+        const float wm = warp_max(abs_halves_max(m));
+        if (lane == 0) sm.red[slot][dw] = wm;
+      } else {
+        // ---- encode item: scale rows [apref[g] + 32 item, +32) of scope group g
+        const float senc = sm.tsenc[slot];
+        const int64_t s0 = apref[g] + item * kItemRows;
+        const int64_t grows = aoffs[g + 1] - aoffs[g];
+        for (int64_t sr = s0 + dw; sr < s0 + kItemRows; sr += kDataWarps) {
+          // scope groups are the layout groups: the data row follows directly
+          const int64_t local = sr - apref[g];
+          const int64_t row = scope == 1 ? (local < grows ? aoffs[g] + local : -1) : data_row(sm.gs, grouped, G, R, sr);
+          process_row<kCh, true>(x, row, C32, ld, false, senc, sm.tab, q, sblk, s32, sr, kt, lane, drop);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.consumed[slot]));
+    }
   }
-  if (threadIdx.x == 0 && pend_g >= 0) release(pend_g, pend_slot);
 }
 
 template <int kCh>
