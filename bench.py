@@ -140,7 +140,10 @@ class Step:
         self.W_d = moe["W_d"].reshape(E * H, F).contiguous()
         self.e_offs_gu = torch.arange(E + 1, device=device, dtype=torch.int64) * (2 * F)
         self.e_offs_d = torch.arange(E + 1, device=device, dtype=torch.int64) * H
+        # one workspace per concurrent branch of the step (error word + scratch)
         self.ws = mx.new_workspace(max(E, 1), device)
+        self.ws_b = mx.new_workspace(max(E, 1), device)
+        self.ws_c = mx.new_workspace(max(E, 1), device)
         u8 = lambda n: torch.empty(max(n, 16), dtype=torch.uint8, device=device)
         f32 = lambda n: torch.empty(max(n, 1), dtype=torch.float32, device=device)
         sb8 = lambda r, c: u8(mx.scale_bytes(mx.FMT_MXFP8, r, c))
@@ -204,7 +207,7 @@ class Step:
         library kernels on the current stream."""
         mx = self.mx
         RC = mx.ROWWISE | mx.COLWISE
-        ws = self.ws
+        ws, ws_b, ws_c = self.ws, self.ws_b, self.ws_c
         return [
             ("mxfp8_quant_rc X", lambda: mx.mx8_quantize_into(self.X, self.Xr, self.SXr, self.Xc, self.SXc, RC, ws)),
             ("mxfp8_quant_rc W", lambda: mx.mx8_quantize_into(self.W, self.Wr, self.SWr, self.Wc, self.SWc, RC, ws)),
@@ -214,22 +217,83 @@ class Step:
             ("mxfp8_gemm Wgrad", lambda: mx.bs_gemm_into(mx.FMT_MXFP8, self.dYc, self.SdYc, self.Xc, self.SXc, self.T, self.dW, ws=ws)),
             ("dequant_mxfp8 X", lambda: mx.dequantize_into(mx.FMT_MXFP8, self.Xr, self.SXr, self.Xhat)),
             ("dequant_mxfp8 W", lambda: mx.dequantize_into(mx.FMT_MXFP8, self.Wr, self.SWr, self.What)),
-            ("nvfp4_quant_token X", lambda: mx.nvfp4_quantize_into(self.X, self.X4, self.SX4, self.X432, mx.SCOPE_TOKEN, None, ws)),
-            ("nvfp4_quant_tensor W", lambda: mx.nvfp4_quantize_into(self.W, self.W4, self.SW4, self.W432, mx.SCOPE_TENSOR, None, ws)),
+            ("nvfp4_quant_token X", lambda: mx.nvfp4_quantize_into(self.X, self.X4, self.SX4, self.X432, mx.SCOPE_TOKEN, None, ws_b)),
+            ("nvfp4_quant_tensor W", lambda: mx.nvfp4_quantize_into(self.W, self.W4, self.SW4, self.W432, mx.SCOPE_TENSOR, None, ws_b)),
             ("nvfp4_gemm Fprop", lambda: mx.bs_gemm_into(mx.FMT_NVFP4, self.X4, self.SX4, self.W4, self.SW4, self.H_, self.Y4,
-                                                         self.X432, self.W432, ws=ws, a32_mode=mx.S32_ROW, b32_mode=mx.S32_TENSOR)),
-            ("nvfp4_quant_token moe_act", lambda: mx.nvfp4_quantize_into(self.A_moe, self.A4, self.SA4, self.A432, mx.SCOPE_TOKEN, self.offs, ws)),
+                                                         self.X432, self.W432, ws=ws_b, a32_mode=mx.S32_ROW, b32_mode=mx.S32_TENSOR)),
+            ("nvfp4_quant_token moe_act", lambda: mx.nvfp4_quantize_into(self.A_moe, self.A4, self.SA4, self.A432, mx.SCOPE_TOKEN, self.offs, ws_c)),
             ("nvfp4_quant_expert W_gu", lambda: mx.nvfp4_quantize_into(self.W_gu, self.Wgu4.view(-1, self.H_ // 2), self.SWgu4, self.Wgu432,
-                                                                       mx.SCOPE_GROUP, self.e_offs_gu, ws)),
+                                                                       mx.SCOPE_GROUP, self.e_offs_gu, ws_c)),
             ("nvfp4_quant_expert W_d", lambda: mx.nvfp4_quantize_into(self.W_d, self.Wd4.view(-1, self.F // 2), self.SWd4, self.Wd432,
-                                                                      mx.SCOPE_GROUP, self.e_offs_d, ws)),
+                                                                      mx.SCOPE_GROUP, self.e_offs_d, ws_c)),
             ("nvfp4_grouped_gemm gate_up", lambda: mx.bs_grouped_gemm_into(mx.FMT_NVFP4, self.offs, self.A4, self.SA4, self.Wgu4, self.SWgu4,
-                                                                            self.H_, self.GU, self.A432, self.Wgu432, ws)),
+                                                                            self.H_, self.GU, self.A432, self.Wgu432, ws_c)),
             ("swiglu", lambda: mx.swiglu_into(self.GU, self.Hs)),
-            ("nvfp4_quant_token moe_h", lambda: mx.nvfp4_quantize_into(self.Hs, self.H4, self.SH4, self.H432, mx.SCOPE_TOKEN, self.offs, ws)),
+            ("nvfp4_quant_token moe_h", lambda: mx.nvfp4_quantize_into(self.Hs, self.H4, self.SH4, self.H432, mx.SCOPE_TOKEN, self.offs, ws_c)),
             ("nvfp4_grouped_gemm down", lambda: mx.bs_grouped_gemm_into(mx.FMT_NVFP4, self.offs, self.H4, self.SH4, self.Wd4, self.SWd4,
-                                                                         self.F, self.OUT, self.H432, self.Wd432, ws)),
+                                                                         self.F, self.OUT, self.H432, self.Wd432, ws_c)),
         ]
+
+    # The step's three independent chains: the MXFP8 linear layer, the NVFP4
+    # linear Fprop and the NVFP4 MoE layer.  The end-to-end measurement runs
+    # each on its own stream (its own workspace), so one chain's host copies
+    # overlap another's kernels; within a chain the order is the data order
+    # above.
+    BRANCHES = (
+        ("mxfp8_quant_rc X", "mxfp8_quant_rc W", "mxfp8_quant_rc dY", "mxfp8_gemm Fprop", "mxfp8_gemm Dgrad",
+         "mxfp8_gemm Wgrad", "dequant_mxfp8 X", "dequant_mxfp8 W"),
+        ("nvfp4_quant_token X", "nvfp4_quant_tensor W", "nvfp4_gemm Fprop"),
+        ("nvfp4_quant_token moe_act", "nvfp4_quant_expert W_gu", "nvfp4_quant_expert W_d",
+         "nvfp4_grouped_gemm gate_up", "swiglu", "nvfp4_quant_token moe_h", "nvfp4_grouped_gemm down"),
+    )
+
+    def workspaces(self):
+        return (self.ws, self.ws_b, self.ws_c)
+
+    def run_concurrent(self, streams, io=False):
+        """Launches the step as its three branches on `streams` (the first is
+        the caller's current stream), forked from and joined back into it.  With
+        io, each branch first copies its inputs from pinned host memory and last
+        copies its results back (the e2e measurement)."""
+        torch = self.torch
+        fns = dict(self.launches())
+        s0 = streams[0]
+        fork = torch.cuda.Event()
+        fork.record(s0)
+        done = []
+        for b, labels in enumerate(self.BRANCHES):
+            st = streams[b]
+            with torch.cuda.stream(st):
+                if b > 0:
+                    st.wait_event(fork)
+                if io:
+                    for d, h in self.io_in[b]:
+                        d.copy_(h, non_blocking=True)
+                    if b == 0:               # X is also an input of branch 1
+                        self.x_ready.record(st)
+                if io and b == 1:
+                    st.wait_event(self.x_ready)
+                for lab in labels:
+                    fns[lab]()
+                if io:
+                    for d, h in self.io_out[b]:
+                        h.copy_(d, non_blocking=True)
+                if b > 0:
+                    e = torch.cuda.Event()
+                    e.record(st)
+                    done.append(e)
+        for e in done:
+            s0.wait_event(e)
+
+    def setup_io(self):
+        """Pinned host copies of each branch's per-step inputs and results."""
+        torch = self.torch
+        pin = lambda t: t.detach().cpu().pin_memory()
+        self.io_in = ([(self.X, pin(self.X)), (self.dY, pin(self.dY))], [], [(self.A_moe, pin(self.A_moe))])
+        empty = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        self.io_out = ([(self.Y, empty(self.Y)), (self.dX, empty(self.dX))], [(self.Y4, empty(self.Y4))],
+                       [(self.OUT, empty(self.OUT))])
+        self.x_ready = torch.cuda.Event()
 
     # kernels each label launches (amax pass + quantize for group/tensor scope)
     KERNELS_PER_LABEL = {}   # every label is one kernel launch (plus, for group/tensor scope, a memset)
@@ -296,12 +360,21 @@ def run_gpu(args):
         for _, fn in launches:
             fn()
 
+    def check_errors(when):
+        for ws in step.workspaces():
+            st = mx.check_device_error(ws)
+            if st != mx.OK:
+                raise RuntimeError(f"device error {when}: {mx.status_string(st)}")
+
+    assert sorted(l for b in step.BRANCHES for l in b) == sorted(l for l, _ in launches)
     for _ in range(args.warmup):
         eager_step()
     torch.cuda.synchronize()
-    st = mx.check_device_error(step.ws)
-    if st != mx.OK:
-        raise RuntimeError(f"device error after warm-up: {mx.status_string(st)}")
+    check_errors("after warm-up")
+    # the step as a CUDA graph, its launches in order on one stream.  (Capturing
+    # the three independent branches on three streams measured slower: the
+    # persistent kernels already fill the GPU, and the group-scope quantizer's
+    # second read loses its L2 residency to the concurrent branches.)
     graph = torch.cuda.CUDAGraph()
     side = torch.cuda.Stream()
     side.wait_stream(stream)
@@ -329,9 +402,7 @@ def run_gpu(args):
     barrier()
     clocks = sampler.stop()
     total_ms = t0.elapsed_time(t1)
-    st = mx.check_device_error(step.ws)
-    if st != mx.OK:
-        raise RuntimeError(f"device error in timed region: {mx.status_string(st)}")
+    check_errors("in timed region")
     t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
     if world > 1:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -412,42 +483,28 @@ def run_gpu(args):
 def run_e2e(step, args, world, dev, graph=None):
     """Same step through the public API with host buffers: every step copies
     its inputs (X, dY, dispatched MoE activations) from pinned host memory
-    and reads its results (Y, dX, MoE output) back; weights stay resident."""
+    and reads its results (Y, dX, NVFP4 Y, MoE output) back; weights stay
+    resident.  The three branches run on their own streams, each copying its
+    own inputs in and results out, so one branch's copies overlap another's
+    kernels."""
     import torch
-    h_in = [(t, t.detach().cpu().pin_memory()) for t in (step.X, step.dY, step.A_moe)]
-    h_out = [(t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True)) for t in (step.Y, step.dX, step.OUT)]
-    launches = step.launches()
-    stream = torch.cuda.current_stream()
+    step.setup_io()
+    streams = [torch.cuda.current_stream()] + [torch.cuda.Stream() for _ in step.BRANCHES[1:]]
+    stream = streams[0]
     K = max(3, min(args.steps, 50))
-
-    def compute():
-        if graph is not None:
-            graph.replay()
-        else:
-            for _, fn in launches:
-                fn()
-
     for _ in range(2):
-        for d, h in h_in:
-            d.copy_(h, non_blocking=True)
-        compute()
-        for d, h in h_out:
-            h.copy_(d, non_blocking=True)
+        step.run_concurrent(streams, io=True)
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
     for _ in range(K):
-        for d, h in h_in:
-            d.copy_(h, non_blocking=True)
-        compute()
-        for d, h in h_out:
-            h.copy_(d, non_blocking=True)
+        step.run_concurrent(streams, io=True)
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / K
-    bi = sum(h.numel() * h.element_size() for _, h in h_in)
-    bo = sum(h.numel() * h.element_size() for _, h in h_out)
+    bi = sum(h.numel() * h.element_size() for br in step.io_in for _, h in br)
+    bo = sum(h.numel() * h.element_size() for br in step.io_out for _, h in br)
     return {"value": round(world * step.gemm_flops() / (ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "steps": K, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
 

@@ -17,7 +17,9 @@
 //   colwise : one thread per (column pair, 32-row block), 32 u32 smem reads
 //             down the column pair, 32-byte stores into the transposed copy;
 // and both 128x4 scale tiles (exactly one 512-byte tensor-core tile each),
-// staged in shared memory and written with 16-byte stores.
+// staged in shared memory and written with 16-byte stores.  |x| maxima are
+// taken two bf16 values per instruction and the products x * 2^-e two per
+// instruction.
 #include "device.cuh"
 #include "kernels.h"
 
@@ -120,19 +122,19 @@ __global__ void __launch_bounds__(kThreads) mxfp8_quant_kernel(
       for (int pass = 0; pass < kTile / 16; ++pass) {
         const int lr = pass * 16 + (tid >> 4);
         const uint4 w = *reinterpret_cast<const uint4*>(tile + lr * (kTile * 2) + cchunk * 16);
-        float v[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
-                      bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
-        float amax = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        // |x| maxima two bf16 values per instruction, then the 4-thread block maximum
+        float amax = abs_halves_max(amax2(amax2(w.x, w.y), amax2(w.z, w.w)));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
         const int e = mx_block_exp(amax);
-        const float sc = exp2_neg(e);
-        uint32_t p0 = cvt_e4m3x2(__fmul_rn(v[0], sc), __fmul_rn(v[1], sc)) |
-                      (static_cast<uint32_t>(cvt_e4m3x2(__fmul_rn(v[2], sc), __fmul_rn(v[3], sc))) << 16);
-        uint32_t p1 = cvt_e4m3x2(__fmul_rn(v[4], sc), __fmul_rn(v[5], sc)) |
-                      (static_cast<uint32_t>(cvt_e4m3x2(__fmul_rn(v[6], sc), __fmul_rn(v[7], sc))) << 16);
+        const uint64_t sc = f32x2_splat(exp2_neg(e));
+        float v[8];                                  // x * 2^-e, two products per instruction
+        mul_bf16x2(w.x, sc, v[0], v[1]);
+        mul_bf16x2(w.y, sc, v[2], v[3]);
+        mul_bf16x2(w.z, sc, v[4], v[5]);
+        mul_bf16x2(w.w, sc, v[6], v[7]);
+        uint32_t p0 = cvt_e4m3x2(v[0], v[1]) | (static_cast<uint32_t>(cvt_e4m3x2(v[2], v[3])) << 16);
+        uint32_t p1 = cvt_e4m3x2(v[4], v[5]) | (static_cast<uint32_t>(cvt_e4m3x2(v[6], v[7])) << 16);
         const int64_t gr = r0 + lr, gc = c0 + cchunk * 8;
         if (gr < R && gc < C)
           *reinterpret_cast<uint2*>(q_row + gr * C + gc) = make_uint2(p0, p1);
@@ -147,22 +149,24 @@ __global__ void __launch_bounds__(kThreads) mxfp8_quant_kernel(
 #pragma unroll
       for (int i = 0; i < 32; ++i)
         w[i] = *reinterpret_cast<const uint32_t*>(tile + (rb * 32 + i) * (kTile * 2) + cp * 4);
-      float a0 = 0.f, a1 = 0.f;
+      // both columns' |x| maxima at once: low halves column 2cp, high halves 2cp + 1
+      uint32_t m = 0;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        a0 = fmaxf(a0, fabsf(bf16_lo(w[i])));
-        a1 = fmaxf(a1, fabsf(bf16_hi(w[i])));
-      }
+      for (int i = 0; i < 32; ++i) m = amax2(m, w[i]);
+      const float a0 = __uint_as_float((m << 16) & 0x7FFFFFFFu), a1 = __uint_as_float(m & 0x7FFF0000u);
       const int e0 = mx_block_exp(a0), e1 = mx_block_exp(a1);
-      const float s0 = exp2_neg(e0), s1 = exp2_neg(e1);
+      const uint64_t s0 = f32x2_splat(exp2_neg(e0)), s1 = f32x2_splat(exp2_neg(e1));
       uint32_t o0[8], o1[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const uint32_t x0 = w[4 * j], x1 = w[4 * j + 1], x2 = w[4 * j + 2], x3 = w[4 * j + 3];
-        o0[j] = cvt_e4m3x2(__fmul_rn(bf16_lo(x0), s0), __fmul_rn(bf16_lo(x1), s0)) |
-                (static_cast<uint32_t>(cvt_e4m3x2(__fmul_rn(bf16_lo(x2), s0), __fmul_rn(bf16_lo(x3), s0))) << 16);
-        o1[j] = cvt_e4m3x2(__fmul_rn(bf16_hi(x0), s1), __fmul_rn(bf16_hi(x1), s1)) |
-                (static_cast<uint32_t>(cvt_e4m3x2(__fmul_rn(bf16_hi(x2), s1), __fmul_rn(bf16_hi(x3), s1))) << 16);
+        float p[8];
+        mul_f32x2(bf16_lo(x0), bf16_lo(x1), s0, p[0], p[1]);
+        mul_f32x2(bf16_lo(x2), bf16_lo(x3), s0, p[2], p[3]);
+        mul_f32x2(bf16_hi(x0), bf16_hi(x1), s1, p[4], p[5]);
+        mul_f32x2(bf16_hi(x2), bf16_hi(x3), s1, p[6], p[7]);
+        o0[j] = cvt_e4m3x2(p[0], p[1]) | (static_cast<uint32_t>(cvt_e4m3x2(p[2], p[3])) << 16);
+        o1[j] = cvt_e4m3x2(p[4], p[5]) | (static_cast<uint32_t>(cvt_e4m3x2(p[6], p[7])) << 16);
       }
       const int64_t gc0 = c0 + 2 * cp, gr = r0 + rb * 32;
       if (gr < R) {

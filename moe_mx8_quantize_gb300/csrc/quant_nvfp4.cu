@@ -77,39 +77,12 @@ __device__ __forceinline__ void nvfp4_scales(float amax, float& senc, float& sde
   sdec = __fdiv_rn(amax, 2688.0f);
 }
 
-// Per bf16 half: the larger magnitude of a and b (its sign bit is not
-// meaningful; abs_halves_max clears it).
-__device__ __forceinline__ uint32_t amax2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
-// Packed |x| maxima of 16 bf16 values (two halves, sign bits not meaningful).
-__device__ __forceinline__ uint32_t absmax16(const uint4& a, const uint4& b) {
-  return amax2(amax2(amax2(a.x, a.y), amax2(a.z, a.w)), amax2(amax2(b.x, b.y), amax2(b.z, b.w)));
-}
-
-__device__ __forceinline__ float abs_halves_max(uint32_t w) {
-  return fmaxf(__uint_as_float((w << 16) & 0x7FFFFFFFu), __uint_as_float(w & 0x7FFF0000u));
-}
-
 // {E4M3 value, RN(1 / value)} per E4M3 code; {0, 0} for code 0.
 __device__ __forceinline__ void init_scale_table(float2* tab) {
   for (int c = threadIdx.x; c < 128; c += blockDim.x) {
     const float b = e4m3_to_f32(static_cast<uint32_t>(c));
     tab[c] = make_float2(b, c == 0 ? 0.f : __frcp_rn(b));
   }
-}
-
-// x * r (IEEE binary32) for the two bf16 values of w.
-__device__ __forceinline__ void mul_bf16x2(uint32_t w, uint64_t rr, float& lo, float& hi) {
-  asm("{\n\t.reg .b64 p, q;\n\t"
-      "mov.b64 p, {%2, %3};\n\t"
-      "mul.rn.f32x2 q, p, %4;\n\t"
-      "mov.b64 {%0, %1}, q;\n\t}"
-      : "=f"(lo), "=f"(hi)
-      : "r"(w << 16), "r"(w & 0xFFFF0000u), "l"(rr));
 }
 
 __device__ __forceinline__ float warp_max(float v) {
