@@ -215,6 +215,11 @@ mx8_status gemm_common_checks(int fmt, int64_t N, int64_t K, const uint8_t* A, c
   return MX8_OK;
 }
 
+// TMA swizzle of the GEMM operand boxes: one swizzle atom of kGemmKBytes.
+CUtensorMapSwizzle gemm_swizzle() {
+  return kGemmKBytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+}
+
 // Output map for the GEMM epilogue's bulk stores: [rows, N] with row stride
 // ldc, box 64 bytes x 32 rows.
 bool encode_output_map(CUtensorMap* map, void* C, int64_t rows, int64_t N, int64_t ldc, int out_dtype) {
@@ -256,12 +261,13 @@ extern "C" mx8_status bs_gemm(int fmt, int64_t M, int64_t N, int64_t K, const ui
 
   const uint64_t kbytes = fmt == MX8_FMT_MXFP8 ? K : K / 2;
   CUtensorMap ma, mb;
-  const uint32_t box[2] = {128, 128};
-  const uint32_t box_b[2] = {128, 128};   // B is loaded in 128-row boxes
+  // one swizzle atom of K per row, 128 rows per box (B is loaded in 128-row boxes)
+  const uint32_t box[2] = {kGemmKBytes, 128};
+  const uint32_t box_b[2] = {kGemmKBytes, 128};
   const uint64_t da[2] = {kbytes, static_cast<uint64_t>(M)}, sa[1] = {kbytes};
   const uint64_t db[2] = {kbytes, static_cast<uint64_t>(N)}, sb[1] = {kbytes};
-  if (!encode_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, A, da, sa, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, B, db, sb, box_b, CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!encode_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, A, da, sa, box, gemm_swizzle()) ||
+      !encode_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, B, db, sb, box_b, gemm_swizzle()))
     return MX8_ERR_CUDA;
   CUtensorMap mc;
   if (!encode_output_map(&mc, C, M, N, ldc, out_dtype)) return MX8_ERR_CUDA;
@@ -292,13 +298,13 @@ extern "C" mx8_status bs_grouped_gemm(int fmt, int num_groups, const int64_t* gr
 
   const uint64_t kbytes = fmt == MX8_FMT_MXFP8 ? K : K / 2;
   CUtensorMap ma, mb;
-  const uint32_t box2[2] = {128, 128};
+  const uint32_t box2[2] = {kGemmKBytes, 128};
   const uint64_t da[2] = {kbytes, static_cast<uint64_t>(total_rows)}, sa[1] = {kbytes};
-  const uint32_t box3[3] = {128, 128, 1};
+  const uint32_t box3[3] = {kGemmKBytes, 128, 1};
   const uint64_t db[3] = {kbytes, static_cast<uint64_t>(N), static_cast<uint64_t>(num_groups)};
   const uint64_t sb[2] = {kbytes, kbytes * static_cast<uint64_t>(N)};
-  if (!encode_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, A, da, sa, box2, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, B, db, sb, box3, CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!encode_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, A, da, sa, box2, gemm_swizzle()) ||
+      !encode_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, B, db, sb, box3, gemm_swizzle()))
     return MX8_ERR_CUDA;
   CUtensorMap mc;
   if (!encode_output_map(&mc, C, total_rows, N, ldc, out_dtype)) return MX8_ERR_CUDA;

@@ -55,26 +55,37 @@ namespace mx8q {
 namespace {
 
 constexpr int BM = 128;
-constexpr int kKBytes = 128;               // bytes of K per stage and row (one swizzle atom)
-constexpr int kTileABytes = BM * kKBytes;  // 16 KB
+constexpr int kKBytes = kGemmKBytes;       // bytes of K per stage and row (one swizzle atom)
+static_assert(kKBytes == 64 || kKBytes == 128, "one 64- or 128-byte swizzle atom per stage row");
+constexpr uint32_t kSwizzle = kKBytes == 128 ? kSwizzle128B : kSwizzle64B;
+constexpr uint32_t kAtomSbo = 8 * kKBytes;  // bytes between 8-row groups of a swizzled operand
+constexpr int kBoxBytes = 128 * kKBytes;   // one 128-row TMA box
+constexpr int kTileABytes = BM * kKBytes;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSmemBudget = 227 * 1024 - 1024;
 
 template <int kFmt>
 struct Cfg;
+// A 512-byte scale tile holds 4 scales for each of 128 rows: 128 K elements
+// for MXFP8, 64 for NVFP4.  A stage covers kElemsPerStage elements of K and
+// needs kSfTiles tiles, from tile (first element of the stage) / kElemsPerTile;
+// an MXFP8 stage of 64 bytes uses half a tile, and selects its scales with
+// the MMA's scale id.
 template <>
-struct Cfg<0> {                 // MXFP8: K = 128 elements per stage, 32 per MMA
-  static constexpr int kElemsPerStage = 128;
+struct Cfg<0> {                 // MXFP8: 1 byte per element, 32 elements per MMA
+  static constexpr int kElemsPerStage = kKBytes;
   static constexpr int kElemsPerMma = 32;
-  static constexpr int kSfTiles = 1;     // 128x4 scale tiles per 128 rows per stage
   static constexpr int kBlock = 32;
+  static constexpr int kElemsPerTile = 128;
+  static constexpr int kSfTiles = 1;
 };
 template <>
-struct Cfg<1> {                 // NVFP4: K = 256 elements per stage, 64 per MMA
-  static constexpr int kElemsPerStage = 256;
+struct Cfg<1> {                 // NVFP4: 2 elements per byte, 64 elements per MMA
+  static constexpr int kElemsPerStage = 2 * kKBytes;
   static constexpr int kElemsPerMma = 64;
-  static constexpr int kSfTiles = 4;
   static constexpr int kBlock = 16;
+  static constexpr int kElemsPerTile = 64;
+  static constexpr int kSfTiles = kElemsPerStage / kElemsPerTile;
 };
 
 template <int kFmt, bool kGrouped, int kBN>
@@ -88,7 +99,7 @@ struct Layout {
   static constexpr int kFixed = 256 + (kBN / 32) * kEpiStageBytes +
                                 (kGrouped ? static_cast<int>(sizeof(GroupSmem)) : 0);
   static constexpr int kStagesFit = (kSmemBudget - kFixed) / kStageBytes;
-  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+  static constexpr int kStages = kStagesFit > 10 ? 10 : kStagesFit;
   static constexpr int kAccBufs = kBN == 128 ? 2 : 1;
   static constexpr uint32_t kSfaCols = 4 * Cfg<kFmt>::kSfTiles;      // tensor-memory columns
   static constexpr uint32_t kSfbCols = 4 * Cfg<kFmt>::kSfTiles * kBRow128;
@@ -256,7 +267,7 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
           }
           const uint32_t full = smem_u32(&sm.full[s]);
           if (prod == 0) {
-            const int64_t sf0 = static_cast<int64_t>(kt) * F::kSfTiles;
+            const int64_t sf0 = static_cast<int64_t>(kt) * F::kElemsPerStage / F::kElemsPerTile;
             const int nsf = static_cast<int>(sf_kt - sf0 < F::kSfTiles ? sf_kt - sf0 : F::kSfTiles);
             mbar_arrive_expect_tx(full, kTileABytes + (1 + L::kBRow128) * nsf * 512);
             tma_load_2d(smem_u32(sm.a[s]), &tmap_a, kt * kKBytes, static_cast<int32_t>(tc.a_row0), full);
@@ -267,12 +278,12 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
           } else {
             // B in 128-row boxes (a 128-row box is 16 KB; boxes stack in shared memory)
             const int h = prod - 1;
-            mbar_arrive_expect_tx(full, 16384);
+            mbar_arrive_expect_tx(full, kBoxBytes);
             if (kGrouped)
-              tma_load_3d(smem_u32(sm.b[s]) + h * 16384, &tmap_b, kt * kKBytes,
+              tma_load_3d(smem_u32(sm.b[s]) + h * kBoxBytes, &tmap_b, kt * kKBytes,
                           static_cast<int32_t>(tc.n0 + h * 128), tc.g, full);
             else
-              tma_load_2d(smem_u32(sm.b[s]) + h * 16384, &tmap_b, kt * kKBytes,
+              tma_load_2d(smem_u32(sm.b[s]) + h * kBoxBytes, &tmap_b, kt * kKBytes,
                           static_cast<int32_t>(tc.n0 + h * 128), full);
           }
         }
@@ -307,7 +318,7 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
             break;
           }
           tc_fence_after();
-          const int64_t sf0 = static_cast<int64_t>(kt) * F::kSfTiles;
+          const int64_t sf0 = static_cast<int64_t>(kt) * F::kElemsPerStage / F::kElemsPerTile;
           const int nsf = static_cast<int>(sf_kt - sf0 < F::kSfTiles ? sf_kt - sf0 : F::kSfTiles);
           // tensor-memory scale layout per stage: A -> 4 columns per K sub-tile;
           // B -> (4 columns x kBRow128) per K sub-tile, the 128-row blocks adjacent
@@ -326,12 +337,14 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
                                                 ? F::kElemsPerStage / F::kElemsPerMma
                                                 : (krem + F::kElemsPerMma - 1) / F::kElemsPerMma);
           const uint32_t a0 = smem_u32(sm.a[s]), b0 = smem_u32(sm.b[s]);
+          // MXFP8: scale id of the stage's first MMA within its 4-scale tile
+          const uint32_t sf_id0 = static_cast<uint32_t>((static_cast<int64_t>(kt) * F::kElemsPerStage / 32) & 3);
           for (int kk = 0; kk < nmma; ++kk) {
-            const uint64_t ad = smem_desc(a0 + kk * 32, 16, 1024, kSwizzle128B);
-            const uint64_t bd = smem_desc(b0 + kk * 32, 16, 1024, kSwizzle128B);
+            const uint64_t ad = smem_desc(a0 + kk * 32, 16, kAtomSbo, kSwizzle);
+            const uint64_t bd = smem_desc(b0 + kk * 32, 16, kAtomSbo, kSwizzle);
             const uint32_t acc = (kt > 0 || kk > 0) ? 1u : 0u;
             if (kFmt == 0)
-              tc_mma_mxf8(d_tmem, ad, bd, make_idesc(0, kBN, kk), tsfa, tsfb, acc);
+              tc_mma_mxf8(d_tmem, ad, bd, make_idesc(0, kBN, sf_id0 + kk), tsfa, tsfb, acc);
             else
               tc_mma_nvf4(d_tmem, ad, bd, make_idesc(1, kBN, 0), tsfa + 4 * kk,
                           tsfb + 4 * L::kBRow128 * kk, acc);

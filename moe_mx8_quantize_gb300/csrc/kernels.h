@@ -7,6 +7,13 @@
 
 namespace mx8q {
 
+// Bytes of K per GEMM pipeline stage and operand row: one swizzle atom, 128
+// (SWIZZLE_128B boxes and descriptors) or 64 (SWIZZLE_64B).  64-byte stages
+// double the stage count in the same shared memory but measured slower on
+// GB300 (MXFP8 Fprop 2048x8192x2048: 78 us against 51 us): each stage's
+// barrier, scale copies and commit cost about the same fixed time.
+constexpr int kGemmKBytes = 128;
+
 constexpr int kMaxGroups = 1024;   // groups (experts) per grouped call
 #define MX8Q_S32_GROUP_MODE 3          // FP32 scale per group (same value as MX8_S32_GROUP)
 
