@@ -67,6 +67,11 @@ def _L():
         lib.or_mxfp8_quantize_rowwise.argtypes = [_p, _i64, _i64, _i64, _p, _p]
         lib.or_mxfp8_quantize_colwise.argtypes = [_p, _i64, _i64, _i64, _p, _p]
         lib.or_dequant_mxfp8.argtypes = [_p, _p, _i64, _i64, _p]
+        lib.or_mxfp4_block_exp.restype = ctypes.c_int
+        lib.or_mxfp4_block_exp.argtypes = [ctypes.c_float]
+        lib.or_mxfp4_quantize_rowwise.argtypes = [_p, _i64, _i64, _i64, _p, _p]
+        lib.or_mxfp4_quantize_colwise.argtypes = [_p, _i64, _i64, _i64, _p, _p]
+        lib.or_dequant_mxfp4.argtypes = [_p, _p, _i64, _i64, _p]
         lib.or_nvfp4_quantize.argtypes = [_p, _i64, _i64, _i64, ctypes.c_int, _p,
                                           ctypes.c_int, _p, _p, _p]
         lib.or_dequant_nvfp4.argtypes = [_p, _p, _p, ctypes.c_int, _p, ctypes.c_int,
@@ -166,6 +171,44 @@ def dequant_mxfp8(q, s):
     return out
 
 
+# ----------------------------------------------------------------- MXFP4
+def mxfp4_block_exp(amax: float) -> int:
+    return _L().or_mxfp4_block_exp(amax)
+
+
+def mxfp4_quantize_rowwise(x_bits):
+    """Rowwise MXFP4 (1x32 blocks along rows) -> (q [R,C/2] packed E2M1,
+    s [R,C/32] E8M0)."""
+    x = _c(x_bits, np.uint16)
+    R, C = x.shape
+    assert C % 32 == 0
+    q = np.zeros((R, C // 2), np.uint8)
+    s = np.empty((R, C // 32), np.uint8)
+    _L().or_mxfp4_quantize_rowwise(_ptr(x), R, C, C, _ptr(q), _ptr(s))
+    return q, s
+
+
+def mxfp4_quantize_colwise(x_bits):
+    """Columnwise MXFP4 (32x1 blocks down columns), stored transposed ->
+    (qT [C,R/2] packed, sT [C,R/32])."""
+    x = _c(x_bits, np.uint16)
+    R, C = x.shape
+    assert R % 32 == 0
+    q = np.zeros((C, R // 2), np.uint8)
+    s = np.empty((C, R // 32), np.uint8)
+    _L().or_mxfp4_quantize_colwise(_ptr(x), R, C, C, _ptr(q), _ptr(s))
+    return q, s
+
+
+def dequant_mxfp4(q, s):
+    q = _c(q, np.uint8)
+    s = _c(s, np.uint8)
+    R, C = q.shape[0], q.shape[1] * 2
+    out = np.empty((R, C), np.float32)
+    _L().or_dequant_mxfp4(_ptr(q), _ptr(s), R, C, _ptr(out))
+    return out
+
+
 # ----------------------------------------------------------------- NVFP4
 SCOPE_TOKEN, SCOPE_GROUP, SCOPE_TENSOR = 0, 1, 2
 
@@ -241,7 +284,8 @@ def _mode_of(v, n):
 def gemm_ref(fmt, A, SA, B, SB, K, a32=None, b32=None, pairs=None):
     """FP64 reference of Y = A^ . B^T over exactly decoded operands.
 
-    A: [M, K] (MXFP8 bytes) or [M, K/2] (packed NVFP4); SA canonical.
+    fmt: 0 MXFP8, 1 NVFP4, 2 MXFP4.
+    A: [M, K] (MXFP8 bytes) or [M, K/2] (packed NVFP4 / MXFP4); SA canonical.
     Returns (ref, absref): [M, N] arrays, or [npairs] for sampled pairs.
     """
     A = _c(A, np.uint8); B = _c(B, np.uint8)

@@ -1,6 +1,6 @@
 /*
- * CPU ORACLE for microscaling quantization (MXFP8, per-token NVFP4) and the
- * block-scaled GEMM those encodings feed.
+ * CPU ORACLE for microscaling quantization (MXFP8, per-token NVFP4, MXFP4)
+ * and the block-scaled GEMM those encodings feed.
  *
  * This file is TEST INFRASTRUCTURE.  Only the test suite, the smoke check and
  * the benchmark's CPU-baseline leg may load it.  It shares no code, header,
@@ -228,6 +228,92 @@ void or_dequant_mxfp8(const uint8_t *q, const uint8_t *s, i64 R, i64 C, float *o
 }
 
 /* ------------------------------------------------------------------ */
+/* MXFP4                                                               */
+/* ------------------------------------------------------------------ */
+
+/* [NV4] "Que es realmente NVFP4": MXFP4 stores 32-element blocks of E2M1
+ * (values +-0, 0.5, 1, 1.5, 2, 3, 4, 6) under one UE8M0 (power-of-two)
+ * scale.  The exponent rule is the MXFP8 one with the E2M1 maximum: the
+ * smallest integer e with amax <= 6 * 2^e, clamped to [-127, 127]
+ * (amax == 0 gives -127), so no element saturates. */
+int or_mxfp4_block_exp(float amax)
+{
+    double a = (double)amax;
+    int e = -127;
+    while (e < 127 && a > ldexp(6.0, e)) e++;
+    return e;
+}
+
+/* Packed E2M1 pair: element 2j in the low nibble, 2j+1 in the high one. */
+static void put_nibble(uint8_t *row, i64 k, uint8_t code)
+{
+    if (k & 1) row[k / 2] = (uint8_t)((row[k / 2] & 0x0F) | (code << 4));
+    else row[k / 2] = (uint8_t)((row[k / 2] & 0xF0) | (code & 0x0F));
+}
+
+/* Rowwise MXFP4: 1x32 blocks along each row.
+ *   q : packed E2M1 [R, C/2]
+ *   s : E8M0 [R, C/32]   (canonical, row-major) */
+void or_mxfp4_quantize_rowwise(const uint16_t *x, i64 R, i64 C, i64 ld,
+                               uint8_t *q, uint8_t *s)
+{
+    i64 nb = C / 32;
+    for (i64 r = 0; r < R; r++) {
+        for (i64 b = 0; b < nb; b++) {
+            const uint16_t *blk = x + r * ld + b * 32;
+            float amax = 0.0f;
+            for (int i = 0; i < 32; i++) {
+                float a = absf_of_bf16(blk[i]);
+                if (a > amax) amax = a;
+            }
+            int e = or_mxfp4_block_exp(amax);
+            s[r * nb + b] = (uint8_t)(e + 127);
+            for (int i = 0; i < 32; i++) {
+                /* x * 2^-e is exact in double; E2M1 rounding happens once. */
+                double scaled = ldexp((double)or_bf16_to_f32(blk[i]), -e);
+                put_nibble(q + r * (C / 2), b * 32 + i, or_e2m1_encode((float)scaled));
+            }
+        }
+    }
+}
+
+/* Columnwise MXFP4: 32x1 blocks down each column of the bf16 input, stored
+ * transposed:  qT : packed E2M1 [C, R/2] (qT row c encodes column c of x);
+ * sT : E8M0 [C, R/32] canonical.  R must be a multiple of 32. */
+void or_mxfp4_quantize_colwise(const uint16_t *x, i64 R, i64 C, i64 ld,
+                               uint8_t *qT, uint8_t *sT)
+{
+    i64 nb = R / 32;
+    for (i64 c = 0; c < C; c++) {
+        for (i64 b = 0; b < nb; b++) {
+            float amax = 0.0f;
+            for (int i = 0; i < 32; i++) {
+                float a = absf_of_bf16(x[(b * 32 + i) * ld + c]);
+                if (a > amax) amax = a;
+            }
+            int e = or_mxfp4_block_exp(amax);
+            sT[c * nb + b] = (uint8_t)(e + 127);
+            for (int i = 0; i < 32; i++) {
+                double scaled = ldexp((double)or_bf16_to_f32(x[(b * 32 + i) * ld + c]), -e);
+                put_nibble(qT + c * (R / 2), b * 32 + i, or_e2m1_encode((float)scaled));
+            }
+        }
+    }
+}
+
+/* out = decode(q) * 2^(s - 127) in double, rounded once to binary32. */
+void or_dequant_mxfp4(const uint8_t *q, const uint8_t *s, i64 R, i64 C, float *out)
+{
+    i64 nb = C / 32;
+    for (i64 r = 0; r < R; r++)
+        for (i64 c = 0; c < C; c++) {
+            uint8_t byte = q[r * (C / 2) + c / 2];
+            uint8_t nib = (c & 1) ? (byte >> 4) : (byte & 15);
+            out[r * C + c] = (float)(or_e2m1_decode(nib) * or_e8m0_decode(s[r * nb + c / 32]));
+        }
+}
+
+/* ------------------------------------------------------------------ */
 /* NVFP4 with an FP32 scale per token / group / tensor                  */
 /* ------------------------------------------------------------------ */
 
@@ -404,7 +490,8 @@ void or_swizzle_scales(const uint8_t *canon, i64 rows, i64 scols,
 
 /* Exact FP64 decode of one operand row: element * block scale * FP32 scale.
  * fmt 0 = MXFP8 (E4M3 bytes, E8M0 per 32), fmt 1 = NVFP4 (packed E2M1,
- * E4M3 per 16).  All products have <= 30 significant bits: exact. */
+ * E4M3 per 16), fmt 2 = MXFP4 (packed E2M1, E8M0 per 32).  All products
+ * have <= 30 significant bits: exact. */
 static void decode_row(int fmt, const uint8_t *qrow, const uint8_t *srow, double s32,
                        i64 K, double *dst)
 {
@@ -415,7 +502,7 @@ static void decode_row(int fmt, const uint8_t *qrow, const uint8_t *srow, double
         } else {
             uint8_t byte = qrow[k / 2];
             uint8_t nib = (k & 1) ? (byte >> 4) : (byte & 15);
-            v = or_e2m1_decode(nib) * or_e4m3_decode(srow[k / 16]);
+            v = or_e2m1_decode(nib) * (fmt == 1 ? or_e4m3_decode(srow[k / 16]) : or_e8m0_decode(srow[k / 32]));
         }
         dst[k] = v * s32;
     }
@@ -432,7 +519,7 @@ void or_gemm_ref(int fmt, i64 M, i64 N, i64 K,
                  const uint8_t *B, const uint8_t *SB, const float *b32, int b32_mode,
                  const i64 *pairs, i64 npairs, double *ref, double *absref, double *scratch)
 {
-    i64 bs = (fmt == 0) ? 32 : 16;
+    i64 bs = (fmt == 1) ? 16 : 32;
     i64 rowbytes = (fmt == 0) ? K : K / 2;
     double *ar = scratch, *br = scratch + K;
     i64 count = pairs ? npairs : M * N;
@@ -469,7 +556,7 @@ void or_grouped_gemm_ref(int fmt, int G, const i64 *offs, i64 N, i64 K,
                          const i64 *pairs, i64 npairs, double *ref, double *absref,
                          double *scratch)
 {
-    i64 bs = (fmt == 0) ? 32 : 16;
+    i64 bs = (fmt == 1) ? 16 : 32;
     i64 rowbytes = (fmt == 0) ? K : K / 2;
     double *ar = scratch, *br = scratch + K;
     i64 last_m = -1;
