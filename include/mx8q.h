@@ -1,5 +1,5 @@
 /*
- * mx8q -- microscaling quantization (MXFP8, per-token NVFP4) and the
+ * mx8q -- microscaling quantization (MXFP8, per-token NVFP4, MXFP4) and the
  * block-scaled tensor-core GEMM it feeds, for GB300 (sm_103a).
  *
  * Plain C ABI: device pointers, sizes and a CUDA stream; no framework types.
@@ -17,7 +17,8 @@
  *         up projections quantized together).
  *   [NV4] "NVIDIA presenta una metodologia de preentrenamiento de 4 bits
  *         utilizando NVFP4" -- "Que es realmente NVFP4" (E2M1 grid, E4M3
- *         block scales, FP32 second-level scale), "La metodologia de
+ *         block scales, FP32 second-level scale; MXFP4 = 32 E2M1 values
+ *         under one power-of-two scale), "La metodologia de
  *         formacion de cuatro partes" (1x16 blocks, round-to-nearest-even).
  *   [REC] "Miles Blackwell MXFP8 / NVFP4 RL recipes" (aib.vote) -- MXFP8
  *         row/column copies, NVFP4 on MoE routed experts with a tensor- or
@@ -27,6 +28,7 @@
  *   MXFP8 block exponent e = smallest integer with amax <= 448 * 2^e,
  *   clamped to [-127, 127]; scale byte = e + 127; element = RNE_E4M3(x*2^-e)
  *   saturating, signed zero kept.
+ *   MXFP4: the same rule with 6 for 448 and RNE_E2M1 for RNE_E4M3.
  *   NVFP4 with scope amax A:  S_enc = min(RN(2688/A), FLT_MAX);
  *   S_dec = RN(A/2688) (stored); per 16-block: sb = RNE_E4M3(RN(RN(amax_b/6)
  *   * S_enc)); r = sb ? min(RN(S_enc/sb), FLT_MAX) : 0;
@@ -39,10 +41,12 @@
  *   MXFP8 data            : uint8 E4M3 [rows, cols].
  *   MXFP8 columnwise data : uint8 E4M3 [cols, rows] -- stored transposed, so
  *                           its 1x32 blocks run along its contiguous axis.
- *   NVFP4 data            : uint8 [rows, cols/2]; element 2j in the low
- *                           nibble of byte j, element 2j+1 in the high nibble.
+ *   NVFP4 / MXFP4 data    : uint8 [rows, cols/2]; element 2j in the low
+ *                           nibble of byte j, element 2j+1 in the high nibble
+ *                           (an MXFP4 columnwise copy: [cols, rows/2]).
  *   Scale factors         : the tensor-core tile layout.  For a logical
- *                           [R, S] scale matrix (S = cols/32 or cols/16),
+ *                           [R, S] scale matrix (S = cols/32 for MXFP8 and
+                           MXFP4, cols/16 for NVFP4),
  *                           scale (r, k) lives at byte
  *                             ((r/128)*ceil(S/4) + k/4)*512
  *                             + (r%32)*16 + ((r%128)/32)*4 + k%4
@@ -87,13 +91,13 @@ typedef enum {
 
 enum { MX8_ROWWISE = 1, MX8_COLWISE = 2 };
 enum { NVFP4_SCOPE_TOKEN = 0, NVFP4_SCOPE_GROUP = 1, NVFP4_SCOPE_TENSOR = 2 };
-enum { MX8_FMT_MXFP8 = 0, MX8_FMT_NVFP4 = 1 };
+enum { MX8_FMT_MXFP8 = 0, MX8_FMT_NVFP4 = 1, MX8_FMT_MXFP4 = 2 };
 enum { MX8_OUT_F32 = 0, MX8_OUT_BF16 = 1 };
 /* How an FP32 decode scale vector applies to the rows of a matrix. */
 enum { MX8_S32_NONE = 0, MX8_S32_ROW = 1, MX8_S32_TENSOR = 2, MX8_S32_GROUP = 3 };
 
 /* Bytes of the tensor-core scale buffer for a [rows, cols] matrix in format
- * fmt (block 32 for MXFP8, 16 for NVFP4). */
+ * fmt (block 32 for MXFP8 and MXFP4, 16 for NVFP4). */
 size_t mx8_scale_bytes(int fmt, int64_t rows, int64_t cols);
 
 /* Upper bound of the grouped scale buffer (every group padded to whole
@@ -123,6 +127,20 @@ int mx8_device_sm_count(void);
 mx8_status mx8_quantize(const void *x, int64_t rows, int64_t cols, int64_t ld, int flags,
                         uint8_t *q_row, uint8_t *s_row, uint8_t *q_col, uint8_t *s_col,
                         void *workspace, size_t workspace_bytes, mx8_stream_t stream);
+
+/*
+ * MXFP4 quantization of a bf16 matrix, rowwise and/or columnwise in one pass
+ * over the input ([NV4] "Que es realmente NVFP4": 32 E2M1 values share one
+ * power-of-two E8M0 scale).  Same arguments, checks and scale layout as
+ * mx8_quantize(), with packed data:
+ *   q_row    : uint8 [rows, cols/2]              (ROWWISE)
+ *   s_row    : mx8_scale_bytes(MXFP4, rows, cols) (ROWWISE)
+ *   q_col    : uint8 [cols, rows/2], transposed  (COLWISE)
+ *   s_col    : mx8_scale_bytes(MXFP4, cols, rows) (COLWISE)
+ */
+mx8_status mxfp4_quantize(const void *x, int64_t rows, int64_t cols, int64_t ld, int flags,
+                          uint8_t *q_row, uint8_t *s_row, uint8_t *q_col, uint8_t *s_col,
+                          void *workspace, size_t workspace_bytes, mx8_stream_t stream);
 
 /*
  * Two-level NVFP4 quantization of a bf16 matrix with the FP32 scale computed
@@ -174,11 +192,12 @@ mx8_status nvfp4_quantize_per_token_noalloc(const void *x, int64_t rows, int64_t
  * "La Compatibilidad..." and [REC]: rebuild high-precision operands from the
  * exact low-precision forward values).
  *   MXFP8: out = e4m3 * 2^(scale-127)            (exact; may overflow to inf)
+ *   MXFP4: out = e2m1 * 2^(scale-127)            (exact; may overflow to inf)
  *   NVFP4: out = RN((e2m1 * sb) * S_dec)
  *   q, s   : as produced by the quantizers (any rowwise-blocked matrix,
  *            including a transposed columnwise copy)
  *   s32, s32_mode : MX8_S32_NONE / ROW ([rows]) / TENSOR ([1]) / GROUP
- *            ([num_groups], needs group_offsets)
+ *            ([num_groups], needs group_offsets); NVFP4 only
  *   group_offsets : grouped scale layout (as in nvfp4_quantize_per_token)
  *   out    : [rows, cols] f32 or bf16 (out_dtype); bf16 = RNE of the f32 value
  */
@@ -191,13 +210,14 @@ mx8_status dequantize(int fmt, const uint8_t *q, const uint8_t *s, const float *
  * Block-scaled GEMM on the tcgen05 tensor cores:
  *     C[m, n] (+)= A32[m] * B32[n] * sum_k A^[m, k] * B^[n, k]
  * where A^ and B^ are the block-scaled decodes (MXFP8: E4M3 * E8M0 per 32
- * along K; NVFP4: E2M1 * E4M3 per 16 along K).  Both operands store K
+ * along K; NVFP4: E2M1 * E4M3 per 16 along K; MXFP4: E2M1 * E8M0 per 32
+ * along K).  Both operands store K
  * contiguously, so Fprop (A = X rowwise, B = W rowwise), Dgrad (A = dY
  * rowwise, B = W columnwise copy) and Wgrad (A = dY columnwise copy,
  * B = X columnwise copy) are all this call ([MRL] "La Compatibilidad...":
  * MXFP8 in forward, weight-gradient and data-gradient GEMMs; [MRL] "Un
  * Cuantizador Compartido...": scale blocks follow the reduction dimension).
- *   A, SA : [M, K] data (K/2 bytes per row for NVFP4) + tensor-core scales
+ *   A, SA : [M, K] data (K/2 bytes per row for NVFP4 and MXFP4) + scales
  *   B, SB : [N, K] data + scales
  *   A32 / a32_mode : MX8_S32_NONE, MX8_S32_ROW ([M], per-token scale),
  *                    MX8_S32_TENSOR ([1])

@@ -1,4 +1,4 @@
-"""GB300-native microscaling quantization (MXFP8, per-token NVFP4) and the
+"""GB300-native microscaling quantization (MXFP8, per-token NVFP4, MXFP4) and the
 block-scaled tcgen05 GEMM it feeds.
 
 This package is a thin ctypes binding over the C ABI of ``_build/libmx8q.so``
@@ -22,13 +22,13 @@ LIB_PATH = os.path.join(_HERE, "_build", "libmx8q.so")
 OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = range(7)
 ROWWISE, COLWISE = 1, 2
 SCOPE_TOKEN, SCOPE_GROUP, SCOPE_TENSOR = 0, 1, 2
-FMT_MXFP8, FMT_NVFP4 = 0, 1
+FMT_MXFP8, FMT_NVFP4, FMT_MXFP4 = 0, 1, 2
 OUT_F32, OUT_BF16 = 0, 1
 S32_NONE, S32_ROW, S32_TENSOR, S32_GROUP = 0, 1, 2, 3
 
 # every C symbol the header declares
 EXPORTS = ("mx8_scale_bytes", "mx8_scale_bytes_grouped", "mx8_workspace_bytes",
-           "mx8_device_sm_count", "mx8_quantize", "nvfp4_quantize_per_token",
+           "mx8_device_sm_count", "mx8_quantize", "mxfp4_quantize", "nvfp4_quantize_per_token",
            "nvfp4_quantize_per_token_noalloc", "dequantize",
            "bs_gemm", "bs_grouped_gemm", "mx8_swiglu", "mx8_check_device_error", "mx8_selftest_bounded_wait",
            "mx8_status_string")
@@ -66,6 +66,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mx8_device_sm_count.argtypes = []
     lib.mx8_quantize.restype = _i
     lib.mx8_quantize.argtypes = [_p, _i64, _i64, _i64, _i, _p, _p, _p, _p, _p, _sz, _p]
+    lib.mxfp4_quantize.restype = _i
+    lib.mxfp4_quantize.argtypes = [_p, _i64, _i64, _i64, _i, _p, _p, _p, _p, _p, _sz, _p]
     lib.nvfp4_quantize_per_token.restype = _i
     lib.nvfp4_quantize_per_token.argtypes = [_p, _i64, _i64, _i64, _i, _p, _i, _p, _p, _p, _p, _sz, _p]
     lib.nvfp4_quantize_per_token_noalloc.restype = _i
@@ -172,6 +174,36 @@ def mx8_quantize(x: torch.Tensor, flags: int = ROWWISE | COLWISE, ws=None, strea
         q_col = torch.empty((C, R), dtype=torch.uint8, device=dev)
         s_col = _u8(scale_bytes(FMT_MXFP8, C, R), dev)
     mx8_quantize_into(x, q_row, s_row, q_col, s_col, flags, ws, stream)
+    return q_row, s_row, q_col, s_col
+
+
+# ---------------------------------------------------------------- MXFP4
+def mxfp4_quantize_into(x, q_row, s_row, q_col, s_col, flags=ROWWISE | COLWISE, ws=None, stream=None):
+    """In-place form of :func:`mxfp4_quantize` (outputs pre-allocated)."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    R, C = x.shape
+    ws = _ws(ws, 1, x.device)
+    _check(load().mxfp4_quantize(_ptr(x), R, C, x.stride(0), flags, _ptr(q_row), _ptr(s_row),
+                                 _ptr(q_col), _ptr(s_col), _ptr(ws), ws.numel(), _stream(stream)),
+           "mxfp4_quantize")
+
+
+def mxfp4_quantize(x: torch.Tensor, flags: int = ROWWISE | COLWISE, ws=None, stream=None):
+    """MXFP4 rowwise and/or columnwise quantization of a bf16 [R, C] matrix.
+
+    Returns (q_row [R,C/2] u8, s_row u8 tiles, q_col [C,R/2] u8, s_col u8
+    tiles); the copies not requested are None.
+    """
+    R, C = x.shape
+    dev = x.device
+    q_row = s_row = q_col = s_col = None
+    if flags & ROWWISE:
+        q_row = torch.empty((R, C // 2), dtype=torch.uint8, device=dev)
+        s_row = _u8(scale_bytes(FMT_MXFP4, R, C), dev)
+    if flags & COLWISE:
+        q_col = torch.empty((C, R // 2), dtype=torch.uint8, device=dev)
+        s_col = _u8(scale_bytes(FMT_MXFP4, C, R), dev)
+    mxfp4_quantize_into(x, q_row, s_row, q_col, s_col, flags, ws, stream)
     return q_row, s_row, q_col, s_col
 
 

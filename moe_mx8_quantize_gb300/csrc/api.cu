@@ -77,13 +77,13 @@ mx8_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MX8_OK : MX8_ERR
 // ===================================================================== sizes
 extern "C" size_t mx8_scale_bytes(int fmt, int64_t rows, int64_t cols) {
   if (rows < 0 || cols < 0) return 0;
-  const int64_t bs = fmt == MX8_FMT_MXFP8 ? 32 : 16;
+  const int64_t bs = fmt == MX8_FMT_NVFP4 ? 16 : 32;
   return static_cast<size_t>(cdiv(rows, 128) * 128 * cdiv(cols / bs, 4) * 4);
 }
 
 extern "C" size_t mx8_scale_bytes_grouped(int fmt, int64_t total_rows, int num_groups, int64_t cols) {
   if (total_rows < 0 || cols < 0 || num_groups < 0) return 0;
-  const int64_t bs = fmt == MX8_FMT_MXFP8 ? 32 : 16;
+  const int64_t bs = fmt == MX8_FMT_NVFP4 ? 16 : 32;
   const int64_t tiles = cdiv(total_rows, 128) + num_groups;
   return static_cast<size_t>(tiles * 128 * cdiv(cols / bs, 4) * 4);
 }
@@ -108,10 +108,11 @@ extern "C" const char* mx8_status_string(mx8_status s) {
   return "unknown status";
 }
 
-// ===================================================================== MXFP8
-extern "C" mx8_status mx8_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int flags,
-                                   uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
-                                   void* workspace, size_t workspace_bytes, mx8_stream_t stream) {
+// ===================================================================== MXFP8 / MXFP4
+namespace {
+mx8_status mx_quantize(bool fp4, const void* x, int64_t rows, int64_t cols, int64_t ld, int flags,
+                       uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                       void* workspace, size_t workspace_bytes, mx8_stream_t stream) {
   const bool row = flags & MX8_ROWWISE, col = flags & MX8_COLWISE;
   if ((flags & ~(MX8_ROWWISE | MX8_COLWISE)) || !(row || col)) return MX8_ERR_INVALID_ARG;
   if (rows < 0 || cols < 0 || ld < cols || cols % 32 != 0) return MX8_ERR_INVALID_ARG;
@@ -134,9 +135,24 @@ extern "C" mx8_status mx8_quantize(const void* x, int64_t rows, int64_t cols, in
   if (!encode_map(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, dims, strides, box,
                   CU_TENSOR_MAP_SWIZZLE_NONE))
     return MX8_ERR_CUDA;
-  return from_cuda(launch_mxfp8_quant(map, rows, cols, row, col, q_row, s_row, q_col, s_col,
+  return from_cuda(launch_mxfp8_quant(map, rows, cols, row, col, fp4, q_row, s_row, q_col, s_col,
                                       err_word(workspace), sm_count_current(),
                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+extern "C" mx8_status mx8_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int flags,
+                                   uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                                   void* workspace, size_t workspace_bytes, mx8_stream_t stream) {
+  return mx_quantize(false, x, rows, cols, ld, flags, q_row, s_row, q_col, s_col, workspace,
+                     workspace_bytes, stream);
+}
+
+extern "C" mx8_status mxfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int flags,
+                                     uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                                     void* workspace, size_t workspace_bytes, mx8_stream_t stream) {
+  return mx_quantize(true, x, rows, cols, ld, flags, q_row, s_row, q_col, s_col, workspace,
+                     workspace_bytes, stream);
 }
 
 // ===================================================================== NVFP4
@@ -169,11 +185,11 @@ extern "C" mx8_status dequantize(int fmt, const uint8_t* q, const uint8_t* s, co
                                  int s32_mode, const int64_t* group_offsets, int num_groups,
                                  int64_t rows, int64_t cols, int out_dtype, void* out,
                                  mx8_stream_t stream) {
-  if (fmt != MX8_FMT_MXFP8 && fmt != MX8_FMT_NVFP4) return MX8_ERR_INVALID_ARG;
+  if (fmt != MX8_FMT_MXFP8 && fmt != MX8_FMT_NVFP4 && fmt != MX8_FMT_MXFP4) return MX8_ERR_INVALID_ARG;
   if (out_dtype != MX8_OUT_F32 && out_dtype != MX8_OUT_BF16) return MX8_ERR_INVALID_ARG;
-  if (rows < 0 || cols < 0 || cols % (fmt == MX8_FMT_MXFP8 ? 32 : 16) != 0) return MX8_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0 || cols % (fmt == MX8_FMT_NVFP4 ? 16 : 32) != 0) return MX8_ERR_INVALID_ARG;
   if (s32_mode < MX8_S32_NONE || s32_mode > MX8_S32_GROUP) return MX8_ERR_INVALID_ARG;
-  if (fmt == MX8_FMT_MXFP8 && s32_mode != MX8_S32_NONE) return MX8_ERR_INVALID_ARG;
+  if (fmt != MX8_FMT_NVFP4 && s32_mode != MX8_S32_NONE) return MX8_ERR_INVALID_ARG;
   if (s32_mode != MX8_S32_NONE && s32 == nullptr) return MX8_ERR_INVALID_ARG;
   if ((s32_mode == MX8_S32_GROUP || group_offsets != nullptr) &&
       (group_offsets == nullptr || num_groups < 1 || num_groups > kMaxGroups))
@@ -204,7 +220,7 @@ namespace {
 mx8_status gemm_common_checks(int fmt, int64_t N, int64_t K, const uint8_t* A, const uint8_t* SA,
                               const uint8_t* B, const uint8_t* SB, int out_dtype, void* C,
                               int64_t ldc) {
-  if (fmt != MX8_FMT_MXFP8 && fmt != MX8_FMT_NVFP4) return MX8_ERR_INVALID_ARG;
+  if (fmt != MX8_FMT_MXFP8 && fmt != MX8_FMT_NVFP4 && fmt != MX8_FMT_MXFP4) return MX8_ERR_INVALID_ARG;
   if (out_dtype != MX8_OUT_F32 && out_dtype != MX8_OUT_BF16) return MX8_ERR_INVALID_ARG;
   if (N < 0 || K < 0 || K % 32 != 0 || ldc < N) return MX8_ERR_INVALID_ARG;
   if (A == nullptr || SA == nullptr || B == nullptr || SB == nullptr || C == nullptr)

@@ -1,6 +1,7 @@
 // Block-scaled GEMM on the 5th-generation tensor cores (tcgen05), for MXFP8
-// (kind::mxf8f6f4, E4M3 x E4M3, UE8M0 scale per 32 along K) and NVFP4
-// (kind::mxf4nvf4, packed E2M1 x E2M1, UE4M3 scale per 16 along K), plain and
+// (kind::mxf8f6f4, E4M3 x E4M3, UE8M0 scale per 32 along K), NVFP4
+// (kind::mxf4nvf4, packed E2M1 x E2M1, UE4M3 scale per 16 along K) and MXFP4
+// (kind::mxf4nvf4, packed E2M1 x E2M1, UE8M0 scale per 32 along K), plain and
 // grouped (MoE routed experts).
 //
 // "Miles Blackwell RL Cambia la Uniformidad BF16 por MXFP8 y NVFP4 Nativos",
@@ -67,7 +68,7 @@ constexpr int kSmemBudget = 227 * 1024 - 1024;
 template <int kFmt>
 struct Cfg;
 // A 512-byte scale tile holds 4 scales for each of 128 rows: 128 K elements
-// for MXFP8, 64 for NVFP4.  A stage covers kElemsPerStage elements of K and
+// for MXFP8 and MXFP4, 64 for NVFP4.  A stage covers kElemsPerStage elements of K and
 // needs kSfTiles tiles, from tile (first element of the stage) / kElemsPerTile;
 // an MXFP8 stage of 64 bytes uses half a tile, and selects its scales with
 // the MMA's scale id.
@@ -85,6 +86,14 @@ struct Cfg<1> {                 // NVFP4: 2 elements per byte, 64 elements per M
   static constexpr int kElemsPerMma = 64;
   static constexpr int kBlock = 16;
   static constexpr int kElemsPerTile = 64;
+  static constexpr int kSfTiles = kElemsPerStage / kElemsPerTile;
+};
+template <>
+struct Cfg<2> {                 // MXFP4: 2 elements per byte, 64 elements (2 scales) per MMA
+  static constexpr int kElemsPerStage = 2 * kKBytes;
+  static constexpr int kElemsPerMma = 64;
+  static constexpr int kBlock = 32;
+  static constexpr int kElemsPerTile = 128;
   static constexpr int kSfTiles = kElemsPerStage / kElemsPerTile;
 };
 
@@ -141,7 +150,7 @@ __device__ __forceinline__ uint32_t make_idesc(int fmt, int n, uint32_t sf_id) {
   d |= etype << 7;
   d |= etype << 10;
   d |= static_cast<uint32_t>(n >> 3) << 17;
-  d |= (fmt == 0 ? 1u : 0u) << 23;
+  d |= (fmt == 1 ? 0u : 1u) << 23;
   d |= static_cast<uint32_t>(BM >> 4) << 24;
   d |= (sf_id & 3u) << 29;
   return d;
@@ -337,7 +346,8 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
                                                 ? F::kElemsPerStage / F::kElemsPerMma
                                                 : (krem + F::kElemsPerMma - 1) / F::kElemsPerMma);
           const uint32_t a0 = smem_u32(sm.a[s]), b0 = smem_u32(sm.b[s]);
-          // MXFP8: scale id of the stage's first MMA within its 4-scale tile
+          // MXFP8: scale id of the stage's first MMA within its 4-scale tile;
+          // MXFP4: MMA kk takes scales 2(kk%2), 2(kk%2)+1 of tile kk/2
           const uint32_t sf_id0 = static_cast<uint32_t>((static_cast<int64_t>(kt) * F::kElemsPerStage / 32) & 3);
           for (int kk = 0; kk < nmma; ++kk) {
             const uint64_t ad = smem_desc(a0 + kk * 32, 16, kAtomSbo, kSwizzle);
@@ -345,6 +355,9 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
             const uint32_t acc = (kt > 0 || kk > 0) ? 1u : 0u;
             if (kFmt == 0)
               tc_mma_mxf8(d_tmem, ad, bd, make_idesc(0, kBN, sf_id0 + kk), tsfa, tsfb, acc);
+            else if (kFmt == 2)
+              tc_mma_mxf4(d_tmem, ad, bd, make_idesc(2, kBN, 2u * (kk & 1)), tsfa + 4 * (kk >> 1),
+                          tsfb + 4 * L::kBRow128 * (kk >> 1), acc);
             else
               tc_mma_nvf4(d_tmem, ad, bd, make_idesc(1, kBN, 0), tsfa + 4 * kk,
                           tsfb + 4 * L::kBRow128 * kk, acc);
@@ -524,6 +537,10 @@ cudaError_t launch_bs_gemm(const GemmArgs& a, const CUtensorMap& tmap_a, const C
   if (a.fmt == 0) {
     return a.grouped ? launch_variant<0, true, BN>(a, tmap_a, tmap_b, tmap_c, sm_count, stream)
                      : launch_variant<0, false, BN>(a, tmap_a, tmap_b, tmap_c, sm_count, stream);
+  }
+  if (a.fmt == 2) {
+    return a.grouped ? launch_variant<2, true, BN>(a, tmap_a, tmap_b, tmap_c, sm_count, stream)
+                     : launch_variant<2, false, BN>(a, tmap_a, tmap_b, tmap_c, sm_count, stream);
   }
   return a.grouped ? launch_variant<1, true, BN>(a, tmap_a, tmap_b, tmap_c, sm_count, stream)
                    : launch_variant<1, false, BN>(a, tmap_a, tmap_b, tmap_c, sm_count, stream);

@@ -1,14 +1,15 @@
-// Dequantization of MXFP8 / NVFP4 matrices back to f32 or bf16: the
+// Dequantization of MXFP8 / NVFP4 / MXFP4 matrices back to f32 or bf16: the
 // "dequantized backward" mode of "Miles Blackwell RL Cambia la Uniformidad
 // BF16 por MXFP8 y NVFP4 Nativos" (section "La Compatibilidad...") rebuilds
 // high-precision operands from the exact low-precision values of the forward
 // pass.
 //   MXFP8: out = e4m3 * 2^(s - 127)          (exact in f32 unless it overflows)
 //   NVFP4: out = RN((e2m1 * sb) * S_dec)     (the inner product is exact)
+//   MXFP4: out = e2m1 * 2^(s - 127)          (exact in f32 unless it overflows)
 // bf16 output is the round-to-nearest-even of the f32 value.
 //
 // Elementwise and bandwidth-bound: each thread turns 16 elements (one NVFP4
-// block or half an MXFP8 block) into 64 bytes of f32 or 32 bytes of bf16 with
+// block or half an MXFP8 / MXFP4 block) into 64 bytes of f32 or 32 bytes of bf16 with
 // 16-byte stores; the block scale is read from the tensor-core tile layout.
 #include <cuda_bf16.h>
 
@@ -59,7 +60,7 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(
   GroupSmem& gs = *reinterpret_cast<GroupSmem*>(smem_raw);
   if (kGrouped || s32_mode == MX8Q_S32_GROUP_MODE) load_group_prefix(gs, offs, G);
 
-  const int64_t bs = (kFmt == 0) ? 32 : 16;
+  const int64_t bs = (kFmt == 1) ? 16 : 32;
   const int64_t kt = (C / bs + 3) / 4;
   const int64_t chunks = C / 16;
   const int64_t total = R * chunks;
@@ -72,8 +73,8 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(
       g = upper_group(gs.offs, G, r);
       if (kGrouped) sr = gs.pref[g] + (r - gs.offs[g]);
     }
-    const float sc = (kFmt == 0) ? e8m0_to_f32(s[sf_byte(sr, c / 32, kt)])
-                                 : e4m3_to_f32(s[sf_byte(sr, c / 16, kt)]);
+    const float sc = (kFmt == 1) ? e4m3_to_f32(s[sf_byte(sr, c / 16, kt)])
+                                 : e8m0_to_f32(s[sf_byte(sr, c / 32, kt)]);
     float v[16];
     if (kFmt == 0) {
       const uint4 w = *reinterpret_cast<const uint4*>(q + r * C + c);
@@ -85,6 +86,14 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(
       }
 #pragma unroll
       for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], sc);
+    } else if (kFmt == 2) {
+      const uint2 w = *reinterpret_cast<const uint2*>(q + r * (C / 2) + c / 2);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t byte = ((j < 4 ? w.x : w.y) >> (8 * (j & 3))) & 0xFFu;
+        v[2 * j] = __fmul_rn(e2m1_to_f32(byte & 15u), sc);
+        v[2 * j + 1] = __fmul_rn(e2m1_to_f32(byte >> 4), sc);
+      }
     } else {
       const uint2 w = *reinterpret_cast<const uint2*>(q + r * (C / 2) + c / 2);
       float sd = 1.f;
@@ -143,6 +152,8 @@ cudaError_t launch_dequant(int fmt, const uint8_t* q, const uint8_t* s, const fl
   } while (0)
   if (fmt == 0) {
     if (grouped) MX8Q_DQ_LAUNCH(0, true); else MX8Q_DQ_LAUNCH(0, false);
+  } else if (fmt == 2) {
+    if (grouped) MX8Q_DQ_LAUNCH(2, true); else MX8Q_DQ_LAUNCH(2, false);
   } else {
     if (grouped) MX8Q_DQ_LAUNCH(1, true); else MX8Q_DQ_LAUNCH(1, false);
   }

@@ -18,7 +18,8 @@ constexpr int kMaxGroups = 1024;   // groups (experts) per grouped call
 #define MX8Q_S32_GROUP_MODE 3          // FP32 scale per group (same value as MX8_S32_GROUP)
 
 size_t mxfp8_quant_smem_bytes();
-cudaError_t launch_mxfp8_quant(const CUtensorMap& tmap_x, int64_t R, int64_t C, bool row, bool col,
+// fp4: MXFP4 (packed E2M1 data) instead of MXFP8 (E4M3 data)
+cudaError_t launch_mxfp8_quant(const CUtensorMap& tmap_x, int64_t R, int64_t C, bool row, bool col, bool fp4,
                                uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
                                int* err, int sm_count, cudaStream_t stream);
 
@@ -38,7 +39,7 @@ cudaError_t launch_swiglu(const uint16_t* gu, int64_t R, int64_t F, int64_t ld_g
                           int64_t ld_h, int sm_count, cudaStream_t stream);
 
 struct GemmArgs {
-  int fmt;                 // 0 MXFP8, 1 NVFP4
+  int fmt;                 // 0 MXFP8, 1 NVFP4, 2 MXFP4
   int64_t M, N, K;         // K in elements
   const uint8_t* SA;       // tensor-core scale tiles of A
   const uint8_t* SB;

@@ -1,5 +1,8 @@
 // MXFP8 quantization: 1x32 E4M3 blocks with one E8M0 (power-of-two) scale,
-// rowwise and columnwise copies from ONE read of the bf16 input.
+// rowwise and columnwise copies from ONE read of the bf16 input.  The same
+// kernel makes MXFP4 (kFP4): 1x32 E2M1 blocks under one E8M0 scale, packed
+// two codes per byte ("NVIDIA presenta una metodologia de preentrenamiento
+// de 4 bits utilizando NVFP4", section "Que es realmente NVFP4").
 //
 // "Miles Blackwell RL Cambia la Uniformidad BF16 por MXFP8 y NVFP4 Nativos",
 // section "La Compatibilidad de Miles Blackwell Ahora Abarca Todo el Ciclo de
@@ -41,15 +44,19 @@ struct __align__(16) QuantSmem {
 };
 
 // Shared exponent of a block from its amax (an f32 holding a bf16 value):
-// the smallest e with amax <= 448 * 2^e, clamped to [-127, 127].
-// amax = (1 + f) * 2^k  ->  e = k - 8 if (1 + f) <= 1.75 else k - 7.
+// the smallest e with amax <= emax * 2^e, clamped to [-127, 127], for the
+// element maximum emax = 448 = 1.75 * 2^8 (E4M3) or 6 = 1.5 * 2^2 (E2M1).
+// amax = (1 + f) * 2^k  ->  E4M3: e = k - 8 if (1 + f) <= 1.75 else k - 7;
+//                           E2M1: e = k - 2 if (1 + f) <= 1.5  else k - 1.
+template <bool kFP4>
 __device__ __forceinline__ int mx_block_exp(float amax) {
   const uint32_t u = __float_as_uint(amax);
   const int ef = static_cast<int>((u >> 23) & 0xFF);
   if (ef == 0) return -127;                      // zero or subnormal: k <= -127
   const int k = ef - 127;
   const uint32_t frac = u & 0x7FFFFFu;
-  int e = (frac <= 0x600000u) ? k - 8 : k - 7;  // 0x600000 / 2^23 = 0.75
+  int e = kFP4 ? ((frac <= 0x400000u) ? k - 2 : k - 1)    // 0x400000 / 2^23 = 0.5
+               : ((frac <= 0x600000u) ? k - 8 : k - 7);   // 0x600000 / 2^23 = 0.75
   return e < -127 ? -127 : (e > 127 ? 127 : e);
 }
 
@@ -64,7 +71,7 @@ __device__ __forceinline__ int swz(int r, int k) {  // offset inside a 128x4 til
   return (r & 31) * 16 + ((r >> 5) & 3) * 4 + (k & 3);
 }
 
-template <bool kRow, bool kCol>
+template <bool kRow, bool kCol, bool kFP4>
 __global__ void __launch_bounds__(kThreads) mxfp8_quant_kernel(
     const __grid_constant__ CUtensorMap tmap_x, int64_t R, int64_t C, uint8_t* __restrict__ q_row,
     uint8_t* __restrict__ s_row, uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col,
@@ -126,18 +133,22 @@ __global__ void __launch_bounds__(kThreads) mxfp8_quant_kernel(
         float amax = abs_halves_max(amax2(amax2(w.x, w.y), amax2(w.z, w.w)));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        const int e = mx_block_exp(amax);
+        const int e = mx_block_exp<kFP4>(amax);
         const uint64_t sc = f32x2_splat(exp2_neg(e));
         float v[8];                                  // x * 2^-e, two products per instruction
         mul_bf16x2(w.x, sc, v[0], v[1]);
         mul_bf16x2(w.y, sc, v[2], v[3]);
         mul_bf16x2(w.z, sc, v[4], v[5]);
         mul_bf16x2(w.w, sc, v[6], v[7]);
-        uint32_t p0 = cvt_e4m3x2(v[0], v[1]) | (static_cast<uint32_t>(cvt_e4m3x2(v[2], v[3])) << 16);
-        uint32_t p1 = cvt_e4m3x2(v[4], v[5]) | (static_cast<uint32_t>(cvt_e4m3x2(v[6], v[7])) << 16);
         const int64_t gr = r0 + lr, gc = c0 + cchunk * 8;
-        if (gr < R && gc < C)
-          *reinterpret_cast<uint2*>(q_row + gr * C + gc) = make_uint2(p0, p1);
+        if (kFP4) {
+          const uint32_t p = cvt_e2m1x8(v);        // 8 codes, element 0 in the low nibble
+          if (gr < R && gc < C) *reinterpret_cast<uint32_t*>(q_row + gr * (C / 2) + gc / 2) = p;
+        } else {
+          const uint32_t p0 = cvt_e4m3x2(v[0], v[1]) | (static_cast<uint32_t>(cvt_e4m3x2(v[2], v[3])) << 16);
+          const uint32_t p1 = cvt_e4m3x2(v[4], v[5]) | (static_cast<uint32_t>(cvt_e4m3x2(v[6], v[7])) << 16);
+          if (gr < R && gc < C) *reinterpret_cast<uint2*>(q_row + gr * C + gc) = make_uint2(p0, p1);
+        }
         if ((tid & 3) == 0) srow[swz(lr, blk)] = static_cast<uint8_t>(e + 127);
       }
     }
@@ -154,31 +165,53 @@ __global__ void __launch_bounds__(kThreads) mxfp8_quant_kernel(
 #pragma unroll
       for (int i = 0; i < 32; ++i) m = amax2(m, w[i]);
       const float a0 = __uint_as_float((m << 16) & 0x7FFFFFFFu), a1 = __uint_as_float(m & 0x7FFF0000u);
-      const int e0 = mx_block_exp(a0), e1 = mx_block_exp(a1);
+      const int e0 = mx_block_exp<kFP4>(a0), e1 = mx_block_exp<kFP4>(a1);
       const uint64_t s0 = f32x2_splat(exp2_neg(e0)), s1 = f32x2_splat(exp2_neg(e1));
-      uint32_t o0[8], o1[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t x0 = w[4 * j], x1 = w[4 * j + 1], x2 = w[4 * j + 2], x3 = w[4 * j + 3];
-        float p[8];
-        mul_f32x2(bf16_lo(x0), bf16_lo(x1), s0, p[0], p[1]);
-        mul_f32x2(bf16_lo(x2), bf16_lo(x3), s0, p[2], p[3]);
-        mul_f32x2(bf16_hi(x0), bf16_hi(x1), s1, p[4], p[5]);
-        mul_f32x2(bf16_hi(x2), bf16_hi(x3), s1, p[6], p[7]);
-        o0[j] = cvt_e4m3x2(p[0], p[1]) | (static_cast<uint32_t>(cvt_e4m3x2(p[2], p[3])) << 16);
-        o1[j] = cvt_e4m3x2(p[4], p[5]) | (static_cast<uint32_t>(cvt_e4m3x2(p[6], p[7])) << 16);
-      }
       const int64_t gc0 = c0 + 2 * cp, gr = r0 + rb * 32;
-      if (gr < R) {
-        if (gc0 < C) {
-          uint4* dst = reinterpret_cast<uint4*>(q_col + gc0 * R + gr);
-          dst[0] = make_uint4(o0[0], o0[1], o0[2], o0[3]);
-          dst[1] = make_uint4(o0[4], o0[5], o0[6], o0[7]);
+      if (kFP4) {
+        // 32 codes per column: four 8-code words each
+        uint32_t o0[4], o1[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float p0[8], p1[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t xa = w[8 * j + 2 * i], xb = w[8 * j + 2 * i + 1];
+            mul_f32x2(bf16_lo(xa), bf16_lo(xb), s0, p0[2 * i], p0[2 * i + 1]);
+            mul_f32x2(bf16_hi(xa), bf16_hi(xb), s1, p1[2 * i], p1[2 * i + 1]);
+          }
+          o0[j] = cvt_e2m1x8(p0);
+          o1[j] = cvt_e2m1x8(p1);
         }
-        if (gc0 + 1 < C) {
-          uint4* dst = reinterpret_cast<uint4*>(q_col + (gc0 + 1) * R + gr);
-          dst[0] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-          dst[1] = make_uint4(o1[4], o1[5], o1[6], o1[7]);
+        if (gr < R) {
+          if (gc0 < C) *reinterpret_cast<uint4*>(q_col + gc0 * (R / 2) + gr / 2) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+          if (gc0 + 1 < C)
+            *reinterpret_cast<uint4*>(q_col + (gc0 + 1) * (R / 2) + gr / 2) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+        }
+      } else {
+        uint32_t o0[8], o1[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t x0 = w[4 * j], x1 = w[4 * j + 1], x2 = w[4 * j + 2], x3 = w[4 * j + 3];
+          float p[8];
+          mul_f32x2(bf16_lo(x0), bf16_lo(x1), s0, p[0], p[1]);
+          mul_f32x2(bf16_lo(x2), bf16_lo(x3), s0, p[2], p[3]);
+          mul_f32x2(bf16_hi(x0), bf16_hi(x1), s1, p[4], p[5]);
+          mul_f32x2(bf16_hi(x2), bf16_hi(x3), s1, p[6], p[7]);
+          o0[j] = cvt_e4m3x2(p[0], p[1]) | (static_cast<uint32_t>(cvt_e4m3x2(p[2], p[3])) << 16);
+          o1[j] = cvt_e4m3x2(p[4], p[5]) | (static_cast<uint32_t>(cvt_e4m3x2(p[6], p[7])) << 16);
+        }
+        if (gr < R) {
+          if (gc0 < C) {
+            uint4* dst = reinterpret_cast<uint4*>(q_col + gc0 * R + gr);
+            dst[0] = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+            dst[1] = make_uint4(o0[4], o0[5], o0[6], o0[7]);
+          }
+          if (gc0 + 1 < C) {
+            uint4* dst = reinterpret_cast<uint4*>(q_col + (gc0 + 1) * R + gr);
+            dst[0] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+            dst[1] = make_uint4(o1[4], o1[5], o1[6], o1[7]);
+          }
         }
       }
       scol[swz(2 * cp, rb)] = static_cast<uint8_t>(e0 + 127);
@@ -215,13 +248,15 @@ __global__ void __launch_bounds__(kThreads) mxfp8_quant_kernel(
 
 size_t mxfp8_quant_smem_bytes() { return sizeof(QuantSmem) + 1024; }
 
-cudaError_t launch_mxfp8_quant(const CUtensorMap& tmap_x, int64_t R, int64_t C, bool row, bool col,
+cudaError_t launch_mxfp8_quant(const CUtensorMap& tmap_x, int64_t R, int64_t C, bool row, bool col, bool fp4,
                                uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
                                int* err, int sm_count, cudaStream_t stream) {
   const int64_t ntiles = ((R + kTile - 1) / kTile) * ((C + kTile - 1) / kTile);
   const size_t smem = mxfp8_quant_smem_bytes();
-  auto kern = row ? (col ? mxfp8_quant_kernel<true, true> : mxfp8_quant_kernel<true, false>)
-                  : mxfp8_quant_kernel<false, true>;
+  auto kern = fp4 ? (row ? (col ? mxfp8_quant_kernel<true, true, true> : mxfp8_quant_kernel<true, false, true>)
+                         : mxfp8_quant_kernel<false, true, true>)
+                  : (row ? (col ? mxfp8_quant_kernel<true, true, false> : mxfp8_quant_kernel<true, false, false>)
+                         : mxfp8_quant_kernel<false, true, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;

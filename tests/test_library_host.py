@@ -38,6 +38,10 @@ def test_scale_and_workspace_sizes(lib):
     assert m.scale_bytes(m.FMT_NVFP4, 1, 16) == 128 * 4
     assert m.scale_bytes(m.FMT_NVFP4, 4096, 2048) == 4096 * 128
     assert m.scale_bytes_grouped(m.FMT_NVFP4, 300, 4, 256) == (3 + 4) * 128 * 16
+    # MXFP4 blocks are 32 wide like MXFP8
+    assert m.scale_bytes(m.FMT_MXFP4, 130, 160) == 256 * 8
+    assert m.scale_bytes(m.FMT_MXFP4, 2048, 2048) == 2048 * 64
+    assert m.scale_bytes_grouped(m.FMT_MXFP4, 300, 4, 256) == (3 + 4) * 128 * 8
     assert m.workspace_bytes(1) >= 16 and m.workspace_bytes(256) >= 256 + 1024
 
 
@@ -60,6 +64,13 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert lib.nvfp4_quantize_per_token(p, 4, 24, 24, 0, None, 0, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
     assert lib.nvfp4_quantize_per_token(p, 4, 32, 32, 1, None, 0, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
     assert lib.nvfp4_quantize_per_token(p, 4, 32, 32, 7, None, 0, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
+    # MXFP4: same rules as MXFP8
+    assert lib.mxfp4_quantize(p, 64, 48, 48, m.ROWWISE, p, p, None, None, p, 4096, None) == m.ERR_INVALID_ARG
+    assert lib.mxfp4_quantize(p, 40, 64, 64, m.COLWISE, None, None, p, p, p, 4096, None) == m.ERR_INVALID_ARG
+    assert lib.mxfp4_quantize(p, 64, 64, 64, 0, p, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
+    assert lib.mxfp4_quantize(q, 64, 64, 64, m.ROWWISE, p, p, None, None, p, 4096, None) == m.ERR_ALIGNMENT
+    assert lib.mxfp4_quantize(p, 64, 64, 64, m.ROWWISE, p, p, None, None, None, 0, None) == m.ERR_WORKSPACE
+    assert lib.mxfp4_quantize(None, 0, 64, 64, m.ROWWISE, None, None, None, None, None, 0, None) == m.OK
     # workspace missing or too small
     assert lib.nvfp4_quantize_per_token(p, 4, 32, 32, 0, None, 0, p, p, p, None, 0, None) == m.ERR_WORKSPACE
     # GEMM: K % 32, ldc < N, accumulate into bf16, bad scale modes
@@ -68,12 +79,19 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert lib.bs_gemm(0, 8, 8, 64, p, p, None, 0, p, p, None, 0, 1, p, 8, 1, p, 4096, None) == m.ERR_UNSUPPORTED
     assert lib.bs_gemm(1, 8, 8, 64, p, p, None, 1, p, p, None, 0, 0, p, 8, 0, p, 4096, None) == m.ERR_INVALID_ARG
     assert lib.bs_gemm(0, 8, 8, 64, p, p, None, 0, p, p, None, 0, 0, p, 12, 0, p, 4096, None) == m.ERR_ALIGNMENT
+    # unknown format; MXFP4 K % 32
+    assert lib.bs_gemm(3, 8, 8, 64, p, p, None, 0, p, p, None, 0, 0, p, 8, 0, p, 4096, None) == m.ERR_INVALID_ARG
+    assert lib.bs_gemm(2, 8, 8, 48, p, p, None, 0, p, p, None, 0, 0, p, 8, 0, p, 4096, None) == m.ERR_INVALID_ARG
     # grouped: group count out of range
     assert lib.bs_grouped_gemm(1, 0, p, 8, 8, 64, p, p, None, p, p, None, 0, p, 8, p, 4096, None) == m.ERR_INVALID_ARG
     assert lib.bs_grouped_gemm(1, 5000, p, 8, 8, 64, p, p, None, p, p, None, 0, p, 8, p, 1 << 20, None) == m.ERR_INVALID_ARG
     # dequantize: MXFP8 takes no FP32 scale, bad dtype
     assert lib.dequantize(0, p, p, p, 1, None, 0, 4, 32, 0, p, None) == m.ERR_INVALID_ARG
     assert lib.dequantize(1, p, p, None, 0, None, 0, 4, 32, 5, p, None) == m.ERR_INVALID_ARG
+    # MXFP4: blocks of 32, no FP32 scale; unknown format
+    assert lib.dequantize(2, p, p, None, 0, None, 0, 4, 16, 0, p, None) == m.ERR_INVALID_ARG
+    assert lib.dequantize(2, p, p, p, 2, None, 0, 4, 32, 0, p, None) == m.ERR_INVALID_ARG
+    assert lib.dequantize(3, p, p, None, 0, None, 0, 4, 32, 0, p, None) == m.ERR_INVALID_ARG
     # empty problems are no-ops
     assert lib.mx8_quantize(None, 0, 64, 64, m.ROWWISE, None, None, None, None, None, 0, None) == m.OK
     assert lib.bs_gemm(0, 0, 8, 64, None, None, None, 0, None, None, None, 0, 0, None, 8, 0, None, 0, None) == m.OK
