@@ -16,7 +16,9 @@ One step = every operation of the hot path, on seeded synthetic inputs:
 
 value = block-scaled GEMM FLOPs of the step / step time (quantizers,
 dequantization and SwiGLU included in the time).  Per-kernel times come from
-CUDA events on the launching stream inside the timed region.
+CUDA events on the launching stream inside the timed region.  The same linear
+layer in MXFP4 (E2M1 x 32 blocks, E8M0 scales) is timed beside the step, per
+kernel, under "extra".
 
 `--impl reference` times the CPU oracle (test infrastructure, single thread)
 on a bounded sample of the same step and extrapolates to the full step.
@@ -302,6 +304,56 @@ class Step:
         return sum(w for _, kind, w in self.plan() if kind in ("fp8", "fp4"))
 
 
+class Mxfp4Linear:
+    """The step's linear layer in MXFP4 (32-element E2M1 blocks under one E8M0
+    scale): rowwise + columnwise quantization of X, W and dY, Fprop, Dgrad and
+    Wgrad, and the dequantized W^.  Measured beside the step (its own timed
+    region), not part of `value`."""
+
+    def __init__(self, step):
+        torch, mx = step.torch, step.mx
+        self.step, self.mx = step, mx
+        T, H, O = step.T, step.H_, step.O
+        dev = step.dev
+        u8 = lambda r, c: torch.empty((r, c), dtype=torch.uint8, device=dev)
+        sb = lambda r, c: torch.empty(max(mx.scale_bytes(mx.FMT_MXFP4, r, c), 16), dtype=torch.uint8, device=dev)
+        self.Xr, self.SXr, self.Xc, self.SXc = u8(T, H // 2), sb(T, H), u8(H, T // 2), sb(H, T)
+        self.Wr, self.SWr, self.Wc, self.SWc = u8(O, H // 2), sb(O, H), u8(H, O // 2), sb(H, O)
+        self.dYr, self.SdYr, self.dYc, self.SdYc = u8(T, O // 2), sb(T, O), u8(O, T // 2), sb(O, T)
+        self.Y = torch.empty((T, O), dtype=torch.bfloat16, device=dev)
+        self.dX = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        self.dW = torch.empty((O, H), dtype=torch.float32, device=dev)
+        self.What = torch.empty((O, H), dtype=torch.bfloat16, device=dev)
+
+    def plan(self):
+        st = self.step
+        T, H, O = st.T, st.H_, st.O
+        q = lambda r, c: (2 + 2 * (0.5 + 1 / 32)) * r * c     # bf16 in, two packed copies + scales out
+        return [
+            ("mxfp4_quant_rc X", "hbm", q(T, H)),
+            ("mxfp4_quant_rc W", "hbm", q(O, H)),
+            ("mxfp4_quant_rc dY", "hbm", q(T, O)),
+            ("mxfp4_gemm Fprop", "fp4", 2.0 * T * O * H),
+            ("mxfp4_gemm Dgrad", "fp4", 2.0 * T * H * O),
+            ("mxfp4_gemm Wgrad", "fp4", 2.0 * O * H * T),
+            ("dequant_mxfp4 W", "hbm", (0.5 + 1 / 32 + 2) * O * H),
+        ]
+
+    def launches(self):
+        mx, st = self.mx, self.step
+        RC = mx.ROWWISE | mx.COLWISE
+        ws = st.ws
+        return [
+            ("mxfp4_quant_rc X", lambda: mx.mxfp4_quantize_into(st.X, self.Xr, self.SXr, self.Xc, self.SXc, RC, ws)),
+            ("mxfp4_quant_rc W", lambda: mx.mxfp4_quantize_into(st.W, self.Wr, self.SWr, self.Wc, self.SWc, RC, ws)),
+            ("mxfp4_quant_rc dY", lambda: mx.mxfp4_quantize_into(st.dY, self.dYr, self.SdYr, self.dYc, self.SdYc, RC, ws)),
+            ("mxfp4_gemm Fprop", lambda: mx.bs_gemm_into(mx.FMT_MXFP4, self.Xr, self.SXr, self.Wr, self.SWr, st.H_, self.Y, ws=ws)),
+            ("mxfp4_gemm Dgrad", lambda: mx.bs_gemm_into(mx.FMT_MXFP4, self.dYr, self.SdYr, self.Wc, self.SWc, st.O, self.dX, ws=ws)),
+            ("mxfp4_gemm Wgrad", lambda: mx.bs_gemm_into(mx.FMT_MXFP4, self.dYc, self.SdYc, self.Xc, self.SXc, st.T, self.dW, ws=ws)),
+            ("dequant_mxfp4 W", lambda: mx.dequantize_into(mx.FMT_MXFP4, self.Wr, self.SWr, self.What)),
+        ]
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "moe_mx8_quantize_gb300", "csrc")
@@ -329,6 +381,64 @@ def read_traffic(label):
 
 
 # ----------------------------------------------------------------- GPU arm
+def time_each(launches, K2, stream):
+    """Per-launch device time (ms, mean of K2 runs) of a list of (label,
+    callable).  Preferred: a graph of the launches with an event pair
+    captured around every launch, replayed K2 times (no host launch gaps
+    inside the pairs); where this PyTorch cannot capture events, eager runs
+    with an event pair around every launch on the launching stream."""
+    import torch
+    try:
+        pairs = [(lab, torch.cuda.Event(enable_timing=True, external=True),
+                  torch.cuda.Event(enable_timing=True, external=True)) for lab, _ in launches]
+        fns = dict(launches)
+        tgraph = torch.cuda.CUDAGraph()
+        tside = torch.cuda.Stream()
+        tside.wait_stream(stream)
+        with torch.cuda.stream(tside):
+            with torch.cuda.graph(tgraph, stream=tside, capture_error_mode="relaxed"):
+                for lab, a, b in pairs:
+                    a.record()
+                    fns[lab]()
+                    b.record()
+        stream.wait_stream(tside)
+        tgraph.replay()
+        torch.cuda.synchronize()
+        acc = {lab: 0.0 for lab, _ in launches}
+        for _ in range(K2):
+            tgraph.replay()
+            torch.cuda.synchronize()
+            for lab, a, b in pairs:
+                acc[lab] += a.elapsed_time(b)
+        return ({lab: v / K2 for lab, v in acc.items()},
+                f"{K2} replays of a graph of the launches with captured CUDA events around each launch")
+    except (TypeError, RuntimeError):
+        pass
+    ev = {lab: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(K2)] for lab, _ in launches}
+    torch.cuda.synchronize()
+    for i in range(K2):
+        for lab, fn in launches:
+            a, b = ev[lab][i]
+            a.record(stream)
+            fn()
+            b.record(stream)
+    torch.cuda.synchronize()
+    return ({lab: statistics.mean(a.elapsed_time(b) for a, b in prs) for lab, prs in ev.items()},
+            f"{K2} eager runs, CUDA events around each launch")
+
+
+def rate_row(lab, kind, work, ms, peaks):
+    """One breakdown entry: achieved rate against the measured peak."""
+    s = ms / 1e3
+    if kind == "hbm":
+        ach, peak, unit = work / s / 1e9, peaks["hbm"], "GB/s"
+    else:
+        ach, peak, unit = work / s / 1e12, peaks["bf16_sus"] * RATIO[kind], "TFLOP/s"
+    return {"kernel": lab, "us": round(ms * 1e3, 2), "achieved": round(ach, 1), "unit": unit,
+            "peak": round(peak, 1), "frac": round(ach / peak, 4)}
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -410,63 +520,12 @@ def run_gpu(args):
     ms_step = total_ms / K
 
     # timed region 2: the per-kernel durations of the breakdown and the
-    # roofline.  Preferred: a second graph of the step with an event pair
-    # captured around every launch, replayed K2 times (no host launch gaps
-    # inside the pairs); where this PyTorch cannot capture events, eager steps
-    # with an event pair around every launch.
+    # roofline (see time_each)
     K2 = max(3, min(K, 100))
-    per, breakdown_from = None, None
-    try:
-        pairs = [(lab, torch.cuda.Event(enable_timing=True, external=True),
-                  torch.cuda.Event(enable_timing=True, external=True)) for lab, _ in launches]
-        fns = dict(launches)
-        tgraph = torch.cuda.CUDAGraph()
-        tside = torch.cuda.Stream()
-        tside.wait_stream(stream)
-        with torch.cuda.stream(tside):
-            with torch.cuda.graph(tgraph, stream=tside, capture_error_mode="relaxed"):
-                for lab, a, b in pairs:
-                    a.record()
-                    fns[lab]()
-                    b.record()
-        stream.wait_stream(tside)
-        tgraph.replay()
-        torch.cuda.synchronize()
-        acc = {lab: 0.0 for lab, _ in launches}
-        for _ in range(K2):
-            tgraph.replay()
-            torch.cuda.synchronize()
-            for lab, a, b in pairs:
-                acc[lab] += a.elapsed_time(b)
-        per = {lab: v / K2 for lab, v in acc.items()}
-        breakdown_from = f"{K2} replays of a graph of the step with captured CUDA events around each launch"
-    except (TypeError, RuntimeError):
-        per = None
-    if per is None:
-        ev = {lab: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                    for _ in range(K2)] for lab, _ in launches}
-        torch.cuda.synchronize()
-        for i in range(K2):
-            for lab, fn in launches:
-                a, b = ev[lab][i]
-                a.record(stream)
-                fn()
-                b.record(stream)
-        torch.cuda.synchronize()
-        per = {lab: statistics.mean(a.elapsed_time(b) for a, b in prs) for lab, prs in ev.items()}
-        breakdown_from = f"{K2} eager steps, CUDA events around each launch"
+    per, breakdown_from = time_each(launches, K2, stream)
     check_errors("in the per-kernel timing")
     peaks = load_peaks()
-    breakdown = []
-    for lab, ms in per.items():
-        kind, w = plan[lab]
-        s = ms / 1e3
-        if kind == "hbm":
-            ach, peak, unit = w / s / 1e9, peaks["hbm"], "GB/s"
-        else:
-            ach, peak, unit = w / s / 1e12, peaks["bf16_sus"] * RATIO[kind], "TFLOP/s"
-        breakdown.append({"kernel": lab, "us": round(ms * 1e3, 2), "achieved": round(ach, 1), "unit": unit,
-                          "peak": round(peak, 1), "frac": round(ach / peak, 4)})
+    breakdown = [rate_row(lab, *plan[lab], ms, peaks) for lab, ms in per.items()]
     dom = max(breakdown, key=lambda b: b["us"])
     dkind, dwork = plan[dom["kernel"]]
     traffic = read_traffic(dom["kernel"])
@@ -480,6 +539,23 @@ def run_gpu(args):
     value = world * flops / (ms_step / 1e3) / 1e12
     launches_per_step = sum(Step.KERNELS_PER_LABEL.get(lab, 1) for lab, _ in launches)
     gpu_launches = launches_per_step * (K + K2)
+
+    # timed region 3: the MXFP4 linear layer, beside the step
+    extra = None
+    if not args.no_extra:
+        fp4 = Mxfp4Linear(step)
+        fl = fp4.launches()
+        for _ in range(3):
+            for _, fn in fl:
+                fn()
+        torch.cuda.synchronize()
+        check_errors("in the MXFP4 warm-up")
+        fper, ffrom = time_each(fl, K2, stream)
+        check_errors("in the MXFP4 timing")
+        fplan = {lab: (kind, w) for lab, kind, w in fp4.plan()}
+        extra = {"mxfp4_linear": [rate_row(lab, *fplan[lab], ms, peaks) for lab, ms in fper.items()],
+                 "from": ffrom}
+        gpu_launches += len(fl) * K2
 
     e2e = None
     if not args.no_e2e:
@@ -499,7 +575,7 @@ def run_gpu(args):
                    "value_definition": "block-scaled GEMM FLOPs / step time incl. quantizers",
                    "parallelism": f"replicas x{world} (no data-path collective)"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-        "gpu_launches": gpu_launches, "breakdown": breakdown,
+        "gpu_launches": gpu_launches, "breakdown": breakdown, "extra": extra,
         "timing": {"value_from": f"{K} CUDA-graph replays of the step",
                    "breakdown_from": breakdown_from,
                    "kernels_sum_ms_per_step": round(sum(b["us"] for b in breakdown) / 1e3, 4)},
@@ -663,6 +739,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the MXFP4 linear-layer measurement")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -1,4 +1,5 @@
-"""CPU oracle for MXFP8 / per-token NVFP4 quantization and block-scaled GEMM.
+"""CPU oracle for MXFP8 / per-token NVFP4 / MXFP4 quantization, the
+block-scaled GEMM and the dequantized-backward BF16 GEMM.
 
 TEST INFRASTRUCTURE ONLY.  The test suite, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg are the only callers; the library's product path
@@ -87,6 +88,7 @@ def _L():
                                             _p, _p, _p, _p, _p, _p,
                                             _p, _i64, _p, _p, _p]
         lib.or_swiglu.argtypes = [_p, _i64, _i64, _p]
+        lib.or_bf16_gemm_ref.argtypes = [_i64, _i64, _i64, _p, _i64, _p, _i64, _p, _i64, _p, _p]
         _lib = lib
     return _lib
 
@@ -327,6 +329,24 @@ def grouped_gemm_ref(fmt, offs, A, SA, B, SB, K, a32=None, b32=None, pairs=None)
     _L().or_grouped_gemm_ref(fmt, G, _ptr(o), N, K, _ptr(A), _ptr(SA), _ptr(a),
                              _ptr(B), _ptr(SB), _ptr(b), _ptr(pr), pr.shape[0],
                              _ptr(ref), _ptr(absref), _ptr(scratch))
+    return ref, absref
+
+
+def bf16_gemm_ref(A_bits, B_bits, pairs=None):
+    """FP64 reference of Y = A . B^T over bf16 operands (bit patterns,
+    A [M, K], B [N, K]): the dequantized-backward BF16 GEMM.
+    Returns (ref, absref): [M, N] arrays, or [npairs] for sampled pairs."""
+    A = _c(A_bits, np.uint16); B = _c(B_bits, np.uint16)
+    (M, K), N = A.shape, B.shape[0]
+    assert B.shape[1] == K
+    pr = None if pairs is None else _c(pairs, np.int64).reshape(-1, 2)
+    n = M * N if pr is None else pr.shape[0]
+    ref = np.empty(n, np.float64)
+    absref = np.empty(n, np.float64)
+    _L().or_bf16_gemm_ref(M, N, K, _ptr(A), K, _ptr(B), K, _ptr(pr), 0 if pr is None else pr.shape[0],
+                          _ptr(ref), _ptr(absref))
+    if pr is None:
+        return ref.reshape(M, N), absref.reshape(M, N)
     return ref, absref
 
 

@@ -1,6 +1,7 @@
 /*
  * CPU ORACLE for microscaling quantization (MXFP8, per-token NVFP4, MXFP4)
- * and the block-scaled GEMM those encodings feed.
+ * and the block-scaled GEMM those encodings feed (plus the plain BF16 GEMM of
+ * the dequantized-backward mode).
  *
  * This file is TEST INFRASTRUCTURE.  Only the test suite, the smoke check and
  * the benchmark's CPU-baseline leg may load it.  It shares no code, header,
@@ -577,6 +578,32 @@ void or_grouped_gemm_ref(int fmt, int G, const i64 *offs, i64 N, i64 K,
         for (i64 k = 0; k < K; k++) {
             acc += ar[k] * br[k];
             aacc += fabs(ar[k]) * fabs(br[k]);
+        }
+        ref[p] = acc;
+        absref[p] = aacc;
+    }
+}
+
+/* Plain GEMM over bf16 operands, for the dequantized-backward mode ([MRL]
+ * "La Compatibilidad...": Dgrad and Wgrad run in BF16 on operands rebuilt
+ * from the low-precision forward copies):
+ *   ref[m,n] = sum_k a[m,k] * b[n,k]   (Y = A * B^T, K contiguous in both)
+ * in double; every product of two bf16 values is exact in double.  Rows of
+ * A and B are lda / ldb elements apart.  pairs / npairs as in or_gemm_ref. */
+void or_bf16_gemm_ref(i64 M, i64 N, i64 K, const uint16_t *A, i64 lda,
+                      const uint16_t *B, i64 ldb, const i64 *pairs, i64 npairs,
+                      double *ref, double *absref)
+{
+    i64 count = pairs ? npairs : M * N;
+    for (i64 p = 0; p < count; p++) {
+        i64 m = pairs ? pairs[2 * p] : p / N;
+        i64 n = pairs ? pairs[2 * p + 1] : p % N;
+        const uint16_t *ar = A + m * lda, *br = B + n * ldb;
+        double acc = 0.0, aacc = 0.0;
+        for (i64 k = 0; k < K; k++) {
+            double x = (double)or_bf16_to_f32(ar[k]), y = (double)or_bf16_to_f32(br[k]);
+            acc += x * y;
+            aacc += fabs(x) * fabs(y);
         }
         ref[p] = acc;
         absref[p] = aacc;

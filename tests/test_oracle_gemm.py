@@ -139,3 +139,65 @@ def test_grouped_swizzle_pads_every_group_to_whole_tiles():
     parts = [_swizzle_by_reshape(canon[offs[g]:offs[g + 1]]) for g in range(4) if offs[g + 1] > offs[g]]
     assert np.array_equal(got, np.concatenate(parts))
     assert got.size == oracle.swizzled_bytes(400, 6, offs) == (2 + 1 + 3) * 128 * 8
+
+
+# ------------------------------------------------------------------ BF16 GEMM
+def _bf16_fraction(bits):
+    """Exact value of bf16 bit patterns, decoded through PyTorch's bfloat16."""
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).double()
+    return [Fraction(v) for v in t.ravel().tolist()]
+
+
+def _rand_bf16(rng, shape):
+    """Finite bf16 patterns with exponents in [-40, 40] and random signs."""
+    sign = rng.integers(0, 2, size=shape).astype(np.uint16) << 15
+    exp = rng.integers(127 - 40, 127 + 40, size=shape).astype(np.uint16) << 7
+    man = rng.integers(0, 128, size=shape).astype(np.uint16)
+    return (sign | exp | man).astype(np.uint16)
+
+
+def test_bf16_gemm_brute_force_exact():
+    rng = np.random.default_rng(21)
+    M, N, K = 3, 2, 24
+    a, b = _rand_bf16(rng, (M, K)), _rand_bf16(rng, (N, K))
+    ref, absref = oracle.bf16_gemm_ref(a, b)
+    for m in range(M):
+        ar = _bf16_fraction(a[m])
+        for n in range(N):
+            br = _bf16_fraction(b[n])
+            exact = sum(x * y for x, y in zip(ar, br))
+            aexact = sum(abs(x * y) for x, y in zip(ar, br))
+            assert abs(Fraction(ref[m, n]) - exact) <= Fraction(1, 10 ** 12) * aexact
+            assert abs(Fraction(absref[m, n]) - aexact) <= Fraction(1, 10 ** 12) * aexact
+
+
+@pytest.mark.parametrize("fmt", [0, 2])
+def test_bf16_gemm_on_dequantized_operands_equals_block_scaled(fmt):
+    """The dequantized-backward identity: E4M3 / E2M1 codes times a power of
+    two are exact in bf16, so the BF16 GEMM over the dequantized operands sums
+    the very products the block-scaled reference sums, in the same order."""
+    from moe_mx8_quantize_gb300 import inputs
+    K = 160
+    xa = inputs.bits(inputs.normal_bf16((5, K), 1.0, torch.Generator().manual_seed(1), "cpu"))
+    xb = inputs.bits(inputs.normal_bf16((7, K), 0.02, torch.Generator().manual_seed(2), "cpu"))
+    if fmt == 0:
+        (qa, sa), (qb, sb) = oracle.mxfp8_quantize_rowwise(xa), oracle.mxfp8_quantize_rowwise(xb)
+        da, db = oracle.dequant_mxfp8(qa, sa), oracle.dequant_mxfp8(qb, sb)
+    else:
+        (qa, sa), (qb, sb) = oracle.mxfp4_quantize_rowwise(xa), oracle.mxfp4_quantize_rowwise(xb)
+        da, db = oracle.dequant_mxfp4(qa, sa), oracle.dequant_mxfp4(qb, sb)
+    ba, bb = oracle.f32_to_bf16(da), oracle.f32_to_bf16(db)
+    assert np.array_equal(oracle.bf16_to_f32(ba), da) and np.array_equal(oracle.bf16_to_f32(bb), db)
+    ref, absref = oracle.bf16_gemm_ref(ba, bb)
+    want, awant = oracle.gemm_ref(fmt, qa, sa, qb, sb, K)
+    assert np.array_equal(ref, want) and np.array_equal(absref, awant)
+
+
+def test_bf16_gemm_sampled_pairs_match_full():
+    rng = np.random.default_rng(22)
+    a, b = _rand_bf16(rng, (9, 40)), _rand_bf16(rng, (6, 40))
+    full, afull = oracle.bf16_gemm_ref(a, b)
+    pairs = np.array([(8, 5), (0, 0), (3, 2), (3, 1)])
+    ref, absref = oracle.bf16_gemm_ref(a, b, pairs)
+    assert np.array_equal(ref, full[pairs[:, 0], pairs[:, 1]])
+    assert np.array_equal(absref, afull[pairs[:, 0], pairs[:, 1]])
