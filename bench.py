@@ -17,7 +17,8 @@ One step = every operation of the hot path, on seeded synthetic inputs:
 value = block-scaled GEMM FLOPs of the step / step time (quantizers,
 dequantization and SwiGLU included in the time).  Per-kernel times come from
 CUDA events on the launching stream inside the timed region.  The same linear
-layer in MXFP4 (E2M1 x 32 blocks, E8M0 scales) is timed beside the step, per
+layer in MXFP4 (E2M1 x 32 blocks, E8M0 scales), and its dequantized-backward
+mode (dequantize + dense BF16 Dgrad / Wgrad), are timed beside the step, per
 kernel, under "extra".
 
 `--impl reference` times the CPU oracle (test infrastructure, single thread)
@@ -60,7 +61,7 @@ def load_peaks():
 
 
 # nominal dense-rate ratios to bf16 on GB300 (2.25 / 4.5 / 13.5 PFLOP/s)
-RATIO = {"fp8": 2.0, "fp4": 6.0}
+RATIO = {"bf16": 1.0, "fp8": 2.0, "fp4": 6.0}
 
 
 # ----------------------------------------------------------------- clocks
@@ -354,6 +355,48 @@ class Mxfp4Linear:
         ]
 
 
+class DequantBackward:
+    """The dequantized-backward mode of the step's linear layer: the MXFP8
+    copies the block-scaled backward uses, rebuilt in bf16 by dequantize(),
+    then Dgrad = deq(dY_row) deq(W_col)^T and Wgrad = deq(dY_col) deq(X_col)^T
+    as dense BF16 tensor-core GEMMs.  Measured beside the step (it reads the
+    step's quantized copies), not part of `value`."""
+
+    def __init__(self, step):
+        torch = step.torch
+        self.step, self.mx = step, step.mx
+        T, H, O = step.T, step.H_, step.O
+        bf = lambda r, c: torch.empty((r, c), dtype=torch.bfloat16, device=step.dev)
+        self.dYr_h, self.Wc_h, self.dYc_h, self.Xc_h = bf(T, O), bf(H, O), bf(O, T), bf(H, T)
+        self.dX = bf(T, H)
+        self.dW = torch.empty((O, H), dtype=torch.float32, device=step.dev)
+
+    def plan(self):
+        st = self.step
+        T, H, O = st.T, st.H_, st.O
+        dq = lambda r, c: (1 + 1 / 32 + 2) * r * c
+        return [
+            ("dequant_mxfp8 dY_row", "hbm", dq(T, O)),
+            ("dequant_mxfp8 W_col", "hbm", dq(H, O)),
+            ("dequant_mxfp8 dY_col", "hbm", dq(O, T)),
+            ("dequant_mxfp8 X_col", "hbm", dq(H, T)),
+            ("bf16_gemm Dgrad", "bf16", 2.0 * T * H * O),
+            ("bf16_gemm Wgrad", "bf16", 2.0 * O * H * T),
+        ]
+
+    def launches(self):
+        mx, st = self.mx, self.step
+        f = mx.FMT_MXFP8
+        return [
+            ("dequant_mxfp8 dY_row", lambda: mx.dequantize_into(f, st.dYr, st.SdYr, self.dYr_h)),
+            ("dequant_mxfp8 W_col", lambda: mx.dequantize_into(f, st.Wc, st.SWc, self.Wc_h)),
+            ("dequant_mxfp8 dY_col", lambda: mx.dequantize_into(f, st.dYc, st.SdYc, self.dYc_h)),
+            ("dequant_mxfp8 X_col", lambda: mx.dequantize_into(f, st.Xc, st.SXc, self.Xc_h)),
+            ("bf16_gemm Dgrad", lambda: mx.bf16_gemm_into(self.dYr_h, self.Wc_h, self.dX, ws=st.ws)),
+            ("bf16_gemm Wgrad", lambda: mx.bf16_gemm_into(self.dYc_h, self.Xc_h, self.dW, ws=st.ws)),
+        ]
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "moe_mx8_quantize_gb300", "csrc")
@@ -540,22 +583,24 @@ def run_gpu(args):
     launches_per_step = sum(Step.KERNELS_PER_LABEL.get(lab, 1) for lab, _ in launches)
     gpu_launches = launches_per_step * (K + K2)
 
-    # timed region 3: the MXFP4 linear layer, beside the step
+    # timed region 3: the MXFP4 linear layer and the dequantized-backward
+    # BF16 GEMMs, beside the step (each in its own graph with event pairs)
     extra = None
     if not args.no_extra:
-        fp4 = Mxfp4Linear(step)
-        fl = fp4.launches()
-        for _ in range(3):
-            for _, fn in fl:
-                fn()
-        torch.cuda.synchronize()
-        check_errors("in the MXFP4 warm-up")
-        fper, ffrom = time_each(fl, K2, stream)
-        check_errors("in the MXFP4 timing")
-        fplan = {lab: (kind, w) for lab, kind, w in fp4.plan()}
-        extra = {"mxfp4_linear": [rate_row(lab, *fplan[lab], ms, peaks) for lab, ms in fper.items()],
-                 "from": ffrom}
-        gpu_launches += len(fl) * K2
+        extra = {}
+        for key, part in (("mxfp4_linear", Mxfp4Linear(step)), ("dequantized_backward", DequantBackward(step))):
+            fl = part.launches()
+            for _ in range(3):
+                for _, fn in fl:
+                    fn()
+            torch.cuda.synchronize()
+            check_errors(f"in the {key} warm-up")
+            fper, ffrom = time_each(fl, K2, stream)
+            check_errors(f"in the {key} timing")
+            fplan = {lab: (kind, w) for lab, kind, w in part.plan()}
+            extra[key] = [rate_row(lab, *fplan[lab], ms, peaks) for lab, ms in fper.items()]
+            extra["from"] = ffrom
+            gpu_launches += len(fl) * K2
 
     e2e = None
     if not args.no_e2e:

@@ -1,6 +1,7 @@
 /*
- * mx8q -- microscaling quantization (MXFP8, per-token NVFP4, MXFP4) and the
- * block-scaled tensor-core GEMM it feeds, for GB300 (sm_103a).
+ * mx8q -- microscaling quantization (MXFP8, per-token NVFP4, MXFP4), the
+ * block-scaled tensor-core GEMM it feeds and the BF16 GEMM of the
+ * dequantized-backward mode, for GB300 (sm_103a).
  *
  * Plain C ABI: device pointers, sizes and a CUDA stream; no framework types.
  *
@@ -255,6 +256,25 @@ mx8_status bs_grouped_gemm(int fmt, int num_groups, const int64_t *group_offsets
                            const uint8_t *B, const uint8_t *SB, const float *B32,
                            int out_dtype, void *C, int64_t ldc,
                            void *workspace, size_t workspace_bytes, mx8_stream_t stream);
+
+/*
+ * Dense BF16 GEMM on the tcgen05 tensor cores, for the dequantized-backward
+ * mode ([MRL] "La Compatibilidad...": the backward GEMMs run in BF16 on
+ * operands rebuilt by dequantize() from the low-precision copies, e.g.
+ * Dgrad = deq(dY rowwise) x deq(W columnwise)^T, Wgrad = deq(dY columnwise)
+ * x deq(X columnwise)^T):
+ *     C[m, n] (+)= sum_k A[m, k] * B[n, k]
+ *   A : bf16 [M, K], row stride lda >= K elements
+ *   B : bf16 [N, K], row stride ldb >= K elements
+ *   C : [M, N] with row stride ldc, f32 or bf16; accumulate=1 adds to C
+ *       (f32 only)
+ * Requires K % 8 == 0, lda/ldb/ldc % 8 == 0, 16-byte aligned pointers.
+ * Accumulation is FP32 in tensor memory.
+ */
+mx8_status bf16_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
+                     const void *B, int64_t ldb, int out_dtype, void *C, int64_t ldc,
+                     int accumulate, void *workspace, size_t workspace_bytes,
+                     mx8_stream_t stream);
 
 /*
  * SwiGLU between the joint gate|up GEMM and the down GEMM of a MoE expert

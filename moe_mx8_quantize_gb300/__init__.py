@@ -30,7 +30,7 @@ S32_NONE, S32_ROW, S32_TENSOR, S32_GROUP = 0, 1, 2, 3
 EXPORTS = ("mx8_scale_bytes", "mx8_scale_bytes_grouped", "mx8_workspace_bytes",
            "mx8_device_sm_count", "mx8_quantize", "mxfp4_quantize", "nvfp4_quantize_per_token",
            "nvfp4_quantize_per_token_noalloc", "dequantize",
-           "bs_gemm", "bs_grouped_gemm", "mx8_swiglu", "mx8_check_device_error", "mx8_selftest_bounded_wait",
+           "bs_gemm", "bs_grouped_gemm", "bf16_gemm", "mx8_swiglu", "mx8_check_device_error", "mx8_selftest_bounded_wait",
            "mx8_status_string")
 
 
@@ -80,6 +80,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bs_grouped_gemm.restype = _i
     lib.bs_grouped_gemm.argtypes = [_i, _i, _p, _i64, _i64, _i64, _p, _p, _p, _p, _p, _p, _i, _p,
                                     _i64, _p, _sz, _p]
+    lib.bf16_gemm.restype = _i
+    lib.bf16_gemm.argtypes = [_i64, _i64, _i64, _p, _i64, _p, _i64, _i, _p, _i64, _i, _p, _sz, _p]
     lib.mx8_swiglu.restype = _i
     lib.mx8_swiglu.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p]
     lib.mx8_check_device_error.restype = _i
@@ -262,6 +264,28 @@ def dequantize(fmt, q, s, s32=None, s32_mode=None, group_offsets=None, out_dtype
             s32_mode = S32_TENSOR
     out = torch.empty((R, C), dtype=out_dtype, device=q.device)
     dequantize_into(fmt, q, s, out, s32, s32_mode, group_offsets, stream)
+    return out
+
+
+# ---------------------------------------------------------------- BF16 GEMM
+def bf16_gemm_into(A, B, out, accumulate=False, ws=None, stream=None):
+    """out (+)= A @ B^T for bf16 A [M, K], B [N, K] (rows K-contiguous, any
+    row stride that is a multiple of 8); out f32 or bf16 [M, N]."""
+    assert A.dtype == torch.bfloat16 and B.dtype == torch.bfloat16
+    assert A.stride(1) == 1 and B.stride(1) == 1 and out.stride(1) == 1
+    (M, K), N = A.shape, B.shape[0]
+    assert B.shape[1] == K and out.shape == (M, N)
+    ws = _ws(ws, 1, A.device)
+    od = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
+    _check(load().bf16_gemm(M, N, K, _ptr(A), A.stride(0), _ptr(B), B.stride(0), od, _ptr(out), out.stride(0),
+                            int(accumulate), _ptr(ws), ws.numel(), _stream(stream)), "bf16_gemm")
+
+
+def bf16_gemm(A, B, out_dtype=torch.float32, ws=None, stream=None):
+    """Dense BF16 GEMM A @ B^T on the tensor cores (the dequantized-backward
+    mode's Dgrad / Wgrad)."""
+    out = torch.empty((A.shape[0], B.shape[0]), dtype=out_dtype, device=A.device)
+    bf16_gemm_into(A, B, out, False, ws, stream)
     return out
 
 

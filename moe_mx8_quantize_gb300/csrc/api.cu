@@ -333,6 +333,45 @@ extern "C" mx8_status bs_grouped_gemm(int fmt, int num_groups, const int64_t* gr
   return from_cuda(launch_bs_gemm(a, ma, mb, mc, sm_count_current(), s));
 }
 
+// ===================================================================== BF16 GEMM
+extern "C" mx8_status bf16_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                                const void* B, int64_t ldb, int out_dtype, void* C, int64_t ldc,
+                                int accumulate, void* workspace, size_t workspace_bytes,
+                                mx8_stream_t stream) {
+  if (M < 0 || N < 0 || K < 0) return MX8_ERR_INVALID_ARG;
+  if (out_dtype != MX8_OUT_F32 && out_dtype != MX8_OUT_BF16) return MX8_ERR_INVALID_ARG;
+  if (K % 8 != 0 || lda < K || ldb < K || ldc < N) return MX8_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return MX8_OK;
+  if (A == nullptr || B == nullptr || C == nullptr) return MX8_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C) || lda % 8 != 0 || ldb % 8 != 0 || ldc % 8 != 0)
+    return MX8_ERR_ALIGNMENT;
+  if (accumulate && out_dtype != MX8_OUT_F32) return MX8_ERR_UNSUPPORTED;
+  if (M > INT32_MAX || N > INT32_MAX) return MX8_ERR_UNSUPPORTED;
+  mx8_status st = check_ws(workspace, workspace_bytes, 1);
+  if (st != MX8_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) return accumulate ? MX8_OK : from_cuda(zero_output(C, ldc, M, N, out_dtype, s));
+
+  // the bf16 rows are moved as bytes: one swizzle atom (64 elements) of K per
+  // row and stage, 128 rows per box
+  CUtensorMap ma, mb, mc;
+  const uint32_t box[2] = {kGemmKBytes, 128};
+  const uint64_t da[2] = {static_cast<uint64_t>(2 * K), static_cast<uint64_t>(M)};
+  const uint64_t sa[1] = {static_cast<uint64_t>(2 * lda)};
+  const uint64_t db[2] = {static_cast<uint64_t>(2 * K), static_cast<uint64_t>(N)};
+  const uint64_t sb[1] = {static_cast<uint64_t>(2 * ldb)};
+  if (!encode_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, A, da, sa, box, gemm_swizzle()) ||
+      !encode_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, B, db, sb, box, gemm_swizzle()) ||
+      !encode_output_map(&mc, C, M, N, ldc, out_dtype))
+    return MX8_ERR_CUDA;
+  GemmArgs a{};
+  a.fmt = 3; a.M = M; a.N = N; a.K = K;
+  a.a32_mode = MX8_S32_NONE; a.b32_mode = MX8_S32_NONE;
+  a.C = C; a.ldc = ldc; a.out_bf16 = out_dtype == MX8_OUT_BF16; a.accumulate = accumulate;
+  a.grouped = 0; a.G = 1; a.offs = nullptr; a.err = err_word(workspace);
+  return from_cuda(launch_bs_gemm(a, ma, mb, mc, sm_count_current(), s));
+}
+
 // ===================================================================== errors
 extern "C" mx8_status mx8_check_device_error(void* workspace, mx8_stream_t stream) {
   if (workspace == nullptr) return MX8_ERR_WORKSPACE;

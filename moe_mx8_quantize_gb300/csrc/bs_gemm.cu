@@ -2,7 +2,8 @@
 // (kind::mxf8f6f4, E4M3 x E4M3, UE8M0 scale per 32 along K), NVFP4
 // (kind::mxf4nvf4, packed E2M1 x E2M1, UE4M3 scale per 16 along K) and MXFP4
 // (kind::mxf4nvf4, packed E2M1 x E2M1, UE8M0 scale per 32 along K), plain and
-// grouped (MoE routed experts).
+// grouped (MoE routed experts); and the plain BF16 GEMM (kind::f16, no block
+// scales) of the dequantized-backward mode, on the same pipeline.
 //
 // "Miles Blackwell RL Cambia la Uniformidad BF16 por MXFP8 y NVFP4 Nativos",
 // section "La Compatibilidad...": MXFP8 serves the forward, weight-gradient
@@ -89,6 +90,14 @@ struct Cfg<1> {                 // NVFP4: 2 elements per byte, 64 elements per M
   static constexpr int kSfTiles = kElemsPerStage / kElemsPerTile;
 };
 template <>
+struct Cfg<3> {                 // BF16: 2 bytes per element, 16 elements per MMA, no scales
+  static constexpr int kElemsPerStage = kKBytes / 2;
+  static constexpr int kElemsPerMma = 16;
+  static constexpr int kBlock = 32;            // unused
+  static constexpr int kElemsPerTile = 128;    // unused
+  static constexpr int kSfTiles = 0;
+};
+template <>
 struct Cfg<2> {                 // MXFP4: 2 elements per byte, 64 elements (2 scales) per MMA
   static constexpr int kElemsPerStage = 2 * kKBytes;
   static constexpr int kElemsPerMma = 64;
@@ -101,8 +110,9 @@ template <int kFmt, bool kGrouped, int kBN>
 struct Layout {
   static constexpr int kBRow128 = kBN / 128;                         // 128-row blocks of B
   static constexpr int kTileBBytes = kBN * kKBytes;
-  static constexpr int kSfaBytes = Cfg<kFmt>::kSfTiles * 512;
-  static constexpr int kSfbBytes = Cfg<kFmt>::kSfTiles * 512 * kBRow128;
+  // (16 bytes of unused placeholder when the format has no block scales)
+  static constexpr int kSfaBytes = Cfg<kFmt>::kSfTiles > 0 ? Cfg<kFmt>::kSfTiles * 512 : 16;
+  static constexpr int kSfbBytes = Cfg<kFmt>::kSfTiles > 0 ? Cfg<kFmt>::kSfTiles * 512 * kBRow128 : 16;
   static constexpr int kStageBytes = kTileABytes + kTileBBytes + kSfaBytes + kSfbBytes;
   static constexpr int kEpiStageBytes = 2048;                         // 32 rows x 64 B per epilogue warp
   static constexpr int kFixed = 256 + (kBN / 32) * kEpiStageBytes +
@@ -153,6 +163,19 @@ __device__ __forceinline__ uint32_t make_idesc(int fmt, int n, uint32_t sf_id) {
   d |= (fmt == 1 ? 0u : 1u) << 23;
   d |= static_cast<uint32_t>(BM >> 4) << 24;
   d |= (sf_id & 3u) << 29;
+  return d;
+}
+
+// Instruction descriptor of the dense BF16 MMA (kind::f16; M = 128, both
+// operands K-major): D format F32 bits 4-5, A/B format BF16 bits 7-9 / 10-12,
+// N >> 3 bits 17-22, M >> 4 bits 24-28.
+__device__ __forceinline__ uint32_t make_idesc_bf16(int n) {
+  uint32_t d = 0;
+  d |= 1u << 4;    // F32 accumulator
+  d |= 1u << 7;    // A: BF16
+  d |= 1u << 10;   // B: BF16
+  d |= static_cast<uint32_t>(n >> 3) << 17;
+  d |= static_cast<uint32_t>(BM >> 4) << 24;
   return d;
 }
 
@@ -244,10 +267,9 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
   const int64_t nunits = tiles_m * tiles_n;          // output tiles, strided over the CTAs
   const int64_t unit0 = blockIdx.x, ustep = gridDim.x;
   auto tile_of = [&](int64_t u) { return decode_tile<kGrouped, kBN>(u, tiles_n, M, gs, args.G); };
-  const int64_t kbytes = kFmt == 0 ? K : K / 2;
+  const int64_t kbytes = kFmt == 0 ? K : (kFmt == 3 ? 2 * K : K / 2);
   const int ktiles = static_cast<int>((kbytes + kKBytes - 1) / kKBytes);
   const int64_t sf_kt = (K / F::kBlock + 3) / 4;          // scale tiles along K
-  const int G = args.G;
 
   // producer index: 0 = warp 0 (A and the scale tiles), 1 + h = B box h
   const int prod = warp == 0 ? 0 : (warp >= 2 + L::kEpiWarps ? warp - 1 - L::kEpiWarps : -1);
@@ -276,14 +298,19 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
           }
           const uint32_t full = smem_u32(&sm.full[s]);
           if (prod == 0) {
-            const int64_t sf0 = static_cast<int64_t>(kt) * F::kElemsPerStage / F::kElemsPerTile;
-            const int nsf = static_cast<int>(sf_kt - sf0 < F::kSfTiles ? sf_kt - sf0 : F::kSfTiles);
-            mbar_arrive_expect_tx(full, kTileABytes + (1 + L::kBRow128) * nsf * 512);
-            tma_load_2d(smem_u32(sm.a[s]), &tmap_a, kt * kKBytes, static_cast<int32_t>(tc.a_row0), full);
-            bulk_load(smem_u32(sm.sfa[s]), sfa_src + sf0 * 512, nsf * 512, full);
+            if constexpr (F::kSfTiles > 0) {
+              const int64_t sf0 = static_cast<int64_t>(kt) * F::kElemsPerStage / F::kElemsPerTile;
+              const int nsf = static_cast<int>(sf_kt - sf0 < F::kSfTiles ? sf_kt - sf0 : F::kSfTiles);
+              mbar_arrive_expect_tx(full, kTileABytes + (1 + L::kBRow128) * nsf * 512);
+              tma_load_2d(smem_u32(sm.a[s]), &tmap_a, kt * kKBytes, static_cast<int32_t>(tc.a_row0), full);
+              bulk_load(smem_u32(sm.sfa[s]), sfa_src + sf0 * 512, nsf * 512, full);
 #pragma unroll
-            for (int h = 0; h < L::kBRow128; ++h)
-              bulk_load(smem_u32(sm.sfb[s]) + h * F::kSfTiles * 512, sfb_src[h] + sf0 * 512, nsf * 512, full);
+              for (int h = 0; h < L::kBRow128; ++h)
+                bulk_load(smem_u32(sm.sfb[s]) + h * F::kSfTiles * 512, sfb_src[h] + sf0 * 512, nsf * 512, full);
+            } else {
+              mbar_arrive_expect_tx(full, kTileABytes);
+              tma_load_2d(smem_u32(sm.a[s]), &tmap_a, kt * kKBytes, static_cast<int32_t>(tc.a_row0), full);
+            }
           } else {
             // B in 128-row boxes (a 128-row box is 16 KB; boxes stack in shared memory)
             const int h = prod - 1;
@@ -328,7 +355,8 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
           }
           tc_fence_after();
           const int64_t sf0 = static_cast<int64_t>(kt) * F::kElemsPerStage / F::kElemsPerTile;
-          const int nsf = static_cast<int>(sf_kt - sf0 < F::kSfTiles ? sf_kt - sf0 : F::kSfTiles);
+          const int nsf = F::kSfTiles == 0 ? 0
+                          : static_cast<int>(sf_kt - sf0 < F::kSfTiles ? sf_kt - sf0 : F::kSfTiles);
           // tensor-memory scale layout per stage: A -> 4 columns per K sub-tile;
           // B -> (4 columns x kBRow128) per K sub-tile, the 128-row blocks adjacent
           const uint32_t tsfa = sf_base + s * L::kSfColsPerStage;
@@ -353,7 +381,9 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
             const uint64_t ad = smem_desc(a0 + kk * 32, 16, kAtomSbo, kSwizzle);
             const uint64_t bd = smem_desc(b0 + kk * 32, 16, kAtomSbo, kSwizzle);
             const uint32_t acc = (kt > 0 || kk > 0) ? 1u : 0u;
-            if (kFmt == 0)
+            if (kFmt == 3)
+              tc_mma_bf16(d_tmem, ad, bd, make_idesc_bf16(kBN), acc);
+            else if (kFmt == 0)
               tc_mma_mxf8(d_tmem, ad, bd, make_idesc(0, kBN, sf_id0 + kk), tsfa, tsfb, acc);
             else if (kFmt == 2)
               tc_mma_mxf4(d_tmem, ad, bd, make_idesc(2, kBN, 2u * (kk & 1)), tsfa + 4 * (kk >> 1),
@@ -537,6 +567,10 @@ cudaError_t launch_bs_gemm(const GemmArgs& a, const CUtensorMap& tmap_a, const C
   if (a.fmt == 0) {
     return a.grouped ? launch_variant<0, true, BN>(a, tmap_a, tmap_b, tmap_c, sm_count, stream)
                      : launch_variant<0, false, BN>(a, tmap_a, tmap_b, tmap_c, sm_count, stream);
+  }
+  if (a.fmt == 3) {
+    return a.grouped ? cudaErrorInvalidValue
+                     : launch_variant<3, false, BN>(a, tmap_a, tmap_b, tmap_c, sm_count, stream);
   }
   if (a.fmt == 2) {
     return a.grouped ? launch_variant<2, true, BN>(a, tmap_a, tmap_b, tmap_c, sm_count, stream)

@@ -39,7 +39,7 @@ cudaError_t launch_swiglu(const uint16_t* gu, int64_t R, int64_t F, int64_t ld_g
                           int64_t ld_h, int sm_count, cudaStream_t stream);
 
 struct GemmArgs {
-  int fmt;                 // 0 MXFP8, 1 NVFP4, 2 MXFP4
+  int fmt;                 // 0 MXFP8, 1 NVFP4, 2 MXFP4, 3 BF16 (no block scales)
   int64_t M, N, K;         // K in elements
   const uint8_t* SA;       // tensor-core scale tiles of A
   const uint8_t* SB;

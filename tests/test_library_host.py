@@ -92,6 +92,12 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert lib.dequantize(2, p, p, None, 0, None, 0, 4, 16, 0, p, None) == m.ERR_INVALID_ARG
     assert lib.dequantize(2, p, p, p, 2, None, 0, 4, 32, 0, p, None) == m.ERR_INVALID_ARG
     assert lib.dequantize(3, p, p, None, 0, None, 0, 4, 32, 0, p, None) == m.ERR_INVALID_ARG
+    # BF16 GEMM: K % 8, lda < K, misaligned stride, accumulate into bf16, empty
+    assert lib.bf16_gemm(8, 8, 12, p, 16, p, 16, 0, p, 8, 0, p, 4096, None) == m.ERR_INVALID_ARG
+    assert lib.bf16_gemm(8, 8, 64, p, 32, p, 64, 0, p, 8, 0, p, 4096, None) == m.ERR_INVALID_ARG
+    assert lib.bf16_gemm(8, 8, 64, p, 68, p, 64, 0, p, 8, 0, p, 4096, None) == m.ERR_ALIGNMENT
+    assert lib.bf16_gemm(8, 8, 64, p, 64, p, 64, 1, p, 8, 1, p, 4096, None) == m.ERR_UNSUPPORTED
+    assert lib.bf16_gemm(0, 8, 64, None, 64, None, 64, 0, None, 8, 0, None, 0, None) == m.OK
     # empty problems are no-ops
     assert lib.mx8_quantize(None, 0, 64, 64, m.ROWWISE, None, None, None, None, None, 0, None) == m.OK
     assert lib.bs_gemm(0, 0, 8, 64, None, None, None, 0, None, None, None, 0, 0, None, 8, 0, None, 0, None) == m.OK
