@@ -10,9 +10,10 @@ One step = every operation of the hot path, on seeded synthetic inputs:
   NVFP4 linear Fprop on the same layer: per-token X, per-tensor W;
   Qwen3-30B-A3B-shaped MoE expert layer with per-token NVFP4: 4096 tokens
     routed top-8 over 128 experts (32768 rows), hidden 2048, FFN 768:
-    per-token activation quantization, per-expert weight quantization
-    (gate|up joint), gate|up grouped GEMM, SwiGLU, per-token quantization,
-    down grouped GEMM.
+    per-token activation quantization of the 4096 tokens (each token encoded
+    once, before dispatch, and written to its 8 dispatched rows), per-expert
+    weight quantization (gate|up joint), the gate|up grouped GEMM with SwiGLU
+    in its epilogue, per-token quantization of h, down grouped GEMM.
 
 value = block-scaled GEMM FLOPs of the step / step time (quantizers,
 dequantization and SwiGLU included in the time).  Per-kernel times come from
@@ -137,7 +138,10 @@ class Step:
         disp = inputs.dispatch(moe["topk_ids"], q["experts"])
         self.offs = disp.offsets
         self.rows = int(disp.offsets[-1].item())
-        self.A_moe = moe["X"][disp.token_of_row].contiguous()       # dispatched activations
+        self.X_moe = moe["X"].contiguous()                          # token-major activations
+        self.a_rows = disp.token_of_row.to(torch.int64).contiguous()  # token of each dispatched row
+        # the topk dispatched rows of each token (inverse of a_rows)
+        self.dest_rows = torch.argsort(self.a_rows, stable=True).to(torch.int64).contiguous()
         E, F = q["experts"], q["ffn"]
         self.W_gu = moe["W_gu"].reshape(E * 2 * F, H).contiguous()
         self.W_d = moe["W_d"].reshape(E * H, F).contiguous()
@@ -167,23 +171,26 @@ class Step:
         self.X4, self.SX4, self.X432 = u8(T * H // 2)[: T * H // 2].view(T, H // 2), sb4(T, H), f32(T)
         self.W4, self.SW4, self.W432 = u8(O * H // 2)[: O * H // 2].view(O, H // 2), sb4(O, H), f32(1)
         self.Y4 = bf(T, O)
-        # MoE
-        R = self.rows
+        # MoE (tokens encoded once, before dispatch, written to their dispatched rows)
+        R, TM = self.rows, q["tokens"]
         self.A4, self.SA4, self.A432 = u8(R * H // 2)[: R * H // 2].view(R, H // 2), sb4g(R, E, H), f32(R)
         self.Wgu4 = u8(E * 2 * F * H // 2)[: E * 2 * F * H // 2].view(E, 2 * F, H // 2)
         self.SWgu4, self.Wgu432 = sb4(E * 2 * F, H), f32(E)
         self.Wd4 = u8(E * H * F // 2)[: E * H * F // 2].view(E, H, F // 2)
         self.SWd4, self.Wd432 = sb4(E * H, F), f32(E)
-        self.GU, self.Hs = bf(R, 2 * F), bf(R, F)
+        self.Hs = bf(R, F)
         self.H4, self.SH4, self.H432 = u8(R * F // 2)[: R * F // 2].view(R, F // 2), sb4g(R, E, F), f32(R)
         self.OUT = bf(R, H)
-        self.E, self.F, self.H_, self.T, self.O = E, F, H, T, O
+        self.E, self.F, self.H_, self.T, self.O, self.TM = E, F, H, T, O, TM
 
     # -- algorithmic work per launch (bytes or FLOPs) and roofline class
     def plan(self):
-        T, H, O, R, E, F = self.T, self.H_, self.O, self.rows, self.E, self.F
+        T, H, O, R, E, F, TM = self.T, self.H_, self.O, self.rows, self.E, self.F, self.TM
         mxq = lambda r, c: 4.0625 * r * c
         nvq = lambda r, c: 2.5625 * r * c + 4 * r
+        # before dispatch: bf16 read once per token; codes, block scales and S_dec
+        # written to each of the token's k dispatched rows
+        nvqd = lambda t, c, k: 2 * t * c + k * (0.5625 * t * c + 4 * t)
         return [
             ("mxfp8_quant_rc X", "hbm", mxq(T, H)),
             ("mxfp8_quant_rc W", "hbm", mxq(O, H)),
@@ -196,11 +203,10 @@ class Step:
             ("nvfp4_quant_token X", "hbm", nvq(T, H)),
             ("nvfp4_quant_tensor W", "hbm", nvq(O, H)),
             ("nvfp4_gemm Fprop", "fp4", 2.0 * T * O * H),
-            ("nvfp4_quant_token moe_act", "hbm", nvq(R, H)),
+            ("nvfp4_quant_token moe_act", "hbm", nvqd(TM, H, QWEN["topk"])),
             ("nvfp4_quant_expert W_gu", "hbm", nvq(E * 2 * F, H)),
             ("nvfp4_quant_expert W_d", "hbm", nvq(E * H, F)),
-            ("nvfp4_grouped_gemm gate_up", "fp4", 2.0 * R * 2 * F * H),
-            ("swiglu", "hbm", 6.0 * R * F),
+            ("nvfp4_moe_gemm gate_up+swiglu", "fp4", 2.0 * R * 2 * F * H),
             ("nvfp4_quant_token moe_h", "hbm", nvq(R, F)),
             ("nvfp4_grouped_gemm down", "fp4", 2.0 * R * H * F),
         ]
@@ -224,14 +230,15 @@ class Step:
             ("nvfp4_quant_tensor W", lambda: mx.nvfp4_quantize_into(self.W, self.W4, self.SW4, self.W432, mx.SCOPE_TENSOR, None, ws_b)),
             ("nvfp4_gemm Fprop", lambda: mx.bs_gemm_into(mx.FMT_NVFP4, self.X4, self.SX4, self.W4, self.SW4, self.H_, self.Y4,
                                                          self.X432, self.W432, ws=ws_b, a32_mode=mx.S32_ROW, b32_mode=mx.S32_TENSOR)),
-            ("nvfp4_quant_token moe_act", lambda: mx.nvfp4_quantize_into(self.A_moe, self.A4, self.SA4, self.A432, mx.SCOPE_TOKEN, self.offs, ws_c)),
+            ("nvfp4_quant_token moe_act", lambda: mx.nvfp4_quantize_dispatch_into(
+                self.X_moe, self.dest_rows, QWEN["topk"], self.offs, self.A4, self.SA4, self.A432, mx.DISPATCH_ROWS, ws_c)),
             ("nvfp4_quant_expert W_gu", lambda: mx.nvfp4_quantize_into(self.W_gu, self.Wgu4.view(-1, self.H_ // 2), self.SWgu4, self.Wgu432,
                                                                        mx.SCOPE_GROUP, self.e_offs_gu, ws_c)),
             ("nvfp4_quant_expert W_d", lambda: mx.nvfp4_quantize_into(self.W_d, self.Wd4.view(-1, self.F // 2), self.SWd4, self.Wd432,
                                                                       mx.SCOPE_GROUP, self.e_offs_d, ws_c)),
-            ("nvfp4_grouped_gemm gate_up", lambda: mx.bs_grouped_gemm_into(mx.FMT_NVFP4, self.offs, self.A4, self.SA4, self.Wgu4, self.SWgu4,
-                                                                            self.H_, self.GU, self.A432, self.Wgu432, ws_c)),
-            ("swiglu", lambda: mx.swiglu_into(self.GU, self.Hs)),
+            ("nvfp4_moe_gemm gate_up+swiglu", lambda: mx.bs_grouped_gemm_fused_into(
+                mx.FMT_NVFP4, self.offs, self.rows, self.A4, self.SA4, self.Wgu4, self.SWgu4, self.H_, self.Hs,
+                self.A432, self.Wgu432, None, mx.EPI_SWIGLU, ws_c)),
             ("nvfp4_quant_token moe_h", lambda: mx.nvfp4_quantize_into(self.Hs, self.H4, self.SH4, self.H432, mx.SCOPE_TOKEN, self.offs, ws_c)),
             ("nvfp4_grouped_gemm down", lambda: mx.bs_grouped_gemm_into(mx.FMT_NVFP4, self.offs, self.H4, self.SH4, self.Wd4, self.SWd4,
                                                                          self.F, self.OUT, self.H432, self.Wd432, ws_c)),
@@ -247,7 +254,7 @@ class Step:
          "mxfp8_gemm Wgrad", "dequant_mxfp8 X", "dequant_mxfp8 W"),
         ("nvfp4_quant_token X", "nvfp4_quant_tensor W", "nvfp4_gemm Fprop"),
         ("nvfp4_quant_token moe_act", "nvfp4_quant_expert W_gu", "nvfp4_quant_expert W_d",
-         "nvfp4_grouped_gemm gate_up", "swiglu", "nvfp4_quant_token moe_h", "nvfp4_grouped_gemm down"),
+         "nvfp4_moe_gemm gate_up+swiglu", "nvfp4_quant_token moe_h", "nvfp4_grouped_gemm down"),
     )
 
     def workspaces(self):
@@ -292,7 +299,7 @@ class Step:
         """Pinned host copies of each branch's per-step inputs and results."""
         torch = self.torch
         pin = lambda t: t.detach().cpu().pin_memory()
-        self.io_in = ([(self.X, pin(self.X)), (self.dY, pin(self.dY))], [], [(self.A_moe, pin(self.A_moe))])
+        self.io_in = ([(self.X, pin(self.X)), (self.dY, pin(self.dY))], [], [(self.X_moe, pin(self.X_moe))])
         empty = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
         self.io_out = ([(self.Y, empty(self.Y)), (self.dX, empty(self.dX))], [(self.Y4, empty(self.Y4))],
                        [(self.OUT, empty(self.OUT))])
@@ -633,7 +640,7 @@ def run_gpu(args):
 
 def run_e2e(step, args, world, dev, graph=None):
     """Same step through the public API with host buffers: every step copies
-    its inputs (X, dY, dispatched MoE activations) from pinned host memory
+    its inputs (X, dY, the MoE layer's token activations) from pinned host memory
     and reads its results (Y, dX, NVFP4 Y, MoE output) back; weights stay
     resident.  The three branches run on their own streams, each copying its
     own inputs in and results out, so one branch's copies overlap another's
@@ -701,7 +708,7 @@ def oracle_step_seconds(budget_s):
     s = timed(lambda: oracle.dequant_mxfp8(xq, xs))
     total += s * (T * H + O * H) / (rows * H)
     # NVFP4 quantizers (token scope cost per element also bounds group/tensor)
-    for r, c in ((T, H), (O, H), (R, H), (E * 2 * F, H), (E * H, F), (R, F)):
+    for r, c in ((T, H), (O, H), (QWEN["tokens"], H), (E * 2 * F, H), (E * H, F), (R, F)):
         x = slab(rows, c)
         s = timed(lambda: oracle.nvfp4_quantize(x))
         total += s * (r * c) / (rows * c)

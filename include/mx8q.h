@@ -94,6 +94,9 @@ enum { MX8_ROWWISE = 1, MX8_COLWISE = 2 };
 enum { NVFP4_SCOPE_TOKEN = 0, NVFP4_SCOPE_GROUP = 1, NVFP4_SCOPE_TENSOR = 2 };
 enum { MX8_FMT_MXFP8 = 0, MX8_FMT_NVFP4 = 1, MX8_FMT_MXFP4 = 2 };
 enum { MX8_OUT_F32 = 0, MX8_OUT_BF16 = 1 };
+enum { MX8_EPI_NONE = 0, MX8_EPI_SWIGLU = 1 };
+/* Where nvfp4_quantize_dispatch() puts codes and S_dec. */
+enum { MX8_DISPATCH_TOKENS = 0, MX8_DISPATCH_ROWS = 1 };
 /* How an FP32 decode scale vector applies to the rows of a matrix. */
 enum { MX8_S32_NONE = 0, MX8_S32_ROW = 1, MX8_S32_TENSOR = 2, MX8_S32_GROUP = 3 };
 
@@ -169,6 +172,37 @@ mx8_status nvfp4_quantize_per_token(const void *x, int64_t rows, int64_t cols, i
                                     uint8_t *q, uint8_t *s_blk, float *s32,
                                     void *workspace, size_t workspace_bytes,
                                     mx8_stream_t stream);
+
+/*
+ * Per-token NVFP4 quantization of MoE tokens once, before dispatch ([MRL]
+ * "La Compatibilidad..." / "Un Cuantizador Compartido...": the FP32 token
+ * scale is computed per token inside the activation quantizer; per-token
+ * scaling makes a token's codes independent of the batch, so quantizing
+ * before the top-k dispatch gives the same bytes as quantizing every
+ * dispatched copy, with 1/topk of the reads and of the encode work).
+ *   x          : bf16 [tokens, cols], row stride ld
+ *   dest_rows  : device int64 [tokens * topk]: the dispatched row of copy j
+ *                of token t at [t * topk + j]; together the entries cover
+ *                every dispatched row [0, group_offsets[G]) exactly once
+ *                (entries outside that range are skipped)
+ *   group_offsets : device int64 [num_groups + 1], the expert row ranges of
+ *                the dispatched order
+ *   layout     : MX8_DISPATCH_ROWS -> every copy written: q [R, cols/2]
+ *                and s32 [R] in dispatched-row order (R = group_offsets[G]),
+ *                the input of bs_grouped_gemm() / bs_grouped_gemm_fused()
+ *                without a_rows;
+ *                MX8_DISPATCH_TOKENS -> q [tokens, cols/2] and s32 [tokens]
+ *                token-major, the input of bs_grouped_gemm_fused() with
+ *                a_rows (the GEMM gathers the code rows)
+ *   s_blk      : E4M3 scales of the DISPATCHED rows in the grouped layout,
+ *                mx8_scale_bytes_grouped(NVFP4, tokens * topk, num_groups, cols)
+ * Requires 1 <= topk <= 16, cols % 16 == 0, ld % 8 == 0, 16-byte aligned
+ * x / q / s_blk.
+ */
+mx8_status nvfp4_quantize_dispatch(const void *x, int64_t tokens, int64_t cols, int64_t ld,
+                                   const int64_t *dest_rows, int topk, const int64_t *group_offsets,
+                                   int num_groups, int layout, uint8_t *q, uint8_t *s_blk, float *s32,
+                                   void *workspace, size_t workspace_bytes, mx8_stream_t stream);
 
 /*
  * nvfp4_quantize_per_token() for callers that cannot allocate device memory
@@ -256,6 +290,38 @@ mx8_status bs_grouped_gemm(int fmt, int num_groups, const int64_t *group_offsets
                            const uint8_t *B, const uint8_t *SB, const float *B32,
                            int out_dtype, void *C, int64_t ldc,
                            void *workspace, size_t workspace_bytes, mx8_stream_t stream);
+
+/*
+ * The MoE expert GEMM with the token dispatch and the SwiGLU fused in
+ * ([MRL] "La Compatibilidad..." / "Un Cuantizador Compartido...": the FP32
+ * token scale is fused into the activation quantizer, so each token is
+ * quantized once, before dispatch -- per-token scaling makes the codes of a
+ * token independent of the batch it sits in -- and SwiGLU experts compute
+ * gate and up in one fused GEMM).  NVFP4 only.  As bs_grouped_gemm(), plus:
+ *   a_rows     : device int64 [total_rows], the token (row of A) of each
+ *                dispatched row, or NULL (A already dispatched, as in
+ *                bs_grouped_gemm).  With a_rows, A and A32 are token-major
+ *                (A [a_src_rows, K/2], A32 [a_src_rows] or NULL) and SA
+ *                holds the dispatched rows' scales in the grouped layout --
+ *                exactly what nvfp4_quantize_dispatch() writes; the GEMM
+ *                gathers the code rows of each tile.  Indices outside
+ *                [0, a_src_rows) are clamped into it.
+ *   epilogue   : MX8_EPI_NONE -> C [total_rows, N] as bs_grouped_gemm();
+ *                MX8_EPI_SWIGLU -> B [G, N, K] holds per expert the gate rows
+ *                [0, F) and the up rows [F, 2F) (N = 2F, F % 128 == 0) and
+ *                C [total_rows, F] bf16 receives
+ *                  h = RN_bf16(silu(g) * u),  g = RN_bf16(gate), u = RN_bf16(up)
+ *                (gate, up: the scaled FP32 GEMM outputs; silu in FP32 as in
+ *                mx8_swiglu()), so the gate|up output never reaches memory.
+ * Other formats return MX8_ERR_UNSUPPORTED.
+ */
+mx8_status bs_grouped_gemm_fused(int fmt, int num_groups, const int64_t *group_offsets,
+                                 int64_t total_rows, int64_t N, int64_t K,
+                                 const uint8_t *A, const uint8_t *SA, const float *A32,
+                                 const int64_t *a_rows, int64_t a_src_rows,
+                                 const uint8_t *B, const uint8_t *SB, const float *B32,
+                                 int epilogue, int out_dtype, void *C, int64_t ldc,
+                                 void *workspace, size_t workspace_bytes, mx8_stream_t stream);
 
 /*
  * Dense BF16 GEMM on the tcgen05 tensor cores, for the dequantized-backward

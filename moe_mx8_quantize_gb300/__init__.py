@@ -24,13 +24,16 @@ ROWWISE, COLWISE = 1, 2
 SCOPE_TOKEN, SCOPE_GROUP, SCOPE_TENSOR = 0, 1, 2
 FMT_MXFP8, FMT_NVFP4, FMT_MXFP4 = 0, 1, 2
 OUT_F32, OUT_BF16 = 0, 1
+EPI_NONE, EPI_SWIGLU = 0, 1
+DISPATCH_TOKENS, DISPATCH_ROWS = 0, 1
 S32_NONE, S32_ROW, S32_TENSOR, S32_GROUP = 0, 1, 2, 3
 
 # every C symbol the header declares
 EXPORTS = ("mx8_scale_bytes", "mx8_scale_bytes_grouped", "mx8_workspace_bytes",
            "mx8_device_sm_count", "mx8_quantize", "mxfp4_quantize", "nvfp4_quantize_per_token",
+           "nvfp4_quantize_dispatch",
            "nvfp4_quantize_per_token_noalloc", "dequantize",
-           "bs_gemm", "bs_grouped_gemm", "bf16_gemm", "mx8_swiglu", "mx8_check_device_error", "mx8_selftest_bounded_wait",
+           "bs_gemm", "bs_grouped_gemm", "bs_grouped_gemm_fused", "bf16_gemm", "mx8_swiglu", "mx8_check_device_error", "mx8_selftest_bounded_wait",
            "mx8_status_string")
 
 
@@ -80,6 +83,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bs_grouped_gemm.restype = _i
     lib.bs_grouped_gemm.argtypes = [_i, _i, _p, _i64, _i64, _i64, _p, _p, _p, _p, _p, _p, _i, _p,
                                     _i64, _p, _sz, _p]
+    lib.nvfp4_quantize_dispatch.restype = _i
+    lib.nvfp4_quantize_dispatch.argtypes = [_p, _i64, _i64, _i64, _p, _i, _p, _i, _i, _p, _p, _p, _p, _sz, _p]
+    lib.bs_grouped_gemm_fused.restype = _i
+    lib.bs_grouped_gemm_fused.argtypes = [_i, _i, _p, _i64, _i64, _i64, _p, _p, _p, _p, _i64, _p, _p, _p, _i,
+                                          _i, _p, _i64, _p, _sz, _p]
     lib.bf16_gemm.restype = _i
     lib.bf16_gemm.argtypes = [_i64, _i64, _i64, _p, _i64, _p, _i64, _i, _p, _i64, _i, _p, _sz, _p]
     lib.mx8_swiglu.restype = _i
@@ -241,6 +249,33 @@ def nvfp4_quantize_per_token(x: torch.Tensor, scope: int = SCOPE_TOKEN, group_of
     return q, s_blk, s32[:n32]
 
 
+def nvfp4_quantize_dispatch_into(x, dest_rows, topk, group_offsets, q, s_blk, s32, layout=DISPATCH_ROWS,
+                                 ws=None, stream=None):
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    T, C = x.shape
+    G = group_offsets.numel() - 1
+    ws = _ws(ws, G, x.device)
+    _check(load().nvfp4_quantize_dispatch(_ptr(x), T, C, x.stride(0), _ptr(dest_rows), topk, _ptr(group_offsets),
+                                          G, layout, _ptr(q), _ptr(s_blk), _ptr(s32), _ptr(ws), ws.numel(),
+                                          _stream(stream)),
+           "nvfp4_quantize_dispatch")
+
+
+def nvfp4_quantize_dispatch(x, dest_rows, topk, group_offsets, layout=DISPATCH_ROWS, ws=None, stream=None):
+    """Per-token NVFP4 of MoE tokens, encoded once before dispatch.  Returns
+    (q, s_blk, s32): s_blk holds the dispatched rows' scales in the grouped
+    layout; q [rows, C/2] and s32 [rows] are in dispatched-row order
+    (DISPATCH_ROWS) or token-major [T, C/2], [T] (DISPATCH_TOKENS)."""
+    T, C = x.shape
+    G = group_offsets.numel() - 1
+    n = T * topk if layout == DISPATCH_ROWS else T
+    q = torch.empty((n, C // 2), dtype=torch.uint8, device=x.device)
+    s_blk = _u8(scale_bytes_grouped(FMT_NVFP4, T * topk, G, C), x.device)
+    s32 = torch.empty(max(n, 1), dtype=torch.float32, device=x.device)
+    nvfp4_quantize_dispatch_into(x, dest_rows, topk, group_offsets, q, s_blk, s32, layout, ws, stream)
+    return q, s_blk, s32[:n]
+
+
 # ---------------------------------------------------------------- dequantize
 def dequantize_into(fmt, q, s, out, s32=None, s32_mode=S32_NONE, group_offsets=None, stream=None):
     R = q.shape[0]
@@ -335,6 +370,36 @@ def bs_grouped_gemm(fmt, group_offsets, A, SA, B, SB, K, A32=None, B32=None,
     B: [G, N, K] (or [G, N, K/2]) u8; SB the [G*N, K/bs] scale tiles."""
     out = torch.empty((A.shape[0], B.shape[1]), dtype=out_dtype, device=A.device)
     bs_grouped_gemm_into(fmt, group_offsets, A, SA, B, SB, K, out, A32, B32, ws, stream)
+    return out
+
+
+def bs_grouped_gemm_fused_into(fmt, group_offsets, total_rows, A, SA, B, SB, K, out, A32=None, B32=None,
+                               a_rows=None, epilogue=EPI_NONE, ws=None, stream=None):
+    """In-place form of :func:`bs_grouped_gemm_fused`."""
+    G = group_offsets.numel() - 1
+    N = B.shape[1]
+    ws = _ws(ws, G, A.device)
+    od = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
+    src_rows = A.shape[0] if a_rows is not None else 0
+    _check(load().bs_grouped_gemm_fused(fmt, G, _ptr(group_offsets), total_rows, N, K, _ptr(A), _ptr(SA),
+                                        _ptr(A32), _ptr(a_rows), src_rows, _ptr(B), _ptr(SB), _ptr(B32),
+                                        epilogue, od, _ptr(out), out.stride(0), _ptr(ws), ws.numel(),
+                                        _stream(stream)), "bs_grouped_gemm_fused")
+
+
+def bs_grouped_gemm_fused(fmt, group_offsets, A, SA, B, SB, K, A32=None, B32=None, a_rows=None,
+                          epilogue=EPI_NONE, out_dtype=torch.bfloat16, ws=None, stream=None):
+    """MoE expert GEMM with the dispatch gather and / or the SwiGLU fused in.
+
+    a_rows (device int64 [rows]): token of each dispatched row; A, SA, A32
+    are then the token-major quantize output (plain scale layout).
+    epilogue=EPI_SWIGLU: B holds gate rows [0, F) and up rows [F, 2F) per
+    expert; returns h [rows, F] bf16 instead of the gate|up output."""
+    rows = a_rows.numel() if a_rows is not None else A.shape[0]
+    n_out = B.shape[1] // 2 if epilogue == EPI_SWIGLU else B.shape[1]
+    out = torch.empty((rows, n_out), dtype=out_dtype, device=A.device)
+    bs_grouped_gemm_fused_into(fmt, group_offsets, rows, A, SA, B, SB, K, out, A32, B32, a_rows, epilogue,
+                               ws, stream)
     return out
 
 

@@ -180,6 +180,27 @@ extern "C" mx8_status nvfp4_quantize_per_token(const void* x, int64_t rows, int6
                                       sm_count_current(), reinterpret_cast<cudaStream_t>(stream)));
 }
 
+extern "C" mx8_status nvfp4_quantize_dispatch(const void* x, int64_t tokens, int64_t cols, int64_t ld,
+                                              const int64_t* dest_rows, int topk, const int64_t* group_offsets,
+                                              int num_groups, int layout, uint8_t* q, uint8_t* s_blk, float* s32,
+                                              void* workspace, size_t workspace_bytes, mx8_stream_t stream) {
+  if (tokens < 0 || cols < 0 || ld < cols || cols % 16 != 0) return MX8_ERR_INVALID_ARG;
+  if (layout != MX8_DISPATCH_TOKENS && layout != MX8_DISPATCH_ROWS) return MX8_ERR_INVALID_ARG;
+  if (topk < 1 || topk > kMaxTopk) return MX8_ERR_INVALID_ARG;
+  if (group_offsets == nullptr || num_groups < 1 || num_groups > kMaxGroups) return MX8_ERR_INVALID_ARG;
+  if (cols > (int64_t{1} << 30)) return MX8_ERR_UNSUPPORTED;
+  if (tokens == 0 || cols == 0) return MX8_OK;
+  if (x == nullptr || q == nullptr || s_blk == nullptr || s32 == nullptr || dest_rows == nullptr)
+    return MX8_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(s_blk) || ld % 8 != 0) return MX8_ERR_ALIGNMENT;
+  mx8_status st = check_ws(workspace, workspace_bytes, num_groups);
+  if (st != MX8_OK) return st;
+  return from_cuda(launch_nvfp4_dispatch(static_cast<const uint16_t*>(x), tokens, cols, ld, dest_rows, topk,
+                                         group_offsets, num_groups, layout == MX8_DISPATCH_ROWS, q, s_blk, s32,
+                                         sm_count_current(),
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
 // ===================================================================== dequantize
 extern "C" mx8_status dequantize(int fmt, const uint8_t* q, const uint8_t* s, const float* s32,
                                  int s32_mode, const int64_t* group_offsets, int num_groups,
@@ -330,6 +351,53 @@ extern "C" mx8_status bs_grouped_gemm(int fmt, int num_groups, const int64_t* gr
   a.B32 = B32; a.b32_mode = B32 ? MX8_S32_GROUP : MX8_S32_NONE;
   a.C = C; a.ldc = ldc; a.out_bf16 = out_dtype == MX8_OUT_BF16; a.accumulate = 0;
   a.grouped = 1; a.G = num_groups; a.offs = group_offsets; a.err = err_word(workspace);
+  return from_cuda(launch_bs_gemm(a, ma, mb, mc, sm_count_current(), s));
+}
+
+// ===================================================================== fused MoE GEMM
+extern "C" mx8_status bs_grouped_gemm_fused(int fmt, int num_groups, const int64_t* group_offsets,
+                                            int64_t total_rows, int64_t N, int64_t K, const uint8_t* A,
+                                            const uint8_t* SA, const float* A32, const int64_t* a_rows,
+                                            int64_t a_src_rows, const uint8_t* B, const uint8_t* SB,
+                                            const float* B32, int epilogue, int out_dtype, void* C,
+                                            int64_t ldc, void* workspace, size_t workspace_bytes,
+                                            mx8_stream_t stream) {
+  if (num_groups < 1 || num_groups > kMaxGroups || group_offsets == nullptr || total_rows < 0)
+    return MX8_ERR_INVALID_ARG;
+  if (epilogue != MX8_EPI_NONE && epilogue != MX8_EPI_SWIGLU) return MX8_ERR_INVALID_ARG;
+  const bool swiglu = epilogue == MX8_EPI_SWIGLU;
+  if (swiglu && (N % 256 != 0 || out_dtype != MX8_OUT_BF16)) return MX8_ERR_INVALID_ARG;
+  const int64_t n_out = swiglu ? N / 2 : N;
+  if (a_rows != nullptr && (a_src_rows < 1 || a_src_rows > INT32_MAX)) return MX8_ERR_INVALID_ARG;
+  if (total_rows == 0 || N == 0) return MX8_OK;
+  mx8_status st = gemm_common_checks(fmt, n_out, K, A, SA, B, SB, out_dtype, C, ldc);
+  if (st != MX8_OK) return st;
+  if (fmt != MX8_FMT_NVFP4) return MX8_ERR_UNSUPPORTED;
+  if (total_rows > INT32_MAX || N > INT32_MAX) return MX8_ERR_UNSUPPORTED;
+  st = check_ws(workspace, workspace_bytes, num_groups);
+  if (st != MX8_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) return from_cuda(zero_output(C, ldc, total_rows, n_out, out_dtype, s));
+
+  const uint64_t kbytes = K / 2;
+  const uint64_t a_rows_map = a_rows != nullptr ? static_cast<uint64_t>(a_src_rows) : static_cast<uint64_t>(total_rows);
+  CUtensorMap ma, mb, mc;
+  const uint32_t box2[2] = {kGemmKBytes, 128};
+  const uint64_t da[2] = {kbytes, a_rows_map}, sa[1] = {kbytes};
+  const uint32_t box3[3] = {kGemmKBytes, 128, 1};
+  const uint64_t db[3] = {kbytes, static_cast<uint64_t>(N), static_cast<uint64_t>(num_groups)};
+  const uint64_t sb[2] = {kbytes, kbytes * static_cast<uint64_t>(N)};
+  if (!encode_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, A, da, sa, box2, gemm_swizzle()) ||
+      !encode_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, B, db, sb, box3, gemm_swizzle()) ||
+      !encode_output_map(&mc, C, total_rows, n_out, ldc, out_dtype))
+    return MX8_ERR_CUDA;
+  GemmArgs a{};
+  a.fmt = fmt; a.M = total_rows; a.N = N; a.K = K;
+  a.SA = SA; a.SB = SB; a.A32 = A32; a.a32_mode = A32 ? MX8_S32_ROW : MX8_S32_NONE;
+  a.B32 = B32; a.b32_mode = B32 ? MX8_S32_GROUP : MX8_S32_NONE;
+  a.C = C; a.ldc = ldc; a.out_bf16 = out_dtype == MX8_OUT_BF16; a.accumulate = 0;
+  a.grouped = 1; a.G = num_groups; a.offs = group_offsets; a.err = err_word(workspace);
+  a.A = A; a.a_rows = a_rows; a.a_src_rows = a_rows ? a_src_rows : 0; a.ffn = swiglu ? N / 2 : 0;
   return from_cuda(launch_bs_gemm(a, ma, mb, mc, sm_count_current(), s));
 }
 

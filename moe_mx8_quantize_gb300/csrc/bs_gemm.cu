@@ -106,7 +106,16 @@ struct Cfg<2> {                 // MXFP4: 2 elements per byte, 64 elements (2 sc
   static constexpr int kSfTiles = kElemsPerStage / kElemsPerTile;
 };
 
-template <int kFmt, bool kGrouped, int kBN>
+// Fused MoE modes of the grouped GEMM (bit flags):
+//   kModeGather : A is the token-major quantized matrix; the producer gathers
+//                 the rows of each tile (and their scales) through a row ->
+//                 token map, so tokens are quantized once, before dispatch;
+//   kModeSwiGLU : B holds gate rows [0, F) and up rows [F, 2F) per expert; a
+//                 tile pairs gate rows n0.. and up rows F + n0.. (128 each),
+//                 and the epilogue writes h = silu(g) * u for 128 columns.
+constexpr int kModeGather = 1, kModeSwiGLU = 2;
+
+template <int kFmt, bool kGrouped, int kBN, int kMode>
 struct Layout {
   static constexpr int kBRow128 = kBN / 128;                         // 128-row blocks of B
   static constexpr int kTileBBytes = kBN * kKBytes;
@@ -125,16 +134,19 @@ struct Layout {
   static constexpr uint32_t kSfColsPerStage = kSfaCols + kSfbCols;
   static constexpr uint32_t kAccCols = kAccBufs * kBN;
   static constexpr int kEpiWarps = kBN / 32;                         // 128 columns per warp
-  static constexpr int kProducers = 1 + kBRow128;                    // warp 0 + one warp per B box
+  // warp 0 + one warp per B box (+ the 32 lanes of warp 0 that gather A rows,
+  // each arriving when its copies have landed)
+  static constexpr int kProducers = 1 + kBRow128 + ((kMode & kModeGather) ? 32 : 0);
   // warp 0 producer, warp 1 MMA, warps 2 .. 1 + kEpiWarps epilogue, then the B producers
   static constexpr int kThreads = 64 + 32 * kEpiWarps + 32 * kBRow128;
   static_assert(kStages >= 3, "pipeline too shallow");
+  static_assert(!(kMode & kModeSwiGLU) || kBN == 256, "the SwiGLU epilogue pairs two 128-row boxes");
   static_assert(kAccCols + kStages * kSfColsPerStage <= kTmemCols, "tensor memory overflow");
 };
 
-template <int kFmt, bool kGrouped, int kBN>
+template <int kFmt, bool kGrouped, int kBN, int kMode>
 struct __align__(1024) GemmSmem {
-  using L = Layout<kFmt, kGrouped, kBN>;
+  using L = Layout<kFmt, kGrouped, kBN, kMode>;
   uint8_t a[L::kStages][kTileABytes];
   uint8_t b[L::kStages][L::kTileBBytes];
   uint8_t sfa[L::kStages][L::kSfaBytes];
@@ -147,6 +159,7 @@ struct __align__(1024) GemmSmem {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
+  int32_t gtok[BM];                                   // gathered mode: source rows of the tile
 };
 
 // Instruction descriptor of the block-scaled MMA (M = 128, both operands
@@ -188,7 +201,7 @@ struct TileCoord {
   int64_t n0;
 };
 
-template <bool kGrouped, int kBN>
+template <bool kGrouped, int kNT>
 __device__ __forceinline__ TileCoord decode_tile(int64_t t, int64_t tiles_n, int64_t M,
                                                  const GroupSmem* gs, int G) {
   TileCoord c;
@@ -199,7 +212,7 @@ __device__ __forceinline__ TileCoord decode_tile(int64_t t, int64_t tiles_n, int
     c.a_row0 = mt * BM;
     c.rows = M - c.a_row0 < BM ? M - c.a_row0 : BM;
     c.sfa_tile = mt;
-    c.n0 = nt * kBN;
+    c.n0 = nt * kNT;
     return c;
   }
   const int64_t gmt = t / tiles_n;                   // global m-tile band
@@ -213,18 +226,21 @@ __device__ __forceinline__ TileCoord decode_tile(int64_t t, int64_t tiles_n, int
   c.a_row0 = gs->offs[g] + mt * BM;
   c.rows = ng - mt * BM < BM ? ng - mt * BM : BM;
   c.sfa_tile = mt0 + mt;
-  c.n0 = nt * kBN;
+  c.n0 = nt * kNT;
   return c;
 }
 
-template <int kFmt, bool kGrouped, int kBN>
-__global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
+template <int kFmt, bool kGrouped, int kBN, int kMode>
+__global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 1)
     bs_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_c, const GemmArgs args) {
-  using L = Layout<kFmt, kGrouped, kBN>;
+  using L = Layout<kFmt, kGrouped, kBN, kMode>;
   using F = Cfg<kFmt>;
-  using Smem = GemmSmem<kFmt, kGrouped, kBN>;
+  using Smem = GemmSmem<kFmt, kGrouped, kBN, kMode>;
+  constexpr bool kGather = (kMode & kModeGather) != 0;
+  constexpr bool kSwiGLU = (kMode & kModeSwiGLU) != 0;
+  static_assert(kGather <= kGrouped && kSwiGLU <= kGrouped, "fused modes are grouped only");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   Smem& sm = *reinterpret_cast<Smem*>(base);
@@ -261,34 +277,119 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
   const uint32_t tmem = sm.tmem_base;
 
   const int64_t M = args.M, N = args.N, K = args.K;
-  const int64_t tiles_n = (N + kBN - 1) / kBN;
+  // output columns per tile: BN, or 128 h columns (from 128 gate + 128 up rows of B)
+  constexpr int kNT = kSwiGLU ? 128 : kBN;
+  const int64_t F_ = args.ffn;                            // SwiGLU: B rows of the up half start at F
+  const int64_t n_out = kSwiGLU ? F_ : N;
+  const int64_t tiles_n = (n_out + kNT - 1) / kNT;
   const int64_t n_rt = (N + 127) / 128;                   // 128-row scale tiles of B (per group)
   const int64_t tiles_m = kGrouped ? gs->pref[args.G] / BM : (M + BM - 1) / BM;
   const int64_t nunits = tiles_m * tiles_n;          // output tiles, strided over the CTAs
   const int64_t unit0 = blockIdx.x, ustep = gridDim.x;
-  auto tile_of = [&](int64_t u) { return decode_tile<kGrouped, kBN>(u, tiles_n, M, gs, args.G); };
+  auto tile_of = [&](int64_t u) { return decode_tile<kGrouped, kNT>(u, tiles_n, M, gs, args.G); };
+  // first B row (within the group) of 128-row box h of a tile
+  auto b_row0 = [&](const TileCoord& tc, int h) -> int64_t {
+    return kSwiGLU ? tc.n0 + h * F_ : tc.n0 + h * 128;
+  };
   const int64_t kbytes = kFmt == 0 ? K : (kFmt == 3 ? 2 * K : K / 2);
   const int ktiles = static_cast<int>((kbytes + kKBytes - 1) / kKBytes);
   const int64_t sf_kt = (K / F::kBlock + 3) / 4;          // scale tiles along K
 
   // producer index: 0 = warp 0 (A and the scale tiles), 1 + h = B box h
   const int prod = warp == 0 ? 0 : (warp >= 2 + L::kEpiWarps ? warp - 1 - L::kEpiWarps : -1);
+  // B scale tiles of a tile's 128-row boxes
+  auto b_scale_srcs = [&](const TileCoord& tc, const uint8_t* (&src)[L::kBRow128]) {
+    const int64_t gbase = kGrouped ? static_cast<int64_t>(tc.g) * n_rt : 0;
+#pragma unroll
+    for (int h = 0; h < L::kBRow128; ++h) {
+      // a 128-row block of B past N has zero data; reuse a valid scale tile for it
+      const int64_t rt = b_row0(tc, h) / 128 < n_rt ? gbase + b_row0(tc, h) / 128 : gbase + tc.n0 / 128;
+      src[h] = args.SB + rt * sf_kt * 512;
+    }
+  };
+  auto scale_tiles_of_stage = [&](int kt, int64_t& sf0) -> int {
+    sf0 = static_cast<int64_t>(kt) * F::kElemsPerStage / F::kElemsPerTile;
+    return F::kSfTiles == 0 ? 0 : static_cast<int>(sf_kt - sf0 < F::kSfTiles ? sf_kt - sf0 : F::kSfTiles);
+  };
+
   if (prod >= 0) {
     // ------------------------------------------------------------ producers
-    if (lane == 0) {
+    if (kGather && prod == 0) {
+      // Gathered A (dispatch fused into the GEMM): the 32 lanes copy each
+      // tile's 128 rows from the token-major codes with 16-byte cp.async, 8
+      // lanes per 128-byte row segment (4 rows per instruction), into the
+      // swizzled K-major layout the MMA reads: the 16-byte chunk at offset o
+      // of the tile goes to o ^ (((o >> 7) % atom rows) << 4).  Each lane
+      // arrives on the stage's barrier once its copies have landed (the MMA
+      // thread fences them for the tensor core's reads).  Lane 0 also loads
+      // the A and B scale tiles (the dispatched rows' scales are laid out by
+      // the quantizer, grouped, so they arrive as whole tiles).
+      constexpr uint32_t kAtomMask = kKBytes == 128 ? 7u : 3u;
+      const uint32_t sub = static_cast<uint32_t>(lane & 7);   // 16-byte chunk of the row segment
+      const int rq = lane >> 3;                                // row within a group of 4
+      int it = 0;
+      bool ok = true;
+      for (int64_t u = unit0; ok && u < nunits; u += ustep) {
+        const TileCoord tc = tile_of(u);
+        __syncwarp();                          // the previous tile's row list is no longer read
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = lane + 32 * i;
+          const int64_t t = args.a_rows[tc.a_row0 + (r < tc.rows ? r : 0)];
+          sm.gtok[r] = static_cast<int32_t>(t < 0 ? 0 : (t >= args.a_src_rows ? args.a_src_rows - 1 : t));
+        }
+        __syncwarp();
+        const uint8_t* sfa_src = args.SA + tc.sfa_tile * sf_kt * 512;
+        const uint8_t* sfb_src[L::kBRow128];
+        b_scale_srcs(tc, sfb_src);
+        for (int kt = 0; kt < ktiles; ++kt, ++it) {
+          const int s = it % L::kStages;
+          const uint32_t ph = (it / L::kStages) & 1;
+          bool w = true;
+          if (lane == 0) w = mbar_wait(smem_u32(&sm.empty[s]), ph ^ 1, err, kErrWaitProducer, &sm.abort);
+          if (!__shfl_sync(0xffffffffu, w, 0)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = smem_u32(&sm.full[s]);
+          if (lane == 0) {
+            int64_t sf0;
+            const int nsf = scale_tiles_of_stage(kt, sf0);
+            mbar_arrive_expect_tx(full, (1 + L::kBRow128) * nsf * 512);
+            bulk_load(smem_u32(sm.sfa[s]), sfa_src + sf0 * 512, nsf * 512, full);
+#pragma unroll
+            for (int h = 0; h < L::kBRow128; ++h)
+              bulk_load(smem_u32(sm.sfb[s]) + h * F::kSfTiles * 512, sfb_src[h] + sf0 * 512, nsf * 512, full);
+          }
+          const uint32_t a_s = smem_u32(sm.a[s]);
+          const int64_t kb = static_cast<int64_t>(kt) * kKBytes + 16 * sub;
+          const int64_t rem = kbytes - kb;
+          const uint32_t nb = rem >= 16 ? 16u : (rem > 0 ? static_cast<uint32_t>(rem) : 0u);
+#pragma unroll 8
+          for (int i = 0; i < BM / 4; ++i) {
+            const uint32_t r = static_cast<uint32_t>(4 * i + rq);
+            const uint8_t* src = nb ? args.A + static_cast<int64_t>(sm.gtok[r]) * kbytes + kb : args.A;
+            const uint32_t o = r * kKBytes + 16u * sub;
+            cp_async_16(a_s + (o ^ (((o >> 7) & kAtomMask) << 4)), src, nb);
+          }
+          cp_async_arrive_noinc(full);
+        }
+      }
+      cp_async_wait_all();                     // no copy may land after the block exits
+      if (lane == 0 && !ok) {
+        // let the scale copies already issued land before the block exits
+        for (int j = (it > L::kStages ? it - L::kStages : 0); j < it; ++j)
+          mbar_wait(smem_u32(&sm.full[j % L::kStages]), (j / L::kStages) & 1, err, kErrWaitTeardown,
+                    nullptr, 100000000ull);
+      }
+    } else if (lane == 0) {
       int it = 0;
       bool ok = true;
       for (int64_t u = unit0; ok && u < nunits; u += ustep) {
         const TileCoord tc = tile_of(u);
         const uint8_t* sfa_src = args.SA + tc.sfa_tile * sf_kt * 512;
-        const int64_t brt0 = (kGrouped ? static_cast<int64_t>(tc.g) * n_rt : 0) + tc.n0 / 128;
         const uint8_t* sfb_src[L::kBRow128];
-#pragma unroll
-        for (int h = 0; h < L::kBRow128; ++h) {
-          // a 128-row block of B past N has zero data; reuse a valid scale tile for it
-          const int64_t rt = (tc.n0 / 128 + h < n_rt) ? brt0 + h : brt0;
-          sfb_src[h] = args.SB + rt * sf_kt * 512;
-        }
+        b_scale_srcs(tc, sfb_src);
         for (int kt = 0; kt < ktiles; ++kt, ++it) {
           const int s = it % L::kStages;
           const uint32_t ph = (it / L::kStages) & 1;
@@ -299,8 +400,8 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
           const uint32_t full = smem_u32(&sm.full[s]);
           if (prod == 0) {
             if constexpr (F::kSfTiles > 0) {
-              const int64_t sf0 = static_cast<int64_t>(kt) * F::kElemsPerStage / F::kElemsPerTile;
-              const int nsf = static_cast<int>(sf_kt - sf0 < F::kSfTiles ? sf_kt - sf0 : F::kSfTiles);
+              int64_t sf0;
+              const int nsf = scale_tiles_of_stage(kt, sf0);
               mbar_arrive_expect_tx(full, kTileABytes + (1 + L::kBRow128) * nsf * 512);
               tma_load_2d(smem_u32(sm.a[s]), &tmap_a, kt * kKBytes, static_cast<int32_t>(tc.a_row0), full);
               bulk_load(smem_u32(sm.sfa[s]), sfa_src + sf0 * 512, nsf * 512, full);
@@ -317,10 +418,10 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
             mbar_arrive_expect_tx(full, kBoxBytes);
             if (kGrouped)
               tma_load_3d(smem_u32(sm.b[s]) + h * kBoxBytes, &tmap_b, kt * kKBytes,
-                          static_cast<int32_t>(tc.n0 + h * 128), tc.g, full);
+                          static_cast<int32_t>(b_row0(tc, h)), tc.g, full);
             else
               tma_load_2d(smem_u32(sm.b[s]) + h * kBoxBytes, &tmap_b, kt * kKBytes,
-                          static_cast<int32_t>(tc.n0 + h * 128), full);
+                          static_cast<int32_t>(b_row0(tc, h)), full);
           }
         }
       }
@@ -354,9 +455,9 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
             break;
           }
           tc_fence_after();
-          const int64_t sf0 = static_cast<int64_t>(kt) * F::kElemsPerStage / F::kElemsPerTile;
-          const int nsf = F::kSfTiles == 0 ? 0
-                          : static_cast<int>(sf_kt - sf0 < F::kSfTiles ? sf_kt - sf0 : F::kSfTiles);
+          if (kGather) fence_proxy_async_smem();   // the gathered rows were written by cp.async
+          int64_t sf0;
+          const int nsf = scale_tiles_of_stage(kt, sf0);
           // tensor-memory scale layout per stage: A -> 4 columns per K sub-tile;
           // B -> (4 columns x kBRow128) per K sub-tile, the 128-row blocks adjacent
           const uint32_t tsfa = sf_base + s * L::kSfColsPerStage;
@@ -415,9 +516,15 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       uint32_t r[4][32];
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + as * kBN + col0;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + as * kBN;
+      // SwiGLU: this warp's 64 h columns need gate columns 64*half.. (chunks 0,
+      // 1) and the matching up columns 128 + 64*half.. (chunks 2, 3)
+      const int half = ew / 4;
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) tmem_ld_32x32b_x32(taddr + ch * 32, r[ch]);
+      for (int ch = 0; ch < 4; ++ch)
+        tmem_ld_32x32b_x32(taddr + (kSwiGLU ? (ch < 2 ? 64 * half + 32 * ch : 128 + 64 * half + 32 * (ch - 2))
+                                            : col0 + ch * 32),
+                           r[ch]);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.acc_empty[as]));   // accumulator drained into registers
@@ -427,7 +534,14 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
       const int64_t m = tc.a_row0 + r_in_tile;
       float sa = 1.f;
       if (row_ok) {
-        if (args.a32_mode == 1) sa = args.A32[m];
+        if (args.a32_mode == 1) {
+          int64_t src = m;
+          if (kGather) {
+            src = args.a_rows[m];
+            src = src < 0 ? 0 : (src >= args.a_src_rows ? args.a_src_rows - 1 : src);
+          }
+          sa = args.A32[src];
+        }
         else if (args.a32_mode == 2) sa = args.A32[0];
       }
       float sg = 1.f;
@@ -437,6 +551,30 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
       // the two FP32 decode scales are combined first: acc * A32 alone can
       // overflow for tokens whose amax is near the bf16 maximum
       const float s_ab = __fmul_rn(sa, sg);
+      if constexpr (kSwiGLU) {
+        // g and u rounded to bf16 exactly as the unfused gate|up output would
+        // be, then h = RN_bf16(silu(g) * u): 64 columns, 128 contiguous bytes
+        if (!row_ok) continue;
+        uint4* hrow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.C) + m * args.ldc + tc.n0 + 64 * half);
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) {
+          uint32_t p[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float hv[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int c = q8 * 8 + j * 2 + e;
+              const float g = bf16_round(__fmul_rn(__uint_as_float(r[c >> 5][c & 31]), s_ab));
+              const float uu = bf16_round(__fmul_rn(__uint_as_float(r[2 + (c >> 5)][c & 31]), s_ab));
+              hv[e] = silu_mul(g, uu);
+            }
+            p[j] = pack_bf16x2(hv[0], hv[1]);
+          }
+          hrow[q8] = make_uint4(p[0], p[1], p[2], p[3]);
+        }
+        continue;
+      }
       // Whole 32-row slabs leave through shared memory and bulk tensor stores
       // (full lines, asynchronous); a slab that crosses the end of its group
       // or that accumulates into C is stored directly, row by row.
@@ -540,18 +678,18 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN>::kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int kFmt, bool kGrouped, int kBN>
+template <int kFmt, bool kGrouped, int kBN, int kMode = 0>
 cudaError_t launch_variant(const GemmArgs& a, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                            const CUtensorMap& tmap_c, int sm_count, cudaStream_t stream) {
-  using L = Layout<kFmt, kGrouped, kBN>;
-  const int64_t tiles_n = (a.N + kBN - 1) / kBN;
+  using L = Layout<kFmt, kGrouped, kBN, kMode>;
+  const int64_t tiles_n = (kMode & kModeSwiGLU) ? (a.ffn + 127) / 128 : (a.N + kBN - 1) / kBN;
   int64_t tiles_m = (a.M + BM - 1) / BM;
   if (a.grouped) tiles_m += a.G;                  // upper bound: every group pads a tile
   const int64_t ntiles = tiles_m * tiles_n;
   const unsigned grid = static_cast<unsigned>(ntiles < sm_count ? ntiles : sm_count);
   if (grid == 0) return cudaSuccess;
-  auto k = bs_gemm_kernel<kFmt, kGrouped, kBN>;
-  constexpr size_t smem = sizeof(GemmSmem<kFmt, kGrouped, kBN>) + (kGrouped ? sizeof(GroupSmem) : 0) + 1024;
+  auto k = bs_gemm_kernel<kFmt, kGrouped, kBN, kMode>;
+  constexpr size_t smem = sizeof(GemmSmem<kFmt, kGrouped, kBN, kMode>) + (kGrouped ? sizeof(GroupSmem) : 0) + 1024;
   static_assert(smem <= 227 * 1024, "shared memory over the per-block limit");
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -564,6 +702,14 @@ cudaError_t launch_variant(const GemmArgs& a, const CUtensorMap& tmap_a, const C
 cudaError_t launch_bs_gemm(const GemmArgs& a, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                            const CUtensorMap& tmap_c, int sm_count, cudaStream_t stream) {
   constexpr int BN = MX8Q_GEMM_BN;
+  const int mode = (a.a_rows != nullptr ? kModeGather : 0) | (a.ffn > 0 ? kModeSwiGLU : 0);
+  if (mode != 0) {
+    // fused MoE modes: NVFP4 grouped only
+    if (a.fmt != 1 || !a.grouped || BN != 256) return cudaErrorInvalidValue;
+    if (mode == kModeGather) return launch_variant<1, true, 256, kModeGather>(a, tmap_a, tmap_b, tmap_c, sm_count, stream);
+    if (mode == kModeSwiGLU) return launch_variant<1, true, 256, kModeSwiGLU>(a, tmap_a, tmap_b, tmap_c, sm_count, stream);
+    return launch_variant<1, true, 256, kModeGather | kModeSwiGLU>(a, tmap_a, tmap_b, tmap_c, sm_count, stream);
+  }
   if (a.fmt == 0) {
     return a.grouped ? launch_variant<0, true, BN>(a, tmap_a, tmap_b, tmap_c, sm_count, stream)
                      : launch_variant<0, false, BN>(a, tmap_a, tmap_b, tmap_c, sm_count, stream);

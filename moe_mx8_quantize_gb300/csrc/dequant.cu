@@ -186,14 +186,7 @@ __global__ void __launch_bounds__(kThreads) swiglu_kernel(const uint16_t* __rest
       const float gv[2] = {bf16_lo(gw[j]), bf16_hi(gw[j])};
       const float uv[2] = {bf16_lo(uw[j]), bf16_hi(uw[j])};
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        // silu(g) = g * sigmoid(g); the exponent is taken of -|g| so it never
-        // overflows: sigmoid(g) = 1/(1+e^-g) for g >= 0, e^g/(1+e^g) for g < 0
-        const float t = expf(-fabsf(gv[k]));
-        const float num = gv[k] >= 0.f ? gv[k] : __fmul_rn(gv[k], t);
-        const float silu = __fdiv_rn(num, __fadd_rn(1.0f, t));
-        v[k] = __fmul_rn(silu, uv[k]);
-      }
+      for (int k = 0; k < 2; ++k) v[k] = silu_mul(gv[k], uv[k]);
       o[j] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[0]))) |
              (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[1]))) << 16);
     }

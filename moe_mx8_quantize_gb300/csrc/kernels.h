@@ -31,6 +31,14 @@ cudaError_t launch_nvfp4_quant(const uint16_t* x, int64_t R, int64_t C, int64_t 
                                const int64_t* offs, int G, uint8_t* q, uint8_t* sblk, float* s32,
                                void* scratch, int* err, int sm_count, cudaStream_t stream);
 
+// Per-token NVFP4 of T tokens before dispatch: scale words to the grouped
+// scale rows of each token's topk dispatched copies (dest [T * topk], offs
+// [G + 1]); codes and S_dec to the copies' rows (disp_codes) or token-major.
+constexpr int kMaxTopk = 16;
+cudaError_t launch_nvfp4_dispatch(const uint16_t* x, int64_t T, int64_t C, int64_t ld, const int64_t* dest,
+                                  int topk, const int64_t* offs, int G, int disp_codes, uint8_t* q, uint8_t* sblk,
+                                  float* s32, int sm_count, cudaStream_t stream);
+
 cudaError_t launch_dequant(int fmt, const uint8_t* q, const uint8_t* s, const float* s32,
                            int s32_mode, const int64_t* offs, int G, int64_t R, int64_t C,
                            int out_bf16, void* out, int sm_count, cudaStream_t stream);
@@ -55,6 +63,11 @@ struct GemmArgs {
   int grouped;
   int G;
   const int64_t* offs;
+  // fused MoE modes (grouped only)
+  const uint8_t* A;        // gathered mode: token-major A data [a_src_rows, K bytes]
+  const int64_t* a_rows;   // gathered mode: token of each dispatched row [M]
+  int64_t a_src_rows;      // gathered mode: rows of the token-major A
+  int64_t ffn;             // SwiGLU mode: F (up rows of B start at F; output has F columns)
   int* err;
 };
 

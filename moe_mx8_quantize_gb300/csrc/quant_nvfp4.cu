@@ -151,12 +151,25 @@ __device__ __forceinline__ uint32_t row_absmax_lane(const uint16_t* __restrict__
   return m;
 }
 
+// Where an encoded row goes: out.codes(byte offset, 8 bytes of codes),
+// out.scale(4-block group k4, 32-bit scale word in the tensor-core tile
+// layout) and out.sdec(S_dec) (lane 0).  RowOut writes one row; the
+// before-dispatch quantizer writes a token to its dispatched copies.
+struct RowOut {
+  uint8_t* qr;        // the row's codes
+  uint8_t* swr;       // its first scale word
+  float* s32;         // its S_dec
+  __device__ __forceinline__ void codes(int off, uint2 v) const { *reinterpret_cast<uint2*>(qr + off) = v; }
+  __device__ __forceinline__ void scale(int k4, uint32_t w) const { *reinterpret_cast<uint32_t*>(swr + k4 * 512) = w; }
+  __device__ __forceinline__ void sdec(float v) const { *s32 = v; }
+};
+
 // Encodes 512-element chunk j of a row: lane l encodes the 16-element block
-// [512 j + 16 l, +16) held in (a, b); qr is the row's codes, swr its first
-// scale word in the tensor-core tile layout.
+// [512 j + 16 l, +16) held in (a, b); the 4 scales of a 4-block group are
+// gathered by shuffles into one 32-bit word.
+template <typename Out>
 __device__ __forceinline__ void encode_chunk(const uint4& a, const uint4& b, int j, int C, int lane, float senc,
-                                             const float2* __restrict__ tab, uint8_t* __restrict__ qr,
-                                             uint8_t* __restrict__ swr, int kt) {
+                                             const float2* __restrict__ tab, const Out& out, int kt) {
   const int c = j * 512 + lane * 16;
   const float bmax = abs_halves_max(absmax16(a, b));
   constexpr float kInv6 = 1.0f / 6.0f;                     // RN(1/6)
@@ -175,30 +188,21 @@ __device__ __forceinline__ void encode_chunk(const uint4& a, const uint4& b, int
     mul_bf16x2(w[4 + i], rr, v1[2 * i], v1[2 * i + 1]);
   }
   const uint32_t p0 = cvt_e2m1x8(v0), p1 = cvt_e2m1x8(v1);
-  if (c < C) *reinterpret_cast<uint2*>(qr + (c >> 1)) = make_uint2(p0, p1);
+  if (c < C) out.codes(c >> 1, make_uint2(p0, p1));
   const uint32_t s1 = __shfl_down_sync(0xffffffffu, sb, 1);
   const uint32_t s2 = __shfl_down_sync(0xffffffffu, sb, 2);
   const uint32_t s3 = __shfl_down_sync(0xffffffffu, sb, 3);
   const int k4 = j * 8 + (lane >> 2);
-  if ((lane & 3) == 0 && k4 < kt)
-    *reinterpret_cast<uint32_t*>(swr + k4 * 512) = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+  if ((lane & 3) == 0 && k4 < kt) out.scale(k4, sb | (s1 << 8) | (s2 << 16) | (s3 << 24));
 }
 
-// Encodes data row `row` (or zeros scale row sr when row < 0) with scale S_enc;
-// for scope_token the amax and S_dec come from the row itself.
-template <int kCh, bool kHint = false>
-__device__ __forceinline__ void process_row(const uint16_t* __restrict__ x, int64_t row, int C, int64_t ld,
-                                            bool scope_token, float senc_given, const float2* __restrict__ tab,
-                                            uint8_t* __restrict__ q, uint8_t* __restrict__ sblk,
-                                            float* __restrict__ s32, int64_t sr, int kt, int lane,
-                                            uint64_t pol = 0) {
-  uint8_t* swr = sblk + sf_row_base(sr, kt);
-  if (row < 0) {  // padding row of the scale tile
-    for (int k4 = lane; k4 < kt; k4 += 32) *reinterpret_cast<uint32_t*>(swr + k4 * 512) = 0u;
-    return;
-  }
+// Encodes data row `row` with scale S_enc (for scope_token the amax and
+// S_dec come from the row itself) into out.
+template <int kCh, bool kHint, typename Out>
+__device__ __forceinline__ void encode_row(const uint16_t* __restrict__ x, int64_t row, int C, int64_t ld,
+                                           bool scope_token, float senc_given, const float2* __restrict__ tab,
+                                           const Out& out, int kt, int lane, uint64_t pol) {
   const uint16_t* xr = x + row * ld;
-  uint8_t* qr = q + row * (C / 2);
   if (kCh > 0) {
     const int nch = (C + 511) / 512;
     uint4 w[2 * (kCh > 0 ? kCh : 1)];
@@ -216,26 +220,42 @@ __device__ __forceinline__ void process_row(const uint16_t* __restrict__ x, int6
       for (int i = 0; i < kCh; ++i) m = amax2(m, absmax16(w[2 * i], w[2 * i + 1]));
       float sdec;
       nvfp4_scales(warp_max(abs_halves_max(m)), senc, sdec);
-      if (lane == 0) s32[row] = sdec;
+      if (lane == 0) out.sdec(sdec);
     }
 #pragma unroll
     for (int i = 0; i < kCh; ++i)
-      if (i < nch) encode_chunk(w[2 * i], w[2 * i + 1], i, C, lane, senc, tab, qr, swr, kt);
+      if (i < nch) encode_chunk(w[2 * i], w[2 * i + 1], i, C, lane, senc, tab, out, kt);
   } else {
     float senc = senc_given;
     if (scope_token) {
       float sdec;
       nvfp4_scales(warp_max(abs_halves_max(row_absmax_lane<0, kHint>(xr, C, lane, pol))), senc, sdec);
-      if (lane == 0) s32[row] = sdec;
+      if (lane == 0) out.sdec(sdec);
     }
     for (int j = 0; j * 512 < C; ++j) {
       const int c = j * 512 + lane * 16;
       const bool ok = c < C;
       const uint4 a = ok ? ld_row16<kHint>(xr + c, pol) : make_uint4(0, 0, 0, 0);
       const uint4 b = ok ? ld_row16<kHint>(xr + c + 8, pol) : make_uint4(0, 0, 0, 0);
-      encode_chunk(a, b, j, C, lane, senc, tab, qr, swr, kt);
+      encode_chunk(a, b, j, C, lane, senc, tab, out, kt);
     }
   }
+}
+
+// Encodes data row `row` (or zeros scale row sr when row < 0) into scale row sr.
+template <int kCh, bool kHint = false>
+__device__ __forceinline__ void process_row(const uint16_t* __restrict__ x, int64_t row, int C, int64_t ld,
+                                            bool scope_token, float senc_given, const float2* __restrict__ tab,
+                                            uint8_t* __restrict__ q, uint8_t* __restrict__ sblk,
+                                            float* __restrict__ s32, int64_t sr, int kt, int lane,
+                                            uint64_t pol = 0) {
+  uint8_t* swr = sblk + sf_row_base(sr, kt);
+  if (row < 0) {  // padding row of the scale tile
+    for (int k4 = lane; k4 < kt; k4 += 32) *reinterpret_cast<uint32_t*>(swr + k4 * 512) = 0u;
+    return;
+  }
+  const RowOut out{q + row * (C / 2), swr, s32 + row};
+  encode_row<kCh, kHint>(x, row, C, ld, scope_token, senc_given, tab, out, kt, lane, pol);
 }
 
 // Data row behind scale row sr (-1 for padding).
@@ -270,6 +290,91 @@ __global__ void __launch_bounds__(kThreads, kCh >= 8 || kCh == 0 ? 1 : 4) nvfp4_
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
   for (int64_t sr = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); sr < TP; sr += nwarps)
     process_row<kCh>(x, data_row(gs, grouped, G, R, sr), C32, ld, true, 0.f, tab, q, sblk, s32, sr, kt, lane);
+}
+
+// ------------------------------------------------------------------ token scope, before dispatch
+// Each token is encoded once; its copies are the dispatched rows
+// dest[t * topk + j] (grouped by the dispatch offsets).  The scale words go
+// to the copies' scale rows in the grouped layout; the codes and S_dec go to
+// the copies' rows too (disp_codes: a plain grouped GEMM reads them) or stay
+// token-major (q [T, C/2], s32 [T]: the GEMM gathers the rows).  Per-token
+// scaling makes this byte-identical to quantizing the dispatched rows.
+struct DispatchOut {
+  const int64_t* srow;   // [topk] scale rows of the copies (-1: skipped)
+  const int64_t* drow;   // [topk] dispatched rows of the copies (-1: skipped)
+  int n;
+  bool disp_codes;
+  int64_t token;
+  int64_t c2;            // code bytes per row
+  int kt;
+  uint8_t* q;
+  uint8_t* sblk;
+  float* s32;
+  __device__ __forceinline__ void codes(int off, uint2 v) const {
+    if (!disp_codes) {
+      *reinterpret_cast<uint2*>(q + token * c2 + off) = v;
+      return;
+    }
+    for (int j = 0; j < n; ++j)
+      if (drow[j] >= 0) *reinterpret_cast<uint2*>(q + drow[j] * c2 + off) = v;
+  }
+  __device__ __forceinline__ void scale(int k4, uint32_t w) const {
+    for (int j = 0; j < n; ++j)
+      if (srow[j] >= 0) *reinterpret_cast<uint32_t*>(sblk + sf_row_base(srow[j], kt) + k4 * 512) = w;
+  }
+  __device__ __forceinline__ void sdec(float v) const {
+    if (!disp_codes) {
+      s32[token] = v;
+      return;
+    }
+    for (int j = 0; j < n; ++j)
+      if (drow[j] >= 0) s32[drow[j]] = v;
+  }
+};
+
+// Warps first take the T tokens, then the scale rows, zeroing the padding
+// rows of each group's last tile.
+template <int kCh>
+__global__ void __launch_bounds__(kThreads, kCh >= 8 || kCh == 0 ? 1 : 4) nvfp4_dispatch_kernel(
+    const uint16_t* __restrict__ x, int64_t T, int64_t C, int64_t ld, const int64_t* __restrict__ dest,
+    int topk, const int64_t* __restrict__ offs, int G, int disp_codes, uint8_t* __restrict__ q,
+    uint8_t* __restrict__ sblk, float* __restrict__ s32) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  GroupSmem& gs = *reinterpret_cast<GroupSmem*>(smem_raw);
+  __shared__ float2 tab[128];
+  __shared__ int64_t dsr[kWarps][kMaxTopk];          // copies' scale rows ...
+  __shared__ int64_t ddr[kWarps][kMaxTopk];          // ... and dispatched rows, for a warp's token
+  init_scale_table(tab);
+  __syncthreads();
+  load_group_prefix(gs, offs, G);
+  const int64_t R = gs.offs[G], TP = gs.pref[G];
+  const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
+  const int C32 = static_cast<int>(C);
+  const int kt = (C32 / 16 + 3) / 4;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
+  for (int64_t u = static_cast<int64_t>(blockIdx.x) * kWarps + wl; u < T + TP; u += nwarps) {
+    if (u < T) {
+      if (lane < topk) {
+        int64_t dr = dest[u * topk + lane];
+        int64_t sr = -1;                              // rows outside [0, R) are skipped
+        if (dr >= 0 && dr < R) {
+          const int g = upper_group(gs.offs, G, dr);
+          sr = gs.pref[g] + (dr - gs.offs[g]);
+        } else {
+          dr = -1;
+        }
+        dsr[wl][lane] = sr;
+        ddr[wl][lane] = dr;
+      }
+      __syncwarp();
+      const DispatchOut out{dsr[wl], ddr[wl], topk, disp_codes != 0, u, C / 2, kt, q, sblk, s32};
+      encode_row<kCh, false>(x, u, C32, ld, true, 0.f, tab, out, kt, lane, 0);
+      __syncwarp();
+    } else {
+      const int64_t sr = u - T;
+      if (data_row(gs, true, G, R, sr) < 0) process_row<kCh>(x, -1, C32, ld, true, 0.f, tab, q, sblk, s32, sr, kt, lane);
+    }
+  }
 }
 
 // ------------------------------------------------------------------ group / tensor scope
@@ -522,6 +627,18 @@ __global__ void __launch_bounds__(kScopedThreads, kCh >= 8 || kCh == 0 ? 1 : 4) 
 }
 
 template <int kCh>
+cudaError_t launch_dispatch(unsigned grid, cudaStream_t stream, const uint16_t* x, int64_t T, int64_t C,
+                            int64_t ld, const int64_t* dest, int topk, const int64_t* offs, int G, int disp_codes,
+                            uint8_t* q, uint8_t* sblk, float* s32) {
+  auto k = nvfp4_dispatch_kernel<kCh>;
+  const size_t smem = sizeof(GroupSmem);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  k<<<grid, kThreads, smem, stream>>>(x, T, C, ld, dest, topk, offs, G, disp_codes, q, sblk, s32);
+  return cudaGetLastError();
+}
+
+template <int kCh>
 cudaError_t launch_token(unsigned grid, size_t smem, cudaStream_t stream, const uint16_t* x, int64_t R,
                          int64_t C, int64_t ld, const int64_t* offs, int G, uint8_t* q, uint8_t* sblk,
                          float* s32) {
@@ -584,6 +701,21 @@ cudaError_t launch_nvfp4_quant(const uint16_t* x, int64_t R, int64_t C, int64_t 
   if (C <= 4096) return launch_token<8>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32);
   if (C <= 8192) return launch_token<16>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32);
   return launch_token<0>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32);
+}
+
+cudaError_t launch_nvfp4_dispatch(const uint16_t* x, int64_t T, int64_t C, int64_t ld, const int64_t* dest,
+                                  int topk, const int64_t* offs, int G, int disp_codes, uint8_t* q, uint8_t* sblk,
+                                  float* s32, int sm_count, cudaStream_t stream) {
+  const int64_t units = T + (T * topk + 127 * static_cast<int64_t>(G) + 127) / 128 * 128;
+  const int64_t want = (units + kWarps - 1) / kWarps;
+  const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+  unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
+  if (grid == 0) grid = 1;
+  if (C <= 1024) return launch_dispatch<2>(grid, stream, x, T, C, ld, dest, topk, offs, G, disp_codes, q, sblk, s32);
+  if (C <= 2048) return launch_dispatch<4>(grid, stream, x, T, C, ld, dest, topk, offs, G, disp_codes, q, sblk, s32);
+  if (C <= 4096) return launch_dispatch<8>(grid, stream, x, T, C, ld, dest, topk, offs, G, disp_codes, q, sblk, s32);
+  if (C <= 8192) return launch_dispatch<16>(grid, stream, x, T, C, ld, dest, topk, offs, G, disp_codes, q, sblk, s32);
+  return launch_dispatch<0>(grid, stream, x, T, C, ld, dest, topk, offs, G, disp_codes, q, sblk, s32);
 }
 
 }  // namespace mx8q

@@ -1,0 +1,141 @@
+"""GPU parity of the fused MoE expert GEMM: tokens quantized once before
+dispatch and gathered by the GEMM's producer, and the SwiGLU of the joint
+gate|up output done in the epilogue ("Miles Blackwell RL Cambia la
+Uniformidad BF16 por MXFP8 y NVFP4 Nativos", sections "La Compatibilidad..."
+and "Un Cuantizador Compartido...").  References are the oracle's FP64
+grouped GEMM over the dispatched operands (per-token quantization commutes
+with the dispatch gather: an oracle pin; the before-dispatch quantizer is
+checked byte for byte) and, for h, silu(g) * u
+in FP64 over those references, with the GEMM tolerance carried through."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import moe_mx8_quantize_gb300 as mx
+from moe_mx8_quantize_gb300 import inputs
+from tests._lib import ensure_built, gemm_tolerance_ok, host, dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+def _case(T, H, E, N, topk, seed, zipf=False):
+    """Token-major NVFP4 activations and per-expert weights [E, N, H] with
+    one FP32 scale per expert; N = 2F rows (gate then up)."""
+    d = inputs.moe(seed, "cpu", T, H, E, N // 2, topk, routing="zipf" if zipf else "uniform",
+                   with_weights=True)
+    disp = inputs.dispatch(d["topk_ids"], E)
+    offs = disp.offsets.numpy()
+    tor = disp.token_of_row.numpy()
+    Xb = inputs.bits(d["X"])
+    Aq, SAq, a32 = oracle.nvfp4_quantize(Xb)                              # per token, before dispatch
+    Wb = inputs.bits(d["W_gu"]).reshape(E * N, H)
+    B, SB, b32 = oracle.nvfp4_quantize(Wb, oracle.SCOPE_GROUP, np.arange(E + 1) * N)
+    return offs, tor, Xb, Aq, SAq, a32, B.reshape(E, N, H // 2), SB, b32
+
+
+def _dispatched(tor, Aq, SAq, a32):
+    return Aq[tor], SAq[tor], a32[tor]
+
+
+def _dest_rows(tor, topk):
+    """Inverse of the row -> token map: the topk dispatched rows of each token."""
+    return np.argsort(tor, kind="stable").reshape(-1, topk)
+
+
+@pytest.mark.parametrize("layout", [mx.DISPATCH_ROWS, mx.DISPATCH_TOKENS])
+@pytest.mark.parametrize("T,H,E,topk,zipf", [(64, 256, 5, 2, False), (300, 2048, 16, 8, True),
+                                             (40, 96, 7, 1, False), (33, 4096, 3, 3, False)])
+def test_quantize_dispatch_bit_exact(T, H, E, topk, zipf, layout):
+    """Codes and S_dec (per dispatched row, or token-major) and the
+    dispatched rows' block scales in the grouped layout (padding zero), byte
+    for byte against the oracle's quantization of the dispatched rows."""
+    offs, tor, Xb, Aq, SAq, a32, *_ = _case(T, H, E, 128, topk, seed=T + 7, zipf=zipf)
+    dest = torch.tensor(_dest_rows(tor, topk), dtype=torch.int64, device="cuda")
+    go = torch.tensor(offs, dtype=torch.int64, device="cuda")
+    q, sb, s32 = mx.nvfp4_quantize_dispatch(dev(Xb), dest, topk, go, layout)
+    dq, dsc, d32 = oracle.nvfp4_quantize(Xb[tor])          # the dispatched rows, quantized directly
+    if layout == mx.DISPATCH_ROWS:
+        assert np.array_equal(host(q), dq)
+        assert np.array_equal(host(s32).view(np.uint32), d32.view(np.uint32))
+    else:
+        assert np.array_equal(host(q), Aq)
+        assert np.array_equal(host(s32).view(np.uint32), a32.view(np.uint32))
+    sw = oracle.swizzle_scales(dsc, offs)
+    assert np.array_equal(host(sb)[: sw.size], sw)
+
+
+def _check(y, ref, absref, bf16=False, K=None):
+    ok, bad = gemm_tolerance_ok(y, ref, absref, bf16, K)
+    if not ok:
+        yf = np.asarray(y, np.float64).ravel()
+        i = bad[:5]
+        raise AssertionError(f"{bad.size} outputs out of tolerance; e.g. idx {i}: "
+                             f"got {yf[i]}, ref {ref.ravel()[i]}, abs {absref.ravel()[i]}")
+
+
+@pytest.mark.parametrize("T,H,E,N,topk,zipf", [(64, 256, 5, 256, 2, False), (300, 512, 16, 384, 4, True),
+                                               (40, 96, 7, 136, 1, False)])
+def test_gathered_grouped_gemm(T, H, E, N, topk, zipf):
+    offs, tor, _, Aq, SAq, a32, B, SB, b32 = _case(T, H, E, N, topk, seed=T + 1, zipf=zipf)
+    go = torch.tensor(offs, dtype=torch.int64, device="cuda")
+    rows_t = torch.tensor(tor, dtype=torch.int64, device="cuda")
+    y = host(mx.bs_grouped_gemm_fused(mx.FMT_NVFP4, go, dev(Aq), dev(oracle.swizzle_scales(SAq[tor], offs)), dev(B),
+                                      dev(oracle.swizzle_scales(SB, np.arange(E + 1) * N)), H, dev(a32), dev(b32),
+                                      a_rows=rows_t, out_dtype=torch.float32))
+    A, SA, ad = _dispatched(tor, Aq, SAq, a32)
+    rows = A.shape[0]
+    pairs = np.array([(m, n) for m in range(rows) for n in range(N)])
+    ref, absref = oracle.grouped_gemm_ref(1, offs, A, SA, B, SB, H, ad, b32, pairs)
+    _check(y.ravel(), ref, absref, K=H)
+
+
+def _h_tolerance(g, ag, u, au, K):
+    """|h - silu(g) u| allowed: each GEMM output within 1e-5 sum|a||b| +
+    K 2^-126 and then rounded to bf16 (2^-8 relative, generously); silu has
+    slope in [-0.1, 1.1]; h itself is rounded to bf16 and silu/expf in FP32
+    add a few FP32 units."""
+    dg = 1e-5 * ag + K * 2.0 ** -126 + 2.0 ** -8 * np.abs(g)
+    du = 1e-5 * au + K * 2.0 ** -126 + 2.0 ** -8 * np.abs(u)
+    sil = g / (1.0 + np.exp(-g))
+    h = sil * u
+    tol = 1.1 * (np.abs(u) + du) * dg + (np.abs(sil) + 1.1 * dg) * du + 2.0 ** -7 * np.abs(h) + 1e-30
+    return h, tol
+
+
+@pytest.mark.parametrize("gather", [True, False])
+@pytest.mark.parametrize("T,H,E,F,topk", [(64, 256, 5, 128, 2), (200, 512, 9, 256, 4)])
+def test_swiglu_epilogue(gather, T, H, E, F, topk):
+    N = 2 * F
+    offs, tor, _, Aq, SAq, a32, B, SB, b32 = _case(T, H, E, N, topk, seed=T + F)
+    A, SA, ad = _dispatched(tor, Aq, SAq, a32)
+    go = torch.tensor(offs, dtype=torch.int64, device="cuda")
+    sbw = dev(oracle.swizzle_scales(SB, np.arange(E + 1) * N))
+    if gather:
+        h = mx.bs_grouped_gemm_fused(mx.FMT_NVFP4, go, dev(Aq), dev(oracle.swizzle_scales(SA, offs)), dev(B), sbw, H,
+                                     dev(a32), dev(b32), a_rows=torch.tensor(tor, dtype=torch.int64, device="cuda"),
+                                     epilogue=mx.EPI_SWIGLU)
+    else:
+        h = mx.bs_grouped_gemm_fused(mx.FMT_NVFP4, go, dev(A), dev(oracle.swizzle_scales(SA, offs)), dev(B), sbw, H,
+                                     dev(ad), dev(b32), epilogue=mx.EPI_SWIGLU)
+    hh = oracle.bf16_to_f32(host(h)).astype(np.float64)
+    rows = A.shape[0]
+    pg = np.array([(m, n) for m in range(rows) for n in range(F)])
+    pu = pg + np.array([0, F])
+    g, ag = oracle.grouped_gemm_ref(1, offs, A, SA, B, SB, H, ad, b32, pg)
+    u, au = oracle.grouped_gemm_ref(1, offs, A, SA, B, SB, H, ad, b32, pu)
+    href, tol = _h_tolerance(g, ag, u, au, H)
+    err = np.abs(hh.ravel() - href)
+    bad = np.nonzero(err > tol)[0]
+    assert bad.size == 0, f"{bad.size} h values out of tolerance, e.g. {hh.ravel()[bad[:4]]} vs {href[bad[:4]]}"
+    # the fused epilogue rounds g and u to bf16 exactly where the unfused
+    # gate|up output would be rounded, so it matches that path's SwiGLU
+    gu = mx.bs_grouped_gemm(mx.FMT_NVFP4, go, dev(A), dev(oracle.swizzle_scales(SA, offs)), dev(B), sbw, H,
+                            dev(ad), dev(b32), out_dtype=torch.bfloat16)
+    h2 = mx.swiglu(gu)
+    assert torch.equal(h.view(torch.int16), h2.view(torch.int16))

@@ -98,6 +98,23 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert lib.bf16_gemm(8, 8, 64, p, 68, p, 64, 0, p, 8, 0, p, 4096, None) == m.ERR_ALIGNMENT
     assert lib.bf16_gemm(8, 8, 64, p, 64, p, 64, 1, p, 8, 1, p, 4096, None) == m.ERR_UNSUPPORTED
     assert lib.bf16_gemm(0, 8, 64, None, 64, None, 64, 0, None, 8, 0, None, 0, None) == m.OK
+    # quantize before dispatch: topk range, missing offsets, cols % 16
+    assert lib.nvfp4_quantize_dispatch(p, 4, 32, 32, p, 0, p, 2, 1, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
+    assert lib.nvfp4_quantize_dispatch(p, 4, 32, 32, p, 17, p, 2, 1, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
+    assert lib.nvfp4_quantize_dispatch(p, 4, 32, 32, p, 2, None, 2, 1, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
+    assert lib.nvfp4_quantize_dispatch(p, 4, 24, 24, p, 2, p, 2, 1, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
+    assert lib.nvfp4_quantize_dispatch(p, 4, 32, 32, p, 2, p, 2, 7, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
+    # fused MoE GEMM: bad epilogue, SwiGLU needs N % 256 and bf16, formats other than NVFP4
+    assert lib.bs_grouped_gemm_fused(1, 2, p, 8, 256, 64, p, p, None, None, 0, p, p, None, 5, 1, p, 128, p, 4096,
+                                     None) == m.ERR_INVALID_ARG
+    assert lib.bs_grouped_gemm_fused(1, 2, p, 8, 384, 64, p, p, None, None, 0, p, p, None, 1, 1, p, 192, p, 4096,
+                                     None) == m.ERR_INVALID_ARG
+    assert lib.bs_grouped_gemm_fused(1, 2, p, 8, 256, 64, p, p, None, None, 0, p, p, None, 1, 0, p, 128, p, 4096,
+                                     None) == m.ERR_INVALID_ARG
+    assert lib.bs_grouped_gemm_fused(1, 2, p, 8, 256, 64, p, p, None, p, 0, p, p, None, 0, 1, p, 256, p, 4096,
+                                     None) == m.ERR_INVALID_ARG
+    assert lib.bs_grouped_gemm_fused(0, 2, p, 8, 256, 64, p, p, None, None, 0, p, p, None, 0, 1, p, 256, p, 4096,
+                                     None) == m.ERR_UNSUPPORTED
     # empty problems are no-ops
     assert lib.mx8_quantize(None, 0, 64, 64, m.ROWWISE, None, None, None, None, None, 0, None) == m.OK
     assert lib.bs_gemm(0, 0, 8, 64, None, None, None, 0, None, None, None, 0, 0, None, 8, 0, None, 0, None) == m.OK

@@ -149,3 +149,20 @@ def test_fp32_scale_is_the_token_amax_over_2688():
     # S_dec = RN_f32(amax / 2688): compare with the correctly rounded quotient
     exact = amax.astype(np.float64) / 2688.0
     assert np.array_equal(s32, exact.astype(np.float32))
+
+
+def test_quantize_before_dispatch_is_bit_identical():
+    """Per-token scaling makes the codes of a token independent of the batch:
+    quantizing the MoE-dispatched rows (each token repeated top-k times,
+    grouped by expert) gives the gathered rows of the token-major
+    quantization, byte for byte -- the reason the fused MoE GEMM may gather
+    tokens quantized once before dispatch."""
+    from moe_mx8_quantize_gb300 import inputs
+    d = inputs.moe(4, "cpu", 96, 256, 6, 128, 3, with_weights=False)
+    tor = inputs.dispatch(d["topk_ids"], 6).token_of_row.numpy()
+    Xb = inputs.bits(d["X"])
+    q, s, t = oracle.nvfp4_quantize(Xb)
+    q2, s2, t2 = oracle.nvfp4_quantize(Xb[tor])
+    assert len(tor) == 96 * 3
+    assert np.array_equal(q2, q[tor]) and np.array_equal(s2, s[tor])
+    assert np.array_equal(t2.view(np.uint32), t[tor].view(np.uint32))
