@@ -88,6 +88,7 @@ def _L():
                                             _p, _p, _p, _p, _p, _p,
                                             _p, _i64, _p, _p, _p]
         lib.or_swiglu.argtypes = [_p, _i64, _i64, _p]
+        lib.or_nvfp4_quantize_2d.argtypes = [_p, _i64, _i64, _i64, _p, _p, _p, _p, _p]
         lib.or_bf16_gemm_ref.argtypes = [_i64, _i64, _i64, _p, _i64, _p, _i64, _p, _i64, _p, _p]
         _lib = lib
     return _lib
@@ -238,6 +239,22 @@ def nvfp4_quantize(x_bits, scope=SCOPE_TOKEN, offs=None):
 
 
 S32_NONE, S32_ROW, S32_TENSOR, S32_GROUP = 0, 1, 2, 3
+
+
+def nvfp4_quantize_2d(x_bits):
+    """NVFP4 weights with 16x16 block scales and one FP32 tensor scale ->
+    (q_row [R,C/2], s_row [R,C/16], q_col [C,R/2], s_col [C,R/16], s32 [1]);
+    the columnwise copy is the transpose of the rowwise one."""
+    x = _c(x_bits, np.uint16)
+    R, C = x.shape
+    assert R % 16 == 0 and C % 16 == 0
+    q_row = np.zeros((R, C // 2), np.uint8)
+    s_row = np.empty((R, C // 16), np.uint8)
+    q_col = np.zeros((C, R // 2), np.uint8)
+    s_col = np.empty((C, R // 16), np.uint8)
+    s32 = np.empty(1, np.float32)
+    _L().or_nvfp4_quantize_2d(_ptr(x), R, C, C, _ptr(q_row), _ptr(s_row), _ptr(q_col), _ptr(s_col), _ptr(s32))
+    return q_row, s_row, q_col, s_col, s32
 
 
 def dequant_nvfp4(q, s, s32=None, s32_mode=S32_ROW, offs=None):

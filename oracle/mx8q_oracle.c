@@ -412,6 +412,62 @@ void or_nvfp4_quantize(const uint16_t *x, i64 R, i64 C, i64 ld, int scope,
     }
 }
 
+/* NVFP4 weights with 2-D 16x16 block scaling ([NV4] "La metodologia de
+ * formacion de cuatro partes": the backward pass uses the transposed weight,
+ * so 1x16 blocks would quantize forward and backward weights differently;
+ * 16x16 blocks give one quantized representation for both passes).  One
+ * FP32 scale for the tensor, as for tensor-scope NVFP4; per 16x16 block
+ * (rows 16 bi.., columns 16 bj..):
+ *   amax_b = max |x| over the 256 elements
+ *   sb, r  = as for a 1x16 block (E4M3 scale of RN(amax_b / 6) * S_enc)
+ *   code   = RNE_E2M1_satfinite( RN(x * r) )
+ * Outputs: the rowwise copy q_row [R, C/2] with s_row [R, C/16] (row n takes
+ * its block's sb) and the columnwise copy q_col [C, R/2] with s_col
+ * [C, R/16]: exactly the transposes of the rowwise codes and scales.
+ * Requires R % 16 == 0 and C % 16 == 0. */
+void or_nvfp4_quantize_2d(const uint16_t *x, i64 R, i64 C, i64 ld,
+                          uint8_t *q_row, uint8_t *s_row, uint8_t *q_col, uint8_t *s_col,
+                          float *s32)
+{
+    float amax = 0.0f;
+    for (i64 r = 0; r < R; r++) {
+        float a = row_amax(x + r * ld, C);
+        if (a > amax) amax = a;
+    }
+    float senc, sdec;
+    nvfp4_scales_from_amax(amax, &senc, &sdec);
+    s32[0] = sdec;
+    for (i64 bi = 0; bi < R / 16; bi++)
+        for (i64 bj = 0; bj < C / 16; bj++) {
+            float amax_b = 0.0f;
+            for (int i = 0; i < 16; i++)
+                for (int j = 0; j < 16; j++) {
+                    float a = absf_of_bf16(x[(bi * 16 + i) * ld + bj * 16 + j]);
+                    if (a > amax_b) amax_b = a;
+                }
+            float t = amax_b / 6.0f;
+            t = t * senc;
+            uint8_t sb = or_e4m3_encode(t);
+            float sbv = (float)or_e4m3_decode(sb);
+            float r = 0.0f;
+            if (sb != 0) {
+                r = senc / sbv;
+                if (!(r <= FLT_MAX)) r = FLT_MAX;
+            }
+            for (int i = 0; i < 16; i++) {
+                i64 n = bi * 16 + i;
+                s_row[n * (C / 16) + bj] = sb;
+                for (int j = 0; j < 16; j++) {
+                    i64 k = bj * 16 + j;
+                    if (i == 0) s_col[k * (R / 16) + bi] = sb;
+                    uint8_t code = or_e2m1_encode(or_bf16_to_f32(x[n * ld + k]) * r);
+                    put_nibble(q_row + n * (C / 2), k, code);
+                    put_nibble(q_col + k * (R / 2), n, code);
+                }
+            }
+        }
+}
+
 /* FP32 decode scale of row r under s32_mode: 0 none (1), 1 per row,
  * 2 per tensor, 3 per group (offs, G). */
 static double s32_of_row(const float *s32, int mode, const i64 *offs, int G, i64 r)
