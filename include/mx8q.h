@@ -205,6 +205,26 @@ mx8_status nvfp4_quantize_dispatch(const void *x, int64_t tokens, int64_t cols, 
                                    void *workspace, size_t workspace_bytes, mx8_stream_t stream);
 
 /*
+ * NVFP4 weights with 2-D 16x16 block scaling ([NV4] "La metodologia de
+ * formacion de cuatro partes": one quantized representation for the forward
+ * weight and the transposed backward weight).  One FP32 tensor scale
+ * (S_enc / S_dec from the tensor amax, as NVFP4_SCOPE_TENSOR); per 16x16
+ * block the NVFP4 block scale and codes of that scale.
+ *   flags  : MX8_ROWWISE | MX8_COLWISE
+ *   q_row  : uint8 [rows, cols/2]; s_row: mx8_scale_bytes(NVFP4, rows, cols),
+ *            each row holding its block's scale (the tensor cores read 1x16)
+ *   q_col  : uint8 [cols, rows/2], the transposed copy; s_col:
+ *            mx8_scale_bytes(NVFP4, cols, rows) -- codes and scales are the
+ *            exact transposes of the rowwise ones
+ *   s32    : float [1], S_dec
+ * Requires rows % 32 == 0, cols % 32 == 0, ld % 8 == 0, 16-byte aligned
+ * pointers.  Two launches (tensor amax, then encode).
+ */
+mx8_status nvfp4_quantize_2d(const void *x, int64_t rows, int64_t cols, int64_t ld, int flags,
+                             uint8_t *q_row, uint8_t *s_row, uint8_t *q_col, uint8_t *s_col,
+                             float *s32, void *workspace, size_t workspace_bytes, mx8_stream_t stream);
+
+/*
  * nvfp4_quantize_per_token() for callers that cannot allocate device memory
  * and so cannot provide a workspace (for instance a plugin whose host
  * application owns every allocation).  Same arguments and results, minus the

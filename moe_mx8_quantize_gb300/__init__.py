@@ -31,7 +31,7 @@ S32_NONE, S32_ROW, S32_TENSOR, S32_GROUP = 0, 1, 2, 3
 # every C symbol the header declares
 EXPORTS = ("mx8_scale_bytes", "mx8_scale_bytes_grouped", "mx8_workspace_bytes",
            "mx8_device_sm_count", "mx8_quantize", "mxfp4_quantize", "nvfp4_quantize_per_token",
-           "nvfp4_quantize_dispatch",
+           "nvfp4_quantize_dispatch", "nvfp4_quantize_2d",
            "nvfp4_quantize_per_token_noalloc", "dequantize",
            "bs_gemm", "bs_grouped_gemm", "bs_grouped_gemm_fused", "bf16_gemm", "mx8_swiglu", "mx8_check_device_error", "mx8_selftest_bounded_wait",
            "mx8_status_string")
@@ -85,6 +85,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                     _i64, _p, _sz, _p]
     lib.nvfp4_quantize_dispatch.restype = _i
     lib.nvfp4_quantize_dispatch.argtypes = [_p, _i64, _i64, _i64, _p, _i, _p, _i, _i, _p, _p, _p, _p, _sz, _p]
+    lib.nvfp4_quantize_2d.restype = _i
+    lib.nvfp4_quantize_2d.argtypes = [_p, _i64, _i64, _i64, _i, _p, _p, _p, _p, _p, _p, _sz, _p]
     lib.bs_grouped_gemm_fused.restype = _i
     lib.bs_grouped_gemm_fused.argtypes = [_i, _i, _p, _i64, _i64, _i64, _p, _p, _p, _p, _i64, _p, _p, _p, _i,
                                           _i, _p, _i64, _p, _sz, _p]
@@ -274,6 +276,32 @@ def nvfp4_quantize_dispatch(x, dest_rows, topk, group_offsets, layout=DISPATCH_R
     s32 = torch.empty(max(n, 1), dtype=torch.float32, device=x.device)
     nvfp4_quantize_dispatch_into(x, dest_rows, topk, group_offsets, q, s_blk, s32, layout, ws, stream)
     return q, s_blk, s32[:n]
+
+
+def nvfp4_quantize_2d_into(x, q_row, s_row, q_col, s_col, s32, flags=ROWWISE | COLWISE, ws=None, stream=None):
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    R, C = x.shape
+    ws = _ws(ws, 1, x.device)
+    _check(load().nvfp4_quantize_2d(_ptr(x), R, C, x.stride(0), flags, _ptr(q_row), _ptr(s_row), _ptr(q_col),
+                                    _ptr(s_col), _ptr(s32), _ptr(ws), ws.numel(), _stream(stream)),
+           "nvfp4_quantize_2d")
+
+
+def nvfp4_quantize_2d(x, flags=ROWWISE | COLWISE, ws=None, stream=None):
+    """NVFP4 weights with 16x16 block scales: (q_row [R,C/2], s_row tiles,
+    q_col [C,R/2], s_col tiles, s32 [1]); copies not requested are None."""
+    R, C = x.shape
+    dev = x.device
+    q_row = s_row = q_col = s_col = None
+    if flags & ROWWISE:
+        q_row = torch.empty((R, C // 2), dtype=torch.uint8, device=dev)
+        s_row = _u8(scale_bytes(FMT_NVFP4, R, C), dev)
+    if flags & COLWISE:
+        q_col = torch.empty((C, R // 2), dtype=torch.uint8, device=dev)
+        s_col = _u8(scale_bytes(FMT_NVFP4, C, R), dev)
+    s32 = torch.empty(1, dtype=torch.float32, device=dev)
+    nvfp4_quantize_2d_into(x, q_row, s_row, q_col, s_col, s32, flags, ws, stream)
+    return q_row, s_row, q_col, s_col, s32
 
 
 # ---------------------------------------------------------------- dequantize

@@ -39,6 +39,12 @@ cudaError_t launch_nvfp4_dispatch(const uint16_t* x, int64_t T, int64_t C, int64
                                   int topk, const int64_t* offs, int G, int disp_codes, uint8_t* q, uint8_t* sblk,
                                   float* s32, int sm_count, cudaStream_t stream);
 
+// NVFP4 with 16x16 block scales and one FP32 tensor scale (rowwise and/or
+// the transposed copy); amax_bits: 4 bytes of device scratch.
+cudaError_t launch_nvfp4_2d(const uint16_t* x, int64_t R, int64_t C, int64_t ld, bool row, bool col,
+                            uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, float* s32,
+                            uint32_t* amax_bits, int sm_count, cudaStream_t stream);
+
 cudaError_t launch_dequant(int fmt, const uint8_t* q, const uint8_t* s, const float* s32,
                            int s32_mode, const int64_t* offs, int G, int64_t R, int64_t C,
                            int out_bf16, void* out, int sm_count, cudaStream_t stream);

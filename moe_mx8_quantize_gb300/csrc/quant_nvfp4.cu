@@ -70,12 +70,6 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kItemRows = 32;                 // rows (or scale rows) per work item
 constexpr int64_t kL2LeadBytes = 32ll << 20;  // input bytes between a group's amax and encode items
 
-__device__ __forceinline__ void nvfp4_scales(float amax, float& senc, float& sdec) {
-  float e = __fdiv_rn(2688.0f, amax);          // 2688 = 6 (E2M1 max) * 448 (E4M3 max)
-  if (!(e <= FLT_MAX)) e = FLT_MAX;
-  senc = e;
-  sdec = __fdiv_rn(amax, 2688.0f);
-}
 
 // {E4M3 value, RN(1 / value)} per E4M3 code; {0, 0} for code 0.
 __device__ __forceinline__ void init_scale_table(float2* tab) {
@@ -85,11 +79,6 @@ __device__ __forceinline__ void init_scale_table(float2* tab) {
   }
 }
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int d = 16; d >= 1; d >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, d));
-  return v;
-}
 
 __device__ __forceinline__ uint4 ld_nc(const uint16_t* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));

@@ -104,6 +104,11 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert lib.nvfp4_quantize_dispatch(p, 4, 32, 32, p, 2, None, 2, 1, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
     assert lib.nvfp4_quantize_dispatch(p, 4, 24, 24, p, 2, p, 2, 1, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
     assert lib.nvfp4_quantize_dispatch(p, 4, 32, 32, p, 2, p, 2, 7, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
+    # 2-D block-scaled NVFP4: rows and cols % 32, flags
+    assert lib.nvfp4_quantize_2d(p, 48, 64, 64, 3, p, p, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
+    assert lib.nvfp4_quantize_2d(p, 64, 48, 48, 3, p, p, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
+    assert lib.nvfp4_quantize_2d(p, 64, 64, 64, 0, p, p, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
+    assert lib.nvfp4_quantize_2d(p, 64, 64, 64, 3, p, p, p, p, None, p, 4096, None) == m.ERR_INVALID_ARG
     # fused MoE GEMM: bad epilogue, SwiGLU needs N % 256 and bf16, formats other than NVFP4
     assert lib.bs_grouped_gemm_fused(1, 2, p, 8, 256, 64, p, p, None, None, 0, p, p, None, 5, 1, p, 128, p, 4096,
                                      None) == m.ERR_INVALID_ARG
