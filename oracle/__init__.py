@@ -89,6 +89,8 @@ def _L():
                                             _p, _i64, _p, _p, _p]
         lib.or_swiglu.argtypes = [_p, _i64, _i64, _p]
         lib.or_nvfp4_quantize_2d.argtypes = [_p, _i64, _i64, _i64, _p, _p, _p, _p, _p]
+        lib.or_rht16.argtypes = [_p, ctypes.c_uint, _p]
+        lib.or_nvfp4_quantize_rht_colwise.argtypes = [_p, _i64, _i64, _i64, ctypes.c_uint, _p, _p, _p]
         lib.or_bf16_gemm_ref.argtypes = [_i64, _i64, _i64, _p, _i64, _p, _i64, _p, _i64, _p, _p]
         _lib = lib
     return _lib
@@ -255,6 +257,27 @@ def nvfp4_quantize_2d(x_bits):
     s32 = np.empty(1, np.float32)
     _L().or_nvfp4_quantize_2d(_ptr(x), R, C, C, _ptr(q_row), _ptr(s_row), _ptr(q_col), _ptr(s_col), _ptr(s32))
     return q_row, s_row, q_col, s_col, s32
+
+
+def rht16(x, sign_mask):
+    """y = H16 diag(s) x / 4 in binary32 (fast Walsh-Hadamard order)."""
+    xi = np.ascontiguousarray(np.asarray(x, np.float32).reshape(16))
+    y = np.empty(16, np.float32)
+    _L().or_rht16(_ptr(xi), int(sign_mask) & 0xFFFF, _ptr(y))
+    return y
+
+
+def nvfp4_quantize_rht_colwise(x_bits, sign_mask):
+    """Transposed NVFP4 copy of a Wgrad input with the 16x16 random Hadamard
+    transform along its rows -> (qT [C,R/2], sT [C,R/16], s32 [1])."""
+    x = _c(x_bits, np.uint16)
+    R, C = x.shape
+    assert R % 16 == 0
+    qT = np.zeros((C, R // 2), np.uint8)
+    sT = np.empty((C, R // 16), np.uint8)
+    s32 = np.empty(1, np.float32)
+    _L().or_nvfp4_quantize_rht_colwise(_ptr(x), R, C, C, int(sign_mask) & 0xFFFF, _ptr(qT), _ptr(sT), _ptr(s32))
+    return qT, sT, s32
 
 
 def dequant_nvfp4(q, s, s32=None, s32_mode=S32_ROW, offs=None):

@@ -29,6 +29,7 @@
  * operation below must be a single IEEE round-to-nearest operation).
  */
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 #include <math.h>
 #include <float.h>
@@ -466,6 +467,87 @@ void or_nvfp4_quantize_2d(const uint16_t *x, i64 R, i64 C, i64 ld,
                 }
             }
         }
+}
+
+/* 16x16 random Hadamard transform ([NV4] "La metodologia de formacion de
+ * cuatro partes": the Wgrad inputs are multiplied, in 16-element tiles along
+ * the reduction dimension, by a 16x16 Hadamard matrix combined with one
+ * random +-1 sign vector shared by all linear layers; the transform is
+ * orthogonal, so it cancels inside the Wgrad dot products):
+ *   y = (1/4) * H16 * diag(s) * x,   H16[i][j] = (-1)^popcount(i & j),
+ *   s_i = -1 where bit i of sign_mask is set.
+ * Evaluated in binary32 as the natural-order fast Walsh-Hadamard transform:
+ * v_i = s_i x_i (exact), then for h = 1, 2, 4, 8 and every pair (i, i + h)
+ * with (i & h) == 0: (v_i, v_{i+h}) <- (v_i + v_{i+h}, v_i - v_{i+h}), each
+ * one IEEE round-to-nearest operation; finally y_i = v_i * 0.25 (exact). */
+void or_rht16(const float *x, unsigned sign_mask, float *y)
+{
+    float v[16];
+    for (int i = 0; i < 16; i++) v[i] = ((sign_mask >> i) & 1u) ? -x[i] : x[i];
+    for (int h = 1; h < 16; h <<= 1)
+        for (int i = 0; i < 16; i++)
+            if ((i & h) == 0) {
+                float a = v[i], b = v[i + h];
+                v[i] = a + b;
+                v[i + h] = a - b;
+            }
+    for (int i = 0; i < 16; i++) y[i] = v[i] * 0.25f;
+}
+
+/* NVFP4 encode of one 16-element block of binary32 values (the steps of
+ * nvfp4_encode_row, from f32 instead of bf16 inputs). */
+static void nvfp4_encode_block_f32(const float *v, float senc, uint8_t *codes, uint8_t *sb_out)
+{
+    float amax_b = 0.0f;
+    for (int i = 0; i < 16; i++) {
+        float a = fabsf(v[i]);
+        if (a > amax_b) amax_b = a;
+    }
+    float t = amax_b / 6.0f;
+    t = t * senc;
+    uint8_t sb = or_e4m3_encode(t);
+    float sbv = (float)or_e4m3_decode(sb);
+    float r = 0.0f;
+    if (sb != 0) {
+        r = senc / sbv;
+        if (!(r <= FLT_MAX)) r = FLT_MAX;
+    }
+    *sb_out = sb;
+    for (int i = 0; i < 16; i++) codes[i] = or_e2m1_encode(v[i] * r);
+}
+
+/* The columnwise (transposed) NVFP4 copy of a Wgrad input x [R, C] (R the
+ * reduction dimension, e.g. tokens) with the 16x16 random Hadamard transform
+ * applied to every 16-row chunk of every column before quantization:
+ *   y[c][16 k .. 16 k + 15] = or_rht16(x[16 k .. 16 k + 15][c])
+ *   one FP32 scale from the amax of y (tensor scope), then per 16-block of y
+ *   the NVFP4 block scale and codes.
+ * qT [C, R/2], sT [C, R/16] canonical, s32[1] = S_dec.  R % 16 == 0. */
+void or_nvfp4_quantize_rht_colwise(const uint16_t *x, i64 R, i64 C, i64 ld, unsigned sign_mask,
+                                   uint8_t *qT, uint8_t *sT, float *s32)
+{
+    float *y = (float *)malloc(sizeof(float) * (size_t)(R * C));
+    float amax = 0.0f;
+    for (i64 c = 0; c < C; c++)
+        for (i64 k = 0; k < R / 16; k++) {
+            float in[16];
+            for (int i = 0; i < 16; i++) in[i] = or_bf16_to_f32(x[(k * 16 + i) * ld + c]);
+            or_rht16(in, sign_mask, y + c * R + k * 16);
+            for (int i = 0; i < 16; i++) {
+                float a = fabsf(y[c * R + k * 16 + i]);
+                if (a > amax) amax = a;
+            }
+        }
+    float senc, sdec;
+    nvfp4_scales_from_amax(amax, &senc, &sdec);
+    s32[0] = sdec;
+    for (i64 c = 0; c < C; c++)
+        for (i64 k = 0; k < R / 16; k++) {
+            uint8_t codes[16];
+            nvfp4_encode_block_f32(y + c * R + k * 16, senc, codes, sT + c * (R / 16) + k);
+            for (int i = 0; i < 16; i++) put_nibble(qT + c * (R / 2), k * 16 + i, codes[i]);
+        }
+    free(y);
 }
 
 /* FP32 decode scale of row r under s32_mode: 0 none (1), 1 per row,
