@@ -225,6 +225,28 @@ mx8_status nvfp4_quantize_2d(const void *x, int64_t rows, int64_t cols, int64_t 
                              float *s32, void *workspace, size_t workspace_bytes, mx8_stream_t stream);
 
 /*
+ * The transposed NVFP4 copy of a Wgrad input with the 16x16 random Hadamard
+ * transform ([NV4] "La metodologia de formacion de cuatro partes": Wgrad
+ * inputs are multiplied, in 16-element tiles along the reduction dimension,
+ * by a 16x16 Hadamard matrix combined with one random +-1 sign vector shared
+ * by all linear layers; orthogonal, so no correction is needed in the GEMM
+ * when both Wgrad operands use the same signs).
+ *   x         : bf16 [rows, cols] (rows = the Wgrad reduction dimension,
+ *               e.g. tokens), row stride ld
+ *   sign_mask : bit i set -> sign -1 for element i of every 16-row tile
+ *   per 16 rows of a column: y = (1/4) H16 diag(s) x in binary32, evaluated
+ *               as the natural-order fast Walsh-Hadamard butterfly; then
+ *               NVFP4 of y with one FP32 tensor scale from the amax of y
+ *   q_col     : uint8 [cols, rows/2]; s_col: mx8_scale_bytes(NVFP4, cols,
+ *               rows); s32: float [1] S_dec
+ * Requires rows % 32 == 0, cols % 8 == 0, ld % 8 == 0, 16-byte aligned
+ * pointers.  Two launches (transformed amax, then encode).
+ */
+mx8_status nvfp4_quantize_rht_colwise(const void *x, int64_t rows, int64_t cols, int64_t ld,
+                                      uint32_t sign_mask, uint8_t *q_col, uint8_t *s_col, float *s32,
+                                      void *workspace, size_t workspace_bytes, mx8_stream_t stream);
+
+/*
  * nvfp4_quantize_per_token() for callers that cannot allocate device memory
  * and so cannot provide a workspace (for instance a plugin whose host
  * application owns every allocation).  Same arguments and results, minus the

@@ -31,7 +31,7 @@ S32_NONE, S32_ROW, S32_TENSOR, S32_GROUP = 0, 1, 2, 3
 # every C symbol the header declares
 EXPORTS = ("mx8_scale_bytes", "mx8_scale_bytes_grouped", "mx8_workspace_bytes",
            "mx8_device_sm_count", "mx8_quantize", "mxfp4_quantize", "nvfp4_quantize_per_token",
-           "nvfp4_quantize_dispatch", "nvfp4_quantize_2d",
+           "nvfp4_quantize_dispatch", "nvfp4_quantize_2d", "nvfp4_quantize_rht_colwise",
            "nvfp4_quantize_per_token_noalloc", "dequantize",
            "bs_gemm", "bs_grouped_gemm", "bs_grouped_gemm_fused", "bf16_gemm", "mx8_swiglu", "mx8_check_device_error", "mx8_selftest_bounded_wait",
            "mx8_status_string")
@@ -87,6 +87,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.nvfp4_quantize_dispatch.argtypes = [_p, _i64, _i64, _i64, _p, _i, _p, _i, _i, _p, _p, _p, _p, _sz, _p]
     lib.nvfp4_quantize_2d.restype = _i
     lib.nvfp4_quantize_2d.argtypes = [_p, _i64, _i64, _i64, _i, _p, _p, _p, _p, _p, _p, _sz, _p]
+    lib.nvfp4_quantize_rht_colwise.restype = _i
+    lib.nvfp4_quantize_rht_colwise.argtypes = [_p, _i64, _i64, _i64, ctypes.c_uint32, _p, _p, _p, _p, _sz, _p]
     lib.bs_grouped_gemm_fused.restype = _i
     lib.bs_grouped_gemm_fused.argtypes = [_i, _i, _p, _i64, _i64, _i64, _p, _p, _p, _p, _i64, _p, _p, _p, _i,
                                           _i, _p, _i64, _p, _sz, _p]
@@ -302,6 +304,26 @@ def nvfp4_quantize_2d(x, flags=ROWWISE | COLWISE, ws=None, stream=None):
     s32 = torch.empty(1, dtype=torch.float32, device=dev)
     nvfp4_quantize_2d_into(x, q_row, s_row, q_col, s_col, s32, flags, ws, stream)
     return q_row, s_row, q_col, s_col, s32
+
+
+def nvfp4_quantize_rht_colwise_into(x, sign_mask, q_col, s_col, s32, ws=None, stream=None):
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    R, C = x.shape
+    ws = _ws(ws, 1, x.device)
+    _check(load().nvfp4_quantize_rht_colwise(_ptr(x), R, C, x.stride(0), int(sign_mask), _ptr(q_col), _ptr(s_col),
+                                             _ptr(s32), _ptr(ws), ws.numel(), _stream(stream)),
+           "nvfp4_quantize_rht_colwise")
+
+
+def nvfp4_quantize_rht_colwise(x, sign_mask, ws=None, stream=None):
+    """Transposed NVFP4 copy of a Wgrad input [R, C] with the 16x16 random
+    Hadamard transform along R: (q_col [C, R/2], s_col tiles, s32 [1])."""
+    R, C = x.shape
+    q_col = torch.empty((C, R // 2), dtype=torch.uint8, device=x.device)
+    s_col = _u8(scale_bytes(FMT_NVFP4, C, R), x.device)
+    s32 = torch.empty(1, dtype=torch.float32, device=x.device)
+    nvfp4_quantize_rht_colwise_into(x, sign_mask, q_col, s_col, s32, ws, stream)
+    return q_col, s_col, s32
 
 
 # ---------------------------------------------------------------- dequantize

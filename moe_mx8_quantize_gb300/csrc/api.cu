@@ -224,6 +224,23 @@ extern "C" mx8_status nvfp4_quantize_2d(const void* x, int64_t rows, int64_t col
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
+extern "C" mx8_status nvfp4_quantize_rht_colwise(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                                 uint32_t sign_mask, uint8_t* q_col, uint8_t* s_col, float* s32,
+                                                 void* workspace, size_t workspace_bytes, mx8_stream_t stream) {
+  if (rows < 0 || cols < 0 || ld < cols || rows % 32 != 0 || cols % 8 != 0 || sign_mask > 0xFFFFu)
+    return MX8_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return MX8_OK;
+  if (x == nullptr || q_col == nullptr || s_col == nullptr || s32 == nullptr) return MX8_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q_col) || !aligned16(s_col) || ld % 8 != 0) return MX8_ERR_ALIGNMENT;
+  if (rows > INT32_MAX || cols > INT32_MAX) return MX8_ERR_UNSUPPORTED;
+  mx8_status st = check_ws(workspace, workspace_bytes, 1);
+  if (st != MX8_OK) return st;
+  uint32_t* amax_bits = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + kErrWordBytes);
+  return from_cuda(launch_nvfp4_rht_colwise(static_cast<const uint16_t*>(x), rows, cols, ld, sign_mask, q_col,
+                                            s_col, s32, amax_bits, sm_count_current(),
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
 // ===================================================================== dequantize
 extern "C" mx8_status dequantize(int fmt, const uint8_t* q, const uint8_t* s, const float* s32,
                                  int s32_mode, const int64_t* group_offsets, int num_groups,
