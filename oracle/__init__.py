@@ -90,7 +90,14 @@ def _L():
         lib.or_swiglu.argtypes = [_p, _i64, _i64, _p]
         lib.or_nvfp4_quantize_2d.argtypes = [_p, _i64, _i64, _i64, _p, _p, _p, _p, _p]
         lib.or_rht16.argtypes = [_p, ctypes.c_uint, _p]
-        lib.or_nvfp4_quantize_rht_colwise.argtypes = [_p, _i64, _i64, _i64, ctypes.c_uint, _p, _p, _p]
+        lib.or_nvfp4_quantize_rht_colwise.argtypes = [_p, _i64, _i64, _i64, ctypes.c_uint, ctypes.c_int,
+                                                      ctypes.c_uint64, _p, _p, _p]
+        lib.or_philox4x64_10.argtypes = [_p, _p, _p]
+        lib.or_sr_bits.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
+        lib.or_sr_bits.restype = ctypes.c_uint32
+        lib.or_e2m1_sr.argtypes = [ctypes.c_float, ctypes.c_uint32]
+        lib.or_e2m1_sr.restype = ctypes.c_uint8
+        lib.or_nvfp4_quantize_sr.argtypes = [_p, _i64, _i64, _i64, ctypes.c_uint64, _p, _p, _p]
         lib.or_bf16_gemm_ref.argtypes = [_i64, _i64, _i64, _p, _i64, _p, _i64, _p, _i64, _p, _p]
         _lib = lib
     return _lib
@@ -267,17 +274,48 @@ def rht16(x, sign_mask):
     return y
 
 
-def nvfp4_quantize_rht_colwise(x_bits, sign_mask):
+def nvfp4_quantize_rht_colwise(x_bits, sign_mask, stochastic=False, seed=0):
     """Transposed NVFP4 copy of a Wgrad input with the 16x16 random Hadamard
-    transform along its rows -> (qT [C,R/2], sT [C,R/16], s32 [1])."""
+    transform along its rows -> (qT [C,R/2], sT [C,R/16], s32 [1]); the
+    codes by stochastic rounding under `seed` when `stochastic`."""
     x = _c(x_bits, np.uint16)
     R, C = x.shape
     assert R % 16 == 0
     qT = np.zeros((C, R // 2), np.uint8)
     sT = np.empty((C, R // 16), np.uint8)
     s32 = np.empty(1, np.float32)
-    _L().or_nvfp4_quantize_rht_colwise(_ptr(x), R, C, C, int(sign_mask) & 0xFFFF, _ptr(qT), _ptr(sT), _ptr(s32))
+    _L().or_nvfp4_quantize_rht_colwise(_ptr(x), R, C, C, int(sign_mask) & 0xFFFF, int(bool(stochastic)), int(seed),
+                                       _ptr(qT), _ptr(sT), _ptr(s32))
     return qT, sT, s32
+
+
+def philox4x64_10(counter, key):
+    """Philox4x64-10 block: 4 x uint64 counter, 2 x uint64 key -> 4 x uint64."""
+    c = np.ascontiguousarray(np.asarray(counter, np.uint64).reshape(4))
+    k = np.ascontiguousarray(np.asarray(key, np.uint64).reshape(2))
+    out = np.empty(4, np.uint64)
+    _L().or_philox4x64_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def sr_bits(seed, e):
+    return int(_L().or_sr_bits(int(seed), int(e)))
+
+
+def e2m1_sr(v, bits):
+    return int(_L().or_e2m1_sr(float(v), int(bits) & 0xFFFFFFFF))
+
+
+def nvfp4_quantize_sr(x_bits, seed):
+    """Per-token NVFP4 with stochastically rounded codes -> (q, s, s32)."""
+    x = _c(x_bits, np.uint16)
+    R, C = x.shape
+    assert C % 16 == 0
+    q = np.zeros((R, C // 2), np.uint8)
+    s = np.empty((R, C // 16), np.uint8)
+    s32 = np.empty(R, np.float32)
+    _L().or_nvfp4_quantize_sr(_ptr(x), R, C, C, int(seed), _ptr(q), _ptr(s), _ptr(s32))
+    return q, s, s32
 
 
 def dequant_nvfp4(q, s, s32=None, s32_mode=S32_ROW, offs=None):

@@ -469,6 +469,67 @@ void or_nvfp4_quantize_2d(const uint16_t *x, i64 R, i64 C, i64 ld,
         }
 }
 
+/* Stochastic rounding for gradients ([NV4] "La metodologia de formacion de
+ * cuatro partes": round-to-nearest-even biases gradient tensors; stochastic
+ * rounding picks one of the two nearest representable values with
+ * probability given by the distance to each, which removes the bias; it is
+ * applied to gradients only).
+ *
+ * Random bits: the counter-based generator Philox4x64-10 (Salmon, Moraes,
+ * Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011): ten
+ * rounds of two 64x64->128-bit multiplications with the round constants
+ * M0 = 0xD2E7470EE14C6C93, M1 = 0xCA5A826395121157 and Weyl key increments
+ * W0 = 0x9E3779B97F4A7C15, W1 = 0xBB67AE8584CAA73B:
+ *   (hi0, lo0) = M0 * c0, (hi1, lo1) = M1 * c2,
+ *   c = (hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0);  k += (W0, W1) between rounds. */
+void or_philox4x64_10(const uint64_t *ctr_in, const uint64_t *key_in, uint64_t *out)
+{
+    const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+    const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+    uint64_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+    uint64_t k0 = key_in[0], k1 = key_in[1];
+    for (int round = 0; round < 10; round++) {
+        if (round > 0) { k0 += W0; k1 += W1; }
+        unsigned __int128 p0 = (unsigned __int128)M0 * c0, p1 = (unsigned __int128)M1 * c2;
+        uint64_t hi0 = (uint64_t)(p0 >> 64), lo0 = (uint64_t)p0;
+        uint64_t hi1 = (uint64_t)(p1 >> 64), lo1 = (uint64_t)p1;
+        uint64_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* The 32 random bits of element e of a quantized tensor under seed: one
+ * Philox block (counter (e / 8, 0, 0, 0), key (seed, 0)) gives 8 words of 32
+ * bits; element e takes word e % 8 (the low half of 64-bit output (e % 8) / 2
+ * for even e, the high half for odd e). */
+uint32_t or_sr_bits(uint64_t seed, uint64_t e)
+{
+    uint64_t ctr[4] = {e >> 3, 0, 0, 0}, key[2] = {seed, 0}, out[4];
+    or_philox4x64_10(ctr, key, out);
+    uint64_t w = out[(e & 7) >> 1];
+    return (e & 1) ? (uint32_t)(w >> 32) : (uint32_t)w;
+}
+
+/* E2M1 code of v by stochastic rounding with 32 random bits:
+ *   |v| >= 6: 6 (saturate).  Otherwise lo <= |v| < hi are the neighbouring
+ *   grid values of {0, .5, 1, 1.5, 2, 3, 4, 6}, p = (|v| - lo) / (hi - lo)
+ *   (exact: the spacing is a power of two), and |v| rounds up to hi when
+ *   (bits >> 8) < p * 2^24, i.e. with probability p (to 2^-24).
+ *   The sign is kept (a negative value rounding to 0 gives code 0x8). */
+uint8_t or_e2m1_sr(float v, uint32_t bits)
+{
+    static const float grid[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+    uint8_t sign = signbit(v) ? 8 : 0;
+    float a = fabsf(v);
+    if (a >= 6.0f) return (uint8_t)(sign | 7);
+    int i = 0;
+    while (i < 6 && grid[i + 1] <= a) i++;          /* grid[i] <= a < grid[i+1] */
+    float p = (a - grid[i]) / (grid[i + 1] - grid[i]);
+    int up = (float)(bits >> 8) < p * 16777216.0f;
+    return (uint8_t)(sign | (i + up));
+}
+
 /* 16x16 random Hadamard transform ([NV4] "La metodologia de formacion de
  * cuatro partes": the Wgrad inputs are multiplied, in 16-element tiles along
  * the reduction dimension, by a 16x16 Hadamard matrix combined with one
@@ -521,10 +582,11 @@ static void nvfp4_encode_block_f32(const float *v, float senc, uint8_t *codes, u
  * applied to every 16-row chunk of every column before quantization:
  *   y[c][16 k .. 16 k + 15] = or_rht16(x[16 k .. 16 k + 15][c])
  *   one FP32 scale from the amax of y (tensor scope), then per 16-block of y
- *   the NVFP4 block scale and codes.
+ *   the NVFP4 block scale and codes (stochastic rounding of the codes when
+ *   `stochastic`, for gradient inputs).
  * qT [C, R/2], sT [C, R/16] canonical, s32[1] = S_dec.  R % 16 == 0. */
 void or_nvfp4_quantize_rht_colwise(const uint16_t *x, i64 R, i64 C, i64 ld, unsigned sign_mask,
-                                   uint8_t *qT, uint8_t *sT, float *s32)
+                                   int stochastic, uint64_t seed, uint8_t *qT, uint8_t *sT, float *s32)
 {
     float *y = (float *)malloc(sizeof(float) * (size_t)(R * C));
     float amax = 0.0f;
@@ -545,9 +607,58 @@ void or_nvfp4_quantize_rht_colwise(const uint16_t *x, i64 R, i64 C, i64 ld, unsi
         for (i64 k = 0; k < R / 16; k++) {
             uint8_t codes[16];
             nvfp4_encode_block_f32(y + c * R + k * 16, senc, codes, sT + c * (R / 16) + k);
+            if (stochastic) {
+                /* same block scale; codes by stochastic rounding, element index
+                 * = its position c * R + t in the transposed copy */
+                uint8_t sb = sT[c * (R / 16) + k];
+                float r = 0.0f;
+                if (sb != 0) {
+                    r = senc / (float)or_e4m3_decode(sb);
+                    if (!(r <= FLT_MAX)) r = FLT_MAX;
+                }
+                for (int i = 0; i < 16; i++)
+                    codes[i] = or_e2m1_sr(y[c * R + k * 16 + i] * r,
+                                          or_sr_bits(seed, (uint64_t)(c * R + k * 16 + i)));
+            }
             for (int i = 0; i < 16; i++) put_nibble(qT + c * (R / 2), k * 16 + i, codes[i]);
         }
     free(y);
+}
+
+/* Per-token NVFP4 with stochastic rounding of the element codes: the FP32
+ * scale and the block scales as or_nvfp4_quantize (scope 0, round to
+ * nearest even), each code from or_e2m1_sr(RN(x * r), or_sr_bits(seed,
+ * r * C + c)). */
+void or_nvfp4_quantize_sr(const uint16_t *x, i64 R, i64 C, i64 ld, uint64_t seed,
+                          uint8_t *q, uint8_t *s, float *s32)
+{
+    for (i64 row = 0; row < R; row++) {
+        const uint16_t *xr = x + row * ld;
+        float senc, sdec;
+        nvfp4_scales_from_amax(row_amax(xr, C), &senc, &sdec);
+        s32[row] = sdec;
+        for (i64 b = 0; b < C / 16; b++) {
+            float amax_b = 0.0f;
+            for (int i = 0; i < 16; i++) {
+                float a = absf_of_bf16(xr[b * 16 + i]);
+                if (a > amax_b) amax_b = a;
+            }
+            float t = amax_b / 6.0f;
+            t = t * senc;
+            uint8_t sb = or_e4m3_encode(t);
+            s[row * (C / 16) + b] = sb;
+            float r = 0.0f;
+            if (sb != 0) {
+                r = senc / (float)or_e4m3_decode(sb);
+                if (!(r <= FLT_MAX)) r = FLT_MAX;
+            }
+            for (int i = 0; i < 16; i++) {
+                i64 c = b * 16 + i;
+                float v = or_bf16_to_f32(xr[c]) * r;
+                put_nibble(q + row * (C / 2), c, or_e2m1_sr(v, or_sr_bits(seed, (uint64_t)(row * C + c))));
+            }
+        }
+    }
 }
 
 /* FP32 decode scale of row r under s32_mode: 0 none (1), 1 per row,
