@@ -234,6 +234,9 @@ mx8_status nvfp4_quantize_2d(const void *x, int64_t rows, int64_t cols, int64_t 
  *   x         : bf16 [rows, cols] (rows = the Wgrad reduction dimension,
  *               e.g. tokens), row stride ld
  *   sign_mask : bit i set -> sign -1 for element i of every 16-row tile
+ *   stochastic: 1 -> codes by stochastic rounding (gradient inputs), as in
+ *               nvfp4_quantize_per_token_sr(), element index = position in
+ *               q_col (row * rows + column); 0 -> round to nearest even
  *   per 16 rows of a column: y = (1/4) H16 diag(s) x in binary32, evaluated
  *               as the natural-order fast Walsh-Hadamard butterfly; then
  *               NVFP4 of y with one FP32 tensor scale from the amax of y
@@ -243,8 +246,26 @@ mx8_status nvfp4_quantize_2d(const void *x, int64_t rows, int64_t cols, int64_t 
  * pointers.  Two launches (transformed amax, then encode).
  */
 mx8_status nvfp4_quantize_rht_colwise(const void *x, int64_t rows, int64_t cols, int64_t ld,
-                                      uint32_t sign_mask, uint8_t *q_col, uint8_t *s_col, float *s32,
+                                      uint32_t sign_mask, int stochastic, uint64_t seed,
+                                      uint8_t *q_col, uint8_t *s_col, float *s32,
                                       void *workspace, size_t workspace_bytes, mx8_stream_t stream);
+
+/*
+ * Per-token NVFP4 of a gradient with stochastically rounded codes ([NV4] "La
+ * metodologia de formacion de cuatro partes": round-to-nearest-even biases
+ * gradient tensors; stochastic rounding picks one of the two nearest values
+ * with probability given by the distance to each; gradients only).  S_dec and
+ * the block scales as nvfp4_quantize_per_token() with NVFP4_SCOPE_TOKEN; each
+ * code is the E2M1 value below or above RN(x * r), chosen with 32 random
+ * bits b: above when (b >> 8) < p * 2^24, p the distance to the value below
+ * over the grid spacing; b = Philox4x64-10 (counter (e / 8, 0, 0, 0), key
+ * (seed, 0)), 32-bit word e % 8 of its four 64-bit outputs (low half first),
+ * e = row * cols + column.  Same layouts and requirements as the token scope
+ * of nvfp4_quantize_per_token() (plain scale layout, padding rows zero).
+ */
+mx8_status nvfp4_quantize_per_token_sr(const void *x, int64_t rows, int64_t cols, int64_t ld,
+                                       uint64_t seed, uint8_t *q, uint8_t *s_blk, float *s32,
+                                       mx8_stream_t stream);
 
 /*
  * nvfp4_quantize_per_token() for callers that cannot allocate device memory

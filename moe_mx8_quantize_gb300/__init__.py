@@ -32,6 +32,7 @@ S32_NONE, S32_ROW, S32_TENSOR, S32_GROUP = 0, 1, 2, 3
 EXPORTS = ("mx8_scale_bytes", "mx8_scale_bytes_grouped", "mx8_workspace_bytes",
            "mx8_device_sm_count", "mx8_quantize", "mxfp4_quantize", "nvfp4_quantize_per_token",
            "nvfp4_quantize_dispatch", "nvfp4_quantize_2d", "nvfp4_quantize_rht_colwise",
+           "nvfp4_quantize_per_token_sr",
            "nvfp4_quantize_per_token_noalloc", "dequantize",
            "bs_gemm", "bs_grouped_gemm", "bs_grouped_gemm_fused", "bf16_gemm", "mx8_swiglu", "mx8_check_device_error", "mx8_selftest_bounded_wait",
            "mx8_status_string")
@@ -88,7 +89,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.nvfp4_quantize_2d.restype = _i
     lib.nvfp4_quantize_2d.argtypes = [_p, _i64, _i64, _i64, _i, _p, _p, _p, _p, _p, _p, _sz, _p]
     lib.nvfp4_quantize_rht_colwise.restype = _i
-    lib.nvfp4_quantize_rht_colwise.argtypes = [_p, _i64, _i64, _i64, ctypes.c_uint32, _p, _p, _p, _p, _sz, _p]
+    lib.nvfp4_quantize_rht_colwise.argtypes = [_p, _i64, _i64, _i64, ctypes.c_uint32, _i, ctypes.c_uint64, _p, _p,
+                                               _p, _p, _sz, _p]
+    lib.nvfp4_quantize_per_token_sr.restype = _i
+    lib.nvfp4_quantize_per_token_sr.argtypes = [_p, _i64, _i64, _i64, ctypes.c_uint64, _p, _p, _p, _p]
     lib.bs_grouped_gemm_fused.restype = _i
     lib.bs_grouped_gemm_fused.argtypes = [_i, _i, _p, _i64, _i64, _i64, _p, _p, _p, _p, _i64, _p, _p, _p, _i,
                                           _i, _p, _i64, _p, _sz, _p]
@@ -306,24 +310,46 @@ def nvfp4_quantize_2d(x, flags=ROWWISE | COLWISE, ws=None, stream=None):
     return q_row, s_row, q_col, s_col, s32
 
 
-def nvfp4_quantize_rht_colwise_into(x, sign_mask, q_col, s_col, s32, ws=None, stream=None):
+def nvfp4_quantize_rht_colwise_into(x, sign_mask, q_col, s_col, s32, stochastic=False, seed=0, ws=None,
+                                    stream=None):
     assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
     R, C = x.shape
     ws = _ws(ws, 1, x.device)
-    _check(load().nvfp4_quantize_rht_colwise(_ptr(x), R, C, x.stride(0), int(sign_mask), _ptr(q_col), _ptr(s_col),
-                                             _ptr(s32), _ptr(ws), ws.numel(), _stream(stream)),
+    _check(load().nvfp4_quantize_rht_colwise(_ptr(x), R, C, x.stride(0), int(sign_mask), int(bool(stochastic)),
+                                             int(seed), _ptr(q_col), _ptr(s_col), _ptr(s32), _ptr(ws), ws.numel(),
+                                             _stream(stream)),
            "nvfp4_quantize_rht_colwise")
 
 
-def nvfp4_quantize_rht_colwise(x, sign_mask, ws=None, stream=None):
+def nvfp4_quantize_rht_colwise(x, sign_mask, stochastic=False, seed=0, ws=None, stream=None):
     """Transposed NVFP4 copy of a Wgrad input [R, C] with the 16x16 random
-    Hadamard transform along R: (q_col [C, R/2], s_col tiles, s32 [1])."""
+    Hadamard transform along R: (q_col [C, R/2], s_col tiles, s32 [1]);
+    stochastic rounding of the codes for gradient inputs."""
     R, C = x.shape
     q_col = torch.empty((C, R // 2), dtype=torch.uint8, device=x.device)
     s_col = _u8(scale_bytes(FMT_NVFP4, C, R), x.device)
     s32 = torch.empty(1, dtype=torch.float32, device=x.device)
-    nvfp4_quantize_rht_colwise_into(x, sign_mask, q_col, s_col, s32, ws, stream)
+    nvfp4_quantize_rht_colwise_into(x, sign_mask, q_col, s_col, s32, stochastic, seed, ws, stream)
     return q_col, s_col, s32
+
+
+def nvfp4_quantize_per_token_sr_into(x, seed, q, s_blk, s32, stream=None):
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    R, C = x.shape
+    _check(load().nvfp4_quantize_per_token_sr(_ptr(x), R, C, x.stride(0), int(seed), _ptr(q), _ptr(s_blk),
+                                              _ptr(s32), _stream(stream)),
+           "nvfp4_quantize_per_token_sr")
+
+
+def nvfp4_quantize_per_token_sr(x, seed, stream=None):
+    """Per-token NVFP4 of a gradient with stochastically rounded codes:
+    (q [R, C/2], s_blk tiles, s32 [R])."""
+    R, C = x.shape
+    q = torch.empty((R, C // 2), dtype=torch.uint8, device=x.device)
+    s_blk = _u8(scale_bytes(FMT_NVFP4, R, C), x.device)
+    s32 = torch.empty(max(R, 1), dtype=torch.float32, device=x.device)
+    nvfp4_quantize_per_token_sr_into(x, seed, q, s_blk, s32, stream)
+    return q, s_blk, s32[:R]
 
 
 # ---------------------------------------------------------------- dequantize

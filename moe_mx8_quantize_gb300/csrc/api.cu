@@ -225,8 +225,9 @@ extern "C" mx8_status nvfp4_quantize_2d(const void* x, int64_t rows, int64_t col
 }
 
 extern "C" mx8_status nvfp4_quantize_rht_colwise(const void* x, int64_t rows, int64_t cols, int64_t ld,
-                                                 uint32_t sign_mask, uint8_t* q_col, uint8_t* s_col, float* s32,
-                                                 void* workspace, size_t workspace_bytes, mx8_stream_t stream) {
+                                                 uint32_t sign_mask, int stochastic, uint64_t seed, uint8_t* q_col,
+                                                 uint8_t* s_col, float* s32, void* workspace,
+                                                 size_t workspace_bytes, mx8_stream_t stream) {
   if (rows < 0 || cols < 0 || ld < cols || rows % 32 != 0 || cols % 8 != 0 || sign_mask > 0xFFFFu)
     return MX8_ERR_INVALID_ARG;
   if (rows == 0 || cols == 0) return MX8_OK;
@@ -236,9 +237,20 @@ extern "C" mx8_status nvfp4_quantize_rht_colwise(const void* x, int64_t rows, in
   mx8_status st = check_ws(workspace, workspace_bytes, 1);
   if (st != MX8_OK) return st;
   uint32_t* amax_bits = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + kErrWordBytes);
-  return from_cuda(launch_nvfp4_rht_colwise(static_cast<const uint16_t*>(x), rows, cols, ld, sign_mask, q_col,
-                                            s_col, s32, amax_bits, sm_count_current(),
-                                            reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_nvfp4_rht_colwise(static_cast<const uint16_t*>(x), rows, cols, ld, sign_mask,
+                                            stochastic != 0, seed, q_col, s_col, s32, amax_bits,
+                                            sm_count_current(), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" mx8_status nvfp4_quantize_per_token_sr(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                                  uint64_t seed, uint8_t* q, uint8_t* s_blk, float* s32,
+                                                  mx8_stream_t stream) {
+  if (rows < 0 || cols < 0 || ld < cols || cols % 16 != 0) return MX8_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return MX8_OK;
+  if (x == nullptr || q == nullptr || s_blk == nullptr || s32 == nullptr) return MX8_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(s_blk) || ld % 8 != 0) return MX8_ERR_ALIGNMENT;
+  return from_cuda(launch_nvfp4_sr_token(static_cast<const uint16_t*>(x), rows, cols, ld, seed, q, s_blk, s32,
+                                         sm_count_current(), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 // ===================================================================== dequantize

@@ -47,9 +47,12 @@ cudaError_t launch_nvfp4_2d(const uint16_t* x, int64_t R, int64_t C, int64_t ld,
 
 // Transposed NVFP4 copy of a Wgrad input with the 16x16 random Hadamard
 // transform along its rows (tensor-scope scale from the transformed amax).
-cudaError_t launch_nvfp4_rht_colwise(const uint16_t* x, int64_t R, int64_t C, int64_t ld, uint32_t mask,
-                                     uint8_t* qT, uint8_t* sT, float* s32, uint32_t* amax_bits, int sm_count,
-                                     cudaStream_t stream);
+cudaError_t launch_nvfp4_rht_colwise(const uint16_t* x, int64_t R, int64_t C, int64_t ld, uint32_t mask, bool sr,
+                                     uint64_t seed, uint8_t* qT, uint8_t* sT, float* s32, uint32_t* amax_bits,
+                                     int sm_count, cudaStream_t stream);
+// Per-token NVFP4 of a gradient with stochastically rounded codes.
+cudaError_t launch_nvfp4_sr_token(const uint16_t* x, int64_t R, int64_t C, int64_t ld, uint64_t seed, uint8_t* q,
+                                  uint8_t* sblk, float* s32, int sm_count, cudaStream_t stream);
 
 cudaError_t launch_dequant(int fmt, const uint8_t* q, const uint8_t* s, const float* s32,
                            int s32_mode, const int64_t* offs, int G, int64_t R, int64_t C,

@@ -41,6 +41,32 @@ def test_rht_colwise_shapes(shape, mask):
     _check(xb, mask)
 
 
+@pytest.mark.parametrize("seed", [0, 0xFEEDFACE12345678])
+def test_rht_colwise_stochastic(seed):
+    """Gradient inputs: codes by stochastic rounding with the Philox bits of
+    each element's position, bit-exact against the oracle."""
+    xb = inputs.bits(inputs.normal_bf16((256, 200), 1e-3, torch.Generator().manual_seed(8), "cpu", 0.01, 20))
+    q, s, s32 = mx.nvfp4_quantize_rht_colwise(dev(xb), MASK, stochastic=True, seed=seed)
+    oq, os_, o32 = oracle.nvfp4_quantize_rht_colwise(xb, MASK, stochastic=True, seed=seed)
+    assert host(s32).view(np.uint32)[0] == o32.view(np.uint32)[0]
+    assert np.array_equal(host(q), oq)
+    sw = oracle.swizzle_scales(os_)
+    assert np.array_equal(host(s)[: sw.size], sw)
+
+
+@pytest.mark.parametrize("shape", [(5, 16), (130, 96), (2048, 8192), (33, 4096)])
+def test_per_token_stochastic(shape):
+    """Per-token NVFP4 of a gradient with stochastic codes, bit-exact against
+    the oracle (codes, scale tiles with padding, S_dec)."""
+    xb = inputs.bits(inputs.normal_bf16(shape, 1e-3, torch.Generator().manual_seed(shape[0]), "cpu", 0.01, 30))
+    q, s, s32 = mx.nvfp4_quantize_per_token_sr(dev(xb), 1234567 + shape[0])
+    oq, os_, o32 = oracle.nvfp4_quantize_sr(xb, 1234567 + shape[0])
+    assert np.array_equal(host(s32).view(np.uint32), o32.view(np.uint32))
+    assert np.array_equal(host(q), oq)
+    sw = oracle.swizzle_scales(os_)
+    assert np.array_equal(host(s)[: sw.size], sw)
+
+
 def test_rht_colwise_sweep_values():
     _check(inputs.bits(inputs.sweep(128, 256, seed=13).float().clamp(-3e4, 3e4).to(torch.bfloat16)))
 

@@ -110,9 +110,12 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert lib.nvfp4_quantize_2d(p, 64, 64, 64, 0, p, p, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
     assert lib.nvfp4_quantize_2d(p, 64, 64, 64, 3, p, p, p, p, None, p, 4096, None) == m.ERR_INVALID_ARG
     # RHT columnwise: rows % 32, cols % 8, a sign mask of 16 bits
-    assert lib.nvfp4_quantize_rht_colwise(p, 48, 64, 64, 0, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
-    assert lib.nvfp4_quantize_rht_colwise(p, 64, 12, 12, 0, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
-    assert lib.nvfp4_quantize_rht_colwise(p, 64, 64, 64, 0x10000, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
+    assert lib.nvfp4_quantize_rht_colwise(p, 48, 64, 64, 0, 0, 0, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
+    assert lib.nvfp4_quantize_rht_colwise(p, 64, 12, 12, 0, 0, 0, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
+    assert lib.nvfp4_quantize_rht_colwise(p, 64, 64, 64, 0x10000, 0, 0, p, p, p, p, 4096, None) == m.ERR_INVALID_ARG
+    # stochastic per-token: cols % 16, misaligned stride
+    assert lib.nvfp4_quantize_per_token_sr(p, 4, 24, 24, 1, p, p, p, None) == m.ERR_INVALID_ARG
+    assert lib.nvfp4_quantize_per_token_sr(p, 4, 32, 36, 1, p, p, p, None) == m.ERR_ALIGNMENT
     # fused MoE GEMM: bad epilogue, SwiGLU needs N % 256 and bf16, formats other than NVFP4
     assert lib.bs_grouped_gemm_fused(1, 2, p, 8, 256, 64, p, p, None, None, 0, p, p, None, 5, 1, p, 128, p, 4096,
                                      None) == m.ERR_INVALID_ARG
