@@ -18,9 +18,11 @@ One step = every operation of the hot path, on seeded synthetic inputs:
 value = block-scaled GEMM FLOPs of the step / step time (quantizers,
 dequantization and SwiGLU included in the time).  Per-kernel times come from
 CUDA events on the launching stream inside the timed region.  The same linear
-layer in MXFP4 (E2M1 x 32 blocks, E8M0 scales), and its dequantized-backward
-mode (dequantize + dense BF16 Dgrad / Wgrad), are timed beside the step, per
-kernel, under "extra".
+layer in MXFP4 (E2M1 x 32 blocks, E8M0 scales), its dequantized-backward mode
+(dequantize + dense BF16 Dgrad / Wgrad) and its NVFP4 pretraining-recipe
+variant (2-D weight blocks, random Hadamard transform on the Wgrad inputs,
+stochastic rounding of gradients) are timed beside the step, per kernel,
+under "extra".
 
 `--impl reference` times the CPU oracle (test infrastructure, single thread)
 on a bounded sample of the same step and extrapolates to the full step.
@@ -404,6 +406,71 @@ class DequantBackward:
         ]
 
 
+class Nvfp4RecipeLinear:
+    """The step's linear layer under the NVFP4 pretraining recipe's variants:
+    W with 2-D 16x16 block scales (one copy for the forward and its transpose
+    for Dgrad), X per token, the gradient dY per token with stochastically
+    rounded codes, and the Wgrad inputs dY and X quantized columnwise after
+    the 16x16 random Hadamard transform (stochastic codes for dY); then
+    Fprop, Dgrad and Wgrad.  Measured beside the step, not part of `value`."""
+
+    SIGNS = 0xB2D5          # the shared random sign vector of the transform
+    KERNELS = {"nvfp4_2d W": 2, "nvfp4_rht_colwise_sr dY": 2, "nvfp4_rht_colwise X": 2}
+
+    def __init__(self, step):
+        torch, mx = step.torch, step.mx
+        self.step, self.mx = step, mx
+        T, H, O = step.T, step.H_, step.O
+        dev = step.dev
+        u8 = lambda r, c: torch.empty((r, c), dtype=torch.uint8, device=dev)
+        sb = lambda r, c: torch.empty(max(mx.scale_bytes(mx.FMT_NVFP4, r, c), 16), dtype=torch.uint8, device=dev)
+        f32 = lambda n: torch.empty(n, dtype=torch.float32, device=dev)
+        self.Wr, self.SWr, self.Wc, self.SWc, self.W32 = u8(O, H // 2), sb(O, H), u8(H, O // 2), sb(H, O), f32(1)
+        self.Xr, self.SXr, self.X32 = u8(T, H // 2), sb(T, H), f32(T)
+        self.dYr, self.SdYr, self.dY32 = u8(T, O // 2), sb(T, O), f32(T)
+        self.dYc, self.SdYc, self.dYc32 = u8(O, T // 2), sb(O, T), f32(1)
+        self.Xc, self.SXc, self.Xc32 = u8(H, T // 2), sb(H, T), f32(1)
+        self.Y = torch.empty((T, O), dtype=torch.bfloat16, device=dev)
+        self.dX = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        self.dW = torch.empty((O, H), dtype=torch.float32, device=dev)
+
+    def plan(self):
+        st = self.step
+        T, H, O = st.T, st.H_, st.O
+        nvq = lambda r, c: 2.5625 * r * c + 4 * r
+        return [
+            ("nvfp4_2d W", "hbm", (2 + 2 * 0.5625) * O * H),
+            ("nvfp4_quant_token X", "hbm", nvq(T, H)),
+            ("nvfp4_quant_token_sr dY", "hbm", nvq(T, O)),
+            ("nvfp4_rht_colwise_sr dY", "hbm", 2.5625 * T * O),
+            ("nvfp4_rht_colwise X", "hbm", 2.5625 * T * H),
+            ("nvfp4_gemm Fprop", "fp4", 2.0 * T * O * H),
+            ("nvfp4_gemm Dgrad", "fp4", 2.0 * T * H * O),
+            ("nvfp4_gemm Wgrad", "fp4", 2.0 * O * H * T),
+        ]
+
+    def launches(self):
+        mx, st = self.mx, self.step
+        ws = st.ws_b
+        RC = mx.ROWWISE | mx.COLWISE
+        return [
+            ("nvfp4_2d W", lambda: mx.nvfp4_quantize_2d_into(st.W, self.Wr, self.SWr, self.Wc, self.SWc, self.W32, RC, ws)),
+            ("nvfp4_quant_token X", lambda: mx.nvfp4_quantize_into(st.X, self.Xr, self.SXr, self.X32, mx.SCOPE_TOKEN, None, ws)),
+            ("nvfp4_quant_token_sr dY", lambda: mx.nvfp4_quantize_per_token_sr_into(st.dY, 77, self.dYr, self.SdYr, self.dY32)),
+            ("nvfp4_rht_colwise_sr dY", lambda: mx.nvfp4_quantize_rht_colwise_into(st.dY, self.SIGNS, self.dYc, self.SdYc,
+                                                                                    self.dYc32, True, 78, ws)),
+            ("nvfp4_rht_colwise X", lambda: mx.nvfp4_quantize_rht_colwise_into(st.X, self.SIGNS, self.Xc, self.SXc,
+                                                                                self.Xc32, False, 0, ws)),
+            ("nvfp4_gemm Fprop", lambda: mx.bs_gemm_into(mx.FMT_NVFP4, self.Xr, self.SXr, self.Wr, self.SWr, st.H_, self.Y,
+                                                         self.X32, self.W32, ws=ws, a32_mode=mx.S32_ROW, b32_mode=mx.S32_TENSOR)),
+            ("nvfp4_gemm Dgrad", lambda: mx.bs_gemm_into(mx.FMT_NVFP4, self.dYr, self.SdYr, self.Wc, self.SWc, st.O, self.dX,
+                                                         self.dY32, self.W32, ws=ws, a32_mode=mx.S32_ROW, b32_mode=mx.S32_TENSOR)),
+            ("nvfp4_gemm Wgrad", lambda: mx.bs_gemm_into(mx.FMT_NVFP4, self.dYc, self.SdYc, self.Xc, self.SXc, st.T, self.dW,
+                                                         self.dYc32, self.Xc32, ws=ws, a32_mode=mx.S32_TENSOR,
+                                                         b32_mode=mx.S32_TENSOR)),
+        ]
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "moe_mx8_quantize_gb300", "csrc")
@@ -595,7 +662,8 @@ def run_gpu(args):
     extra = None
     if not args.no_extra:
         extra = {}
-        for key, part in (("mxfp4_linear", Mxfp4Linear(step)), ("dequantized_backward", DequantBackward(step))):
+        for key, part in (("mxfp4_linear", Mxfp4Linear(step)), ("dequantized_backward", DequantBackward(step)),
+                          ("nvfp4_recipe_linear", Nvfp4RecipeLinear(step))):
             fl = part.launches()
             for _ in range(3):
                 for _, fn in fl:
@@ -607,7 +675,7 @@ def run_gpu(args):
             fplan = {lab: (kind, w) for lab, kind, w in part.plan()}
             extra[key] = [rate_row(lab, *fplan[lab], ms, peaks) for lab, ms in fper.items()]
             extra["from"] = ffrom
-            gpu_launches += len(fl) * K2
+            gpu_launches += sum(getattr(part, "KERNELS", {}).get(lab, 1) for lab, _ in fl) * K2
 
     e2e = None
     if not args.no_e2e:
