@@ -162,6 +162,24 @@ def test_nvfp4_group_scope_interleaved_work_order():
     _nv_check(inputs.bits(W), mx.SCOPE_GROUP, list(range(0, 24 * 1536 + 1, 1536)))
 
 
+def test_nvfp4_group_scope_one_group_too_large_to_stay_resident():
+    """One group of 8192 x 2048 bf16 (32 MB) needs more row chunks than the
+    GPU has CTAs, so the one-read resident kernel declines the whole tensor
+    and the ticket kernel quantizes every group (both small and large)."""
+    g = torch.Generator(device="cuda").manual_seed(19)
+    W = inputs.normal_bf16((8192 + 300, 2048), 0.02, g, "cuda", 0.001, 30.0)
+    _nv_check(inputs.bits(W), mx.SCOPE_GROUP, [0, 100, 100, 8292, 8492])
+
+
+def test_nvfp4_group_scope_ragged_groups_resident():
+    """Ragged groups (empty, one row, 129 rows, several chunks) with columns
+    that are not a multiple of 512: the resident kernel's chunking, its
+    padding scale rows and the empty groups' zero decode scales."""
+    xb = inputs.bits(inputs.sweep(1200, 800, seed=23))
+    _nv_check(xb, mx.SCOPE_GROUP, [0, 0, 1, 130, 130, 700, 1200])
+    _nv_check(xb[:300], mx.SCOPE_TENSOR)
+
+
 def test_nvfp4_tensor_scope_large():
     g = torch.Generator(device="cuda").manual_seed(18)
     W = inputs.normal_bf16((8192, 2048), 0.02, g, "cuda")
