@@ -247,6 +247,92 @@ __device__ __forceinline__ void process_row(const uint16_t* __restrict__ x, int6
   encode_row<kCh, kHint>(x, row, C, ld, scope_token, senc_given, tab, out, kt, lane, pol);
 }
 
+// ------------------------------------------------------------------ paired rows
+// Rows of C = 256 or 768 elements fill 512-element chunks only partly (for
+// 768, half the lanes of the second chunk would idle), so a warp takes two
+// rows ra, rb as one virtual row of 2C = 512 kP elements: virtual block v is
+// block v of ra for v < C/16, else block v - C/16 of rb.  A 4-block scale
+// group never straddles the two rows (C/16 is a multiple of 4).  rb = -1 (or
+// ra = -1) is a missing row: zeros in, codes not written, scale words zero.
+struct PairOut {
+  uint8_t* qa;        // codes of ra (nullptr: none)
+  uint8_t* qb;
+  uint8_t* swa;       // first scale word of ra's / rb's scale row
+  uint8_t* swb;
+  int half;           // code bytes per row, C / 2
+  int g4;             // 4-block groups per row, C / 64
+  __device__ __forceinline__ void codes(int off, uint2 v) const {
+    if (off < half) {
+      if (qa) *reinterpret_cast<uint2*>(qa + off) = v;
+    } else if (qb) {
+      *reinterpret_cast<uint2*>(qb + off - half) = v;
+    }
+  }
+  __device__ __forceinline__ void scale(int k4, uint32_t w) const {
+    if (k4 < g4) *reinterpret_cast<uint32_t*>(swa + k4 * 512) = w;
+    else *reinterpret_cast<uint32_t*>(swb + (k4 - g4) * 512) = w;
+  }
+};
+
+template <int kP, bool kHint>
+__device__ __forceinline__ void load_pair(const uint16_t* __restrict__ x, int64_t ra, int64_t rb, int C, int64_t ld,
+                                          int lane, uint64_t pol, uint4 (&w)[2 * kP]) {
+#pragma unroll
+  for (int i = 0; i < kP; ++i) {
+    const int cv = i * 512 + lane * 16;
+    const int64_t row = cv < C ? ra : rb;
+    const int c = cv < C ? cv : cv - C;
+    const uint16_t* p = x + row * ld + c;
+    w[2 * i] = row >= 0 ? ld_row16<kHint>(p, pol) : make_uint4(0, 0, 0, 0);
+    w[2 * i + 1] = row >= 0 ? ld_row16<kHint>(p + 8, pol) : make_uint4(0, 0, 0, 0);
+  }
+}
+
+// This lane's packed |x| maximum over its blocks of the two rows together.
+template <int kP, bool kHint>
+__device__ __forceinline__ uint32_t pair_absmax_lane(const uint16_t* __restrict__ x, int64_t ra, int64_t rb, int C,
+                                                     int64_t ld, int lane, uint64_t pol) {
+  uint4 w[2 * kP];
+  load_pair<kP, kHint>(x, ra, rb, C, ld, lane, pol, w);
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < kP; ++i) m = amax2(m, absmax16(w[2 * i], w[2 * i + 1]));
+  return m;
+}
+
+// Encodes rows ra, rb (scale rows sra, srb); scope_token: each row's own amax
+// gives its S_enc and S_dec, else both use senc_given.
+template <int kP, bool kHint>
+__device__ __forceinline__ void encode_pair(const uint16_t* __restrict__ x, int64_t ra, int64_t rb, int C, int64_t ld,
+                                            bool scope_token, float senc_given, const float2* __restrict__ tab,
+                                            uint8_t* __restrict__ q, uint8_t* __restrict__ sblk,
+                                            float* __restrict__ s32, int64_t sra, int64_t srb, int kt, int lane,
+                                            uint64_t pol) {
+  uint4 w[2 * kP];
+  load_pair<kP, kHint>(x, ra, rb, C, ld, lane, pol, w);
+  float senc_a = senc_given, senc_b = senc_given;
+  if (scope_token) {
+    uint32_t ma = 0, mb = 0;
+#pragma unroll
+    for (int i = 0; i < kP; ++i) {
+      const uint32_t m = absmax16(w[2 * i], w[2 * i + 1]);
+      if (i * 512 + lane * 16 < C) ma = amax2(ma, m); else mb = amax2(mb, m);
+    }
+    float sdec_a, sdec_b;
+    nvfp4_scales(warp_max(abs_halves_max(ma)), senc_a, sdec_a);
+    nvfp4_scales(warp_max(abs_halves_max(mb)), senc_b, sdec_b);
+    if (lane == 0) {
+      if (ra >= 0) s32[ra] = sdec_a;
+      if (rb >= 0) s32[rb] = sdec_b;
+    }
+  }
+  const PairOut out{ra >= 0 ? q + ra * (C / 2) : nullptr, rb >= 0 ? q + rb * (C / 2) : nullptr,
+                    sblk + sf_row_base(sra, kt), sblk + sf_row_base(srb, kt), C / 2, C / 64};
+#pragma unroll
+  for (int i = 0; i < kP; ++i)
+    encode_chunk(w[2 * i], w[2 * i + 1], i, 2 * C, lane, i * 512 + lane * 16 < C ? senc_a : senc_b, tab, out, C / 32);
+}
+
 // Data row behind scale row sr (-1 for padding).
 __device__ __forceinline__ int64_t data_row(const GroupSmem& gs, bool grouped, int G, int64_t R, int64_t sr) {
   if (!grouped) return sr < R ? sr : -1;
@@ -277,8 +363,14 @@ __global__ void __launch_bounds__(kThreads, kCh >= 8 || kCh == 0 ? 1 : 4) nvfp4_
   const int C32 = static_cast<int>(C);
   const int kt = (C32 / 16 + 3) / 4;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
-  for (int64_t sr = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); sr < TP; sr += nwarps)
-    process_row<kCh>(x, data_row(gs, grouped, G, R, sr), C32, ld, true, 0.f, tab, q, sblk, s32, sr, kt, lane);
+  if constexpr (kCh < 0) {           // pairs of scale rows (TP is a multiple of 128)
+    for (int64_t sp = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); 2 * sp < TP; sp += nwarps)
+      encode_pair<-kCh, false>(x, data_row(gs, grouped, G, R, 2 * sp), data_row(gs, grouped, G, R, 2 * sp + 1), C32,
+                               ld, true, 0.f, tab, q, sblk, s32, 2 * sp, 2 * sp + 1, kt, lane, 0);
+  } else {
+    for (int64_t sr = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); sr < TP; sr += nwarps)
+      process_row<kCh>(x, data_row(gs, grouped, G, R, sr), C32, ld, true, 0.f, tab, q, sblk, s32, sr, kt, lane);
+  }
 }
 
 // ------------------------------------------------------------------ token scope, before dispatch
@@ -593,8 +685,13 @@ __global__ void __launch_bounds__(kScopedThreads, kCh >= 8 || kCh == 0 ? 1 : 4) 
         const int64_t r0 = aoffs[g] + item * kItemRows;
         const int64_t r1 = r0 + kItemRows < aoffs[g + 1] ? r0 + kItemRows : aoffs[g + 1];
         uint32_t m = 0;
-        for (int64_t row = r0 + dw; row < r1; row += kDataWarps)
-          m = amax2(m, row_absmax_lane<kCh, true>(x + row * ld, C32, lane, keep));
+        if constexpr (kCh < 0) {
+          for (int64_t row = r0 + 2 * dw; row < r1; row += 2 * kDataWarps)
+            m = amax2(m, pair_absmax_lane<-kCh, true>(x, row, row + 1 < r1 ? row + 1 : -1, C32, ld, lane, keep));
+        } else {
+          for (int64_t row = r0 + dw; row < r1; row += kDataWarps)
+            m = amax2(m, row_absmax_lane<kCh, true>(x + row * ld, C32, lane, keep));
+        }
         const float wm = warp_max(abs_halves_max(m));
         if (lane == 0) sm.red[slot][dw] = wm;
       } else {
@@ -602,11 +699,18 @@ __global__ void __launch_bounds__(kScopedThreads, kCh >= 8 || kCh == 0 ? 1 : 4) 
         const float senc = sm.tsenc[slot];
         const int64_t s0 = apref[g] + item * kItemRows;
         const int64_t grows = aoffs[g + 1] - aoffs[g];
-        for (int64_t sr = s0 + dw; sr < s0 + kItemRows; sr += kDataWarps) {
-          // scope groups are the layout groups: the data row follows directly
+        // scope groups are the layout groups: the data row follows directly
+        auto row_of = [&](int64_t sr) -> int64_t {
           const int64_t local = sr - apref[g];
-          const int64_t row = scope == 1 ? (local < grows ? aoffs[g] + local : -1) : data_row(sm.gs, grouped, G, R, sr);
-          process_row<kCh, true>(x, row, C32, ld, false, senc, sm.tab, q, sblk, s32, sr, kt, lane, drop);
+          return scope == 1 ? (local < grows ? aoffs[g] + local : -1) : data_row(sm.gs, grouped, G, R, sr);
+        };
+        if constexpr (kCh < 0) {
+          for (int64_t sr = s0 + 2 * dw; sr < s0 + kItemRows; sr += 2 * kDataWarps)
+            encode_pair<-kCh, true>(x, row_of(sr), row_of(sr + 1), C32, ld, false, senc, sm.tab, q, sblk, s32, sr,
+                                    sr + 1, kt, lane, drop);
+        } else {
+          for (int64_t sr = s0 + dw; sr < s0 + kItemRows; sr += kDataWarps)
+            process_row<kCh, true>(x, row_of(sr), C32, ld, false, senc, sm.tab, q, sblk, s32, sr, kt, lane, drop);
         }
       }
       __syncwarp();
@@ -672,6 +776,8 @@ cudaError_t launch_nvfp4_quant(const uint16_t* x, int64_t R, int64_t C, int64_t 
     cudaError_t e = cudaMemsetAsync(scratch, 0, nvfp4_scratch_bytes(Gs), stream);
     if (e != cudaSuccess) return e;
     uint32_t* sc = static_cast<uint32_t*>(scratch);
+    if (C == 256) return launch_scoped<-1>(sm_count, stream, x, R, C, ld, scope, offs, G, q, sblk, s32, sc, err);
+    if (C == 768) return launch_scoped<-3>(sm_count, stream, x, R, C, ld, scope, offs, G, q, sblk, s32, sc, err);
     if (C <= 1024) return launch_scoped<2>(sm_count, stream, x, R, C, ld, scope, offs, G, q, sblk, s32, sc, err);
     if (C <= 2048) return launch_scoped<4>(sm_count, stream, x, R, C, ld, scope, offs, G, q, sblk, s32, sc, err);
     if (C <= 4096) return launch_scoped<8>(sm_count, stream, x, R, C, ld, scope, offs, G, q, sblk, s32, sc, err);
@@ -685,6 +791,8 @@ cudaError_t launch_nvfp4_quant(const uint16_t* x, int64_t R, int64_t C, int64_t 
   unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
   if (grid == 0) grid = 1;
   const size_t smem = grouped ? sizeof(GroupSmem) : 0;
+  if (C == 256) return launch_token<-1>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32);
+  if (C == 768) return launch_token<-3>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32);
   if (C <= 1024) return launch_token<2>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32);
   if (C <= 2048) return launch_token<4>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32);
   if (C <= 4096) return launch_token<8>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32);

@@ -111,7 +111,8 @@ def test_nvfp4_pr1():
     _nv_check(inputs.bits(d["W"]), mx.SCOPE_TENSOR)
 
 
-@pytest.mark.parametrize("shape", [(5, 16), (7, 48), (130, 80), (64, 208), (300, 768), (9, 4096), (33, 7168), (5, 8448)])
+@pytest.mark.parametrize("shape", [(5, 16), (7, 48), (130, 80), (64, 208), (300, 768), (9, 4096), (33, 7168), (5, 8448),
+                                   (7, 256), (131, 768), (1, 768)])
 def test_nvfp4_ragged(shape):
     rows, cols = shape
     wide = inputs.sweep(rows, (cols + 31) // 32 * 32, seed=rows)
@@ -162,10 +163,23 @@ def test_nvfp4_group_scope_interleaved_work_order():
     _nv_check(inputs.bits(W), mx.SCOPE_GROUP, list(range(0, 24 * 1536 + 1, 1536)))
 
 
-def test_nvfp4_group_scope_one_group_too_large_to_stay_resident():
-    """One group of 8192 x 2048 bf16 (32 MB) needs more row chunks than the
-    GPU has CTAs, so the one-read resident kernel declines the whole tensor
-    and the ticket kernel quantizes every group (both small and large)."""
+@pytest.mark.parametrize("cols", [256, 768])
+def test_nvfp4_paired_rows_group_and_token_scopes(cols):
+    """Rows of 256 or 768 columns are encoded two per warp: group scope over
+    ragged groups (odd sizes, empty groups, groups ending inside a row pair)
+    and token scope with the grouped layout, bit-exact."""
+    xb = inputs.bits(inputs.sweep(517, cols, seed=cols))
+    offs = [0, 3, 3, 130, 257, 258, 517]
+    _nv_check(xb, mx.SCOPE_GROUP, offs)
+    _nv_check(xb, mx.SCOPE_TOKEN, offs)
+    _nv_check(xb, mx.SCOPE_TENSOR)
+    W = inputs.bits(inputs.normal_bf16((8 * 256, cols), 0.02, torch.Generator().manual_seed(cols), "cpu"))
+    _nv_check(W, mx.SCOPE_GROUP, list(range(0, 8 * 256 + 1, 256)))
+
+
+def test_nvfp4_group_scope_one_large_group():
+    """One group of 8192 x 2048 bf16 (32 MB) among small ones: its amax items
+    span many blocks before any of its encode items can run."""
     g = torch.Generator(device="cuda").manual_seed(19)
     W = inputs.normal_bf16((8192 + 300, 2048), 0.02, g, "cuda", 0.001, 30.0)
     _nv_check(inputs.bits(W), mx.SCOPE_GROUP, [0, 100, 100, 8292, 8492])
