@@ -39,6 +39,11 @@ cudaError_t launch_nvfp4_dispatch(const uint16_t* x, int64_t T, int64_t C, int64
                                   int topk, const int64_t* offs, int G, int disp_codes, uint8_t* q, uint8_t* sblk,
                                   float* s32, int sm_count, cudaStream_t stream);
 
+// Tensor abs-max of a bf16 matrix (C % 8 == 0) as f32 bits in *amax_bits
+// (zeroed here on the stream).
+cudaError_t launch_absmax(const uint16_t* x, int64_t R, int64_t C, int64_t ld, uint32_t* amax_bits, int sm_count,
+                          cudaStream_t stream);
+
 // NVFP4 with 16x16 block scales and one FP32 tensor scale (rowwise and/or
 // the transposed copy); amax_bits: 4 bytes of device scratch.
 cudaError_t launch_nvfp4_2d(const uint16_t* x, int64_t R, int64_t C, int64_t ld, bool row, bool col,

@@ -345,7 +345,8 @@ __device__ __forceinline__ int64_t data_row(const GroupSmem& gs, bool grouped, i
 template <int kCh>
 __global__ void __launch_bounds__(kThreads, kCh >= 8 || kCh == 0 ? 1 : 4) nvfp4_token_kernel(
     const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ld, const int64_t* __restrict__ offs, int G,
-    uint8_t* __restrict__ q, uint8_t* __restrict__ sblk, float* __restrict__ s32) {
+    uint8_t* __restrict__ q, uint8_t* __restrict__ sblk, float* __restrict__ s32,
+    const uint32_t* __restrict__ tensor_amax) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   GroupSmem& gs = *reinterpret_cast<GroupSmem*>(smem_raw);
   __shared__ float2 tab[128];
@@ -363,13 +364,22 @@ __global__ void __launch_bounds__(kThreads, kCh >= 8 || kCh == 0 ? 1 : 4) nvfp4_
   const int C32 = static_cast<int>(C);
   const int kt = (C32 / 16 + 3) / 4;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
+  // tensor scope: the amax of the whole tensor comes from the amax launch
+  const bool per_token = tensor_amax == nullptr;
+  float senc = 0.f;
+  if (!per_token) {
+    float sdec;
+    nvfp4_scales(__uint_as_float(*tensor_amax), senc, sdec);
+    if (blockIdx.x == 0 && threadIdx.x == 0) s32[0] = sdec;
+  }
   if constexpr (kCh < 0) {           // pairs of scale rows (TP is a multiple of 128)
     for (int64_t sp = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); 2 * sp < TP; sp += nwarps)
       encode_pair<-kCh, false>(x, data_row(gs, grouped, G, R, 2 * sp), data_row(gs, grouped, G, R, 2 * sp + 1), C32,
-                               ld, true, 0.f, tab, q, sblk, s32, 2 * sp, 2 * sp + 1, kt, lane, 0);
+                               ld, per_token, senc, tab, q, sblk, s32, 2 * sp, 2 * sp + 1, kt, lane, 0);
   } else {
     for (int64_t sr = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); sr < TP; sr += nwarps)
-      process_row<kCh>(x, data_row(gs, grouped, G, R, sr), C32, ld, true, 0.f, tab, q, sblk, s32, sr, kt, lane);
+      process_row<kCh>(x, data_row(gs, grouped, G, R, sr), C32, ld, per_token, senc, tab, q, sblk, s32, sr, kt,
+                       lane);
   }
 }
 
@@ -734,13 +744,13 @@ cudaError_t launch_dispatch(unsigned grid, cudaStream_t stream, const uint16_t* 
 template <int kCh>
 cudaError_t launch_token(unsigned grid, size_t smem, cudaStream_t stream, const uint16_t* x, int64_t R,
                          int64_t C, int64_t ld, const int64_t* offs, int G, uint8_t* q, uint8_t* sblk,
-                         float* s32) {
+                         float* s32, const uint32_t* tensor_amax) {
   auto k = nvfp4_token_kernel<kCh>;
   if (smem > 0) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  k<<<grid, kThreads, smem, stream>>>(x, R, C, ld, offs, G, q, sblk, s32);
+  k<<<grid, kThreads, smem, stream>>>(x, R, C, ld, offs, G, q, sblk, s32, tensor_amax);
   return cudaGetLastError();
 }
 
@@ -771,6 +781,17 @@ cudaError_t launch_nvfp4_quant(const uint16_t* x, int64_t R, int64_t C, int64_t 
                                const int64_t* offs, int G, uint8_t* q, uint8_t* sblk, float* s32,
                                void* scratch, int* err, int sm_count, cudaStream_t stream) {
   const bool grouped = offs != nullptr;
+  // tensor scope on a tensor that fits in L2: one abs-max launch, then the
+  // token kernel encodes with the tensor's S_enc (its read of x hits L2);
+  // larger tensors and group scope take the ticket kernel
+  const uint32_t* tensor_amax = nullptr;
+  if (scope == 2 && R * C * 2 <= (int64_t{64} << 20) && C % 8 == 0) {
+    uint32_t* amax_word = static_cast<uint32_t*>(scratch);
+    cudaError_t e = launch_absmax(x, R, C, ld, amax_word, sm_count, stream);
+    if (e != cudaSuccess) return e;
+    tensor_amax = amax_word;
+    scope = 0;
+  }
   if (scope != 0) {
     const int Gs = scope == 1 ? G : 1;
     cudaError_t e = cudaMemsetAsync(scratch, 0, nvfp4_scratch_bytes(Gs), stream);
@@ -791,13 +812,13 @@ cudaError_t launch_nvfp4_quant(const uint16_t* x, int64_t R, int64_t C, int64_t 
   unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
   if (grid == 0) grid = 1;
   const size_t smem = grouped ? sizeof(GroupSmem) : 0;
-  if (C == 256) return launch_token<-1>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32);
-  if (C == 768) return launch_token<-3>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32);
-  if (C <= 1024) return launch_token<2>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32);
-  if (C <= 2048) return launch_token<4>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32);
-  if (C <= 4096) return launch_token<8>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32);
-  if (C <= 8192) return launch_token<16>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32);
-  return launch_token<0>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32);
+  if (C == 256) return launch_token<-1>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32, tensor_amax);
+  if (C == 768) return launch_token<-3>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32, tensor_amax);
+  if (C <= 1024) return launch_token<2>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32, tensor_amax);
+  if (C <= 2048) return launch_token<4>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32, tensor_amax);
+  if (C <= 4096) return launch_token<8>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32, tensor_amax);
+  if (C <= 8192) return launch_token<16>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32, tensor_amax);
+  return launch_token<0>(grid, smem, stream, x, R, C, ld, offs, G, q, sblk, s32, tensor_amax);
 }
 
 cudaError_t launch_nvfp4_dispatch(const uint16_t* x, int64_t T, int64_t C, int64_t ld, const int64_t* dest,

@@ -164,6 +164,17 @@ __global__ void __launch_bounds__(k2dThreads) nvfp4_2d_kernel(
 
 }  // namespace
 
+cudaError_t launch_absmax(const uint16_t* x, int64_t R, int64_t C, int64_t ld, uint32_t* amax_bits, int sm_count,
+                          cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(amax_bits, 0, sizeof(uint32_t), stream);
+  if (e != cudaSuccess) return e;
+  const int64_t work = R * (C / 8);
+  const int64_t ga = (work + k2dThreads - 1) / k2dThreads;
+  const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+  absmax_kernel<<<static_cast<unsigned>(ga < cap ? ga : cap), k2dThreads, 0, stream>>>(x, R, C, ld, amax_bits);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_nvfp4_2d(const uint16_t* x, int64_t R, int64_t C, int64_t ld, bool row, bool col,
                             uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col, float* s32,
                             uint32_t* amax_bits, int sm_count, cudaStream_t stream) {
