@@ -87,6 +87,7 @@ class Dispatch:
     token_of_row: torch.Tensor   # int64 [T*k]
     expert_of_row: torch.Tensor  # int64 [T*k]
     offsets: torch.Tensor        # int64 [E+1]
+    row_of_slot: torch.Tensor    # int64 [T, k]: the row holding token t's j-th expert choice
 
 
 def dispatch(topk_ids: torch.Tensor, experts: int) -> Dispatch:
@@ -98,7 +99,18 @@ def dispatch(topk_ids: torch.Tensor, experts: int) -> Dispatch:
     counts = torch.bincount(flat, minlength=experts)
     offsets = torch.zeros(experts + 1, dtype=torch.int64, device=topk_ids.device)
     offsets[1:] = torch.cumsum(counts, 0)
-    return Dispatch(token, expert, offsets)
+    row_of_slot = torch.empty_like(order)
+    row_of_slot[order] = torch.arange(order.numel(), device=order.device, dtype=torch.int64)
+    return Dispatch(token, expert, offsets, row_of_slot.reshape(T, k))
+
+
+def route_weights(tokens: int, topk: int, seed: int, device) -> torch.Tensor:
+    """Router weights of the top-k choices: a softmax over k N(0,1) logits per
+    token, float32 [tokens, topk] (own generator, so other inputs keep their
+    streams)."""
+    g = _gen(seed + 1000, device)
+    logits = torch.randn((tokens, topk), generator=g, device=device, dtype=torch.float32)
+    return torch.softmax(logits, dim=1).contiguous()
 
 
 # ------------------------------------------------------------------ MoE

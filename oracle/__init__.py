@@ -98,6 +98,7 @@ def _L():
         lib.or_e2m1_sr.argtypes = [ctypes.c_float, ctypes.c_uint32]
         lib.or_e2m1_sr.restype = ctypes.c_uint8
         lib.or_nvfp4_quantize_sr.argtypes = [_p, _i64, _i64, _i64, ctypes.c_uint64, _p, _p, _p]
+        lib.or_moe_combine.argtypes = [_p, _i64, _i64, _p, _p, _i64, ctypes.c_int, _p]
         lib.or_bf16_gemm_ref.argtypes = [_i64, _i64, _i64, _p, _i64, _p, _i64, _p, _i64, _p, _p]
         _lib = lib
     return _lib
@@ -426,6 +427,17 @@ def bf16_gemm_ref(A_bits, B_bits, pairs=None):
     if pr is None:
         return ref.reshape(M, N), absref.reshape(M, N)
     return ref, absref
+
+
+def moe_combine(y_bits, rows, w):
+    """out [T, H] f32 = sum_j w[t, j] * y[rows[t, j]] in binary32, j in order."""
+    y = _c(y_bits, np.uint16)
+    r = _c(rows, np.int64)
+    ww = _c(w, np.float32)
+    T, k = r.shape
+    out = np.empty((T, y.shape[1]), np.float32)
+    _L().or_moe_combine(_ptr(y), y.shape[0], y.shape[1], _ptr(r), _ptr(ww), T, k, _ptr(out))
+    return out
 
 
 # ----------------------------------------------------------------- SwiGLU

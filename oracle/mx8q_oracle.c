@@ -859,6 +859,30 @@ void or_bf16_gemm_ref(i64 M, i64 N, i64 K, const uint16_t *A, i64 lda,
     }
 }
 
+/* MoE combine: each token's expert outputs, weighted by its router weights,
+ * summed back in token order (the step that closes the routed-expert layer
+ * around the grouped GEMMs of [MRL] "Un Cuantizador Compartido..." and
+ * [REC]'s NVFP4 MoE experts):
+ *   out[t][h] = sum_{j<k} w[t][j] * y[rows[t][j]][h]
+ * accumulated in binary32 in the order j = 0, 1, ..., each product and each
+ * sum one round-to-nearest operation (acc = RN(acc + RN(w * y))).  y is bf16
+ * [R, H]; out is f32 [T, H] (a bf16 output is RNE of it).  Rows outside
+ * [0, R) contribute nothing. */
+void or_moe_combine(const uint16_t *y, i64 R, i64 H, const i64 *rows, const float *w, i64 T, int k, float *out)
+{
+    for (i64 t = 0; t < T; t++)
+        for (i64 h = 0; h < H; h++) {
+            float acc = 0.0f;
+            for (int j = 0; j < k; j++) {
+                i64 r = rows[t * k + j];
+                if (r < 0 || r >= R) continue;
+                float prod = w[t * k + j] * or_bf16_to_f32(y[r * H + h]);
+                acc = acc + prod;
+            }
+            out[t * H + h] = acc;
+        }
+}
+
 /* ------------------------------------------------------------------ */
 /* SwiGLU between the MoE gate|up and down GEMMs                        */
 /* ------------------------------------------------------------------ */

@@ -201,3 +201,34 @@ def test_bf16_gemm_sampled_pairs_match_full():
     ref, absref = oracle.bf16_gemm_ref(a, b, pairs)
     assert np.array_equal(ref, full[pairs[:, 0], pairs[:, 1]])
     assert np.array_equal(absref, afull[pairs[:, 0], pairs[:, 1]])
+
+
+# ------------------------------------------------------------------ MoE combine
+def test_moe_combine_one_hot_is_a_gather():
+    rng = np.random.default_rng(31)
+    y = rng.integers(0, 2 ** 16, size=(40, 24), dtype=np.uint16)
+    y[(y & 0x7F80) == 0x7F80] = 0x3F80            # no inf / nan patterns
+    rows = rng.integers(0, 40, size=(10, 3))
+    w = np.zeros((10, 3), np.float32)
+    pick = rng.integers(0, 3, 10)
+    w[np.arange(10), pick] = 1.0
+    out = oracle.moe_combine(y, rows, w)
+    assert np.array_equal(out, oracle.bf16_to_f32(y[rows[np.arange(10), pick]]))
+
+
+def test_moe_combine_exact_on_small_integers_and_skips_bad_rows():
+    """Small integers and weights that are multiples of 1/8: every binary32
+    step is exact, so the result is the exact weighted sum; rows outside the
+    matrix contribute nothing."""
+    rng = np.random.default_rng(32)
+    yv = rng.integers(-50, 50, size=(30, 16)).astype(np.float32)
+    y = torch.tensor(yv).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    rows = rng.integers(0, 30, size=(12, 8))
+    rows[3, 5] = -1
+    rows[7, 0] = 30
+    w = (rng.integers(0, 9, size=(12, 8)) / 8.0).astype(np.float32)
+    out = oracle.moe_combine(y, rows, w)
+    valid = (rows >= 0) & (rows < 30)
+    want = np.einsum("tj,tjh->th", np.where(valid, w, 0).astype(np.float64),
+                     yv[np.clip(rows, 0, 29)].astype(np.float64))
+    assert np.array_equal(out.astype(np.float64), want)
