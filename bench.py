@@ -13,7 +13,8 @@ One step = every operation of the hot path, on seeded synthetic inputs:
     per-token activation quantization of the 4096 tokens (each token encoded
     once, before dispatch, and written to its 8 dispatched rows), per-expert
     weight quantization (gate|up joint), the gate|up grouped GEMM with SwiGLU
-    in its epilogue, per-token quantization of h, down grouped GEMM.
+    in its epilogue, per-token quantization of h, down grouped GEMM, and the
+    combine of each token's 8 expert outputs weighted by its router weights.
 
 value = block-scaled GEMM FLOPs of the step / step time (quantizers,
 dequantization and SwiGLU included in the time).  Per-kernel times come from
@@ -49,7 +50,7 @@ QWEN = dict(tokens=4096, hidden=2048, experts=128, ffn=768, topk=8)
 METRIC = "quantize HBM GB/s; MXFP8/NVFP4 block-scaled GEMM TFLOPS vs dense peak"
 WORKLOAD = ("MXFP8 linear 2048x2048->8192 fwd+bwd (rowwise+colwise quant, Fprop/Dgrad/Wgrad, "
             "dequantized-backward operands) + NVFP4 linear Fprop + Qwen3-30B-A3B-shaped NVFP4 MoE "
-            "expert layer (4096 tok, top-8 of 128 experts, hidden 2048, FFN 768)")
+            "expert layer (4096 tok, top-8 of 128 experts, hidden 2048, FFN 768; dispatch, SwiGLU, combine)")
 
 
 # ----------------------------------------------------------------- peaks
@@ -144,6 +145,8 @@ class Step:
         self.a_rows = disp.token_of_row.to(torch.int64).contiguous()  # token of each dispatched row
         # the topk dispatched rows of each token (inverse of a_rows)
         self.dest_rows = torch.argsort(self.a_rows, stable=True).to(torch.int64).contiguous()
+        self.rows_of_slot = disp.row_of_slot.contiguous()               # token, choice -> row
+        self.route_w = inputs.route_weights(q["tokens"], q["topk"], 2 + seed_base, device)
         E, F = q["experts"], q["ffn"]
         self.W_gu = moe["W_gu"].reshape(E * 2 * F, H).contiguous()
         self.W_d = moe["W_d"].reshape(E * H, F).contiguous()
@@ -183,6 +186,7 @@ class Step:
         self.Hs = bf(R, F)
         self.H4, self.SH4, self.H432 = u8(R * F // 2)[: R * F // 2].view(R, F // 2), sb4g(R, E, F), f32(R)
         self.OUT = bf(R, H)
+        self.Y_moe = bf(TM, H)                                          # combined, token order
         self.E, self.F, self.H_, self.T, self.O, self.TM = E, F, H, T, O, TM
 
     # -- algorithmic work per launch (bytes or FLOPs) and roofline class
@@ -211,6 +215,7 @@ class Step:
             ("nvfp4_moe_gemm gate_up+swiglu", "fp4", 2.0 * R * 2 * F * H),
             ("nvfp4_quant_token moe_h", "hbm", nvq(R, F)),
             ("nvfp4_grouped_gemm down", "fp4", 2.0 * R * H * F),
+            ("moe_combine", "hbm", 2.0 * R * H + 2.0 * TM * H + 12.0 * R),
         ]
 
     def launches(self):
@@ -244,6 +249,7 @@ class Step:
             ("nvfp4_quant_token moe_h", lambda: mx.nvfp4_quantize_into(self.Hs, self.H4, self.SH4, self.H432, mx.SCOPE_TOKEN, self.offs, ws_c)),
             ("nvfp4_grouped_gemm down", lambda: mx.bs_grouped_gemm_into(mx.FMT_NVFP4, self.offs, self.H4, self.SH4, self.Wd4, self.SWd4,
                                                                          self.F, self.OUT, self.H432, self.Wd432, ws_c)),
+            ("moe_combine", lambda: mx.moe_combine_into(self.OUT, self.rows_of_slot, self.route_w, self.Y_moe)),
         ]
 
     # The step's three independent chains: the MXFP8 linear layer, the NVFP4
@@ -256,7 +262,7 @@ class Step:
          "mxfp8_gemm Wgrad", "dequant_mxfp8 X", "dequant_mxfp8 W"),
         ("nvfp4_quant_token X", "nvfp4_quant_tensor W", "nvfp4_gemm Fprop"),
         ("nvfp4_quant_token moe_act", "nvfp4_quant_expert W_gu", "nvfp4_quant_expert W_d",
-         "nvfp4_moe_gemm gate_up+swiglu", "nvfp4_quant_token moe_h", "nvfp4_grouped_gemm down"),
+         "nvfp4_moe_gemm gate_up+swiglu", "nvfp4_quant_token moe_h", "nvfp4_grouped_gemm down", "moe_combine"),
     )
 
     def workspaces(self):
@@ -304,11 +310,12 @@ class Step:
         self.io_in = ([(self.X, pin(self.X)), (self.dY, pin(self.dY))], [], [(self.X_moe, pin(self.X_moe))])
         empty = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
         self.io_out = ([(self.Y, empty(self.Y)), (self.dX, empty(self.dX))], [(self.Y4, empty(self.Y4))],
-                       [(self.OUT, empty(self.OUT))])
+                       [(self.Y_moe, empty(self.Y_moe))])
         self.x_ready = torch.cuda.Event()
 
     # kernels each label launches (amax pass + quantize for group/tensor scope)
-    KERNELS_PER_LABEL = {}   # every label is one kernel launch (plus, for group/tensor scope, a memset)
+    # kernel launches per label (the rest launch one; group scope adds a memset)
+    KERNELS_PER_LABEL = {"nvfp4_quant_tensor W": 2}   # tensor abs-max, then the encode
 
     def gemm_flops(self):
         return sum(w for _, kind, w in self.plan() if kind in ("fp8", "fp4"))
@@ -709,7 +716,7 @@ def run_gpu(args):
 def run_e2e(step, args, world, dev, graph=None):
     """Same step through the public API with host buffers: every step copies
     its inputs (X, dY, the MoE layer's token activations) from pinned host memory
-    and reads its results (Y, dX, NVFP4 Y, MoE output) back; weights stay
+    and reads its results (Y, dX, NVFP4 Y, the combined MoE output) back; weights stay
     resident.  The three branches run on their own streams, each copying its
     own inputs in and results out, so one branch's copies overlap another's
     kernels."""
@@ -784,6 +791,12 @@ def oracle_step_seconds(budget_s):
     gu = slab(rows, 2 * F)
     s = timed(lambda: oracle.swiglu(gu))
     total += s * R / rows
+    # combine: `rows` tokens of 8 choices each
+    yy = slab(rows * 8, H)
+    rws = np.arange(rows * 8, dtype=np.int64).reshape(rows, 8)
+    ww = np.full((rows, 8), 0.125, np.float32)
+    s = timed(lambda: oracle.moe_combine(yy, rws, ww))
+    total += s * QWEN["tokens"] / rows
     # GEMMs: sampled outputs, scaled per output
     rng = np.random.default_rng(0)
     for fmt, (M, N, K) in ((0, (T, O, H)), (0, (T, H, O)), (0, (O, H, T)), (1, (T, O, H)),

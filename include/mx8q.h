@@ -419,6 +419,27 @@ mx8_status bf16_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda
 mx8_status mx8_swiglu(const void *gate_up, int64_t rows, int64_t ffn, int64_t ld_gate_up,
                       void *h, int64_t ld_h, mx8_stream_t stream);
 
+/*
+ * MoE combine, the step that closes the routed-expert layer: each token's
+ * top-k expert outputs, weighted by its router weights, summed back in token
+ * order:
+ *     out[t, h] = sum_{j<topk} w[t, j] * y[rows_of_slot[t, j], h]
+ * in binary32 in the order j = 0, 1, ... (each product and each sum one
+ * round-to-nearest operation), so the result is deterministic; a bf16 output
+ * is the RNE of that value.
+ *   y            : bf16 [rows_y, hidden], row stride ld_y (the down GEMM's
+ *                  output in dispatched-row order)
+ *   rows_of_slot : device int64 [tokens, topk]; rows outside [0, rows_y)
+ *                  contribute nothing
+ *   weights      : device float [tokens, topk]
+ *   out          : [tokens, hidden] f32 or bf16, row stride ld_out
+ * Requires hidden % 8 == 0, 1 <= topk <= 16, 16-byte aligned y / out,
+ * strides % 8 == 0.
+ */
+mx8_status mx8_moe_combine(const void *y, int64_t rows_y, int64_t ld_y, const int64_t *rows_of_slot,
+                           const float *weights, int64_t tokens, int64_t hidden, int topk,
+                           int out_dtype, void *out, int64_t ld_out, mx8_stream_t stream);
+
 /* Synchronises the stream, reads and clears the workspace error word:
  * MX8_OK, or MX8_ERR_TIMEOUT if a bounded device wait ran out. */
 mx8_status mx8_check_device_error(void *workspace, mx8_stream_t stream);

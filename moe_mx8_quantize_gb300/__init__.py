@@ -34,7 +34,7 @@ EXPORTS = ("mx8_scale_bytes", "mx8_scale_bytes_grouped", "mx8_workspace_bytes",
            "nvfp4_quantize_dispatch", "nvfp4_quantize_2d", "nvfp4_quantize_rht_colwise",
            "nvfp4_quantize_per_token_sr",
            "nvfp4_quantize_per_token_noalloc", "dequantize",
-           "bs_gemm", "bs_grouped_gemm", "bs_grouped_gemm_fused", "bf16_gemm", "mx8_swiglu", "mx8_check_device_error", "mx8_selftest_bounded_wait",
+           "bs_gemm", "bs_grouped_gemm", "bs_grouped_gemm_fused", "bf16_gemm", "mx8_moe_combine", "mx8_swiglu", "mx8_check_device_error", "mx8_selftest_bounded_wait",
            "mx8_status_string")
 
 
@@ -96,6 +96,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bs_grouped_gemm_fused.restype = _i
     lib.bs_grouped_gemm_fused.argtypes = [_i, _i, _p, _i64, _i64, _i64, _p, _p, _p, _p, _i64, _p, _p, _p, _i,
                                           _i, _p, _i64, _p, _sz, _p]
+    lib.mx8_moe_combine.restype = _i
+    lib.mx8_moe_combine.argtypes = [_p, _i64, _i64, _p, _p, _i64, _i64, _i, _i, _p, _i64, _p]
     lib.bf16_gemm.restype = _i
     lib.bf16_gemm.argtypes = [_i64, _i64, _i64, _p, _i64, _p, _i64, _i, _p, _i64, _i, _p, _sz, _p]
     lib.mx8_swiglu.restype = _i
@@ -476,6 +478,24 @@ def bs_grouped_gemm_fused(fmt, group_offsets, A, SA, B, SB, K, A32=None, B32=Non
     out = torch.empty((rows, n_out), dtype=out_dtype, device=A.device)
     bs_grouped_gemm_fused_into(fmt, group_offsets, rows, A, SA, B, SB, K, out, A32, B32, a_rows, epilogue,
                                ws, stream)
+    return out
+
+
+# ---------------------------------------------------------------- MoE combine
+def moe_combine_into(y, rows_of_slot, weights, out, stream=None):
+    """out [T, H] = sum_j weights[t, j] * y[rows_of_slot[t, j]] (binary32, j
+    in order); y bf16 [R, H]; out f32 or bf16."""
+    assert y.dtype == torch.bfloat16 and y.stride(1) == 1 and out.stride(1) == 1
+    T, k = rows_of_slot.shape
+    od = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
+    _check(load().mx8_moe_combine(_ptr(y), y.shape[0], y.stride(0), _ptr(rows_of_slot), _ptr(weights), T,
+                                  y.shape[1], k, od, _ptr(out), out.stride(0), _stream(stream)),
+           "mx8_moe_combine")
+
+
+def moe_combine(y, rows_of_slot, weights, out_dtype=torch.bfloat16, stream=None):
+    out = torch.empty((rows_of_slot.shape[0], y.shape[1]), dtype=out_dtype, device=y.device)
+    moe_combine_into(y, rows_of_slot, weights, out, stream)
     return out
 
 

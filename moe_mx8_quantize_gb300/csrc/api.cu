@@ -287,6 +287,22 @@ extern "C" mx8_status mx8_swiglu(const void* gate_up, int64_t rows, int64_t ffn,
                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// ===================================================================== MoE combine
+extern "C" mx8_status mx8_moe_combine(const void* y, int64_t rows_y, int64_t ld_y, const int64_t* rows_of_slot,
+                                      const float* weights, int64_t tokens, int64_t hidden, int topk,
+                                      int out_dtype, void* out, int64_t ld_out, mx8_stream_t stream) {
+  if (rows_y < 0 || tokens < 0 || hidden < 0 || hidden % 8 != 0 || ld_y < hidden || ld_out < hidden)
+    return MX8_ERR_INVALID_ARG;
+  if (topk < 1 || topk > kMaxTopk) return MX8_ERR_INVALID_ARG;
+  if (out_dtype != MX8_OUT_F32 && out_dtype != MX8_OUT_BF16) return MX8_ERR_INVALID_ARG;
+  if (tokens == 0 || hidden == 0) return MX8_OK;
+  if (y == nullptr || rows_of_slot == nullptr || weights == nullptr || out == nullptr) return MX8_ERR_INVALID_ARG;
+  if (!aligned16(y) || !aligned16(out) || ld_y % 8 != 0 || ld_out % 8 != 0) return MX8_ERR_ALIGNMENT;
+  return from_cuda(launch_combine(static_cast<const uint16_t*>(y), ld_y, rows_y, rows_of_slot, weights, tokens,
+                                  hidden, topk, out_dtype == MX8_OUT_BF16, out, ld_out, sm_count_current(),
+                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
 // ===================================================================== GEMM
 namespace {
 

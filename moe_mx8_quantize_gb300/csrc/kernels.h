@@ -63,6 +63,11 @@ cudaError_t launch_dequant(int fmt, const uint8_t* q, const uint8_t* s, const fl
                            int s32_mode, const int64_t* offs, int G, int64_t R, int64_t C,
                            int out_bf16, void* out, int sm_count, cudaStream_t stream);
 
+// out[t] = sum_j w[t][j] * y[rows[t][j]], binary32 in j order (rows outside
+// [0, R) skipped); H % 8 == 0.
+cudaError_t launch_combine(const uint16_t* y, int64_t ldy, int64_t R, const int64_t* rows, const float* w, int64_t T,
+                           int64_t H, int k, bool bf16_out, void* out, int64_t ldo, int sm_count, cudaStream_t stream);
+
 cudaError_t launch_swiglu(const uint16_t* gu, int64_t R, int64_t F, int64_t ld_gu, uint16_t* h,
                           int64_t ld_h, int sm_count, cudaStream_t stream);
 

@@ -139,3 +139,22 @@ def test_swiglu_epilogue(gather, T, H, E, F, topk):
                             dev(ad), dev(b32), out_dtype=torch.bfloat16)
     h2 = mx.swiglu(gu)
     assert torch.equal(h.view(torch.int16), h2.view(torch.int16))
+
+
+@pytest.mark.parametrize("T,H,E,topk,out_dtype", [(64, 256, 5, 2, torch.float32), (300, 512, 16, 8, torch.bfloat16),
+                                                  (4096, 2048, 128, 8, torch.bfloat16)])
+def test_moe_combine_bit_exact(T, H, E, topk, out_dtype):
+    """The router-weighted sum of each token's expert outputs, bit for bit
+    against the oracle's binary32 evaluation in the same order."""
+    d = inputs.moe(T + 3, "cpu", T, H, E, 64, topk, with_weights=False)
+    disp = inputs.dispatch(d["topk_ids"], E)
+    rows = disp.row_of_slot
+    w = inputs.route_weights(T, topk, T, "cpu")
+    R = T * topk
+    y = inputs.bits(inputs.normal_bf16((R, H), 1.0, torch.Generator().manual_seed(H), "cpu", 0.01, 30))
+    out = mx.moe_combine(dev(y), rows.cuda(), w.cuda(), out_dtype=out_dtype)
+    ref = oracle.moe_combine(y, rows.numpy(), w.numpy())
+    if out_dtype == torch.float32:
+        assert np.array_equal(host(out).view(np.uint32), ref.view(np.uint32))
+    else:
+        assert np.array_equal(host(out), oracle.f32_to_bf16(ref))

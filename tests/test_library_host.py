@@ -116,6 +116,10 @@ def test_invalid_arguments_rejected_on_host(lib):
     # stochastic per-token: cols % 16, misaligned stride
     assert lib.nvfp4_quantize_per_token_sr(p, 4, 24, 24, 1, p, p, p, None) == m.ERR_INVALID_ARG
     assert lib.nvfp4_quantize_per_token_sr(p, 4, 32, 36, 1, p, p, p, None) == m.ERR_ALIGNMENT
+    # MoE combine: hidden % 8, topk range, bad dtype
+    assert lib.mx8_moe_combine(p, 8, 12, p, p, 4, 12, 2, 1, p, 12, None) == m.ERR_INVALID_ARG
+    assert lib.mx8_moe_combine(p, 8, 16, p, p, 4, 16, 0, 1, p, 16, None) == m.ERR_INVALID_ARG
+    assert lib.mx8_moe_combine(p, 8, 16, p, p, 4, 16, 2, 7, p, 16, None) == m.ERR_INVALID_ARG
     # fused MoE GEMM: bad epilogue, SwiGLU needs N % 256 and bf16, formats other than NVFP4
     assert lib.bs_grouped_gemm_fused(1, 2, p, 8, 256, 64, p, p, None, None, 0, p, p, None, 5, 1, p, 128, p, 4096,
                                      None) == m.ERR_INVALID_ARG
