@@ -195,6 +195,72 @@ __global__ void __launch_bounds__(kThreads) swiglu_kernel(const uint16_t* __rest
 }
 }  // namespace
 
+// MoE combine: out[t] = sum_j w[t][j] * y[rows[t][j]] in binary32, j in
+// order (acc = RN(acc + RN(w * y))), so the result is deterministic and
+// equal to a serial evaluation; each thread owns 8 columns of one token and
+// reads the k rows' 16-byte pieces (coalesced along the row).
+namespace {
+template <bool kBf16Out>
+__global__ void __launch_bounds__(kThreads) combine_kernel(const uint16_t* __restrict__ y, int64_t ldy, int64_t R,
+                                                          const int64_t* __restrict__ rows,
+                                                          const float* __restrict__ w, int64_t T, int64_t H, int k,
+                                                          void* __restrict__ out, int64_t ldo) {
+  const int64_t chunks = H / 8;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < T * chunks;
+       i += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const int64_t t = i / chunks, c = (i % chunks) * 8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      // the (up to) 8 rows' loads are issued together, then summed in order
+      uint4 v[8];
+      float wj[8];
+      bool ok[8];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const int j = j0 + jj;
+        const int64_t r = j < k ? rows[t * k + j] : -1;
+        ok[jj] = r >= 0 && r < R;
+        wj[jj] = ok[jj] ? w[t * k + j] : 0.f;
+        v[jj] = ok[jj] ? __ldg(reinterpret_cast<const uint4*>(y + r * ldy + c)) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        if (!ok[jj]) continue;             // a missing row contributes nothing (not +0)
+        const uint32_t ws[4] = {v[jj].x, v[jj].y, v[jj].z, v[jj].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc[2 * e] = __fadd_rn(acc[2 * e], __fmul_rn(wj[jj], bf16_lo(ws[e])));
+          acc[2 * e + 1] = __fadd_rn(acc[2 * e + 1], __fmul_rn(wj[jj], bf16_hi(ws[e])));
+        }
+      }
+    }
+    if (kBf16Out) {
+      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + t * ldo + c) =
+          make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                     pack_bf16x2(acc[6], acc[7]));
+    } else {
+      float4* d = reinterpret_cast<float4*>(static_cast<float*>(out) + t * ldo + c);
+      d[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      d[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+  }
+}
+}  // namespace
+
+cudaError_t launch_combine(const uint16_t* y, int64_t ldy, int64_t R, const int64_t* rows, const float* w, int64_t T,
+                           int64_t H, int k, bool bf16_out, void* out, int64_t ldo, int sm_count, cudaStream_t stream) {
+  const int64_t total = T * (H / 8);
+  if (total == 0) return cudaSuccess;
+  const int64_t want = (total + kThreads - 1) / kThreads;
+  const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+  const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
+  if (bf16_out)
+    combine_kernel<true><<<grid, kThreads, 0, stream>>>(y, ldy, R, rows, w, T, H, k, out, ldo);
+  else
+    combine_kernel<false><<<grid, kThreads, 0, stream>>>(y, ldy, R, rows, w, T, H, k, out, ldo);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_swiglu(const uint16_t* gu, int64_t R, int64_t F, int64_t ld_gu, uint16_t* h,
                           int64_t ld_h, int sm_count, cudaStream_t stream) {
   const int64_t total = R * (F / 8);
