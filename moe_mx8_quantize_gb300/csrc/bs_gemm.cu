@@ -402,20 +402,26 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
             if constexpr (F::kSfTiles > 0) {
               int64_t sf0;
               const int nsf = scale_tiles_of_stage(kt, sf0);
-              mbar_arrive_expect_tx(full, kTileABytes + (1 + L::kBRow128) * nsf * 512);
+              mbar_arrive_expect_tx(full, kTileABytes + nsf * 512);
               tma_load_2d(smem_u32(sm.a[s]), &tmap_a, kt * kKBytes, static_cast<int32_t>(tc.a_row0), full);
               bulk_load(smem_u32(sm.sfa[s]), sfa_src + sf0 * 512, nsf * 512, full);
-#pragma unroll
-              for (int h = 0; h < L::kBRow128; ++h)
-                bulk_load(smem_u32(sm.sfb[s]) + h * F::kSfTiles * 512, sfb_src[h] + sf0 * 512, nsf * 512, full);
             } else {
               mbar_arrive_expect_tx(full, kTileABytes);
               tma_load_2d(smem_u32(sm.a[s]), &tmap_a, kt * kKBytes, static_cast<int32_t>(tc.a_row0), full);
             }
           } else {
-            // B in 128-row boxes (a 128-row box is 16 KB; boxes stack in shared memory)
+            // B in 128-row boxes (a 128-row box is 16 KB; boxes stack in shared
+            // memory), each with its scale tiles, so every issuer moves about
+            // the same bytes per stage
             const int h = prod - 1;
-            mbar_arrive_expect_tx(full, kBoxBytes);
+            if constexpr (F::kSfTiles > 0) {
+              int64_t sf0;
+              const int nsf = scale_tiles_of_stage(kt, sf0);
+              mbar_arrive_expect_tx(full, kBoxBytes + nsf * 512);
+              bulk_load(smem_u32(sm.sfb[s]) + h * F::kSfTiles * 512, sfb_src[h] + sf0 * 512, nsf * 512, full);
+            } else {
+              mbar_arrive_expect_tx(full, kBoxBytes);
+            }
             if (kGrouped)
               tma_load_3d(smem_u32(sm.b[s]) + h * kBoxBytes, &tmap_b, kt * kKBytes,
                           static_cast<int32_t>(b_row0(tc, h)), tc.g, full);
