@@ -27,16 +27,29 @@
 //                 about 50 GB/s per SM on this GPU, several in separate warps
 //                 move several times that, so the operand stream of a stage
 //                 is split over 1 + BN/128 issuers;
-//   warp 1      : allocates tensor memory; one thread copies each stage's
-//                 scale tiles into tensor memory (tcgen05.cp) and issues the
-//                 block-scaled MMAs (M = 128, N = BN) into an FP32 accumulator
-//                 in tensor memory, commits each stage back to the producer
-//                 and each finished accumulator to the epilogue;
+//   warp 1      : allocates tensor memory; one thread issues the block-scaled
+//                 MMAs (M = 128, N = BN) into an FP32 accumulator in tensor
+//                 memory once a stage's operands have landed and its scales
+//                 are in tensor memory, commits each stage back to the
+//                 producers and each finished accumulator to the epilogue;
 //   epilogue    : BN/32 warps, two per 32-lane quarter of tensor memory when
-//                 BN = 256; each pulls its 32 rows x 128 columns into
-//                 registers, releases the accumulator at once (so the next
-//                 tile's MMAs start), then applies the FP32 scales, converts
-//                 and stores.
+//                 BN = 256.  When the accumulator is full each warp pulls its
+//                 32 rows x 128 columns into registers, releases it at once
+//                 (so the next tile's MMAs start), then applies the FP32
+//                 scales, converts and stores.
+// Scales into tensor memory, two ways:
+//   - single GEMM: while an accumulator fills, the epilogue warps move each
+//     landed stage's scale tiles from shared into tensor memory (ld.shared +
+//     tcgen05.st into their own lane quarter, A's tiles by one warp of the
+//     quarter, B's by the other), also between the pieces of their stores,
+//     so the tensor pipe runs MMAs only.  A tcgen05.cp of a 512-byte scale
+//     tile costs the in-order tensor pipe about 45 ns; NVFP4 copies 12 per
+//     stage, which was 40% of the Fprop GEMM (39 -> 31 us on 2048x2048->8192);
+//   - grouped GEMM: the MMA thread copies them (tcgen05.cp) right before the
+//     stage's MMAs.  The MoE GEMMs have short K per tile (3 stages for the
+//     768-wide down projection) and, for gate|up, a SwiGLU epilogue, and the
+//     epilogue warps then could not keep the MMAs fed (gate|up 214 us against
+//     115 us with the copies).
 // BN = 128 keeps two accumulators (epilogue fully overlapped); BN = 256 moves
 // half the operand bytes per FLOP of BN = 128 and keeps one accumulator (the
 // 512 tensor-memory columns hold 256 accumulator columns plus the scales).
@@ -154,6 +167,8 @@ struct __align__(1024) GemmSmem {
   uint8_t cstage[L::kEpiWarps][L::kEpiStageBytes];   // epilogue staging for bulk stores
   uint64_t full[L::kStages];
   uint64_t empty[L::kStages];
+  uint64_t sf_full[L::kStages];                       // a stage's scale tiles have landed
+  uint64_t sf_ready[L::kStages];                      // a stage's scales are in tensor memory
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t drain;
@@ -240,6 +255,8 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
   using Smem = GemmSmem<kFmt, kGrouped, kBN, kMode>;
   constexpr bool kGather = (kMode & kModeGather) != 0;
   constexpr bool kSwiGLU = (kMode & kModeSwiGLU) != 0;
+  // scales moved into tensor memory by the epilogue warps (else tcgen05.cp)
+  constexpr bool kWarpScales = F::kSfTiles > 0 && !kGrouped;
   static_assert(kGather <= kGrouped && kSwiGLU <= kGrouped, "fused modes are grouped only");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -257,6 +274,8 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(smem_u32(&sm.full[s]), L::kProducers);
       mbar_init(smem_u32(&sm.empty[s]), 1);
+      mbar_init(smem_u32(&sm.sf_full[s]), 1 + L::kBRow128);
+      mbar_init(smem_u32(&sm.sf_ready[s]), L::kEpiWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sm.acc_full[i]), 1);
@@ -322,8 +341,9 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
       // of the tile goes to o ^ (((o >> 7) % atom rows) << 4).  Each lane
       // arrives on the stage's barrier once its copies have landed (the MMA
       // thread fences them for the tensor core's reads).  Lane 0 also loads
-      // the A and B scale tiles (the dispatched rows' scales are laid out by
-      // the quantizer, grouped, so they arrive as whole tiles).
+      // A's scale tiles (the dispatched rows' scales are laid out by the
+      // quantizer, grouped, so they arrive as whole tiles); the B producers
+      // load B's.
       constexpr uint32_t kAtomMask = kKBytes == 128 ? 7u : 3u;
       const uint32_t sub = static_cast<uint32_t>(lane & 7);   // 16-byte chunk of the row segment
       const int rq = lane >> 3;                                // row within a group of 4
@@ -340,8 +360,6 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
         }
         __syncwarp();
         const uint8_t* sfa_src = args.SA + tc.sfa_tile * sf_kt * 512;
-        const uint8_t* sfb_src[L::kBRow128];
-        b_scale_srcs(tc, sfb_src);
         for (int kt = 0; kt < ktiles; ++kt, ++it) {
           const int s = it % L::kStages;
           const uint32_t ph = (it / L::kStages) & 1;
@@ -355,11 +373,8 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
           if (lane == 0) {
             int64_t sf0;
             const int nsf = scale_tiles_of_stage(kt, sf0);
-            mbar_arrive_expect_tx(full, (1 + L::kBRow128) * nsf * 512);
+            mbar_arrive_expect_tx(full, nsf * 512);   // the gathered rows arrive below, lane by lane
             bulk_load(smem_u32(sm.sfa[s]), sfa_src + sf0 * 512, nsf * 512, full);
-#pragma unroll
-            for (int h = 0; h < L::kBRow128; ++h)
-              bulk_load(smem_u32(sm.sfb[s]) + h * F::kSfTiles * 512, sfb_src[h] + sf0 * 512, nsf * 512, full);
           }
           const uint32_t a_s = smem_u32(sm.a[s]);
           const int64_t kb = static_cast<int64_t>(kt) * kKBytes + 16 * sub;
@@ -398,30 +413,37 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
             break;
           }
           const uint32_t full = smem_u32(&sm.full[s]);
-          if (prod == 0) {
-            if constexpr (F::kSfTiles > 0) {
-              int64_t sf0;
-              const int nsf = scale_tiles_of_stage(kt, sf0);
-              mbar_arrive_expect_tx(full, kTileABytes + nsf * 512);
-              tma_load_2d(smem_u32(sm.a[s]), &tmap_a, kt * kKBytes, static_cast<int32_t>(tc.a_row0), full);
-              bulk_load(smem_u32(sm.sfa[s]), sfa_src + sf0 * 512, nsf * 512, full);
+          // Each issuer also loads its scale tiles (A's, or its B box's).  When
+          // the epilogue warps move them into tensor memory they land on the
+          // stage's scale barrier: small, they arrive well before the operand
+          // tiles and are moved while the operands are still in flight.
+          // Otherwise they land with the operands.
+          const uint32_t op_bytes = prod == 0 ? static_cast<uint32_t>(kTileABytes) : static_cast<uint32_t>(kBoxBytes);
+          if constexpr (F::kSfTiles > 0) {
+            int64_t sf0;
+            const int nsf = scale_tiles_of_stage(kt, sf0);
+            const uint32_t sbar = kWarpScales ? smem_u32(&sm.sf_full[s]) : full;
+            if (kWarpScales) {
+              mbar_arrive_expect_tx(sbar, nsf * 512);
+              mbar_arrive_expect_tx(full, op_bytes);
             } else {
-              mbar_arrive_expect_tx(full, kTileABytes);
-              tma_load_2d(smem_u32(sm.a[s]), &tmap_a, kt * kKBytes, static_cast<int32_t>(tc.a_row0), full);
+              mbar_arrive_expect_tx(full, op_bytes + nsf * 512);
             }
+            if (prod == 0)
+              bulk_load(smem_u32(sm.sfa[s]), sfa_src + sf0 * 512, nsf * 512, sbar);
+            else
+              bulk_load(smem_u32(sm.sfb[s]) + (prod - 1) * F::kSfTiles * 512, sfb_src[prod - 1] + sf0 * 512,
+                        nsf * 512, sbar);
+          } else {
+            mbar_arrive_expect_tx(full, op_bytes);
+          }
+          if (prod == 0) {
+            tma_load_2d(smem_u32(sm.a[s]), &tmap_a, kt * kKBytes, static_cast<int32_t>(tc.a_row0), full);
           } else {
             // B in 128-row boxes (a 128-row box is 16 KB; boxes stack in shared
-            // memory), each with its scale tiles, so every issuer moves about
-            // the same bytes per stage
+            // memory), one issuer each, so every issuer moves about the same
+            // bytes per stage
             const int h = prod - 1;
-            if constexpr (F::kSfTiles > 0) {
-              int64_t sf0;
-              const int nsf = scale_tiles_of_stage(kt, sf0);
-              mbar_arrive_expect_tx(full, kBoxBytes + nsf * 512);
-              bulk_load(smem_u32(sm.sfb[s]) + h * F::kSfTiles * 512, sfb_src[h] + sf0 * 512, nsf * 512, full);
-            } else {
-              mbar_arrive_expect_tx(full, kBoxBytes);
-            }
             if (kGrouped)
               tma_load_3d(smem_u32(sm.b[s]) + h * kBoxBytes, &tmap_b, kt * kKBytes,
                           static_cast<int32_t>(b_row0(tc, h)), tc.g, full);
@@ -433,9 +455,13 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
       }
       if (!ok) {
         // let the copies already issued land before the block exits
-        for (int j = (it > L::kStages ? it - L::kStages : 0); j < it; ++j)
+        for (int j = (it > L::kStages ? it - L::kStages : 0); j < it; ++j) {
           mbar_wait(smem_u32(&sm.full[j % L::kStages]), (j / L::kStages) & 1, err, kErrWaitTeardown,
                     nullptr, 100000000ull);
+          if (kWarpScales)
+            mbar_wait(smem_u32(&sm.sf_full[j % L::kStages]), (j / L::kStages) & 1, err, kErrWaitTeardown,
+                      nullptr, 100000000ull);
+        }
       }
     }
   } else if (warp == 1) {
@@ -460,21 +486,30 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
             ok = false;
             break;
           }
+          if constexpr (kWarpScales) {
+            if (!mbar_wait(smem_u32(&sm.sf_ready[s]), ph, err, kErrWaitScales, &sm.abort)) {
+              ok = false;
+              break;
+            }
+          }
           tc_fence_after();
           if (kGather) fence_proxy_async_smem();   // the gathered rows were written by cp.async
-          int64_t sf0;
-          const int nsf = scale_tiles_of_stage(kt, sf0);
-          // tensor-memory scale layout per stage: A -> 4 columns per K sub-tile;
-          // B -> (4 columns x kBRow128) per K sub-tile, the 128-row blocks adjacent
+          // tensor-memory scale layout per stage: A -> 4 columns per K
+          // sub-tile; B -> (4 columns x kBRow128) per K sub-tile, the 128-row
+          // blocks adjacent
           const uint32_t tsfa = sf_base + s * L::kSfColsPerStage;
           const uint32_t tsfb = tsfa + L::kSfaCols;
-          for (int j = 0; j < nsf; ++j) {
-            tc_cp_32x128b_x4(tsfa + 4 * j, smem_desc(smem_u32(sm.sfa[s]) + 512 * j, 128, 128, kSwizzleNone));
+          if constexpr (F::kSfTiles > 0 && !kWarpScales) {
+            int64_t sf0;
+            const int nsf = scale_tiles_of_stage(kt, sf0);
+            for (int j = 0; j < nsf; ++j) {
+              tc_cp_32x128b_x4(tsfa + 4 * j, smem_desc(smem_u32(sm.sfa[s]) + 512 * j, 128, 128, kSwizzleNone));
 #pragma unroll
-            for (int h = 0; h < L::kBRow128; ++h)
-              tc_cp_32x128b_x4(tsfb + (j * L::kBRow128 + h) * 4,
-                               smem_desc(smem_u32(sm.sfb[s]) + (h * F::kSfTiles + j) * 512, 128, 128,
-                                         kSwizzleNone));
+              for (int h = 0; h < L::kBRow128; ++h)
+                tc_cp_32x128b_x4(tsfb + (j * L::kBRow128 + h) * 4,
+                                 smem_desc(smem_u32(sm.sfb[s]) + (h * F::kSfTiles + j) * 512, 128, 128,
+                                           kSwizzleNone));
+            }
           }
           const int64_t krem = K - static_cast<int64_t>(kt) * F::kElemsPerStage;
           const int nmma = static_cast<int>(krem >= F::kElemsPerStage
@@ -514,12 +549,85 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
     const int quarter = warp & 3;              // tcgen05.ld lane quarter of this warp
     const int col0 = (ew / 4) * 128;           // this warp's 128 accumulator columns
     const int r_in_tile = quarter * 32 + lane;
+    // Scale staging.  Each 512-byte scale tile is 32 rows of 16 bytes; every
+    // lane quarter of tensor memory gets the same 32 x 16 bytes, row i in
+    // lane i of the quarter, over the tile's 4 columns (the layout the
+    // block-scaled MMA reads).  Stages are staged in order as their scale
+    // tiles land: a stage can only be refilled after its MMAs, which wait for
+    // its scales, so a stage's barriers are never more than one phase ahead.
+    const int cta_tiles = unit0 < nunits ? static_cast<int>((nunits - 1 - unit0) / ustep + 1) : 0;
+    const int total_stages = kWarpScales ? cta_tiles * ktiles : 0;
+    const bool stage_a = ew / 4 == 0, stage_b = ew / 4 == L::kBRow128 - 1;
+    int staged = 0;
+    auto stage_scales = [&](int it) {
+      const int s = it % L::kStages;
+      const uint32_t tq = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + L::kAccCols +
+                          static_cast<uint32_t>(s) * L::kSfColsPerStage;
+      if (stage_a) {
+#pragma unroll
+        for (int j = 0; j < F::kSfTiles; ++j)
+          tmem_st_32x32b_x4(tq + 4 * j, *reinterpret_cast<const uint4*>(sm.sfa[s] + 512 * j + 16 * lane));
+      }
+      if (stage_b) {
+#pragma unroll
+        for (int j = 0; j < F::kSfTiles; ++j)
+#pragma unroll
+          for (int h = 0; h < L::kBRow128; ++h)
+            tmem_st_32x32b_x4(tq + L::kSfaCols + (j * L::kBRow128 + h) * 4,
+                              *reinterpret_cast<const uint4*>(sm.sfb[s] + (h * F::kSfTiles + j) * 512 + 16 * lane));
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.sf_ready[s]));
+    };
+    // Stages every stage whose scale tiles have landed (warp-uniform, never
+    // blocks); called between the pieces of the epilogue's own work too, so
+    // the MMAs of the next tile keep their scales while a tile is stored.
+    auto stage_landed = [&]() -> bool {
+      bool any = false;
+      if constexpr (kWarpScales) {
+        while (staged < total_stages &&
+               __all_sync(0xffffffffu, mbar_test_wait(smem_u32(&sm.sf_full[staged % L::kStages]),
+                                                      (staged / L::kStages) & 1))) {
+          stage_scales(staged++);
+          any = true;
+        }
+      }
+      return any;
+    };
+    // Waits (warp-uniformly, bounded) for accumulator `as` to fill, staging
+    // every stage that lands meanwhile.
+    auto wait_accumulator = [&](int as, uint32_t aph) -> bool {
+      if constexpr (!kWarpScales) {
+        return __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.acc_full[as]), aph, err, kErrWaitEpilogue, &sm.abort));
+      } else {
+        uint64_t t0 = 0;
+        while (true) {
+          if (__all_sync(0xffffffffu, mbar_test_wait(smem_u32(&sm.acc_full[as]), aph))) return true;
+          if (stage_landed()) {
+            t0 = 0;
+            continue;
+          }
+          if (__any_sync(0xffffffffu, *reinterpret_cast<volatile int*>(&sm.abort) != 0)) return false;
+          const uint64_t now = __shfl_sync(0xffffffffu, globaltimer(), 0);
+          if (t0 == 0) {
+            t0 = now;
+          } else if (now - t0 > kWaitLimitNs) {
+            if (lane == 0) {
+              atomicCAS(err, 0, staged < total_stages ? kErrWaitScales : kErrWaitEpilogue);
+              sm.abort = 1;
+            }
+            return false;
+          }
+        }
+      }
+    };
     int tcount = 0;
     for (int64_t u = unit0; u < nunits; u += ustep, ++tcount) {
       const int as = tcount % L::kAccBufs;
       const uint32_t aph = (tcount / L::kAccBufs) & 1;
-      const bool ok = mbar_wait(smem_u32(&sm.acc_full[as]), aph, err, kErrWaitEpilogue, &sm.abort);
-      if (!__all_sync(0xffffffffu, ok)) break;
+      if (!wait_accumulator(as, aph)) break;
       tc_fence_after();
       uint32_t r[4][32];
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + as * kBN;
@@ -534,6 +642,7 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.acc_empty[as]));   // accumulator drained into registers
+      stage_landed();
 
       const TileCoord tc = tile_of(u);
       const bool row_ok = r_in_tile < tc.rows;
@@ -589,6 +698,7 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
         const int32_t y = static_cast<int32_t>(tc.a_row0 + quarter * 32);
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
+          if (ch > 0) stage_landed();
           const int64_t n0 = tc.n0 + col0 + ch * 32;
           if (n0 >= N) break;
           float v[32];
