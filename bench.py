@@ -478,22 +478,47 @@ class Nvfp4RecipeLinear:
         ]
 
 
-def kernel_source_hash():
+CSRC = os.path.join(ROOT, "moe_mx8_quantize_gb300", "csrc")
+# Translation units holding the kernels of each bench label (first matching
+# prefix wins).  A kernel's code is its translation unit plus the launch
+# setup in api.cu and the shared headers.
+KERNEL_TUS = (
+    ("mxfp8_quant_rc", ("quant_mxfp8.cu",)), ("mxfp4_quant_rc", ("quant_mxfp8.cu",)),
+    ("dequant_", ("dequant.cu",)), ("moe_combine", ("dequant.cu",)),
+    ("nvfp4_quant_tensor", ("quant_nvfp4.cu", "quant_nvfp4_2d.cu")),
+    ("nvfp4_quant_token_sr", ("quant_wgrad.cu",)), ("nvfp4_rht", ("quant_wgrad.cu",)),
+    ("nvfp4_2d", ("quant_nvfp4_2d.cu",)), ("nvfp4_quant", ("quant_nvfp4.cu",)),
+    ("mxfp8_gemm", ("bs_gemm.cu",)), ("mxfp4_gemm", ("bs_gemm.cu",)), ("nvfp4_gemm", ("bs_gemm.cu",)),
+    ("nvfp4_moe_gemm", ("bs_gemm.cu",)), ("nvfp4_grouped_gemm", ("bs_gemm.cu",)), ("bf16_gemm", ("bs_gemm.cu",)),
+)
+
+
+def kernel_source_hash(label=None, names=None, read=None):
+    """sha256 (first 16 hex) of the kernel sources: of every file in csrc/, or,
+    for a bench label, of its translation units + api.cu + the headers.
+    `names` / `read` give another source state (file list, name -> bytes)."""
+    names = sorted(names if names is not None else os.listdir(CSRC))
+    if read is None:
+        def read(name):
+            with open(os.path.join(CSRC, name), "rb") as f:
+                return f.read()
+    if label is not None:
+        tus = next((t for prefix, t in KERNEL_TUS if label.startswith(prefix)), None)
+        if tus is not None:
+            names = [n for n in names if n in tus or n == "api.cu" or n.endswith((".cuh", ".h"))]
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "moe_mx8_quantize_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+    for name in names:
+        h.update(read(name))
     return h.hexdigest()[:16]
 
 
 def read_traffic(label):
     """dram bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources."""
+    on the current sources of this label's kernels."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(p):
         return None
-    cur = kernel_source_hash()
+    cur = kernel_source_hash(label)
     with open(p) as f:
         for line in f:
             if line.startswith("#") or not line.strip():
