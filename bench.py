@@ -529,6 +529,54 @@ def read_traffic(label):
     return None
 
 
+# ----------------------------------------------------------------- ranks
+class Ranks:
+    """Rank layout of a run under torchrun (RANK / WORLD_SIZE / LOCAL_RANK)
+    and the host-side collectives of a replicas-only job: every rank runs its
+    own copy of the step; ranks meet only at the barriers around a timed
+    region and in the max over ranks of its duration.  `backend` "nccl" on
+    GPUs, "gloo" for CPU tests; a single rank needs no process group."""
+
+    def __init__(self, backend=None):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.dist = None
+        if self.world > 1 and backend is not None:
+            import torch.distributed as dist
+            dist.init_process_group(backend)
+            self.dist = dist
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def max(self, x, device="cpu"):
+        """Max over ranks of a float (a timed region's duration)."""
+        if self.dist is None:
+            return float(x)
+        import torch
+        t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def emit(self, out, file=None):
+        """Rank 0 prints the job's one JSON line."""
+        if self.rank == 0:
+            print(json.dumps(out), file=file or sys.stdout, flush=True)
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.destroy_process_group()
+            self.dist = None
+
+
+def job_tflops(world, flops_per_replica, ms_step):
+    """Whole-job throughput of `world` replicas, each doing flops_per_replica
+    per step, when a step takes ms_step (the max over ranks): TFLOP/s."""
+    return world * flops_per_replica / (ms_step / 1e3) / 1e12
+
+
 # ----------------------------------------------------------------- GPU arm
 def time_each(launches, K2, stream):
     """Per-launch device time (ms, mean of K2 runs) of a list of (label,
@@ -590,29 +638,23 @@ def rate_row(lab, kind, work, ms, peaks):
 
 def run_gpu(args):
     import torch
-    import torch.distributed as dist
     import __graft_entry__
     import moe_mx8_quantize_gb300 as mx
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl")
+    ranks = Ranks("nccl")
+    world, rank, local = ranks.world, ranks.rank, ranks.local
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     __graft_entry__.build() if rank == 0 or world == 1 else None
     if world > 1:
-        dist.barrier()
+        ranks.barrier()
         mx.load()
     step = Step(dev, seed_base=0)
     launches = step.launches()
     plan = {lab: (kind, w) for lab, kind, w in step.plan()}
     stream = torch.cuda.current_stream()
 
-    def barrier():
-        if world > 1:
-            dist.barrier()
+    barrier = ranks.barrier
 
     # warm-up (eager), then capture one step as a CUDA graph
     def eager_step():
@@ -662,10 +704,7 @@ def run_gpu(args):
     clocks = sampler.stop()
     total_ms = t0.elapsed_time(t1)
     check_errors("in timed region")
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = ranks.max(total_ms, dev)
     ms_step = total_ms / K
 
     # timed region 2: the per-kernel durations of the breakdown and the
@@ -685,7 +724,7 @@ def run_gpu(args):
                 + ("hbm copy" if dkind == "hbm" else f"bf16 sustained x {RATIO[dkind]:g} ({dkind} nominal ratio)")}
 
     flops = step.gemm_flops()
-    value = world * flops / (ms_step / 1e3) / 1e12
+    value = job_tflops(world, flops, ms_step)
     launches_per_step = sum(Step.KERNELS_PER_LABEL.get(lab, 1) for lab, _ in launches)
     gpu_launches = launches_per_step * (K + K2)
 
@@ -711,7 +750,7 @@ def run_gpu(args):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(step, args, world, dev, graph)
+        e2e = run_e2e(step, args, ranks, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -732,13 +771,11 @@ def run_gpu(args):
                    "breakdown_from": breakdown_from,
                    "kernels_sum_ms_per_step": round(sum(b["us"] for b in breakdown) / 1e3, 4)},
     }
-    if rank == 0:
-        print(json.dumps(out), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    ranks.emit(out)
+    ranks.close()
 
 
-def run_e2e(step, args, world, dev, graph=None):
+def run_e2e(step, args, ranks, dev):
     """Same step through the public API with host buffers: every step copies
     its inputs (X, dY, the MoE layer's token activations) from pinned host memory
     and reads its results (Y, dX, NVFP4 Y, the combined MoE output) back; weights stay
@@ -755,15 +792,18 @@ def run_e2e(step, args, world, dev, graph=None):
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
+    ranks.barrier()
+    torch.cuda.synchronize()
     a.record(stream)
     for _ in range(K):
         step.run_concurrent(streams, io=True)
     b.record(stream)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / K
+    ranks.barrier()
+    ms = ranks.max(a.elapsed_time(b), dev) / K
     bi = sum(h.numel() * h.element_size() for br in step.io_in for _, h in br)
     bo = sum(h.numel() * h.element_size() for br in step.io_out for _, h in br)
-    return {"value": round(world * step.gemm_flops() / (ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+    return {"value": round(job_tflops(ranks.world, step.gemm_flops(), ms), 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "steps": K, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
 
 
@@ -857,9 +897,11 @@ def oracle_baseline(budget_s):
 
 
 def run_reference(args):
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    if rank != 0:
+    # the oracle on the host cores: rank 0 alone runs and prints; under
+    # torchrun the other ranks exit at once without work
+    ranks = Ranks()
+    world = ranks.world
+    if ranks.rank != 0:
         return
     K = args.steps
     # each step times a sample sized so the whole run stays near two minutes
@@ -885,7 +927,7 @@ def run_reference(args):
                             "wall_s": round(wall, 2)},
            "e2e": {"value": round(value, 8), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
-    print(json.dumps(out), flush=True)
+    ranks.emit(out)
 
 
 def main():
