@@ -21,9 +21,10 @@
 //   producers   : TMA loads of A (128 rows) and B (BN rows) tiles of 128
 //                 bytes of K with the 128-byte swizzle, plus the matching
 //                 512-byte scale tiles, into a ring of shared-memory stages
-//                 guarded by mbarriers.  One thread of warp 0 issues A and the
+//                 guarded by mbarriers.  One thread of warp 0 issues A and its
 //                 scale tiles, one thread in each of BN/128 further warps one
-//                 128-row box of B: a single issuing thread moves at most
+//                 128-row box of B and its scale tiles: a single issuing
+//                 thread moves at most
 //                 about 50 GB/s per SM on this GPU, several in separate warps
 //                 move several times that, so the operand stream of a stage
 //                 is split over 1 + BN/128 issuers;
@@ -48,8 +49,8 @@
 //   - grouped GEMM: the MMA thread copies them (tcgen05.cp) right before the
 //     stage's MMAs.  The MoE GEMMs have short K per tile (3 stages for the
 //     768-wide down projection) and, for gate|up, a SwiGLU epilogue, and the
-//     epilogue warps then could not keep the MMAs fed (gate|up 214 us against
-//     115 us with the copies).
+//     epilogue warps then could not keep the MMAs fed (gate|up 154-214 us
+//     against 115 us with the copies).
 // BN = 128 keeps two accumulators (epilogue fully overlapped); BN = 256 moves
 // half the operand bytes per FLOP of BN = 128 and keeps one accumulator (the
 // 512 tensor-memory columns hold 256 accumulator columns plus the scales).
