@@ -887,16 +887,54 @@ void or_moe_combine(const uint16_t *y, i64 R, i64 H, const i64 *rows, const floa
 /* SwiGLU between the MoE gate|up and down GEMMs                        */
 /* ------------------------------------------------------------------ */
 
-/* h[r, j] = RN_bf16( silu(g) * u ), silu(g) = g / (1 + e^-g), evaluated in
- * double ("Un Cuantizador Compartido Es el Mecanismo Real": gate and up of a
- * SwiGLU expert are one fused GEMM output).  gu: bf16 [R, 2F]; h: bf16 [R, F]. */
+/* Correctly rounded bf16 of a binary64 value, in one rounding step (no
+ * intermediate binary32): round to nearest, ties to even, or, with
+ * ties_toward_zero, a tie goes to the neighbour of smaller magnitude.
+ * Overflow gives infinity; bf16 subnormals are kept (spacing 2^-133). */
+static uint16_t f64_to_bf16(double v, int ties_toward_zero)
+{
+    if (isnan(v)) return 0x7FC0u;
+    uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return (uint16_t)(sign | 0x7F80u);
+    int e;
+    frexp(a, &e);                    /* a in [2^(e-1), 2^e) */
+    int k = e - 1;
+    if (k < -126) k = -126;          /* below the normal range the spacing stays 2^-133 */
+    double q = ldexp(a, 7 - k);      /* a in units of the bf16 spacing 2^(k-7): exact */
+    double n = floor(q);
+    double rest = q - n;             /* exact */
+    if (rest > 0.5 || (rest == 0.5 && !ties_toward_zero && fmod(n, 2.0) != 0.0)) n += 1.0;
+    double r = ldexp(n, k - 7);
+    if (r >= 0x1p128) return (uint16_t)(sign | 0x7F80u);
+    float f = (float)r;              /* exact: at most 9 significant bits, in binary32 range */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | (u >> 16));
+}
+
+/* h[r, j] = RN_bf16( silu(g) * u ), silu(g) = g / (1 + e^-g): the exact real
+ * value rounded once to bf16 ("Un Cuantizador Compartido Es el Mecanismo
+ * Real": gate and up of a SwiGLU expert are one fused GEMM output).
+ * Evaluated in binary64 and rounded directly to bf16.  Where 1 + e^-g == 1
+ * in binary64 (g > 36.7) the quotient would return g*u itself, which can be
+ * a bf16 tie; the exact value g*u*(1 - e^-g/(1 + e^-g)) lies just inside
+ * g*u (less than one binary64 unit), so it rounds like g*u except that a tie
+ * goes toward zero.  g*u is exact in binary64 (two 8-bit significands).
+ * Elsewhere the value is never a tie (silu(g) is transcendental for g != 0)
+ * and the binary64 evaluation is a few units of 2^-53 from it.
+ * gu: bf16 [R, 2F] (gate columns, then up columns); h: bf16 [R, F]. */
 void or_swiglu(const uint16_t *gu, i64 R, i64 F, uint16_t *h)
 {
     for (i64 r = 0; r < R; r++)
         for (i64 j = 0; j < F; j++) {
             double g = (double)or_bf16_to_f32(gu[r * 2 * F + j]);
             double u = (double)or_bf16_to_f32(gu[r * 2 * F + F + j]);
-            double v = g / (1.0 + exp(-g)) * u;
-            h[r * F + j] = or_f32_to_bf16((float)v);
+            double t = exp(-g);
+            if (1.0 + t == 1.0)
+                h[r * F + j] = f64_to_bf16(g * u, 1);
+            else
+                h[r * F + j] = f64_to_bf16(g / (1.0 + t) * u, 0);
         }
 }
