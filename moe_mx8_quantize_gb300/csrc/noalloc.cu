@@ -11,10 +11,18 @@
 // every GPU that loads it: two words per group for up to kNoAllocMaxGroups
 // groups plus a counter and an error word (about 8 KB).  Its device
 // address is looked up once per device, on the first call made with that
-// device current; make that first call before capturing any stream.  Every
-// call shares the one array: its words are cleared at the start of each call,
-// and calls that overlap on the GPU (different streams, or different host
-// threads without ordering) race on it and must be serialised.
+// device current; make that first call before capturing any stream.  The
+// address is kept for the life of the process, so neither entry point may be
+// used on a device after cudaDeviceReset() (the module, and with it the
+// array, is loaded again at a new address).  Every call shares the one
+// array: its scratch words are cleared at the start of each call, and calls
+// that overlap on the GPU (different streams, or different host threads
+// without ordering) race on it and must be serialised.
+//
+// A bounded device wait that runs out (see the workspace entry points)
+// records its code in the array's error word; calls do not clear that word,
+// so nvfp4_noalloc_check_error() reports a timeout of any call made since it
+// was last called, and clears it.
 #include <mutex>
 
 #include "mx8q.h"
@@ -84,4 +92,16 @@ extern "C" mx8_status nvfp4_quantize_per_token_noalloc(const void* x, int64_t ro
                                                  group_offsets, G, q, s_blk, s32, scratch, err, sm_count(),
                                                  reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MX8_OK : MX8_ERR_CUDA;
+}
+
+extern "C" mx8_status nvfp4_noalloc_check_error(mx8_stream_t stream) {
+  uint32_t* scratch = nullptr;
+  if (scratch_address(&scratch) != cudaSuccess) return MX8_ERR_CUDA;
+  int* err = reinterpret_cast<int*>(scratch + kNoAllocWords - 4);
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return MX8_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MX8_ERR_CUDA;
+  if (word == 0) return MX8_OK;
+  if (cudaMemset(err, 0, sizeof(int)) != cudaSuccess) return MX8_ERR_CUDA;
+  return MX8_ERR_TIMEOUT;
 }
