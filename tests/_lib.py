@@ -65,3 +65,24 @@ def grouped_padded_row(offs):
         g = np.searchsorted(offs, rows, side="right") - 1
         return pref[g] + (rows - offs[g])
     return f
+
+
+def swiglu_tolerance(g, ag, u, au, K):
+    """Allowed |h - silu(g) u| for the GPU's h = RN_bf16(silu(g~) u~), where
+    g, u are the FP64 references of the gate and up outputs (ag, au their
+    sums of |a||b|) and g~, u~ the GPU's outputs: each within the GEMM
+    tolerance 1e-5 sum|a||b| + K 2^-126 of its reference, then rounded to
+    bf16 (at most half a unit, 2^-8 relative).  silu has slope in [-0.1,
+    1.1]; silu(g~) u~ in binary32 with expf is within 2^-20 relative of the
+    exact product; the final bf16 rounding adds at most half a unit (2^-8
+    relative) and 2^-134 absolute (half the smallest bf16 subnormal).
+    Returns (the FP64 reference of h, the tolerance)."""
+    eg = 1e-5 * ag + K * 2.0 ** -126
+    eu = 1e-5 * au + K * 2.0 ** -126
+    dg = eg + 2.0 ** -8 * (np.abs(g) + eg)
+    du = eu + 2.0 ** -8 * (np.abs(u) + eu)
+    sil = g / (1.0 + np.exp(-g))
+    h = sil * u
+    prop = 1.1 * (np.abs(u) + du) * dg + np.abs(sil) * du
+    tol = prop + 2.0 ** -8 * (np.abs(h) + prop) + 2.0 ** -20 * np.abs(h) + 2.0 ** -134
+    return h, tol
