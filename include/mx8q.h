@@ -275,15 +275,25 @@ mx8_status nvfp4_quantize_per_token_sr(const void *x, int64_t rows, int64_t cols
  * inside the library (at most 1024 groups; more return MX8_ERR_INVALID_ARG),
  * resident on each GPU that loads the library until the process exits.
  * No allocation of any kind happens in this call.  The first call on a device
- * looks up that array's device address; make it before any stream capture.
- * All calls share the array (cleared at the start of each call), so calls
- * that could run at the same time on the GPU race and must be serialised.
+ * looks up that array's device address; make it before any stream capture,
+ * and do not use this entry point on a device after cudaDeviceReset().
+ * All calls share the array (its scratch is cleared at the start of each
+ * call), so calls that could run at the same time on the GPU race and must
+ * be serialised.  A bounded device wait that runs out is recorded in the
+ * array's error word, which nvfp4_noalloc_check_error() reads.
  * The pages describe no such variant; it exists for this library's callers.
  */
 mx8_status nvfp4_quantize_per_token_noalloc(const void *x, int64_t rows, int64_t cols, int64_t ld,
                                             int scope, const int64_t *group_offsets, int num_groups,
                                             uint8_t *q, uint8_t *s_blk, float *s32,
                                             mx8_stream_t stream);
+
+/* Synchronises the stream, then reads and clears the error word of the
+ * library-owned array that nvfp4_quantize_per_token_noalloc() uses: MX8_OK,
+ * or MX8_ERR_TIMEOUT if a bounded device wait of any such call since the
+ * last check ran out (that call's outputs are then not valid).  Allocates
+ * nothing.  (No counterpart in the pages.) */
+mx8_status nvfp4_noalloc_check_error(mx8_stream_t stream);
 
 /*
  * Dequantization back to f32 or bf16 (the dequantized-backward mode of [MRL]
@@ -387,6 +397,38 @@ mx8_status bs_grouped_gemm_fused(int fmt, int num_groups, const int64_t *group_o
                                  void *workspace, size_t workspace_bytes, mx8_stream_t stream);
 
 /*
+ * The gate|up expert GEMM of a SwiGLU MoE layer with the SwiGLU and the
+ * per-token NVFP4 quantization of its output h fused into the epilogue
+ * ([MRL] "Un Cuantizador Compartido...": the activation quantizer emits the
+ * packed FP4 values, block scales and token scales in one operation, and
+ * gate and up come out of one fused GEMM; "Las Curvas de Recompensa...":
+ * a per-token scale computed as a separate step is what slowed NVFP4).
+ * NVFP4 only, A already dispatched (as bs_grouped_gemm()).  Per row m:
+ *     h = RN_bf16(silu(g) * u)   exactly as bs_grouped_gemm_fused() with
+ *                                MX8_EPI_SWIGLU computes it, and
+ *     q_h, s_h, s32_h = what nvfp4_quantize_per_token(h, NVFP4_SCOPE_TOKEN,
+ *                       group_offsets) writes for h, byte for byte.
+ *   B, SB, B32 : [G, N, K] gate rows [0, F) then up rows [F, 2F) per expert,
+ *                N = 2F, N % 256 == 0 and F <= 1024 (the F / 128 column
+ *                tiles of a 128-row band run as one thread-block cluster,
+ *                which exchanges the rows' maxima; larger F returns
+ *                MX8_ERR_UNSUPPORTED)
+ *   q_h        : uint8 [total_rows, F/2] packed E2M1 codes of h
+ *   s_h        : E4M3 block scales of h in the grouped tile layout,
+ *                mx8_scale_bytes_grouped(NVFP4, total_rows, num_groups, F)
+ *   s32_h      : float [total_rows] S_dec of h
+ *   h, ld_h    : optional bf16 [total_rows, F] copy of h (NULL: h is never
+ *                written to memory)
+ * Requires K % 32 == 0 and 16-byte aligned A, SA, B, SB, q_h, s_h (and h).
+ */
+mx8_status bs_grouped_gemm_swiglu_nvfp4(int num_groups, const int64_t *group_offsets, int64_t total_rows,
+                                        int64_t N, int64_t K, const uint8_t *A, const uint8_t *SA,
+                                        const float *A32, const uint8_t *B, const uint8_t *SB,
+                                        const float *B32, uint8_t *q_h, uint8_t *s_h, float *s32_h,
+                                        void *h, int64_t ld_h, void *workspace, size_t workspace_bytes,
+                                        mx8_stream_t stream);
+
+/*
  * Dense BF16 GEMM on the tcgen05 tensor cores, for the dequantized-backward
  * mode ([MRL] "La Compatibilidad...": the backward GEMMs run in BF16 on
  * operands rebuilt by dequantize() from the low-precision copies, e.g.
@@ -410,8 +452,9 @@ mx8_status bf16_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda
  * ([MRL] "Un Cuantizador Compartido...": SwiGLU experts compute gate and up
  * in one fused GEMM):
  *     h[r, j] = RN_bf16( silu(g) * u ),  g = gate_up[r, j], u = gate_up[r, ffn + j]
- * with silu(g) = g / (1 + exp(-g)) in FP32 (exp from the CUDA math library,
- * so h can differ from a correctly rounded result by one bf16 unit).
+ * with silu(g) = g / (1 + exp(-g)) in FP32 (a few units of 2^-24 from the
+ * exact value before the bf16 rounding, so h can differ from the correctly
+ * rounded result by one bf16 unit).
  *   gate_up : bf16 [rows, 2*ffn], row stride ld_gate_up
  *   h       : bf16 [rows, ffn], row stride ld_h
  * Requires ffn % 8 == 0, 16-byte aligned pointers and strides % 8 == 0.

@@ -33,8 +33,8 @@ EXPORTS = ("mx8_scale_bytes", "mx8_scale_bytes_grouped", "mx8_workspace_bytes",
            "mx8_device_sm_count", "mx8_quantize", "mxfp4_quantize", "nvfp4_quantize_per_token",
            "nvfp4_quantize_dispatch", "nvfp4_quantize_2d", "nvfp4_quantize_rht_colwise",
            "nvfp4_quantize_per_token_sr",
-           "nvfp4_quantize_per_token_noalloc", "dequantize",
-           "bs_gemm", "bs_grouped_gemm", "bs_grouped_gemm_fused", "bf16_gemm", "mx8_moe_combine", "mx8_swiglu", "mx8_check_device_error", "mx8_selftest_bounded_wait",
+           "nvfp4_quantize_per_token_noalloc", "nvfp4_noalloc_check_error", "dequantize",
+           "bs_gemm", "bs_grouped_gemm", "bs_grouped_gemm_fused", "bs_grouped_gemm_swiglu_nvfp4", "bf16_gemm", "mx8_moe_combine", "mx8_swiglu", "mx8_check_device_error", "mx8_selftest_bounded_wait",
            "mx8_status_string")
 
 
@@ -76,6 +76,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.nvfp4_quantize_per_token.argtypes = [_p, _i64, _i64, _i64, _i, _p, _i, _p, _p, _p, _p, _sz, _p]
     lib.nvfp4_quantize_per_token_noalloc.restype = _i
     lib.nvfp4_quantize_per_token_noalloc.argtypes = [_p, _i64, _i64, _i64, _i, _p, _i, _p, _p, _p, _p]
+    lib.nvfp4_noalloc_check_error.restype = _i
+    lib.nvfp4_noalloc_check_error.argtypes = [_p]
     lib.dequantize.restype = _i
     lib.dequantize.argtypes = [_i, _p, _p, _p, _i, _p, _i, _i64, _i64, _i, _p, _p]
     lib.bs_gemm.restype = _i
@@ -96,6 +98,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bs_grouped_gemm_fused.restype = _i
     lib.bs_grouped_gemm_fused.argtypes = [_i, _i, _p, _i64, _i64, _i64, _p, _p, _p, _p, _i64, _p, _p, _p, _i,
                                           _i, _p, _i64, _p, _sz, _p]
+    lib.bs_grouped_gemm_swiglu_nvfp4.restype = _i
+    lib.bs_grouped_gemm_swiglu_nvfp4.argtypes = [_i, _p, _i64, _i64, _i64, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p,
+                                                 _i64, _p, _sz, _p]
     lib.mx8_moe_combine.restype = _i
     lib.mx8_moe_combine.argtypes = [_p, _i64, _i64, _p, _p, _i64, _i64, _i, _i, _p, _i64, _p]
     lib.bf16_gemm.restype = _i
@@ -482,6 +487,35 @@ def bs_grouped_gemm_fused(fmt, group_offsets, A, SA, B, SB, K, A32=None, B32=Non
 
 
 # ---------------------------------------------------------------- MoE combine
+def bs_grouped_gemm_swiglu_nvfp4_into(group_offsets, total_rows, A, SA, B, SB, K, q_h, s_h, s32_h, A32=None,
+                                      B32=None, h=None, ws=None, stream=None):
+    """In-place form of :func:`bs_grouped_gemm_swiglu_nvfp4`."""
+    G = group_offsets.numel() - 1
+    N = B.shape[1]
+    ws = _ws(ws, G, A.device)
+    _check(load().bs_grouped_gemm_swiglu_nvfp4(G, _ptr(group_offsets), total_rows, N, K, _ptr(A), _ptr(SA),
+                                               _ptr(A32), _ptr(B), _ptr(SB), _ptr(B32), _ptr(q_h), _ptr(s_h),
+                                               _ptr(s32_h), _ptr(h), h.stride(0) if h is not None else 0,
+                                               _ptr(ws), ws.numel(), _stream(stream)),
+           "bs_grouped_gemm_swiglu_nvfp4")
+
+
+def bs_grouped_gemm_swiglu_nvfp4(group_offsets, A, SA, B, SB, K, A32=None, B32=None, with_h=False, ws=None,
+                                 stream=None):
+    """gate|up expert GEMM + SwiGLU + per-token NVFP4 of h in one kernel.
+    B: [G, 2F, K/2] (gate rows, then up rows).  Returns (q_h [R, F/2],
+    s_h grouped scale tiles, s32_h [R]) and, with with_h, the bf16 h too."""
+    G = group_offsets.numel() - 1
+    R = A.shape[0]
+    F = B.shape[1] // 2
+    q_h = torch.empty((R, F // 2), dtype=torch.uint8, device=A.device)
+    s_h = _u8(scale_bytes_grouped(FMT_NVFP4, R, G, F), A.device)
+    s32_h = torch.empty(max(R, 1), dtype=torch.float32, device=A.device)
+    h = torch.empty((R, F), dtype=torch.bfloat16, device=A.device) if with_h else None
+    bs_grouped_gemm_swiglu_nvfp4_into(group_offsets, R, A, SA, B, SB, K, q_h, s_h, s32_h, A32, B32, h, ws, stream)
+    return (q_h, s_h, s32_h, h) if with_h else (q_h, s_h, s32_h)
+
+
 def moe_combine_into(y, rows_of_slot, weights, out, stream=None):
     """out [T, H] = sum_j weights[t, j] * y[rows_of_slot[t, j]] (binary32, j
     in order); y bf16 [R, H]; out f32 or bf16."""

@@ -469,6 +469,57 @@ extern "C" mx8_status bs_grouped_gemm_fused(int fmt, int num_groups, const int64
   return from_cuda(launch_bs_gemm(a, ma, mb, mc, sm_count_current(), s));
 }
 
+// ===================================================================== gate|up + SwiGLU + NVFP4 of h
+extern "C" mx8_status bs_grouped_gemm_swiglu_nvfp4(int num_groups, const int64_t* group_offsets, int64_t total_rows,
+                                                   int64_t N, int64_t K, const uint8_t* A, const uint8_t* SA,
+                                                   const float* A32, const uint8_t* B, const uint8_t* SB,
+                                                   const float* B32, uint8_t* q_h, uint8_t* s_h, float* s32_h,
+                                                   void* h, int64_t ld_h, void* workspace, size_t workspace_bytes,
+                                                   mx8_stream_t stream) {
+  if (num_groups < 1 || num_groups > kMaxGroups || group_offsets == nullptr || total_rows < 0)
+    return MX8_ERR_INVALID_ARG;
+  if (N < 0 || N % 256 != 0) return MX8_ERR_INVALID_ARG;
+  const int64_t F = N / 2;
+  if (F / 128 > 8) return MX8_ERR_UNSUPPORTED;          // h tiles of a band = CTAs of one cluster
+  if (h != nullptr && ld_h < F) return MX8_ERR_INVALID_ARG;
+  if (total_rows == 0 || N == 0) return MX8_OK;
+  if (K <= 0 || K % 32 != 0) return MX8_ERR_INVALID_ARG;
+  if (A == nullptr || SA == nullptr || B == nullptr || SB == nullptr || q_h == nullptr || s_h == nullptr ||
+      s32_h == nullptr)
+    return MX8_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(SA) || !aligned16(B) || !aligned16(SB) || !aligned16(q_h) || !aligned16(s_h) ||
+      (reinterpret_cast<uintptr_t>(s32_h) & 3u) != 0 || (h != nullptr && (!aligned16(h) || ld_h % 8 != 0)))
+    return MX8_ERR_ALIGNMENT;
+  if (total_rows > INT32_MAX || N > INT32_MAX) return MX8_ERR_UNSUPPORTED;
+  mx8_status st = check_ws(workspace, workspace_bytes, num_groups);
+  if (st != MX8_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const uint64_t kbytes = K / 2;
+  CUtensorMap ma, mb, mc;
+  const uint32_t box2[2] = {kGemmKBytes, 128};
+  const uint64_t da[2] = {kbytes, static_cast<uint64_t>(total_rows)}, sa[1] = {kbytes};
+  const uint32_t box3[3] = {kGemmKBytes, 128, 1};
+  const uint64_t db[3] = {kbytes, static_cast<uint64_t>(N), static_cast<uint64_t>(num_groups)};
+  const uint64_t sb[2] = {kbytes, kbytes * static_cast<uint64_t>(N)};
+  // the output map is not used by this epilogue (h leaves with plain stores);
+  // it is encoded over h, or over the codes of h, so the kernel's tensor-map
+  // prefetch sees a valid map
+  const bool map_ok = h != nullptr ? encode_output_map(&mc, h, total_rows, F, ld_h, MX8_OUT_BF16)
+                                   : encode_output_map(&mc, q_h, total_rows, F / 4, F / 4, MX8_OUT_BF16);
+  if (!encode_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, A, da, sa, box2, gemm_swizzle()) ||
+      !encode_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, B, db, sb, box3, gemm_swizzle()) || !map_ok)
+    return MX8_ERR_CUDA;
+  GemmArgs a{};
+  a.fmt = MX8_FMT_NVFP4; a.M = total_rows; a.N = N; a.K = K;
+  a.SA = SA; a.SB = SB; a.A32 = A32; a.a32_mode = A32 ? MX8_S32_ROW : MX8_S32_NONE;
+  a.B32 = B32; a.b32_mode = B32 ? MX8_S32_GROUP : MX8_S32_NONE;
+  a.C = h; a.ldc = h != nullptr ? ld_h : F; a.out_bf16 = 1; a.accumulate = 0;
+  a.grouped = 1; a.G = num_groups; a.offs = group_offsets; a.err = err_word(workspace);
+  a.A = A; a.a_rows = nullptr; a.a_src_rows = 0; a.ffn = F;
+  a.qh = q_h; a.qh_scales = s_h; a.qh_s32 = s32_h;
+  return from_cuda(launch_bs_gemm(a, ma, mb, mc, sm_count_current(), s));
+}
+
 // ===================================================================== BF16 GEMM
 extern "C" mx8_status bf16_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
                                 const void* B, int64_t ldb, int out_dtype, void* C, int64_t ldc,

@@ -126,8 +126,17 @@ struct Cfg<2> {                 // MXFP4: 2 elements per byte, 64 elements (2 sc
 //                 token map, so tokens are quantized once, before dispatch;
 //   kModeSwiGLU : B holds gate rows [0, F) and up rows [F, 2F) per expert; a
 //                 tile pairs gate rows n0.. and up rows F + n0.. (128 each),
-//                 and the epilogue writes h = silu(g) * u for 128 columns.
-constexpr int kModeGather = 1, kModeSwiGLU = 2;
+//                 and the epilogue writes h = silu(g) * u for 128 columns;
+//   kModeQuantH : (with kModeSwiGLU) the epilogue also quantizes h per token
+//                 to NVFP4.  The F / 128 tiles of a 128-row band are computed
+//                 at the same time by the CTAs of one thread-block cluster
+//                 (CTA rank = h tile); each CTA sends the row maxima of its
+//                 128 h columns to every CTA of the cluster (distributed
+//                 shared memory), so every CTA knows each row's amax, and
+//                 encodes its own columns from registers: codes, block scales
+//                 and S_dec of h, with no bf16 h round trip through memory.
+constexpr int kModeGather = 1, kModeSwiGLU = 2, kModeQuantH = 4;
+constexpr int kMaxClusterTiles = 8;          // h tiles of a band = CTAs of a cluster (portable maximum)
 
 template <int kFmt, bool kGrouped, int kBN, int kMode>
 struct Layout {
@@ -138,7 +147,7 @@ struct Layout {
   static constexpr int kSfbBytes = Cfg<kFmt>::kSfTiles > 0 ? Cfg<kFmt>::kSfTiles * 512 * kBRow128 : 16;
   static constexpr int kStageBytes = kTileABytes + kTileBBytes + kSfaBytes + kSfbBytes;
   static constexpr int kEpiStageBytes = 2048;                         // 32 rows x 64 B per epilogue warp
-  static constexpr int kFixed = 256 + (kBN / 32) * kEpiStageBytes +
+  static constexpr int kFixed = 256 + (kBN / 32) * kEpiStageBytes + ((kMode & kModeQuantH) ? 1024 + 32 : 0) +
                                 (kGrouped ? static_cast<int>(sizeof(GroupSmem)) : 0);
   static constexpr int kStagesFit = (kSmemBudget - kFixed) / kStageBytes;
   static constexpr int kStages = kStagesFit > 10 ? 10 : kStagesFit;
@@ -155,6 +164,12 @@ struct Layout {
   static constexpr int kThreads = 64 + 32 * kEpiWarps + 32 * kBRow128;
   static_assert(kStages >= 3, "pipeline too shallow");
   static_assert(!(kMode & kModeSwiGLU) || kBN == 256, "the SwiGLU epilogue pairs two 128-row boxes");
+  static_assert(!(kMode & kModeQuantH) || ((kMode & kModeSwiGLU) && !(kMode & kModeGather)),
+                "h is quantized in the SwiGLU epilogue of dispatched rows");
+  // h quantization: the row maxima of a band, [2 buffers][2 halves x tiles][128 rows] floats,
+  // live in the epilogue staging area (the SwiGLU epilogue stores h directly)
+  static_assert(!(kMode & kModeQuantH) || kEpiWarps * kEpiStageBytes >= 2 * 2 * kMaxClusterTiles * 128 * 4,
+                "row-maximum exchange does not fit the staging area");
   static_assert(kAccCols + kStages * kSfColsPerStage <= kTmemCols, "tensor memory overflow");
 };
 
@@ -176,6 +191,8 @@ struct __align__(1024) GemmSmem {
   uint32_t tmem_base;
   int abort;
   int32_t gtok[BM];                                   // gathered mode: source rows of the tile
+  uint64_t hmax_full[2];                              // h quantization: a band's row maxima are all in
+  float2 tab[(kMode & kModeQuantH) ? 128 : 1];        // h quantization: {E4M3 value, RN(1/value)}
 };
 
 // Instruction descriptor of the block-scaled MMA (M = 128, both operands
@@ -246,6 +263,21 @@ __device__ __forceinline__ TileCoord decode_tile(int64_t t, int64_t tiles_n, int
   return c;
 }
 
+// Grouped band gmt (a 128-row tile of the padded grouped layout) and h tile
+// nt of the cluster mode.
+__device__ __forceinline__ TileCoord decode_band(int64_t gmt, int nt, const GroupSmem* gs, int G) {
+  TileCoord c;
+  const int g = upper_group(gs->pref, G, gmt * BM);
+  const int64_t mt = gmt - gs->pref[g] / BM;
+  const int64_t ng = gs->offs[g + 1] - gs->offs[g];
+  c.g = g;
+  c.a_row0 = gs->offs[g] + mt * BM;
+  c.rows = ng - mt * BM < BM ? ng - mt * BM : BM;
+  c.sfa_tile = gmt;
+  c.n0 = static_cast<int64_t>(nt) * 128;
+  return c;
+}
+
 template <int kFmt, bool kGrouped, int kBN, int kMode>
 __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 1)
     bs_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -256,6 +288,7 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
   using Smem = GemmSmem<kFmt, kGrouped, kBN, kMode>;
   constexpr bool kGather = (kMode & kModeGather) != 0;
   constexpr bool kSwiGLU = (kMode & kModeSwiGLU) != 0;
+  constexpr bool kQuantH = (kMode & kModeQuantH) != 0;
   // scales moved into tensor memory by the epilogue warps (else tcgen05.cp)
   constexpr bool kWarpScales = F::kSfTiles > 0 && !kGrouped;
   static_assert(kGather <= kGrouped && kSwiGLU <= kGrouped, "fused modes are grouped only");
@@ -283,9 +316,16 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
       mbar_init(smem_u32(&sm.acc_empty[i]), kEpiThreads);
     }
     mbar_init(smem_u32(&sm.drain), 1);
+    if (kQuantH) {
+      // every epilogue warp of every CTA of the cluster arrives once per band
+      uint32_t nct;
+      asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(nct));
+      for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&sm.hmax_full[i]), L::kEpiWarps * nct);
+    }
     sm.abort = 0;
     fence_barrier_init();
   }
+  if (kQuantH) nvfp4_init_scale_table(sm.tab);
   if (warp == 1) {
     tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
     tmem_relinquish();
@@ -295,6 +335,9 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+  // the other CTAs of the cluster send row maxima to this CTA's barriers:
+  // they must be initialised everywhere first
+  if (kQuantH) cluster_sync_all();
 
   const int64_t M = args.M, N = args.N, K = args.K;
   // output columns per tile: BN, or 128 h columns (from 128 gate + 128 up rows of B)
@@ -304,9 +347,15 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
   const int64_t tiles_n = (n_out + kNT - 1) / kNT;
   const int64_t n_rt = (N + 127) / 128;                   // 128-row scale tiles of B (per group)
   const int64_t tiles_m = kGrouped ? gs->pref[args.G] / BM : (M + BM - 1) / BM;
-  const int64_t nunits = tiles_m * tiles_n;          // output tiles, strided over the CTAs
-  const int64_t unit0 = blockIdx.x, ustep = gridDim.x;
-  auto tile_of = [&](int64_t u) { return decode_tile<kGrouped, kNT>(u, tiles_n, M, gs, args.G); };
+  // output tiles strided over the CTAs; with h quantization, 128-row bands
+  // strided over the clusters, CTA rank r of a cluster taking h tile r
+  const int64_t nunits = kQuantH ? tiles_m : tiles_m * tiles_n;
+  const int64_t unit0 = kQuantH ? cluster_id_x() : blockIdx.x;
+  const int64_t ustep = kQuantH ? cluster_count_x() : gridDim.x;
+  const int ctile = kQuantH ? static_cast<int>(cluster_ctarank()) : 0;
+  auto tile_of = [&](int64_t u) {
+    return kQuantH ? decode_band(u, ctile, gs, args.G) : decode_tile<kGrouped, kNT>(u, tiles_n, M, gs, args.G);
+  };
   // first B row (within the group) of 128-row box h of a tile
   auto b_row0 = [&](const TileCoord& tc, int h) -> int64_t {
     return kSwiGLU ? tc.n0 + h * F_ : tc.n0 + h * 128;
@@ -667,7 +716,7 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
       // the two FP32 decode scales are combined first: acc * A32 alone can
       // overflow for tokens whose amax is near the bf16 maximum
       const float s_ab = __fmul_rn(sa, sg);
-      if constexpr (kSwiGLU) {
+      if constexpr (kSwiGLU && !kQuantH) {
         // g and u rounded to bf16 exactly as the unfused gate|up output would
         // be, then h = RN_bf16(silu(g) * u): 64 columns, 128 contiguous bytes
         if (!row_ok) continue;
@@ -688,6 +737,83 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
             p[j] = pack_bf16x2(hv[0], hv[1]);
           }
           hrow[q8] = make_uint4(p[0], p[1], p[2], p[3]);
+        }
+        continue;
+      }
+      if constexpr (kQuantH) {
+        // as above, the 64 columns kept as bf16 pairs (column 2j in the low
+        // half of hp[j]; the bf16 h also stored when C is given), then
+        // quantized
+        uint32_t hp[32];
+        uint4* hrow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.C) + m * args.ldc + tc.n0 + 64 * half);
+        const bool store_h = row_ok && args.C != nullptr;
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float hv[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int c = q8 * 8 + j * 2 + e;
+              const float g = bf16_round(__fmul_rn(__uint_as_float(r[c >> 5][c & 31]), s_ab));
+              const float uu = bf16_round(__fmul_rn(__uint_as_float(r[2 + (c >> 5)][c & 31]), s_ab));
+              hv[e] = silu_mul(g, uu);
+            }
+            hp[4 * q8 + j] = pack_bf16x2(hv[0], hv[1]);
+          }
+          if (store_h) hrow[q8] = make_uint4(hp[4 * q8], hp[4 * q8 + 1], hp[4 * q8 + 2], hp[4 * q8 + 3]);
+        }
+        {
+          // Per-token NVFP4 of h.  This thread's row maximum over its 64
+          // columns goes to slot (tile, half) of every CTA of the cluster;
+          // once all 2 x tiles maxima of the band's rows are in (barrier of
+          // this band's buffer), each row's amax gives S_enc and the thread
+          // encodes its 4 blocks of 16.  Two buffers alternate between
+          // bands: a CTA can only send band b + 2's maxima after receiving
+          // everyone's band b + 1 maxima, which each sends after it has read
+          // band b's buffer.
+          uint32_t mx2 = 0;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) mx2 = amax2(mx2, hp[j]);
+          const float hmax = abs_halves_max(mx2);
+          const int buf = tcount & 1;
+          const int ntile = static_cast<int>(F_ / 128);
+          float* red = reinterpret_cast<float*>(&sm.cstage[0][0]) + buf * (2 * kMaxClusterTiles * 128);
+          const uint32_t slot = smem_u32(red + (2 * ctile + half) * 128 + r_in_tile);
+#pragma unroll 1
+          for (int p = 0; p < ntile; ++p) st_cluster_u32(mapa_shared(slot, static_cast<uint32_t>(p)), __float_as_uint(hmax));
+          __syncwarp();
+          const uint32_t bar = smem_u32(&sm.hmax_full[buf]);
+          if (lane == 0) {
+#pragma unroll 1
+            for (int p = 0; p < ntile; ++p) mbar_arrive_cluster(mapa_shared(bar, static_cast<uint32_t>(p)));
+          }
+          if (!__all_sync(0xffffffffu, mbar_wait_cluster(bar, (tcount >> 1) & 1, err, kErrWaitCluster, &sm.abort)))
+            break;
+          float amax = 0.f;
+#pragma unroll 1
+          for (int sl = 0; sl < 2 * ntile; ++sl) amax = fmaxf(amax, red[sl * 128 + r_in_tile]);
+          float senc, sdec;
+          nvfp4_scales(amax, senc, sdec);
+          uint2 cw[4];
+          uint32_t sw = 0;
+#pragma unroll
+          for (int bk = 0; bk < 4; ++bk) {
+            const uint4 a = make_uint4(hp[8 * bk], hp[8 * bk + 1], hp[8 * bk + 2], hp[8 * bk + 3]);
+            const uint4 b = make_uint4(hp[8 * bk + 4], hp[8 * bk + 5], hp[8 * bk + 6], hp[8 * bk + 7]);
+            sw |= nvfp4_encode_block(a, b, senc, sm.tab, cw[bk]) << (8 * bk);
+          }
+          // scale word of h's 4-block group (tc.n0 + 64 half) / 64 in scale row
+          // (band, row): zero for the padding rows of a group's last band
+          const int64_t srow = tc.sfa_tile * BM + r_in_tile;
+          const int64_t k4 = (tc.n0 + 64 * half) / 64;
+          *reinterpret_cast<uint32_t*>(args.qh_scales + sf_row_base(srow, F_ / 64) + k4 * 512) = row_ok ? sw : 0u;
+          if (row_ok) {
+            uint4* qrow = reinterpret_cast<uint4*>(args.qh + m * (F_ / 2) + (tc.n0 + 64 * half) / 2);
+            qrow[0] = make_uint4(cw[0].x, cw[0].y, cw[1].x, cw[1].y);
+            qrow[1] = make_uint4(cw[2].x, cw[2].y, cw[3].x, cw[3].y);
+            if (ctile == 0 && half == 0) args.qh_s32[m] = sdec;
+          }
         }
         continue;
       }
@@ -792,6 +918,8 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // no CTA of a cluster leaves while another may still write to its shared memory
+  if (kQuantH) cluster_sync_all();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -814,12 +942,67 @@ cudaError_t launch_variant(const GemmArgs& a, const CUtensorMap& tmap_a, const C
   return cudaGetLastError();
 }
 
+// The SwiGLU grouped GEMM with h quantized: clusters of F / 128 CTAs (one per
+// h tile of a band), as many clusters as can be resident at once (each
+// persistent over the bands).
+cudaError_t launch_quant_h(const GemmArgs& a, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                           const CUtensorMap& tmap_c, cudaStream_t stream) {
+  constexpr int kMode = kModeSwiGLU | kModeQuantH;
+  using L = Layout<1, true, 256, kMode>;
+  const int cs = static_cast<int>(a.ffn / 128);
+  if (cs < 1 || cs > kMaxClusterTiles || a.ffn % 128 != 0) return cudaErrorInvalidValue;
+  auto k = bs_gemm_kernel<1, true, 256, kMode>;
+  constexpr size_t smem = sizeof(GemmSmem<1, true, 256, kMode>) + sizeof(GroupSmem) + 1024;
+  static_assert(smem <= 227 * 1024, "shared memory over the per-block limit");
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(L::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // clusters that fit on the GPU at once (cached per device and cluster size)
+  static int cache[64][kMaxClusterTiles + 1] = {};
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (cache[dev][cs] == 0) {
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(static_cast<unsigned>((sms / cs) * cs), 1, 1);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, k, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    cache[dev][cs] = n;
+  }
+  const int64_t bands = (a.M + BM - 1) / BM + a.G;     // upper bound: every group pads a band
+  const int64_t ncl = bands < cache[dev][cs] ? bands : cache[dev][cs];
+  if (ncl == 0) return cudaSuccess;
+  cfg.gridDim = dim3(static_cast<unsigned>(ncl * cs), 1, 1);
+  e = cudaLaunchKernelEx(&cfg, k, tmap_a, tmap_b, tmap_c, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_bs_gemm(const GemmArgs& a, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                            const CUtensorMap& tmap_c, int sm_count, cudaStream_t stream) {
   constexpr int BN = MX8Q_GEMM_BN;
   const int mode = (a.a_rows != nullptr ? kModeGather : 0) | (a.ffn > 0 ? kModeSwiGLU : 0);
+  if (a.qh != nullptr) {
+    if (mode != kModeSwiGLU || a.fmt != 1 || !a.grouped || BN != 256) return cudaErrorInvalidValue;
+    return launch_quant_h(a, tmap_a, tmap_b, tmap_c, stream);
+  }
   if (mode != 0) {
     // fused MoE modes: NVFP4 grouped only
     if (a.fmt != 1 || !a.grouped || BN != 256) return cudaErrorInvalidValue;

@@ -165,7 +165,8 @@ cudaError_t launch_dequant(int fmt, const uint8_t* q, const uint8_t* s, const fl
 // the two halves of one fused GEMM output ("Un Cuantizador Compartido Es el
 // Mecanismo Real": SwiGLU experts compute gate and up in one fused GEMM).
 //   h[r, j] = RN_bf16( silu(g) * u ),  silu(g) = g / (1 + exp(-g)),
-//   g = gu[r, j], u = gu[r, F + j]; f32 arithmetic, exp from CUDA's expf,
+//   g = gu[r, j], u = gu[r, F + j]; f32 arithmetic (silu_mul: e^-|g| from
+//   ex2.approx with a split argument, the reciprocal refined by Newton),
 //   evaluated as g*e^-|g|/(1+e^-|g|) for negative g so nothing overflows.
 namespace {
 __global__ void __launch_bounds__(kThreads) swiglu_kernel(const uint16_t* __restrict__ gu, int64_t R,

@@ -93,11 +93,17 @@ struct GemmArgs {
   const int64_t* a_rows;   // gathered mode: token of each dispatched row [M]
   int64_t a_src_rows;      // gathered mode: rows of the token-major A
   int64_t ffn;             // SwiGLU mode: F (up rows of B start at F; output has F columns)
+  // SwiGLU mode with h quantized per token to NVFP4 (C, the bf16 h, optional)
+  uint8_t* qh;             // [M, F/2] packed E2M1 codes of h
+  uint8_t* qh_scales;      // E4M3 block scales of h, grouped tile layout
+  float* qh_s32;           // [M] S_dec of h
   int* err;
 };
 
 // tmap_c: the output [rows, N] as a 2-D map with a box of 64 bytes x 32 rows
 // (element type of the output), used for the epilogue's bulk stores.
+// (qh set: the SwiGLU grouped GEMM with h quantized, launched as clusters of
+// F / 128 CTAs; F / 128 must be 1 .. 8)
 cudaError_t launch_bs_gemm(const GemmArgs& a, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                            const CUtensorMap& tmap_c, int sm_count, cudaStream_t stream);
 

@@ -71,15 +71,6 @@ constexpr int kItemRows = 32;                 // rows (or scale rows) per work i
 constexpr int64_t kL2LeadBytes = 32ll << 20;  // input bytes between a group's amax and encode items
 
 
-// {E4M3 value, RN(1 / value)} per E4M3 code; {0, 0} for code 0.
-__device__ __forceinline__ void init_scale_table(float2* tab) {
-  for (int c = threadIdx.x; c < 128; c += blockDim.x) {
-    const float b = e4m3_to_f32(static_cast<uint32_t>(c));
-    tab[c] = make_float2(b, c == 0 ? 0.f : __frcp_rn(b));
-  }
-}
-
-
 __device__ __forceinline__ uint4 ld_nc(const uint16_t* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));
 }
@@ -102,12 +93,6 @@ __device__ __forceinline__ uint4 ld_hint(const uint16_t* p, uint64_t pol) {
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p), "l"(pol));
   return r;
-}
-
-// Scale-tile byte offset of scale row sr's first 4-scale word; the word of
-// scale columns k4*4..+3 is 512 * k4 bytes further.
-__device__ __forceinline__ int64_t sf_row_base(int64_t sr, int64_t kt) {
-  return (sr >> 7) * kt * 512 + (sr & 31) * 16 + ((sr >> 5) & 3) * 4;
 }
 
 template <bool kHint>
@@ -160,24 +145,9 @@ template <typename Out>
 __device__ __forceinline__ void encode_chunk(const uint4& a, const uint4& b, int j, int C, int lane, float senc,
                                              const float2* __restrict__ tab, const Out& out, int kt) {
   const int c = j * 512 + lane * 16;
-  const float bmax = abs_halves_max(absmax16(a, b));
-  constexpr float kInv6 = 1.0f / 6.0f;                     // RN(1/6)
-  float q = __fmul_rn(bmax, kInv6);
-  q = __fmaf_rn(__fmaf_rn(-q, 6.0f, bmax), kInv6, q);      // RN(bmax / 6)
-  const uint32_t sb = cvt_e4m3x2(__fmul_rn(q, senc), 0.0f) & 0xFFu;
-  const float2 by = tab[sb & 127u];
-  const float q0 = __fmul_rn(senc, by.y);
-  const float r = fminf(__fmaf_rn(__fmaf_rn(-q0, by.x, senc), by.y, q0), FLT_MAX);   // min(RN(senc / sb), FLT_MAX); 0 for sb = 0
-  const uint64_t rr = (static_cast<uint64_t>(__float_as_uint(r)) << 32) | __float_as_uint(r);
-  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-  float v0[8], v1[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    mul_bf16x2(w[i], rr, v0[2 * i], v0[2 * i + 1]);
-    mul_bf16x2(w[4 + i], rr, v1[2 * i], v1[2 * i + 1]);
-  }
-  const uint32_t p0 = cvt_e2m1x8(v0), p1 = cvt_e2m1x8(v1);
-  if (c < C) out.codes(c >> 1, make_uint2(p0, p1));
+  uint2 cw;
+  const uint32_t sb = nvfp4_encode_block(a, b, senc, tab, cw);
+  if (c < C) out.codes(c >> 1, cw);
   const uint32_t s1 = __shfl_down_sync(0xffffffffu, sb, 1);
   const uint32_t s2 = __shfl_down_sync(0xffffffffu, sb, 2);
   const uint32_t s3 = __shfl_down_sync(0xffffffffu, sb, 3);
@@ -350,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, kCh >= 8 || kCh == 0 ? 1 : 4) nvfp4_
   extern __shared__ __align__(16) uint8_t smem_raw[];
   GroupSmem& gs = *reinterpret_cast<GroupSmem*>(smem_raw);
   __shared__ float2 tab[128];
-  init_scale_table(tab);
+  nvfp4_init_scale_table(tab);
   __syncthreads();
   const bool grouped = offs != nullptr;
   int64_t TP;
@@ -435,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, kCh >= 8 || kCh == 0 ? 1 : 4) nvfp4_
   __shared__ float2 tab[128];
   __shared__ int64_t dsr[kWarps][kMaxTopk];          // copies' scale rows ...
   __shared__ int64_t ddr[kWarps][kMaxTopk];          // ... and dispatched rows, for a warp's token
-  init_scale_table(tab);
+  nvfp4_init_scale_table(tab);
   __syncthreads();
   load_group_prefix(gs, offs, G);
   const int64_t R = gs.offs[G], TP = gs.pref[G];
@@ -536,7 +506,7 @@ __global__ void __launch_bounds__(kScopedThreads, kCh >= 8 || kCh == 0 ? 1 : 4) 
   uint32_t* done = scratch + scratch_gp(Gs);
   unsigned long long* ticket = reinterpret_cast<unsigned long long*>(scratch + 2 * scratch_gp(Gs));
 
-  init_scale_table(sm.tab);
+  nvfp4_init_scale_table(sm.tab);
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sm.filled[i]), 1);

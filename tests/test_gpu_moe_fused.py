@@ -14,7 +14,7 @@ import torch
 import oracle
 import moe_mx8_quantize_gb300 as mx
 from moe_mx8_quantize_gb300 import inputs
-from tests._lib import ensure_built, gemm_tolerance_ok, host, dev
+from tests._lib import ensure_built, gemm_tolerance_ok, host, dev, swiglu_tolerance
 
 pytestmark = pytest.mark.gpu
 
@@ -95,19 +95,6 @@ def test_gathered_grouped_gemm(T, H, E, N, topk, zipf):
     _check(y.ravel(), ref, absref, K=H)
 
 
-def _h_tolerance(g, ag, u, au, K):
-    """|h - silu(g) u| allowed: each GEMM output within 1e-5 sum|a||b| +
-    K 2^-126 and then rounded to bf16 (2^-8 relative, generously); silu has
-    slope in [-0.1, 1.1]; h itself is rounded to bf16 and silu/expf in FP32
-    add a few FP32 units."""
-    dg = 1e-5 * ag + K * 2.0 ** -126 + 2.0 ** -8 * np.abs(g)
-    du = 1e-5 * au + K * 2.0 ** -126 + 2.0 ** -8 * np.abs(u)
-    sil = g / (1.0 + np.exp(-g))
-    h = sil * u
-    tol = 1.1 * (np.abs(u) + du) * dg + (np.abs(sil) + 1.1 * dg) * du + 2.0 ** -7 * np.abs(h) + 1e-30
-    return h, tol
-
-
 @pytest.mark.parametrize("gather", [True, False])
 @pytest.mark.parametrize("T,H,E,F,topk", [(64, 256, 5, 128, 2), (200, 512, 9, 256, 4)])
 def test_swiglu_epilogue(gather, T, H, E, F, topk):
@@ -129,7 +116,7 @@ def test_swiglu_epilogue(gather, T, H, E, F, topk):
     pu = pg + np.array([0, F])
     g, ag = oracle.grouped_gemm_ref(1, offs, A, SA, B, SB, H, ad, b32, pg)
     u, au = oracle.grouped_gemm_ref(1, offs, A, SA, B, SB, H, ad, b32, pu)
-    href, tol = _h_tolerance(g, ag, u, au, H)
+    href, tol = swiglu_tolerance(g, ag, u, au, H)
     err = np.abs(hh.ravel() - href)
     bad = np.nonzero(err > tol)[0]
     assert bad.size == 0, f"{bad.size} h values out of tolerance, e.g. {hh.ravel()[bad[:4]]} vs {href[bad[:4]]}"
@@ -158,3 +145,47 @@ def test_moe_combine_bit_exact(T, H, E, topk, out_dtype):
         assert np.array_equal(host(out).view(np.uint32), ref.view(np.uint32))
     else:
         assert np.array_equal(host(out), oracle.f32_to_bf16(ref))
+
+
+@pytest.mark.parametrize("T,H,E,F,topk", [(64, 256, 5, 128, 2), (200, 512, 9, 256, 4), (150, 256, 4, 768, 3),
+                                          (90, 512, 6, 1024, 2)])
+def test_swiglu_quantized_h_bit_exact(T, H, E, F, topk):
+    """gate|up GEMM + SwiGLU + per-token NVFP4 of h in one kernel (clusters of
+    F / 128 CTAs exchanging row maxima): h equals the SwiGLU epilogue's, and
+    the codes, block scales (grouped layout, padding zero) and S_dec of h
+    equal the oracle's per-token quantization of that h byte for byte -- and
+    the separate GPU quantizer's.  Without the h output the bytes are the
+    same."""
+    N = 2 * F
+    offs, tor, _, Aq, SAq, a32, B, SB, b32 = _case(T, H, E, N, topk, seed=T + F + 3, zipf=True)
+    A, SA, ad = _dispatched(tor, Aq, SAq, a32)
+    go = torch.tensor(offs, dtype=torch.int64, device="cuda")
+    sa, sbw = dev(oracle.swizzle_scales(SA, offs)), dev(oracle.swizzle_scales(SB, np.arange(E + 1) * N))
+    h_ref = mx.bs_grouped_gemm_fused(mx.FMT_NVFP4, go, dev(A), sa, dev(B), sbw, H, dev(ad), dev(b32),
+                                     epilogue=mx.EPI_SWIGLU)
+    qh, sh, s32h, h = mx.bs_grouped_gemm_swiglu_nvfp4(go, dev(A), sa, dev(B), sbw, H, dev(ad), dev(b32), with_h=True)
+    assert torch.equal(h.view(torch.int16), h_ref.view(torch.int16))
+    hq, hs, hd = oracle.nvfp4_quantize(host(h))
+    assert np.array_equal(host(qh), hq)
+    assert np.array_equal(host(s32h).view(np.uint32), hd.view(np.uint32))
+    sw = oracle.swizzle_scales(hs, offs)
+    assert np.array_equal(host(sh)[: sw.size], sw)
+    gq, gs, g32 = mx.nvfp4_quantize_per_token(h, group_offsets=go)
+    assert torch.equal(gq, qh) and torch.equal(g32.view(torch.int32), s32h.view(torch.int32))
+    assert torch.equal(gs[: sw.size], sh[: sw.size])
+    qh2, sh2, s32h2 = mx.bs_grouped_gemm_swiglu_nvfp4(go, dev(A), sa, dev(B), sbw, H, dev(ad), dev(b32))
+    assert torch.equal(qh2, qh) and torch.equal(sh2[: sw.size], sh[: sw.size])
+    assert torch.equal(s32h2.view(torch.int32), s32h.view(torch.int32))
+
+
+def test_swiglu_quantized_h_rejects_wide_ffn():
+    """More than 8 h tiles per band (F > 1024) do not fit one cluster."""
+    E, F, H = 2, 1152, 256
+    go = torch.tensor([0, 10, 20], dtype=torch.int64, device="cuda")
+    A = torch.zeros((20, H // 2), dtype=torch.uint8, device="cuda")
+    SA = torch.zeros(mx.scale_bytes_grouped(mx.FMT_NVFP4, 20, E, H), dtype=torch.uint8, device="cuda")
+    B = torch.zeros((E, 2 * F, H // 2), dtype=torch.uint8, device="cuda")
+    SB = torch.zeros(mx.scale_bytes(mx.FMT_NVFP4, E * 2 * F, H), dtype=torch.uint8, device="cuda")
+    with pytest.raises(mx.Mx8Error) as ei:
+        mx.bs_grouped_gemm_swiglu_nvfp4(go, A, SA, B, SB, H)
+    assert ei.value.status == mx.ERR_UNSUPPORTED
