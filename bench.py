@@ -13,8 +13,9 @@ One step = every operation of the hot path, on seeded synthetic inputs:
     per-token activation quantization of the 4096 tokens (each token encoded
     once, before dispatch, and written to its 8 dispatched rows), per-expert
     weight quantization (gate|up joint), the gate|up grouped GEMM with SwiGLU
-    in its epilogue, per-token quantization of h, down grouped GEMM, and the
-    combine of each token's 8 expert outputs weighted by its router weights.
+    and the per-token NVFP4 quantization of h in its epilogue, the down
+    grouped GEMM, and the combine of each token's 8 expert outputs weighted
+    by its router weights.
 
 value = block-scaled GEMM FLOPs of the step / step time (quantizers,
 dequantization and SwiGLU included in the time).  Per-kernel times come from
@@ -23,10 +24,12 @@ layer in MXFP4 (E2M1 x 32 blocks, E8M0 scales), its dequantized-backward mode
 (dequantize + dense BF16 Dgrad / Wgrad) and its NVFP4 pretraining-recipe
 variant (2-D weight blocks, random Hadamard transform on the Wgrad inputs,
 stochastic rounding of gradients) are timed beside the step, per kernel,
-under "extra".
+under "extra", and so are the DeepSeek-V3-shaped MoE layer (its own step, with
+its MXFP8 shared expert) and the quantizer bandwidth sweep (2^20 .. 2^30
+elements).
 
-`--impl reference` times the CPU oracle (test infrastructure, single thread)
-on a bounded sample of the same step and extrapolates to the full step.
+`--impl reference` times the CPU oracle (test infrastructure) on all host
+cores on a bounded sample of the same step and extrapolates to the full step.
 """
 from __future__ import annotations
 
@@ -123,6 +126,119 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------- the step
+class MoeLayer:
+    """One routed-expert layer with per-token NVFP4, resident in HBM: the
+    tokens encoded once before dispatch and written to their top-k
+    dispatched rows, per-expert weight quantization (gate|up joint), the
+    gate|up grouped GEMM with SwiGLU in its epilogue, per-token quantization
+    of h, the down grouped GEMM, and the router-weighted combine back to token
+    order.  Routing (top-k ids -> expert offsets and row maps) is set-up."""
+
+    # fused: h is quantized in the gate|up GEMM's epilogue (one thread-block
+    # cluster per 128-row band, F <= 1024); unfused: in a separate launch
+    LABELS_FUSED = ("nvfp4_quant_token moe_act", "nvfp4_quant_expert W_gu", "nvfp4_quant_expert W_d",
+                    "nvfp4_moe_gemm gate_up+swiglu+quant_h", "nvfp4_grouped_gemm down", "moe_combine")
+    LABELS_UNFUSED = ("nvfp4_quant_token moe_act", "nvfp4_quant_expert W_gu", "nvfp4_quant_expert W_d",
+                      "nvfp4_moe_gemm gate_up+swiglu", "nvfp4_quant_token moe_h", "nvfp4_grouped_gemm down",
+                      "moe_combine")
+
+    def __init__(self, mx, torch, device, d, E, F, topk, route_w, ws):
+        from moe_mx8_quantize_gb300 import inputs
+        self.mx, self.ws = mx, ws
+        H = d["X"].shape[1]
+        TM = d["X"].shape[0]
+        disp = inputs.dispatch(d["topk_ids"], E)
+        self.offs = disp.offsets
+        self.rows = R = int(disp.offsets[-1].item())
+        self.X = d["X"].contiguous()                                         # token-major activations
+        self.a_rows = disp.token_of_row.to(torch.int64).contiguous()       # token of each dispatched row
+        self.dest_rows = torch.argsort(self.a_rows, stable=True).to(torch.int64).contiguous()
+        self.rows_of_slot = disp.row_of_slot.contiguous()                  # (token, choice) -> row
+        self.route_w = route_w
+        self.W_gu = d["W_gu"].reshape(E * 2 * F, H).contiguous()
+        self.W_d = d["W_d"].reshape(E * H, F).contiguous()
+        self.e_offs_gu = torch.arange(E + 1, device=device, dtype=torch.int64) * (2 * F)
+        self.e_offs_d = torch.arange(E + 1, device=device, dtype=torch.int64) * H
+        u8 = lambda n: torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+        f32 = lambda n: torch.empty(max(n, 1), dtype=torch.float32, device=device)
+        sb4 = lambda r, c: u8(mx.scale_bytes(mx.FMT_NVFP4, r, c))
+        sb4g = lambda r, g, c: u8(mx.scale_bytes_grouped(mx.FMT_NVFP4, r, g, c))
+        bf = lambda r, c: torch.empty((r, c), dtype=torch.bfloat16, device=device)
+        self.A4, self.SA4, self.A432 = u8(R * H // 2)[: R * H // 2].view(R, H // 2), sb4g(R, E, H), f32(R)
+        self.Wgu4 = u8(E * 2 * F * H // 2)[: E * 2 * F * H // 2].view(E, 2 * F, H // 2)
+        self.SWgu4, self.Wgu432 = sb4(E * 2 * F, H), f32(E)
+        self.Wd4 = u8(E * H * F // 2)[: E * H * F // 2].view(E, H, F // 2)
+        self.SWd4, self.Wd432 = sb4(E * H, F), f32(E)
+        self.Hs = bf(R, F)
+        self.H4, self.SH4, self.H432 = u8(R * F // 2)[: R * F // 2].view(R, F // 2), sb4g(R, E, F), f32(R)
+        self.OUT = bf(R, H)
+        self.Y = bf(TM, H)                                                   # combined, token order
+        self.E, self.F, self.H, self.TM, self.topk = E, F, H, TM, topk
+        # the step quantizes h in a separate launch: measured faster than the
+        # cluster-fused epilogue (timed beside the step as "moe_gate_up_quant_h")
+        self.fused = False
+        self.LABELS = self.LABELS_FUSED if self.fused else self.LABELS_UNFUSED
+
+    def plan(self):
+        R, E, F, H, TM, k = self.rows, self.E, self.F, self.H, self.TM, self.topk
+        nvq = lambda r, c: 2.5625 * r * c + 4 * r
+        # before dispatch: bf16 read once per token; codes, block scales and S_dec
+        # written to each of the token's k dispatched rows
+        nvqd = lambda t, c: 2 * t * c + k * (0.5625 * t * c + 4 * t)
+        rows = [
+            ("nvfp4_quant_token moe_act", "hbm", nvqd(TM, H)),
+            ("nvfp4_quant_expert W_gu", "hbm", nvq(E * 2 * F, H)),
+            ("nvfp4_quant_expert W_d", "hbm", nvq(E * H, F)),
+            ("nvfp4_moe_gemm gate_up+swiglu+quant_h", "fp4", 2.0 * R * 2 * F * H),
+            ("nvfp4_moe_gemm gate_up+swiglu", "fp4", 2.0 * R * 2 * F * H),
+            ("nvfp4_quant_token moe_h", "hbm", nvq(R, F)),
+            ("nvfp4_grouped_gemm down", "fp4", 2.0 * R * H * F),
+            ("moe_combine", "hbm", 2.0 * R * H + 2.0 * TM * H + 12.0 * R),
+        ]
+        return [r for r in rows if r[0] in self.LABELS]
+
+    def bytes_moved(self):
+        """Algorithmic HBM bytes of the layer's kernels: the quantizers' and
+        the combine's, plus the GEMMs' operands and outputs (NVFP4 codes and
+        scales read; h written as bf16, or as NVFP4 when it is quantized in
+        the gate|up epilogue; the bf16 down output written)."""
+        R, E, F, H = self.rows, self.E, self.F, self.H
+        q = sum(w for _, kind, w in self.plan() if kind == "hbm")
+        h_out = (0.5625 * R * F + 4 * R) if self.fused else 2 * R * F
+        gemm = (0.5625 * R * H + 0.5625 * E * 2 * F * H + h_out          # gate|up: A, W_gu in; h out
+                + 0.5625 * R * F + 0.5625 * E * H * F + 2 * R * H)        # down: h4, W_d in; out
+        return q + gemm
+
+    def launches(self):
+        mx, ws = self.mx, self.ws
+        launches = [
+            ("nvfp4_quant_token moe_act", lambda: mx.nvfp4_quantize_dispatch_into(
+                self.X, self.dest_rows, self.topk, self.offs, self.A4, self.SA4, self.A432, mx.DISPATCH_ROWS, ws)),
+            ("nvfp4_quant_expert W_gu", lambda: mx.nvfp4_quantize_into(self.W_gu, self.Wgu4.view(-1, self.H // 2),
+                                                                       self.SWgu4, self.Wgu432, mx.SCOPE_GROUP,
+                                                                       self.e_offs_gu, ws)),
+            ("nvfp4_quant_expert W_d", lambda: mx.nvfp4_quantize_into(self.W_d, self.Wd4.view(-1, self.F // 2),
+                                                                      self.SWd4, self.Wd432, mx.SCOPE_GROUP,
+                                                                      self.e_offs_d, ws)),
+            ("nvfp4_moe_gemm gate_up+swiglu+quant_h", lambda: mx.bs_grouped_gemm_swiglu_nvfp4_into(
+                self.offs, self.rows, self.A4, self.SA4, self.Wgu4, self.SWgu4, self.H, self.H4, self.SH4,
+                self.H432, self.A432, self.Wgu432, None, ws)),
+            ("nvfp4_moe_gemm gate_up+swiglu", lambda: mx.bs_grouped_gemm_fused_into(
+                mx.FMT_NVFP4, self.offs, self.rows, self.A4, self.SA4, self.Wgu4, self.SWgu4, self.H, self.Hs,
+                self.A432, self.Wgu432, None, mx.EPI_SWIGLU, ws)),
+            ("nvfp4_quant_token moe_h", lambda: mx.nvfp4_quantize_into(self.Hs, self.H4, self.SH4, self.H432,
+                                                                       mx.SCOPE_TOKEN, self.offs, ws)),
+            ("nvfp4_grouped_gemm down", lambda: mx.bs_grouped_gemm_into(mx.FMT_NVFP4, self.offs, self.H4, self.SH4,
+                                                                         self.Wd4, self.SWd4, self.F, self.OUT,
+                                                                         self.H432, self.Wd432, ws)),
+            ("moe_combine", lambda: mx.moe_combine_into(self.OUT, self.rows_of_slot, self.route_w, self.Y)),
+        ]
+        return [l for l in launches if l[0] in self.LABELS]
+
+    def gemm_flops(self):
+        return sum(w for _, kind, w in self.plan() if kind in ("fp8", "fp4"))
+
+
 class Step:
     """All buffers of one hot-path step, resident in HBM, and the launches."""
 
@@ -137,30 +253,17 @@ class Step:
         lin = inputs.linear(seed=1 + seed_base, device=device)
         self.X, self.W, self.dY = lin["X"], lin["W"], lin["dY"]
         q = QWEN
-        moe = inputs.qwen_moe(seed=2 + seed_base, device=device)
-        disp = inputs.dispatch(moe["topk_ids"], q["experts"])
-        self.offs = disp.offsets
-        self.rows = int(disp.offsets[-1].item())
-        self.X_moe = moe["X"].contiguous()                          # token-major activations
-        self.a_rows = disp.token_of_row.to(torch.int64).contiguous()  # token of each dispatched row
-        # the topk dispatched rows of each token (inverse of a_rows)
-        self.dest_rows = torch.argsort(self.a_rows, stable=True).to(torch.int64).contiguous()
-        self.rows_of_slot = disp.row_of_slot.contiguous()               # token, choice -> row
-        self.route_w = inputs.route_weights(q["tokens"], q["topk"], 2 + seed_base, device)
-        E, F = q["experts"], q["ffn"]
-        self.W_gu = moe["W_gu"].reshape(E * 2 * F, H).contiguous()
-        self.W_d = moe["W_d"].reshape(E * H, F).contiguous()
-        self.e_offs_gu = torch.arange(E + 1, device=device, dtype=torch.int64) * (2 * F)
-        self.e_offs_d = torch.arange(E + 1, device=device, dtype=torch.int64) * H
         # one workspace per concurrent branch of the step (error word + scratch)
-        self.ws = mx.new_workspace(max(E, 1), device)
-        self.ws_b = mx.new_workspace(max(E, 1), device)
-        self.ws_c = mx.new_workspace(max(E, 1), device)
+        self.ws = mx.new_workspace(max(q["experts"], 1), device)
+        self.ws_b = mx.new_workspace(max(q["experts"], 1), device)
+        self.ws_c = mx.new_workspace(max(q["experts"], 1), device)
+        moe = inputs.qwen_moe(seed=2 + seed_base, device=device)
+        route_w = inputs.route_weights(q["tokens"], q["topk"], 2 + seed_base, device)
+        self.moe = MoeLayer(mx, torch, device, moe, q["experts"], q["ffn"], q["topk"], route_w, self.ws_c)
         u8 = lambda n: torch.empty(max(n, 16), dtype=torch.uint8, device=device)
         f32 = lambda n: torch.empty(max(n, 1), dtype=torch.float32, device=device)
         sb8 = lambda r, c: u8(mx.scale_bytes(mx.FMT_MXFP8, r, c))
         sb4 = lambda r, c: u8(mx.scale_bytes(mx.FMT_NVFP4, r, c))
-        sb4g = lambda r, g, c: u8(mx.scale_bytes_grouped(mx.FMT_NVFP4, r, g, c))
         bf = lambda r, c: torch.empty((r, c), dtype=torch.bfloat16, device=device)
         # MXFP8 copies
         self.Xr, self.SXr, self.Xc, self.SXc = u8(T * H).view(-1)[: T * H].view(T, H), sb8(T, H), \
@@ -176,27 +279,13 @@ class Step:
         self.X4, self.SX4, self.X432 = u8(T * H // 2)[: T * H // 2].view(T, H // 2), sb4(T, H), f32(T)
         self.W4, self.SW4, self.W432 = u8(O * H // 2)[: O * H // 2].view(O, H // 2), sb4(O, H), f32(1)
         self.Y4 = bf(T, O)
-        # MoE (tokens encoded once, before dispatch, written to their dispatched rows)
-        R, TM = self.rows, q["tokens"]
-        self.A4, self.SA4, self.A432 = u8(R * H // 2)[: R * H // 2].view(R, H // 2), sb4g(R, E, H), f32(R)
-        self.Wgu4 = u8(E * 2 * F * H // 2)[: E * 2 * F * H // 2].view(E, 2 * F, H // 2)
-        self.SWgu4, self.Wgu432 = sb4(E * 2 * F, H), f32(E)
-        self.Wd4 = u8(E * H * F // 2)[: E * H * F // 2].view(E, H, F // 2)
-        self.SWd4, self.Wd432 = sb4(E * H, F), f32(E)
-        self.Hs = bf(R, F)
-        self.H4, self.SH4, self.H432 = u8(R * F // 2)[: R * F // 2].view(R, F // 2), sb4g(R, E, F), f32(R)
-        self.OUT = bf(R, H)
-        self.Y_moe = bf(TM, H)                                          # combined, token order
-        self.E, self.F, self.H_, self.T, self.O, self.TM = E, F, H, T, O, TM
+        self.H_, self.T, self.O = H, T, O
 
     # -- algorithmic work per launch (bytes or FLOPs) and roofline class
     def plan(self):
-        T, H, O, R, E, F, TM = self.T, self.H_, self.O, self.rows, self.E, self.F, self.TM
+        T, H, O = self.T, self.H_, self.O
         mxq = lambda r, c: 4.0625 * r * c
         nvq = lambda r, c: 2.5625 * r * c + 4 * r
-        # before dispatch: bf16 read once per token; codes, block scales and S_dec
-        # written to each of the token's k dispatched rows
-        nvqd = lambda t, c, k: 2 * t * c + k * (0.5625 * t * c + 4 * t)
         return [
             ("mxfp8_quant_rc X", "hbm", mxq(T, H)),
             ("mxfp8_quant_rc W", "hbm", mxq(O, H)),
@@ -209,21 +298,14 @@ class Step:
             ("nvfp4_quant_token X", "hbm", nvq(T, H)),
             ("nvfp4_quant_tensor W", "hbm", nvq(O, H)),
             ("nvfp4_gemm Fprop", "fp4", 2.0 * T * O * H),
-            ("nvfp4_quant_token moe_act", "hbm", nvqd(TM, H, QWEN["topk"])),
-            ("nvfp4_quant_expert W_gu", "hbm", nvq(E * 2 * F, H)),
-            ("nvfp4_quant_expert W_d", "hbm", nvq(E * H, F)),
-            ("nvfp4_moe_gemm gate_up+swiglu", "fp4", 2.0 * R * 2 * F * H),
-            ("nvfp4_quant_token moe_h", "hbm", nvq(R, F)),
-            ("nvfp4_grouped_gemm down", "fp4", 2.0 * R * H * F),
-            ("moe_combine", "hbm", 2.0 * R * H + 2.0 * TM * H + 12.0 * R),
-        ]
+        ] + self.moe.plan()
 
     def launches(self):
         """The step as a list of (label, callable); each callable launches
         library kernels on the current stream."""
         mx = self.mx
         RC = mx.ROWWISE | mx.COLWISE
-        ws, ws_b, ws_c = self.ws, self.ws_b, self.ws_c
+        ws, ws_b = self.ws, self.ws_b
         return [
             ("mxfp8_quant_rc X", lambda: mx.mx8_quantize_into(self.X, self.Xr, self.SXr, self.Xc, self.SXc, RC, ws)),
             ("mxfp8_quant_rc W", lambda: mx.mx8_quantize_into(self.W, self.Wr, self.SWr, self.Wc, self.SWc, RC, ws)),
@@ -237,20 +319,7 @@ class Step:
             ("nvfp4_quant_tensor W", lambda: mx.nvfp4_quantize_into(self.W, self.W4, self.SW4, self.W432, mx.SCOPE_TENSOR, None, ws_b)),
             ("nvfp4_gemm Fprop", lambda: mx.bs_gemm_into(mx.FMT_NVFP4, self.X4, self.SX4, self.W4, self.SW4, self.H_, self.Y4,
                                                          self.X432, self.W432, ws=ws_b, a32_mode=mx.S32_ROW, b32_mode=mx.S32_TENSOR)),
-            ("nvfp4_quant_token moe_act", lambda: mx.nvfp4_quantize_dispatch_into(
-                self.X_moe, self.dest_rows, QWEN["topk"], self.offs, self.A4, self.SA4, self.A432, mx.DISPATCH_ROWS, ws_c)),
-            ("nvfp4_quant_expert W_gu", lambda: mx.nvfp4_quantize_into(self.W_gu, self.Wgu4.view(-1, self.H_ // 2), self.SWgu4, self.Wgu432,
-                                                                       mx.SCOPE_GROUP, self.e_offs_gu, ws_c)),
-            ("nvfp4_quant_expert W_d", lambda: mx.nvfp4_quantize_into(self.W_d, self.Wd4.view(-1, self.F // 2), self.SWd4, self.Wd432,
-                                                                      mx.SCOPE_GROUP, self.e_offs_d, ws_c)),
-            ("nvfp4_moe_gemm gate_up+swiglu", lambda: mx.bs_grouped_gemm_fused_into(
-                mx.FMT_NVFP4, self.offs, self.rows, self.A4, self.SA4, self.Wgu4, self.SWgu4, self.H_, self.Hs,
-                self.A432, self.Wgu432, None, mx.EPI_SWIGLU, ws_c)),
-            ("nvfp4_quant_token moe_h", lambda: mx.nvfp4_quantize_into(self.Hs, self.H4, self.SH4, self.H432, mx.SCOPE_TOKEN, self.offs, ws_c)),
-            ("nvfp4_grouped_gemm down", lambda: mx.bs_grouped_gemm_into(mx.FMT_NVFP4, self.offs, self.H4, self.SH4, self.Wd4, self.SWd4,
-                                                                         self.F, self.OUT, self.H432, self.Wd432, ws_c)),
-            ("moe_combine", lambda: mx.moe_combine_into(self.OUT, self.rows_of_slot, self.route_w, self.Y_moe)),
-        ]
+        ] + self.moe.launches()
 
     # The step's three independent chains: the MXFP8 linear layer, the NVFP4
     # linear Fprop and the NVFP4 MoE layer.  The end-to-end measurement runs
@@ -261,8 +330,7 @@ class Step:
         ("mxfp8_quant_rc X", "mxfp8_quant_rc W", "mxfp8_quant_rc dY", "mxfp8_gemm Fprop", "mxfp8_gemm Dgrad",
          "mxfp8_gemm Wgrad", "dequant_mxfp8 X", "dequant_mxfp8 W"),
         ("nvfp4_quant_token X", "nvfp4_quant_tensor W", "nvfp4_gemm Fprop"),
-        ("nvfp4_quant_token moe_act", "nvfp4_quant_expert W_gu", "nvfp4_quant_expert W_d",
-         "nvfp4_moe_gemm gate_up+swiglu", "nvfp4_quant_token moe_h", "nvfp4_grouped_gemm down", "moe_combine"),
+        MoeLayer.LABELS_UNFUSED,          # the Qwen-shaped layer (FFN 768)
     )
 
     def workspaces(self):
@@ -307,18 +375,117 @@ class Step:
         """Pinned host copies of each branch's per-step inputs and results."""
         torch = self.torch
         pin = lambda t: t.detach().cpu().pin_memory()
-        self.io_in = ([(self.X, pin(self.X)), (self.dY, pin(self.dY))], [], [(self.X_moe, pin(self.X_moe))])
+        self.io_in = ([(self.X, pin(self.X)), (self.dY, pin(self.dY))], [], [(self.moe.X, pin(self.moe.X))])
         empty = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
         self.io_out = ([(self.Y, empty(self.Y)), (self.dX, empty(self.dX))], [(self.Y4, empty(self.Y4))],
-                       [(self.Y_moe, empty(self.Y_moe))])
+                       [(self.moe.Y, empty(self.moe.Y))])
         self.x_ready = torch.cuda.Event()
 
-    # kernels each label launches (amax pass + quantize for group/tensor scope)
     # kernel launches per label (the rest launch one; group scope adds a memset)
     KERNELS_PER_LABEL = {"nvfp4_quant_tensor W": 2}   # tensor abs-max, then the encode
 
     def gemm_flops(self):
         return sum(w for _, kind, w in self.plan() if kind in ("fp8", "fp4"))
+
+
+class FusedQuantH:
+    """The Qwen-shaped layer's gate|up GEMM with SwiGLU and the per-token NVFP4
+    quantization of h fused into its epilogue (clusters of F / 128 CTAs),
+    timed beside the step against the two launches the step uses; it reads
+    the step's operands and writes the same codes, scales and S_dec."""
+
+    def __init__(self, step):
+        self.lay = step.moe
+
+    def plan(self):
+        L = self.lay
+        return [("nvfp4_moe_gemm gate_up+swiglu+quant_h", "fp4", 2.0 * L.rows * 2 * L.F * L.H)]
+
+    def launches(self):
+        L = self.lay
+        mx = L.mx
+        return [("nvfp4_moe_gemm gate_up+swiglu+quant_h", lambda: mx.bs_grouped_gemm_swiglu_nvfp4_into(
+            L.offs, L.rows, L.A4, L.SA4, L.Wgu4, L.SWgu4, L.H, L.H4, L.SH4, L.H432, L.A432, L.Wgu432, None, L.ws))]
+
+
+class Dsv3Moe:
+    """The DeepSeek-V3-shaped routed-expert layer (16384 tokens, hidden 7168,
+    256 experts, FFN 2048, top-8 Zipf(1.1), 0.5% of activations x100), the
+    same launches as the step's MoE layer, timed as its own step beside it."""
+
+    def __init__(self, step, seed=3):
+        torch, mx = step.torch, step.mx
+        from moe_mx8_quantize_gb300 import inputs
+        q = inputs.DSV3_SHAPE
+        self.ws = mx.new_workspace(q["experts"], step.dev)
+        d = inputs.dsv3_moe(seed=seed, device=step.dev)
+        route_w = inputs.route_weights(q["tokens"], q["topk"], seed, step.dev)
+        self.layer = MoeLayer(mx, torch, step.dev, d, q["experts"], q["ffn"], q["topk"], route_w, self.ws)
+        self.shape = q
+
+    def plan(self):
+        return self.layer.plan()
+
+    def launches(self):
+        return self.layer.launches()
+
+
+class Dsv3SharedExpert:
+    """The DeepSeek-V3 shared expert, kept at higher precision than the
+    routed experts: MXFP8 rowwise quantization of the 16384 x 7168 tokens and
+    of its weights, gate|up Fprop (7168 -> 2 x 2048), SwiGLU, MXFP8 of h, down
+    Fprop (2048 -> 7168).  Timed beside the routed layer."""
+
+    def __init__(self, dsv3, seed=31):
+        lay = dsv3.layer
+        mx = lay.mx
+        import torch
+        from moe_mx8_quantize_gb300 import inputs
+        dev = lay.X.device
+        T, H, F = lay.TM, lay.H, lay.F
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        self.X = lay.X
+        self.Wgu = inputs.normal_bf16((2 * F, H), 0.02, g, dev)
+        self.Wd = inputs.normal_bf16((H, F), 0.02, g, dev)
+        u8 = lambda r, c: torch.empty((r, c), dtype=torch.uint8, device=dev)
+        sb = lambda r, c: torch.empty(max(mx.scale_bytes(mx.FMT_MXFP8, r, c), 16), dtype=torch.uint8, device=dev)
+        bf = lambda r, c: torch.empty((r, c), dtype=torch.bfloat16, device=dev)
+        self.Xq, self.SX = u8(T, H), sb(T, H)
+        self.Wguq, self.SWgu = u8(2 * F, H), sb(2 * F, H)
+        self.Wdq, self.SWd = u8(H, F), sb(H, F)
+        self.GU, self.h = bf(T, 2 * F), bf(T, F)
+        self.hq, self.Sh = u8(T, F), sb(T, F)
+        self.Y = bf(T, H)
+        self.mx, self.ws, self.T, self.H, self.F = mx, dsv3.ws, T, H, F
+
+    def plan(self):
+        T, H, F = self.T, self.H, self.F
+        q = lambda r, c: (2 + 1 + 1 / 32) * r * c
+        return [
+            ("mxfp8_quant_row shared X", "hbm", q(T, H)),
+            ("mxfp8_quant_row shared W_gu", "hbm", q(2 * F, H)),
+            ("mxfp8_quant_row shared W_d", "hbm", q(H, F)),
+            ("mxfp8_gemm shared gate_up", "fp8", 2.0 * T * 2 * F * H),
+            ("swiglu shared", "hbm", 6.0 * T * F),
+            ("mxfp8_quant_row shared h", "hbm", q(T, F)),
+            ("mxfp8_gemm shared down", "fp8", 2.0 * T * H * F),
+        ]
+
+    def launches(self):
+        mx, ws = self.mx, self.ws
+        R = mx.ROWWISE
+        return [
+            ("mxfp8_quant_row shared X", lambda: mx.mx8_quantize_into(self.X, self.Xq, self.SX, None, None, R, ws)),
+            ("mxfp8_quant_row shared W_gu", lambda: mx.mx8_quantize_into(self.Wgu, self.Wguq, self.SWgu, None, None, R, ws)),
+            ("mxfp8_quant_row shared W_d", lambda: mx.mx8_quantize_into(self.Wd, self.Wdq, self.SWd, None, None, R, ws)),
+            ("mxfp8_gemm shared gate_up", lambda: mx.bs_gemm_into(mx.FMT_MXFP8, self.Xq, self.SX, self.Wguq, self.SWgu,
+                                                                  self.H, self.GU, ws=ws)),
+            ("swiglu shared", lambda: mx.swiglu_into(self.GU, self.h)),
+            ("mxfp8_quant_row shared h", lambda: mx.mx8_quantize_into(self.h, self.hq, self.Sh, None, None, R, ws)),
+            ("mxfp8_gemm shared down", lambda: mx.bs_gemm_into(mx.FMT_MXFP8, self.hq, self.Sh, self.Wdq, self.SWd,
+                                                               self.F, self.Y, ws=ws)),
+        ]
 
 
 class Mxfp4Linear:
@@ -625,15 +792,153 @@ def time_each(launches, K2, stream):
             f"{K2} eager runs, CUDA events around each launch")
 
 
+# Nominal dense tensor rates per GPU (TFLOP/s) quoted as context: 4.5 PF FP8 and
+# 9 PF FP4 (the targets the GEMMs are judged against), 2.25 PF BF16.
+NOMINAL_TFLOPS = {"bf16": 2250.0, "fp8": 4500.0, "fp4": 9000.0}
+
+
 def rate_row(lab, kind, work, ms, peaks):
-    """One breakdown entry: achieved rate against the measured peak."""
+    """One breakdown entry: achieved rate against the measured peak.  The
+    kernels are timed alone, each inside a sub-second region, so a
+    contraction's peak is the burst bf16 figure times the nominal dtype
+    ratio; its fraction of the nominal dense rate is given beside it."""
     s = ms / 1e3
     if kind == "hbm":
         ach, peak, unit = work / s / 1e9, peaks["hbm"], "GB/s"
     else:
-        ach, peak, unit = work / s / 1e12, peaks["bf16_sus"] * RATIO[kind], "TFLOP/s"
-    return {"kernel": lab, "us": round(ms * 1e3, 2), "achieved": round(ach, 1), "unit": unit,
-            "peak": round(peak, 1), "frac": round(ach / peak, 4)}
+        ach, peak, unit = work / s / 1e12, peaks["bf16"] * RATIO[kind], "TFLOP/s"
+    row = {"kernel": lab, "us": round(ms * 1e3, 2), "achieved": round(ach, 1), "unit": unit,
+           "peak": round(peak, 1), "frac": round(ach / peak, 4)}
+    if kind != "hbm":
+        row["frac_nominal"] = round(ach / NOMINAL_TFLOPS[kind], 4)
+    return row
+
+
+def graph_ms(launches, reps, stream):
+    """Mean device time (ms) of one pass over `launches`, from `reps` replays
+    of a CUDA graph of them between two events on the launching stream."""
+    import torch
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side, capture_error_mode="relaxed"):
+            for _, fn in launches:
+                fn()
+    stream.wait_stream(side)
+    graph.replay()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def time_part(part, K2, stream, peaks, check_errors, key):
+    """Warm-up, per-launch timing (time_each) and the breakdown rows of one
+    part measured beside the step; returns (rows, launches per pass, from)."""
+    import torch
+    fl = part.launches()
+    for _ in range(3):
+        for _, fn in fl:
+            fn()
+    torch.cuda.synchronize()
+    check_errors(f"in the {key} warm-up")
+    fper, ffrom = time_each(fl, K2, stream)
+    check_errors(f"in the {key} timing")
+    fplan = {lab: (kind, w) for lab, kind, w in part.plan()}
+    rows = [rate_row(lab, *fplan[lab], ms, peaks) for lab, ms in fper.items()]
+    return rows, sum(getattr(part, "KERNELS", {}).get(lab, 1) for lab, _ in fl), ffrom
+
+
+def run_dsv3(step, K2, stream, peaks, check_errors):
+    """The DeepSeek-V3-shaped MoE layer as its own step: routed-expert
+    TFLOP/s over the whole layer's time (graph replays), the per-kernel
+    breakdown, and the fraction of its roofline bound max(FLOPs / FP4 peak,
+    bytes / HBM peak); the MXFP8 shared expert beside it."""
+    d = Dsv3Moe(step)
+    lay = d.layer
+    rows, nlaunch, ffrom = time_part(d, K2, stream, peaks, check_errors, "dsv3 layer")
+    reps = max(3, min(K2, 30))
+    ms = graph_ms(d.launches(), reps, stream)
+    check_errors("in the dsv3 step timing")
+    flops = lay.gemm_flops()
+    bytes_ = lay.bytes_moved()
+    t_c = flops / (peaks["bf16"] * RATIO["fp4"] * 1e12)
+    t_b = bytes_ / (peaks["hbm"] * 1e9)
+    bound = max(t_c, t_b)
+    shared = Dsv3SharedExpert(d)
+    srows, snl, _ = time_part(shared, K2, stream, peaks, check_errors, "dsv3 shared expert")
+    sms = graph_ms(shared.launches(), reps, stream)
+    sfl = sum(w for _, kind, w in shared.plan() if kind == "fp8")
+    out = {
+        "workload": "DeepSeek-V3-shaped routed-expert layer, per-token NVFP4: 16384 tokens, hidden 7168, "
+                    "256 experts, FFN 2048, top-8 Zipf(1.1), 0.5% of activations x100 (131072 dispatched rows)",
+        "ms_per_step": round(ms, 4), "steps": reps, "value": round(flops / (ms / 1e3) / 1e12, 2),
+        "unit": "TFLOP/s", "gemm_flops_per_step": flops, "algorithmic_bytes_per_step": bytes_,
+        "roofline": {"bound_ms": round(bound * 1e3, 4), "by": "hbm" if t_b > t_c else "fp4",
+                     "compute_ms": round(t_c * 1e3, 4), "bytes_ms": round(t_b * 1e3, 4),
+                     "frac": round(bound / (ms / 1e3), 4)},
+        "breakdown": rows, "breakdown_from": ffrom,
+        "shared_expert_mxfp8": {"ms_per_step": round(sms, 4), "value": round(sfl / (sms / 1e3) / 1e12, 2),
+                                "unit": "TFLOP/s", "gemm_flops_per_step": sfl, "breakdown": srows},
+    }
+    launches = nlaunch * (K2 + 3 + reps + 1) + snl * (K2 + 3 + reps + 1)
+    del d, shared
+    return out, launches
+
+
+SWEEP = ((1 << 20, 2048), (1 << 24, 4096), (1 << 27, 7168), (1 << 30, 2048))
+
+
+def run_sweep(step, reps, stream, peaks, check_errors):
+    """Quantizer bandwidth sweep, 2^20 .. 2^30 bf16 elements of the sweep's
+    value mix: MXFP8 rowwise + columnwise (4.0625 B per element) and NVFP4
+    per token (2.5625 B per element + 4 B per row).  Each launch is timed
+    alone between CUDA events, after a 512 MB write that evicts L2, so
+    every size streams from HBM."""
+    import torch
+    mx = step.mx
+    from moe_mx8_quantize_gb300 import inputs
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=step.dev)
+    out, launches = [], 0
+    for numel, cols in SWEEP:
+        rows = max(128, (numel // cols) // 128 * 128)
+        x = inputs.sweep(rows, cols, seed=4 + numel.bit_length(), device=step.dev)
+        n = rows * cols
+        u8 = lambda k: torch.empty(max(k, 16), dtype=torch.uint8, device=step.dev)
+        qr, qc = u8(n).view(-1)[:n].view(rows, cols), u8(n)[:n].view(cols, rows)
+        sr, sc = u8(mx.scale_bytes(mx.FMT_MXFP8, rows, cols)), u8(mx.scale_bytes(mx.FMT_MXFP8, cols, rows))
+        q4, s4 = u8(n // 2)[: n // 2].view(rows, cols // 2), u8(mx.scale_bytes(mx.FMT_NVFP4, rows, cols))
+        s32 = torch.empty(rows, dtype=torch.float32, device=step.dev)
+        kinds = (("mxfp8_quant_rc", 4.0625 * n,
+                  lambda: mx.mx8_quantize_into(x, qr, sr, qc, sc, mx.ROWWISE | mx.COLWISE, step.ws)),
+                 ("nvfp4_quant_token", 2.5625 * n + 4 * rows,
+                  lambda: mx.nvfp4_quantize_into(x, q4, s4, s32, mx.SCOPE_TOKEN, None, step.ws)))
+        for name, work, fn in kinds:
+            for _ in range(2):
+                fn()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+            for a, b in ev:
+                flush.fill_(1)
+                a.record(stream)
+                fn()
+                b.record(stream)
+            torch.cuda.synchronize()
+            check_errors(f"in the sweep ({name}, {numel})")
+            ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+            row = rate_row(name, "hbm", work, ms, peaks)
+            row.update({"elements": n, "rows": rows, "cols": cols})
+            out.append(row)
+            launches += reps + 2
+        del x, qr, qc, sr, sc, q4, s4, s32
+    del flush
+    return {"rows": out, "from": f"{reps} launches per point, each alone between CUDA events after a "
+                                  f"512 MB write that evicts L2"}, launches
 
 
 def run_gpu(args):
@@ -721,32 +1026,28 @@ def run_gpu(args):
                 "achieved": dom["achieved"], "peak": dom["peak"], "unit": dom["unit"],
                 "frac": dom["frac"], "traffic": traffic,
                 "algorithmic": dwork, "peak_source": f"{peaks['source']} "
-                + ("hbm copy" if dkind == "hbm" else f"bf16 sustained x {RATIO[dkind]:g} ({dkind} nominal ratio)")}
+                + ("hbm copy" if dkind == "hbm" else f"bf16 burst x {RATIO[dkind]:g} ({dkind} nominal ratio)")}
 
     flops = step.gemm_flops()
     value = job_tflops(world, flops, ms_step)
     launches_per_step = sum(Step.KERNELS_PER_LABEL.get(lab, 1) for lab, _ in launches)
     gpu_launches = launches_per_step * (K + K2)
 
-    # timed region 3: the MXFP4 linear layer and the dequantized-backward
-    # BF16 GEMMs, beside the step (each in its own graph with event pairs)
+    # timed region 3: the MXFP4 linear layer, the dequantized-backward BF16
+    # GEMMs and the NVFP4 recipe variants, beside the step (each in its own
+    # graph with event pairs); then the DeepSeek-V3-shaped MoE layer and the
+    # quantizer bandwidth sweep, each its own timed region
     extra = None
     if not args.no_extra:
         extra = {}
         for key, part in (("mxfp4_linear", Mxfp4Linear(step)), ("dequantized_backward", DequantBackward(step)),
-                          ("nvfp4_recipe_linear", Nvfp4RecipeLinear(step))):
-            fl = part.launches()
-            for _ in range(3):
-                for _, fn in fl:
-                    fn()
-            torch.cuda.synchronize()
-            check_errors(f"in the {key} warm-up")
-            fper, ffrom = time_each(fl, K2, stream)
-            check_errors(f"in the {key} timing")
-            fplan = {lab: (kind, w) for lab, kind, w in part.plan()}
-            extra[key] = [rate_row(lab, *fplan[lab], ms, peaks) for lab, ms in fper.items()]
-            extra["from"] = ffrom
-            gpu_launches += sum(getattr(part, "KERNELS", {}).get(lab, 1) for lab, _ in fl) * K2
+                          ("nvfp4_recipe_linear", Nvfp4RecipeLinear(step)), ("moe_gate_up_quant_h", FusedQuantH(step))):
+            extra[key], nl, extra["from"] = time_part(part, K2, stream, peaks, check_errors, key)
+            gpu_launches += nl * (K2 + 3)
+        extra["dsv3_moe_layer"], nl = run_dsv3(step, K2, stream, peaks, check_errors)
+        gpu_launches += nl
+        extra["quantizer_sweep"], nl = run_sweep(step, 10, stream, peaks, check_errors)
+        gpu_launches += nl
 
     e2e = None
     if not args.no_e2e:
@@ -808,10 +1109,37 @@ def run_e2e(step, args, ranks, dev):
 
 
 # ----------------------------------------------------------------- CPU oracle
-def oracle_step_seconds(budget_s):
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+STEP_FLOPS = (2.0 * 2048 * 8192 * 2048 * 4 + 2.0 * 32768 * 1536 * 2048 + 2.0 * 32768 * 2048 * 768)
+
+
+def oracle_step_seconds(budget_s, threads=1):
     """Times the oracle on a bounded sample of every operation of the step and
-    extrapolates (per element / per output) to the full step.  Returns
-    (seconds for one full step, description of the sample)."""
+    extrapolates (per element / per output) to the full step.  With threads >
+    1 each thread runs the single-thread sample on its own slab (the C
+    oracle releases the interpreter lock), so the sample grows with the
+    threads.  Returns (seconds for one full step, description of the sample,
+    wall seconds of the sample)."""
+    from concurrent.futures import ThreadPoolExecutor
+
     import numpy as np
     import torch
     import oracle
@@ -821,47 +1149,58 @@ def oracle_step_seconds(budget_s):
     T, H, O = LINEAR["tokens"], LINEAR["in_features"], LINEAR["out_features"]
     E, F, R = QWEN["experts"], QWEN["ffn"], QWEN["tokens"] * QWEN["topk"]
     g = torch.Generator().manual_seed(7)
-    # the 64-row / 0.02%-of-outputs sample takes about 1.5 s on one core;
+    # the 64-row / 0.02%-of-outputs sample takes about 3.5 s on one core;
     # scale it to the requested budget
-    factor = max(budget_s / 1.5, 0.02)
+    factor = max(budget_s / 3.5, 0.02)
     rows = max(32, int(round(64 * factor / 32)) * 32)   # colwise blocks need 32-row slabs
     frac_gemm = 0.0002 * factor
+    pool = ThreadPoolExecutor(threads) if threads > 1 else None
+
+    def par(fn, items):
+        if pool is None:
+            for it in items:
+                fn(it)
+        else:
+            list(pool.map(fn, items))
 
     def slab(r, c, std=1.0):
         return inputs.bits(inputs.normal_bf16((r, c), std, g, "cpu"))
 
+    def slabs(r, c):
+        return [slab(r, c) for _ in range(threads)]
+
     total = 0.0
-    parts = []
+    t_wall = time.perf_counter()
 
     def timed(fn):
         t = time.perf_counter()
         fn()
         return time.perf_counter() - t
 
-    # MXFP8 rowwise + colwise quantization: 64-row slabs, scaled per element
+    # MXFP8 rowwise + colwise quantization: `rows`-row slabs, scaled per element
     for name, (r, c) in {"X": (T, H), "W": (O, H), "dY": (T, O)}.items():
-        x = slab(rows, c)
-        s = timed(lambda: (oracle.mxfp8_quantize_rowwise(x), oracle.mxfp8_quantize_colwise(x)))
-        total += s * (r * c) / (rows * c)
+        xs = slabs(rows, c)
+        s = timed(lambda: par(lambda x: (oracle.mxfp8_quantize_rowwise(x), oracle.mxfp8_quantize_colwise(x)), xs))
+        total += s * (r * c) / (threads * rows * c)
     # dequantize X^, W^
-    xq, xs = oracle.mxfp8_quantize_rowwise(slab(rows, H))
-    s = timed(lambda: oracle.dequant_mxfp8(xq, xs))
-    total += s * (T * H + O * H) / (rows * H)
+    qs = [oracle.mxfp8_quantize_rowwise(x) for x in slabs(rows, H)]
+    s = timed(lambda: par(lambda qq: oracle.dequant_mxfp8(*qq), qs))
+    total += s * (T * H + O * H) / (threads * rows * H)
     # NVFP4 quantizers (token scope cost per element also bounds group/tensor)
     for r, c in ((T, H), (O, H), (QWEN["tokens"], H), (E * 2 * F, H), (E * H, F), (R, F)):
-        x = slab(rows, c)
-        s = timed(lambda: oracle.nvfp4_quantize(x))
-        total += s * (r * c) / (rows * c)
+        xs = slabs(rows, c)
+        s = timed(lambda: par(oracle.nvfp4_quantize, xs))
+        total += s * (r * c) / (threads * rows * c)
     # SwiGLU
-    gu = slab(rows, 2 * F)
-    s = timed(lambda: oracle.swiglu(gu))
-    total += s * R / rows
+    gus = slabs(rows, 2 * F)
+    s = timed(lambda: par(oracle.swiglu, gus))
+    total += s * R / (threads * rows)
     # combine: `rows` tokens of 8 choices each
-    yy = slab(rows * 8, H)
+    yys = slabs(rows * 8, H)
     rws = np.arange(rows * 8, dtype=np.int64).reshape(rows, 8)
     ww = np.full((rows, 8), 0.125, np.float32)
-    s = timed(lambda: oracle.moe_combine(yy, rws, ww))
-    total += s * QWEN["tokens"] / rows
+    s = timed(lambda: par(lambda yy: oracle.moe_combine(yy, rws, ww), yys))
+    total += s * QWEN["tokens"] / (threads * rows)
     # GEMMs: sampled outputs, scaled per output
     rng = np.random.default_rng(0)
     for fmt, (M, N, K) in ((0, (T, O, H)), (0, (T, H, O)), (0, (O, H, T)), (1, (T, O, H)),
@@ -876,24 +1215,31 @@ def oracle_step_seconds(budget_s):
         else:
             A, SA, a32 = oracle.nvfp4_quantize(a)
             B, SB, b32 = oracle.nvfp4_quantize(b)
-        pairs = np.stack([rng.integers(0, 32, n_out), rng.integers(0, 64, n_out)], 1)
-        pairs = pairs[np.argsort(pairs[:, 0], kind="stable")]
-        s = timed(lambda: oracle.gemm_ref(fmt, A, SA, B, SB, K, a32, b32, pairs=pairs))
-        total += s * (M * N) / n_out
-    parts.append(f"quantizers/dequant/SwiGLU on {rows}-row slabs of every tensor; GEMMs on "
-                 f"sampled outputs ({frac_gemm * 100:.4f}% of each); extrapolated per element/output")
-    return total, "; ".join(parts)
+        work = []
+        for _ in range(threads):
+            pairs = np.stack([rng.integers(0, 32, n_out), rng.integers(0, 64, n_out)], 1)
+            work.append(pairs[np.argsort(pairs[:, 0], kind="stable")])
+        s = timed(lambda: par(lambda pr: oracle.gemm_ref(fmt, A, SA, B, SB, K, a32, b32, pairs=pr), work))
+        total += s * (M * N) / (threads * n_out)
+    wall = time.perf_counter() - t_wall
+    if pool is not None:
+        pool.shutdown()
+    desc = (f"{threads} thread(s), each: quantizers/dequant/SwiGLU on {rows}-row slabs of every tensor, GEMMs on "
+            f"sampled outputs ({frac_gemm * 100:.4f}% of each); extrapolated per element/output to the full step")
+    return total, desc, wall
 
 
 def oracle_baseline(budget_s):
+    """The oracle timed on the host cores, single-threaded and on all cores."""
     import __graft_entry__  # noqa: F401  (sys.path)
-    t0 = time.perf_counter()
-    secs, sample = oracle_step_seconds(budget_s)
-    wall = time.perf_counter() - t0
-    flops = (2.0 * 2048 * 8192 * 2048 * 4 + 2.0 * 32768 * 1536 * 2048 + 2.0 * 32768 * 2048 * 768)
-    return {"value": round(flops / secs / 1e12, 8), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-            "sample": sample, "sample_wall_s": round(wall, 2), "est_full_step_s": round(secs, 2),
-            "cpu": platform.processor() or platform.machine()}
+    cores = os.cpu_count() or 1
+    secs1, sample1, wall1 = oracle_step_seconds(budget_s, 1)
+    secsn, samplen, walln = oracle_step_seconds(budget_s, cores) if cores > 1 else (secs1, sample1, wall1)
+    return {"value": round(STEP_FLOPS / secsn / 1e12, 8), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": samplen, "sample_wall_s": round(walln, 2), "est_full_step_s": round(secsn, 2),
+            "single_thread": {"value": round(STEP_FLOPS / secs1 / 1e12, 8), "cores": 1, "sample": sample1,
+                              "sample_wall_s": round(wall1, 2), "est_full_step_s": round(secs1, 2)},
+            "cores_available": os.cpu_count(), "cpu": cpu_model()}
 
 
 def run_reference(args):
@@ -904,27 +1250,35 @@ def run_reference(args):
     if ranks.rank != 0:
         return
     K = args.steps
-    # each step times a sample sized so the whole run stays near two minutes
+    cores = os.cpu_count() or 1
+    # each step times a bounded sample of the step's work on all host cores,
+    # sized so the whole run stays near two minutes
     per_step = min(args.cpu_seconds / 4, 120.0 / max(1, K + args.warmup))
     for _ in range(args.warmup):
-        oracle_step_seconds(per_step)
+        oracle_step_seconds(per_step, cores)
     t0 = time.perf_counter()
-    est = []
+    est, walls = [], []
+    desc = ""
     for _ in range(K):
-        est.append(oracle_step_seconds(per_step)[0])
-    wall = time.perf_counter() - t0
+        secs, desc, wall = oracle_step_seconds(per_step, cores)
+        est.append(secs)
+        walls.append(wall)
+    total_wall = time.perf_counter() - t0
     secs = statistics.mean(est)
-    flops = (2.0 * 2048 * 8192 * 2048 * 4 + 2.0 * 32768 * 1536 * 2048 + 2.0 * 32768 * 2048 * 768)
-    value = flops / secs / 1e12
+    value = STEP_FLOPS / secs / 1e12
     out = {"impl": "reference", "metric": METRIC, "value": round(value, 8), "unit": "TFLOP/s",
-           "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(secs * 1e3, 1),
+           "n_gpus": world, "steps": K, "warmup": args.warmup,
+           "ms_per_step": round(statistics.mean(walls) * 1e3, 1),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
            "dtype": "f64 oracle (decoded e4m3/e2m1 operands)", "data": "synthetic",
            "config": {"workload": WORKLOAD, "sampled": True},
-           "cpu_baseline": {"kind": "oracle", "cores": 1, "value": round(value, 8),
-                            "sample": f"each step: the oracle on >=32-row slabs of every tensor and sampled "
-                                      f"GEMM outputs (budget {per_step:.2f} s), extrapolated to the full step",
-                            "wall_s": round(wall, 2)},
+           "timing": {"ms_per_step": "measured wall time of one sampled step (a bounded sample of every "
+                                     "operation of the step), not of the full step",
+                      "value": "throughput of the sample, extrapolated per element / output: full-step "
+                               "FLOPs over the estimated full-step time",
+                      "est_full_step_ms": round(secs * 1e3, 1), "wall_s": round(total_wall, 2)},
+           "cpu_baseline": {"kind": "oracle", "cores": cores, "value": round(value, 8), "sample": desc,
+                            "cpu": cpu_model()},
            "e2e": {"value": round(value, 8), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     ranks.emit(out)
