@@ -47,12 +47,14 @@
 //
 // Group / tensor scope (one FP32 scale per expert weight or per tensor) needs
 // the scope amax before any element is encoded.  A single kernel takes work
-// items from an ordered ticket counter: "amax" items (32 rows: fold their
+// items from an ordered ticket counter: "amax" items (16 rows, 32 for paired rows: fold their
 // maximum into the group's word, then count themselves done) and "encode"
-// items (32 scale rows of the group: wait until all of the group's amax items
-// are done, then encode).  Tickets hand out the amax items of a group about
-// L2-capacity/2 bytes of input ahead of the group's encode items, so the
-// second read of a group is served from L2.  An encode item only waits on
+// items (16 scale rows of the group: wait until all of the group's amax items
+// are done, then encode).  Tickets hand out a lead of amax items first (about
+// 32 MB of input, and at least the largest group), then encode and amax
+// items alternately, so the DRAM reads of the amax items and the L2 reads
+// of the encode items overlap throughout, and the second read of a group,
+// about one lead later, is served from L2.  An encode item only waits on
 // items with smaller tickets, which are already held by running blocks that
 // never wait, so the order cannot deadlock; the wait is bounded anyway.
 #include <float.h>
@@ -67,7 +69,15 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kItemRows = 32;                 // rows (or scale rows) per work item
+// Rows (or scale rows) per work item of the scoped kernel: two per data warp
+// (two pairs for the paired-row shapes).  Smaller items keep the data that
+// the blocks hold between an amax item and its encode item -- about two
+// items per block -- well inside L2 (measured: 16-row items read less from
+// DRAM than 32-row ones; 8-row items cost more in ticket traffic).
+template <int kCh>
+struct ScopedItem {
+  static constexpr int kRows = kCh < 0 ? 32 : 16;
+};
 constexpr int64_t kL2LeadBytes = 32ll << 20;  // input bytes between a group's amax and encode items
 
 
@@ -455,14 +465,14 @@ struct ScopedSmem {
   GroupSmem gs;                       // scale-layout groups (or one group)
   int64_t toffs[2];                   // tensor scope: data rows [0, R) ...
   int64_t tpref[2];                   // ... and scale rows [0, TP)
-  int32_t seg_start[2 * kMaxGroups + 1];
-  int32_t seg_info[2 * kMaxGroups];   // (group << 1) | is_encode
-  int32_t nseg;
+  int32_t ca[kMaxGroups + 1];         // amax items of the scope groups before group g
+  int32_t ce[kMaxGroups + 1];         // encode items of the scope groups before group g
+  int32_t lead;                       // amax items handed out before the first encode item
   float2 tab[128];
   // Two ticket slots, used by alternate work items: the control warp fills
   // the next item's slot while the data warps run the current one.
   int64_t tk[2];
-  int64_t titem[2];                   // item index within its segment
+  int64_t titem[2];                   // item index within its scope group
   int32_t tg[2];                      // scope group
   int32_t tenc[2];                    // 1 = encode item
   int32_t tready[2];                  // encode item whose group amax is known
@@ -500,6 +510,7 @@ __global__ void __launch_bounds__(kScopedThreads, kCh >= 8 || kCh == 0 ? 1 : 4) 
     float* __restrict__ s32, uint32_t* __restrict__ scratch, int* err) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   ScopedSmem& sm = *reinterpret_cast<ScopedSmem*>(smem_raw);
+  constexpr int kItemRows = ScopedItem<kCh>::kRows;
   const bool grouped = offs != nullptr;
   const int Gs = scope == 1 ? G : 1;                       // scope groups
   uint32_t* amax_bits = scratch;
@@ -522,32 +533,57 @@ __global__ void __launch_bounds__(kScopedThreads, kCh >= 8 || kCh == 0 ? 1 : 4) 
   const int64_t* apref = scope == 1 ? sm.gs.pref : sm.tpref;
   if (threadIdx.x == 0) {
     sm.toffs[0] = 0; sm.toffs[1] = R; sm.tpref[0] = 0; sm.tpref[1] = TP;
-    // segment order: amax(0..L-1), then encode(g), amax(g+L) for g = 0..Gs-1
-    const int64_t per_group_bytes = Gs > 0 ? (R * C * 2) / Gs : 0;
-    int lead = per_group_bytes > 0 ? static_cast<int>(kL2LeadBytes / per_group_bytes) : Gs;
-    if (lead < 1) lead = 1;
-    if (lead > Gs) lead = Gs;
-    int nseg = 0;
-    int32_t pos = 0;
-    auto push = [&](int g, int enc) {
-      const int64_t n = enc ? (apref[g + 1] - apref[g]) / kItemRows
-                            : (aoffs[g + 1] - aoffs[g] + kItemRows - 1) / kItemRows;
-      sm.seg_start[nseg] = pos;
-      sm.seg_info[nseg] = (g << 1) | enc;
-      pos += static_cast<int32_t>(n);
-      ++nseg;
-    };
-    for (int g = 0; g < lead; ++g) push(g, 0);
-    for (int g = 0; g < Gs; ++g) {
-      push(g, 1);
-      if (g + lead < Gs) push(g + lead, 0);
-    }
-    sm.seg_start[nseg] = pos;
-    sm.nseg = nseg;
   }
   __syncthreads();
-  const int nseg = sm.nseg;
-  const int64_t total = sm.seg_start[nseg];
+  // Item counts per scope group -- amax items: ceil(rows / 32); encode items:
+  // padded scale rows / 32 -- as exclusive prefix sums (warp 0), and the lead.
+  if (threadIdx.x < 32) {
+    const int lane0 = threadIdx.x;
+    const int per = (Gs + 31) / 32, g0 = lane0 * per;
+    int32_t la = 0, le = 0, mx = 0;
+    for (int g = g0; g < g0 + per && g < Gs; ++g) {
+      const int32_t a = static_cast<int32_t>((aoffs[g + 1] - aoffs[g] + kItemRows - 1) / kItemRows);
+      la += a;
+      le += static_cast<int32_t>((apref[g + 1] - apref[g]) / kItemRows);
+      mx = a > mx ? a : mx;
+    }
+    int32_t ia = la, ie = le;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int32_t oa = __shfl_up_sync(0xffffffffu, ia, d), oe = __shfl_up_sync(0xffffffffu, ie, d);
+      if (lane0 >= d) {
+        ia += oa;
+        ie += oe;
+      }
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, d));
+    }
+    int32_t ra = ia - la, re = ie - le;
+    for (int g = g0; g < g0 + per && g < Gs; ++g) {
+      sm.ca[g] = ra;
+      sm.ce[g] = re;
+      ra += static_cast<int32_t>((aoffs[g + 1] - aoffs[g] + kItemRows - 1) / kItemRows);
+      re += static_cast<int32_t>((apref[g + 1] - apref[g]) / kItemRows);
+    }
+    if (lane0 == 31) {
+      sm.ca[Gs] = ia;
+      sm.ce[Gs] = ie;
+      // about kL2LeadBytes of input between an amax item and the encode item
+      // that reads the same rows again, and never less than the largest
+      // group plus a quarter (no encode item waits for an amax item handed out
+      // after it, and the last amax items of a group have some time to
+      // finish before its first encode items are taken; measured on groups
+      // larger than the lead, the quarter lowers the waits more than it
+      // costs in L2 hits)
+      const int64_t item_bytes = static_cast<int64_t>(kItemRows) * C * 2;
+      int64_t lead = item_bytes > 0 ? (kL2LeadBytes + item_bytes - 1) / item_bytes : 0;
+      if (lead < mx + mx / 4) lead = mx + mx / 4;
+      if (lead > ia) lead = ia;
+      sm.lead = static_cast<int32_t>(lead);
+    }
+  }
+  __syncthreads();
+  const int64_t NA = sm.ca[Gs], NE = sm.ce[Gs], LEAD = sm.lead;
+  const int64_t total = NA + NE;
   // groups with no rows still get their (zero) decode scale
   if (blockIdx.x == 0)
     for (int g = threadIdx.x; g < Gs; g += blockDim.x)
@@ -573,14 +609,33 @@ __global__ void __launch_bounds__(kScopedThreads, kCh >= 8 || kCh == 0 ? 1 : 4) 
     const int64_t t = static_cast<int64_t>(atomicAdd(ticket, 1ull));
     sm.tk[slot] = t;
     if (t >= total) return;
-    int lo = 0, hi = nseg - 1;                 // segment holding ticket t
+    // Ticket order: amax items 0 .. LEAD-1, then encode item j and amax item
+    // LEAD + j alternately, then the encode items left.  Encode item j of
+    // group g follows every amax item of g: the last has index < LEAD + j
+    // (LEAD >= any group's amax items, and g's encode items start at or after
+    // its amax items), so it was handed out before ticket LEAD + 2j.
+    const int64_t P = NA - LEAD;
+    int enc;
+    int64_t k;
+    if (t < LEAD) {
+      enc = 0;
+      k = t;
+    } else if (t - LEAD < 2 * P) {
+      const int64_t u = t - LEAD;
+      enc = (u & 1) == 0;
+      k = enc ? (u >> 1) : LEAD + (u >> 1);
+    } else {
+      enc = 1;
+      k = P + (t - LEAD - 2 * P);
+    }
+    const int32_t* cum = enc ? sm.ce : sm.ca;
+    int lo = 0, hi = Gs - 1;                   // the last group with cum[g] <= k
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (sm.seg_start[mid] <= t) lo = mid; else hi = mid - 1;
+      if (cum[mid] <= k) lo = mid; else hi = mid - 1;
     }
-    const int g = sm.seg_info[lo] >> 1;
-    const int enc = sm.seg_info[lo] & 1;
-    const int64_t item = t - sm.seg_start[lo];
+    const int g = lo;
+    const int64_t item = k - cum[g];
     sm.tg[slot] = g;
     sm.tenc[slot] = enc;
     sm.titem[slot] = item;
