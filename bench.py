@@ -4,7 +4,8 @@
 One step = every operation of the hot path, on seeded synthetic inputs:
 
   MXFP8 linear layer, input [2048, 2048] -> 8192 (forward + backward):
-    rowwise+columnwise MXFP8 quantization of X, W and dY (one pass each),
+    rowwise+columnwise MXFP8 quantization of X, W and dY (one read of each,
+    the three tensors in one launch),
     Fprop Y = X W^T, Dgrad dX = dY W, Wgrad dW = dY^T X (block-scaled
     tcgen05 GEMMs), and the dequantized-backward operands (X^, W^ in bf16);
   NVFP4 linear Fprop on the same layer: per-token X, per-tensor W;
@@ -287,9 +288,7 @@ class Step:
         mxq = lambda r, c: 4.0625 * r * c
         nvq = lambda r, c: 2.5625 * r * c + 4 * r
         return [
-            ("mxfp8_quant_rc X", "hbm", mxq(T, H)),
-            ("mxfp8_quant_rc W", "hbm", mxq(O, H)),
-            ("mxfp8_quant_rc dY", "hbm", mxq(T, O)),
+            ("mxfp8_quant_rc X+W+dY", "hbm", mxq(T, H) + mxq(O, H) + mxq(T, O)),
             ("mxfp8_gemm Fprop", "fp8", 2.0 * T * O * H),
             ("mxfp8_gemm Dgrad", "fp8", 2.0 * T * H * O),
             ("mxfp8_gemm Wgrad", "fp8", 2.0 * O * H * T),
@@ -307,9 +306,10 @@ class Step:
         RC = mx.ROWWISE | mx.COLWISE
         ws, ws_b = self.ws, self.ws_b
         return [
-            ("mxfp8_quant_rc X", lambda: mx.mx8_quantize_into(self.X, self.Xr, self.SXr, self.Xc, self.SXc, RC, ws)),
-            ("mxfp8_quant_rc W", lambda: mx.mx8_quantize_into(self.W, self.Wr, self.SWr, self.Wc, self.SWc, RC, ws)),
-            ("mxfp8_quant_rc dY", lambda: mx.mx8_quantize_into(self.dY, self.dYr, self.SdYr, self.dYc, self.SdYc, RC, ws)),
+            # the layer's three tensors, rowwise + columnwise, in one launch
+            ("mxfp8_quant_rc X+W+dY", lambda: mx.mx8_quantize_batch_into(mx.FMT_MXFP8, (
+                (self.X, self.Xr, self.SXr, self.Xc, self.SXc), (self.W, self.Wr, self.SWr, self.Wc, self.SWc),
+                (self.dY, self.dYr, self.SdYr, self.dYc, self.SdYc)), RC, ws)),
             ("mxfp8_gemm Fprop", lambda: mx.bs_gemm_into(mx.FMT_MXFP8, self.Xr, self.SXr, self.Wr, self.SWr, self.H_, self.Y, ws=ws)),
             ("mxfp8_gemm Dgrad", lambda: mx.bs_gemm_into(mx.FMT_MXFP8, self.dYr, self.SdYr, self.Wc, self.SWc, self.O, self.dX, ws=ws)),
             ("mxfp8_gemm Wgrad", lambda: mx.bs_gemm_into(mx.FMT_MXFP8, self.dYc, self.SdYc, self.Xc, self.SXc, self.T, self.dW, ws=ws)),
@@ -327,8 +327,8 @@ class Step:
     # overlap another's kernels; within a chain the order is the data order
     # above.
     BRANCHES = (
-        ("mxfp8_quant_rc X", "mxfp8_quant_rc W", "mxfp8_quant_rc dY", "mxfp8_gemm Fprop", "mxfp8_gemm Dgrad",
-         "mxfp8_gemm Wgrad", "dequant_mxfp8 X", "dequant_mxfp8 W"),
+        ("mxfp8_quant_rc X+W+dY", "mxfp8_gemm Fprop", "mxfp8_gemm Dgrad", "mxfp8_gemm Wgrad", "dequant_mxfp8 X",
+         "dequant_mxfp8 W"),
         ("nvfp4_quant_token X", "nvfp4_quant_tensor W", "nvfp4_gemm Fprop"),
         MoeLayer.LABELS_UNFUSED,          # the Qwen-shaped layer (FFN 768)
     )
@@ -514,9 +514,7 @@ class Mxfp4Linear:
         T, H, O = st.T, st.H_, st.O
         q = lambda r, c: (2 + 2 * (0.5 + 1 / 32)) * r * c     # bf16 in, two packed copies + scales out
         return [
-            ("mxfp4_quant_rc X", "hbm", q(T, H)),
-            ("mxfp4_quant_rc W", "hbm", q(O, H)),
-            ("mxfp4_quant_rc dY", "hbm", q(T, O)),
+            ("mxfp4_quant_rc X+W+dY", "hbm", q(T, H) + q(O, H) + q(T, O)),
             ("mxfp4_gemm Fprop", "fp4", 2.0 * T * O * H),
             ("mxfp4_gemm Dgrad", "fp4", 2.0 * T * H * O),
             ("mxfp4_gemm Wgrad", "fp4", 2.0 * O * H * T),
@@ -528,9 +526,9 @@ class Mxfp4Linear:
         RC = mx.ROWWISE | mx.COLWISE
         ws = st.ws
         return [
-            ("mxfp4_quant_rc X", lambda: mx.mxfp4_quantize_into(st.X, self.Xr, self.SXr, self.Xc, self.SXc, RC, ws)),
-            ("mxfp4_quant_rc W", lambda: mx.mxfp4_quantize_into(st.W, self.Wr, self.SWr, self.Wc, self.SWc, RC, ws)),
-            ("mxfp4_quant_rc dY", lambda: mx.mxfp4_quantize_into(st.dY, self.dYr, self.SdYr, self.dYc, self.SdYc, RC, ws)),
+            ("mxfp4_quant_rc X+W+dY", lambda: mx.mx8_quantize_batch_into(mx.FMT_MXFP4, (
+                (st.X, self.Xr, self.SXr, self.Xc, self.SXc), (st.W, self.Wr, self.SWr, self.Wc, self.SWc),
+                (st.dY, self.dYr, self.SdYr, self.dYc, self.SdYc)), RC, ws)),
             ("mxfp4_gemm Fprop", lambda: mx.bs_gemm_into(mx.FMT_MXFP4, self.Xr, self.SXr, self.Wr, self.SWr, st.H_, self.Y, ws=ws)),
             ("mxfp4_gemm Dgrad", lambda: mx.bs_gemm_into(mx.FMT_MXFP4, self.dYr, self.SdYr, self.Wc, self.SWc, st.O, self.dX, ws=ws)),
             ("mxfp4_gemm Wgrad", lambda: mx.bs_gemm_into(mx.FMT_MXFP4, self.dYc, self.SdYc, self.Xc, self.SXc, st.T, self.dW, ws=ws)),

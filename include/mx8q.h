@@ -146,6 +146,31 @@ mx8_status mxfp4_quantize(const void *x, int64_t rows, int64_t cols, int64_t ld,
                           uint8_t *q_row, uint8_t *s_row, uint8_t *q_col, uint8_t *s_col,
                           void *workspace, size_t workspace_bytes, mx8_stream_t stream);
 
+/* One input of mx8_quantize_batch(): the arguments of one mx8_quantize()
+ * (or mxfp4_quantize()) call. */
+typedef struct {
+    const void *x;
+    int64_t rows, cols, ld;
+    uint8_t *q_row, *s_row, *q_col, *s_col;
+} mx8_quantize_item;
+
+#define MX8_BATCH_MAX 4
+
+/*
+ * mx8_quantize() (fmt MX8_FMT_MXFP8) or mxfp4_quantize() (MX8_FMT_MXFP4) of
+ * up to MX8_BATCH_MAX tensors in ONE launch, e.g. the input, weight and
+ * output gradient of a linear layer ([MRL] "Un Cuantizador Compartido...":
+ * each tensor's rowwise and columnwise copies come from its high-precision
+ * values).  The tensors' 128x128 tiles form one work list for a persistent
+ * grid, so the launch and memory latency of a small tensor hide behind the
+ * others.  Results are byte for byte those of the separate calls; each item
+ * obeys the same rules (items with rows == 0 or cols == 0 are skipped).
+ * flags applies to every item.  n outside [1, MX8_BATCH_MAX] returns
+ * MX8_ERR_INVALID_ARG.
+ */
+mx8_status mx8_quantize_batch(int fmt, const mx8_quantize_item *items, int n, int flags,
+                              void *workspace, size_t workspace_bytes, mx8_stream_t stream);
+
 /*
  * Two-level NVFP4 quantization of a bf16 matrix with the FP32 scale computed
  * online per token ([MRL] "La Compatibilidad..." and "Un Cuantizador

@@ -30,7 +30,7 @@ S32_NONE, S32_ROW, S32_TENSOR, S32_GROUP = 0, 1, 2, 3
 
 # every C symbol the header declares
 EXPORTS = ("mx8_scale_bytes", "mx8_scale_bytes_grouped", "mx8_workspace_bytes",
-           "mx8_device_sm_count", "mx8_quantize", "mxfp4_quantize", "nvfp4_quantize_per_token",
+           "mx8_device_sm_count", "mx8_quantize", "mxfp4_quantize", "mx8_quantize_batch", "nvfp4_quantize_per_token",
            "nvfp4_quantize_dispatch", "nvfp4_quantize_2d", "nvfp4_quantize_rht_colwise",
            "nvfp4_quantize_per_token_sr",
            "nvfp4_quantize_per_token_noalloc", "nvfp4_noalloc_check_error", "dequantize",
@@ -70,6 +70,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mx8_device_sm_count.argtypes = []
     lib.mx8_quantize.restype = _i
     lib.mx8_quantize.argtypes = [_p, _i64, _i64, _i64, _i, _p, _p, _p, _p, _p, _sz, _p]
+    lib.mx8_quantize_batch.restype = _i
+    lib.mx8_quantize_batch.argtypes = [_i, _p, _i, _i, _p, _sz, _p]
     lib.mxfp4_quantize.restype = _i
     lib.mxfp4_quantize.argtypes = [_p, _i64, _i64, _i64, _i, _p, _p, _p, _p, _p, _sz, _p]
     lib.nvfp4_quantize_per_token.restype = _i
@@ -203,6 +205,31 @@ def mx8_quantize(x: torch.Tensor, flags: int = ROWWISE | COLWISE, ws=None, strea
 
 
 # ---------------------------------------------------------------- MXFP4
+class QuantizeItem(ctypes.Structure):
+    """One input of mx8_quantize_batch (the C struct mx8_quantize_item)."""
+    _fields_ = [("x", _p), ("rows", _i64), ("cols", _i64), ("ld", _i64),
+                ("q_row", _p), ("s_row", _p), ("q_col", _p), ("s_col", _p)]
+
+
+BATCH_MAX = 4
+
+
+def mx8_quantize_batch_into(fmt, items, flags=ROWWISE | COLWISE, ws=None, stream=None):
+    """MXFP8 (fmt FMT_MXFP8) or MXFP4 (FMT_MXFP4) quantization of up to
+    BATCH_MAX tensors in one launch.  items: sequence of (x, q_row, s_row,
+    q_col, s_col) with pre-allocated outputs (None for a copy not in flags);
+    the bytes equal those of one mx8_quantize_into / mxfp4_quantize_into call
+    per tensor."""
+    arr = (QuantizeItem * len(items))()
+    for i, (x, qr, sr, qc, sc) in enumerate(items):
+        assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+        arr[i] = QuantizeItem(x.data_ptr(), x.shape[0], x.shape[1], x.stride(0),
+                              *(t.data_ptr() if t is not None else None for t in (qr, sr, qc, sc)))
+    ws = _ws(ws, 1, items[0][0].device)
+    _check(load().mx8_quantize_batch(fmt, ctypes.cast(arr, _p), len(items), flags, _ptr(ws), ws.numel(),
+                                     _stream(stream)), "mx8_quantize_batch")
+
+
 def mxfp4_quantize_into(x, q_row, s_row, q_col, s_col, flags=ROWWISE | COLWISE, ws=None, stream=None):
     """In-place form of :func:`mxfp4_quantize` (outputs pre-allocated)."""
     assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1

@@ -110,11 +110,12 @@ extern "C" const char* mx8_status_string(mx8_status s) {
 
 // ===================================================================== MXFP8 / MXFP4
 namespace {
-mx8_status mx_quantize(bool fp4, const void* x, int64_t rows, int64_t cols, int64_t ld, int flags,
-                       uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
-                       void* workspace, size_t workspace_bytes, mx8_stream_t stream) {
-  const bool row = flags & MX8_ROWWISE, col = flags & MX8_COLWISE;
-  if ((flags & ~(MX8_ROWWISE | MX8_COLWISE)) || !(row || col)) return MX8_ERR_INVALID_ARG;
+// Checks one quantization input (same rules for mx8_quantize / mxfp4_quantize
+// and their batch form); *empty is set when there is nothing to do.
+mx8_status check_quant_item(bool row, bool col, const void* x, int64_t rows, int64_t cols, int64_t ld,
+                            const uint8_t* q_row, const uint8_t* s_row, const uint8_t* q_col, const uint8_t* s_col,
+                            bool* empty) {
+  *empty = true;
   if (rows < 0 || cols < 0 || ld < cols || cols % 32 != 0) return MX8_ERR_INVALID_ARG;
   if (col && rows % 32 != 0) return MX8_ERR_INVALID_ARG;
   if (rows == 0 || cols == 0) return MX8_OK;
@@ -125,21 +126,72 @@ mx8_status mx_quantize(bool fp4, const void* x, int64_t rows, int64_t cols, int6
       (col && (!aligned16(q_col) || !aligned16(s_col))))
     return MX8_ERR_ALIGNMENT;
   if (rows > INT32_MAX || cols > INT32_MAX) return MX8_ERR_UNSUPPORTED;
-  mx8_status st = check_ws(workspace, workspace_bytes, 1);
-  if (st != MX8_OK) return st;
+  *empty = false;
+  return MX8_OK;
+}
 
-  CUtensorMap map;
+// Adds a checked, non-empty input to the batch: its tensor map and tile range.
+bool add_quant_item(QuantBatch& b, const void* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* q_row,
+                    uint8_t* s_row, uint8_t* q_col, uint8_t* s_col) {
   const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)};
   const uint64_t strides[1] = {static_cast<uint64_t>(ld) * 2};
   const uint32_t box[2] = {128, 128};
-  if (!encode_map(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, dims, strides, box,
+  const int i = b.n;
+  if (!encode_map(&b.maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, dims, strides, box,
                   CU_TENSOR_MAP_SWIZZLE_NONE))
-    return MX8_ERR_CUDA;
-  return from_cuda(launch_mxfp8_quant(map, rows, cols, row, col, fp4, q_row, s_row, q_col, s_col,
-                                      err_word(workspace), sm_count_current(),
+    return false;
+  b.t[i] = QuantTensor{rows, cols, q_row, s_row, q_col, s_col, b.ntiles};
+  b.ntiles += cdiv(rows, 128) * cdiv(cols, 128);
+  b.n = i + 1;
+  return true;
+}
+
+mx8_status mx_quantize(bool fp4, const void* x, int64_t rows, int64_t cols, int64_t ld, int flags,
+                       uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                       void* workspace, size_t workspace_bytes, mx8_stream_t stream) {
+  const bool row = flags & MX8_ROWWISE, col = flags & MX8_COLWISE;
+  if ((flags & ~(MX8_ROWWISE | MX8_COLWISE)) || !(row || col)) return MX8_ERR_INVALID_ARG;
+  bool empty = true;
+  mx8_status st = check_quant_item(row, col, x, rows, cols, ld, q_row, s_row, q_col, s_col, &empty);
+  if (st != MX8_OK || empty) return st;
+  st = check_ws(workspace, workspace_bytes, 1);
+  if (st != MX8_OK) return st;
+  QuantBatch b{};
+  if (!add_quant_item(b, x, rows, cols, ld, q_row, s_row, q_col, s_col)) return MX8_ERR_CUDA;
+  return from_cuda(launch_mxfp8_quant(b, row, col, fp4, err_word(workspace), sm_count_current(),
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 }  // namespace
+
+extern "C" mx8_status mx8_quantize_batch(int fmt, const mx8_quantize_item* items, int n, int flags,
+                                         void* workspace, size_t workspace_bytes, mx8_stream_t stream) {
+  if (fmt != MX8_FMT_MXFP8 && fmt != MX8_FMT_MXFP4) return MX8_ERR_INVALID_ARG;
+  if (n < 1 || n > MX8_BATCH_MAX || items == nullptr) return MX8_ERR_INVALID_ARG;
+  static_assert(MX8_BATCH_MAX <= kQuantBatchMax, "batch larger than the kernel's tensor list");
+  const bool row = flags & MX8_ROWWISE, col = flags & MX8_COLWISE;
+  if ((flags & ~(MX8_ROWWISE | MX8_COLWISE)) || !(row || col)) return MX8_ERR_INVALID_ARG;
+  bool any = false;
+  for (int i = 0; i < n; ++i) {
+    const mx8_quantize_item& it = items[i];
+    bool empty = true;
+    mx8_status st = check_quant_item(row, col, it.x, it.rows, it.cols, it.ld, it.q_row, it.s_row, it.q_col,
+                                     it.s_col, &empty);
+    if (st != MX8_OK) return st;
+    any = any || !empty;
+  }
+  if (!any) return MX8_OK;
+  mx8_status st = check_ws(workspace, workspace_bytes, 1);
+  if (st != MX8_OK) return st;
+  QuantBatch b{};
+  for (int i = 0; i < n; ++i) {
+    const mx8_quantize_item& it = items[i];
+    if (it.rows == 0 || it.cols == 0) continue;
+    if (!add_quant_item(b, it.x, it.rows, it.cols, it.ld, it.q_row, it.s_row, it.q_col, it.s_col))
+      return MX8_ERR_CUDA;
+  }
+  return from_cuda(launch_mxfp8_quant(b, row, col, fmt == MX8_FMT_MXFP4, err_word(workspace), sm_count_current(),
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
 
 extern "C" mx8_status mx8_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int flags,
                                    uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,

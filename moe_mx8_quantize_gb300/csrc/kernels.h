@@ -17,11 +17,28 @@ constexpr int kGemmKBytes = 128;
 constexpr int kMaxGroups = 1024;   // groups (experts) per grouped call
 #define MX8Q_S32_GROUP_MODE 3          // FP32 scale per group (same value as MX8_S32_GROUP)
 
+// Tensors of one MXFP8 / MXFP4 quantization launch: their 128x128 tiles are
+// numbered one after the other (tensor i's tiles start at t[i].tile0).
+constexpr int kQuantBatchMax = 4;
+struct QuantTensor {
+  int64_t R, C;
+  uint8_t* q_row;
+  uint8_t* s_row;
+  uint8_t* q_col;
+  uint8_t* s_col;
+  int64_t tile0;
+};
+struct __align__(64) QuantBatch {
+  CUtensorMap maps[kQuantBatchMax];   // bf16 [R, C] with 128x128 boxes
+  QuantTensor t[kQuantBatchMax];
+  int n;
+  int64_t ntiles;
+};
+
 size_t mxfp8_quant_smem_bytes();
 // fp4: MXFP4 (packed E2M1 data) instead of MXFP8 (E4M3 data)
-cudaError_t launch_mxfp8_quant(const CUtensorMap& tmap_x, int64_t R, int64_t C, bool row, bool col, bool fp4,
-                               uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
-                               int* err, int sm_count, cudaStream_t stream);
+cudaError_t launch_mxfp8_quant(const QuantBatch& batch, bool row, bool col, bool fp4, int* err, int sm_count,
+                               cudaStream_t stream);
 
 // Scratch bytes of the group / tensor scope path (amax, done counts, ticket).
 size_t nvfp4_scratch_bytes(int groups);

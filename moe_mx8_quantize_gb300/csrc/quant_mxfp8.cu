@@ -13,7 +13,9 @@
 // (not by requantizing one copy).
 //
 // Design: a persistent grid; each CTA streams 128x128 bf16 tiles through a
-// TMA -> shared-memory ring (2 stages, 32 KB each).  From the same staged
+// TMA -> shared-memory ring (2 stages, 32 KB each).  One launch may cover up
+// to kQuantBatchMax tensors (the X, W and dY of a linear layer): their tiles
+// form one list, so a small tensor's latency hides behind the others' tiles.  From the same staged
 // tile the CTA emits
 //   rowwise : 16 threads per row, 8 elements each (one 16-byte smem read),
 //             4-thread shuffle for the 1x32 block amax, 8-byte stores;
@@ -72,32 +74,40 @@ __device__ __forceinline__ int swz(int r, int k) {  // offset inside a 128x4 til
 }
 
 template <bool kRow, bool kCol, bool kFP4>
-__global__ void __launch_bounds__(kThreads) mxfp8_quant_kernel(
-    const __grid_constant__ CUtensorMap tmap_x, int64_t R, int64_t C, uint8_t* __restrict__ q_row,
-    uint8_t* __restrict__ s_row, uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col,
-    int* err) {
+__global__ void __launch_bounds__(kThreads) mxfp8_quant_kernel(const __grid_constant__ QuantBatch b, int* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   QuantSmem& sm = *reinterpret_cast<QuantSmem*>(
       smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023));
   const int tid = threadIdx.x;
-
-  const int64_t tiles_c = (C + kTile - 1) / kTile;
-  const int64_t tiles_r = (R + kTile - 1) / kTile;
-  const int64_t ntiles = tiles_r * tiles_c;
+  const int64_t ntiles = b.ntiles;
 
   if (tid == 0) {
-    prefetch_tmap(&tmap_x);
+    for (int i = 0; i < b.n; ++i) prefetch_tmap(&b.maps[i]);
     for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&sm.full[s]), 1);
     sm.abort = 0;
     fence_barrier_init();
   }
   __syncthreads();
 
+  // tile t of the batch -> tensor i and the tile's row / column of it
+  auto locate = [&](int64_t t, int& i, int64_t& tr, int64_t& tc) {
+    i = 0;
+#pragma unroll
+    for (int j = 1; j < kQuantBatchMax; ++j)
+      if (j < b.n && t >= b.t[j].tile0) i = j;
+    const int64_t local = t - b.t[i].tile0;
+    const int64_t tiles_c = (b.t[i].C + kTile - 1) / kTile;
+    tr = local / tiles_c;
+    tc = local % tiles_c;
+  };
+
   auto issue = [&](int64_t t, int stage) {
-    const int64_t tr = t / tiles_c, tc = t % tiles_c;
+    int i;
+    int64_t tr, tc;
+    locate(t, i, tr, tc);
     const uint32_t bar = smem_u32(&sm.full[stage]);
     mbar_arrive_expect_tx(bar, kTileBytes);
-    tma_load_2d(smem_u32(sm.tile[stage]), &tmap_x, static_cast<int32_t>(tc * kTile),
+    tma_load_2d(smem_u32(sm.tile[stage]), &b.maps[i], static_cast<int32_t>(tc * kTile),
                 static_cast<int32_t>(tr * kTile), bar);
   };
 
@@ -115,7 +125,17 @@ __global__ void __launch_bounds__(kThreads) mxfp8_quant_kernel(
     const bool ok = mbar_wait(smem_u32(&sm.full[stage]), parity, err, kErrWaitConsumer, &sm.abort);
     if (!__syncthreads_and(ok)) break;  // every thread leaves together
 
-    const int64_t tr = t / tiles_c, tc = t % tiles_c;
+    int ti;
+    int64_t tr, tc;
+    locate(t, ti, tr, tc);
+    const QuantTensor& qt = b.t[ti];
+    const int64_t R = qt.R, C = qt.C;
+    uint8_t* __restrict__ q_row = qt.q_row;
+    uint8_t* __restrict__ s_row = qt.s_row;
+    uint8_t* __restrict__ q_col = qt.q_col;
+    uint8_t* __restrict__ s_col = qt.s_col;
+    const int64_t tiles_c = (C + kTile - 1) / kTile;
+    const int64_t tiles_r = (R + kTile - 1) / kTile;
     const int64_t r0 = tr * kTile, c0 = tc * kTile;
     const uint8_t* tile = sm.tile[stage];
     uint8_t* srow = sm.srow[it & 1];
@@ -248,10 +268,10 @@ __global__ void __launch_bounds__(kThreads) mxfp8_quant_kernel(
 
 size_t mxfp8_quant_smem_bytes() { return sizeof(QuantSmem) + 1024; }
 
-cudaError_t launch_mxfp8_quant(const CUtensorMap& tmap_x, int64_t R, int64_t C, bool row, bool col, bool fp4,
-                               uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
-                               int* err, int sm_count, cudaStream_t stream) {
-  const int64_t ntiles = ((R + kTile - 1) / kTile) * ((C + kTile - 1) / kTile);
+cudaError_t launch_mxfp8_quant(const QuantBatch& batch, bool row, bool col, bool fp4, int* err, int sm_count,
+                               cudaStream_t stream) {
+  const int64_t ntiles = batch.ntiles;
+  if (ntiles == 0) return cudaSuccess;
   const size_t smem = mxfp8_quant_smem_bytes();
   auto kern = fp4 ? (row ? (col ? mxfp8_quant_kernel<true, true, true> : mxfp8_quant_kernel<true, false, true>)
                          : mxfp8_quant_kernel<false, true, true>)
@@ -266,8 +286,7 @@ cudaError_t launch_mxfp8_quant(const CUtensorMap& tmap_x, int64_t R, int64_t C, 
   if (per_sm < 1) per_sm = 1;
   const int64_t grid = ntiles < static_cast<int64_t>(sm_count) * per_sm ? ntiles
                                                                         : static_cast<int64_t>(sm_count) * per_sm;
-  kern<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmap_x, R, C, q_row, s_row, q_col,
-                                                                s_col, err);
+  kern<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(batch, err);
   return cudaGetLastError();
 }
 

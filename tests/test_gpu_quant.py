@@ -281,3 +281,64 @@ def test_swiglu_within_one_bf16_unit_of_oracle():
     ulps = _bf16_ulps(got, ref)
     assert ulps.max() <= 1
     assert (ulps == 0).mean() >= 0.999
+
+
+def _alloc_copies(fmt, R, C, flags):
+    """Output buffers of one rowwise / columnwise quantization (zeroed, so
+    every byte the kernel must write is compared)."""
+    packed = fmt == mx.FMT_MXFP4
+    z = lambda n: torch.zeros(max(n, 16), dtype=torch.uint8, device="cuda")
+    qr = z(R * C // (2 if packed else 1)) if flags & mx.ROWWISE else None
+    sr = z(mx.scale_bytes(fmt, R, C)) if flags & mx.ROWWISE else None
+    qc = z(R * C // (2 if packed else 1)) if flags & mx.COLWISE else None
+    sc = z(mx.scale_bytes(fmt, C, R)) if flags & mx.COLWISE else None
+    return qr, sr, qc, sc
+
+
+@pytest.mark.parametrize("fmt", [mx.FMT_MXFP8, mx.FMT_MXFP4])
+@pytest.mark.parametrize("flags", [mx.ROWWISE | mx.COLWISE, mx.ROWWISE, mx.COLWISE])
+def test_quantize_batch_equals_separate_calls(fmt, flags):
+    """One launch over the X, W and dY of the 2048 x 2048 -> 8192 linear layer
+    plus a ragged 96 x 160 tensor (partial 128 x 128 tiles): every output byte
+    equals the separate single-tensor calls; the ragged tensor also against
+    the oracle."""
+    lin = inputs.linear(seed=1, device="cuda")
+    rag = inputs.sweep(96, 160, seed=21, device="cuda")
+    xs = [lin["X"], lin["W"], lin["dY"], rag]
+    batch = [(x, *_alloc_copies(fmt, *x.shape, flags)) for x in xs]
+    one = [(x, *_alloc_copies(fmt, *x.shape, flags)) for x in xs]
+    mx.mx8_quantize_batch_into(fmt, batch, flags)
+    single = mx.mx8_quantize_into if fmt == mx.FMT_MXFP8 else mx.mxfp4_quantize_into
+    for x, qr, sr, qc, sc in one:
+        single(x, qr, sr, qc, sc, flags)
+    torch.cuda.synchronize()
+    for b, o in zip(batch, one):
+        for tb, to in zip(b[1:], o[1:]):
+            if tb is not None:
+                assert torch.equal(tb, to)
+    xb = inputs.bits(rag)
+    x, qr, sr, qc, sc = batch[3]
+    if fmt == mx.FMT_MXFP8:
+        rq, rs = oracle.mxfp8_quantize_rowwise(xb)
+        cq, cs = oracle.mxfp8_quantize_colwise(xb)
+    else:
+        rq, rs = oracle.mxfp4_quantize_rowwise(xb)
+        cq, cs = oracle.mxfp4_quantize_colwise(xb)
+    if flags & mx.ROWWISE:
+        assert np.array_equal(host(qr)[: rq.size], rq.ravel())
+        sw = oracle.swizzle_scales(rs)
+        assert np.array_equal(host(sr)[: sw.size], sw)
+    if flags & mx.COLWISE:
+        assert np.array_equal(host(qc)[: cq.size], cq.ravel())
+        sw = oracle.swizzle_scales(cs)
+        assert np.array_equal(host(sc)[: sw.size], sw)
+
+
+def test_quantize_batch_skips_empty_items():
+    x = inputs.sweep(64, 96, seed=3, device="cuda")
+    empty = torch.empty((0, 96), dtype=torch.bfloat16, device="cuda")
+    a = _alloc_copies(mx.FMT_MXFP8, 64, 96, mx.ROWWISE | mx.COLWISE)
+    mx.mx8_quantize_batch_into(mx.FMT_MXFP8, [(empty, None, None, None, None), (x, *a)])
+    q, s = oracle.mxfp8_quantize_rowwise(inputs.bits(x))
+    torch.cuda.synchronize()
+    assert np.array_equal(host(a[0])[: q.size], q.ravel())

@@ -141,3 +141,17 @@ def test_status_strings(lib):
     for s in range(7):
         assert m.status_string(s)
     assert m.status_string(m.ERR_TIMEOUT) == "a bounded device wait ran out"
+
+
+def test_quantize_batch_rejects_bad_counts(lib):
+    import moe_mx8_quantize_gb300 as m
+    items = (m.QuantizeItem * 5)()
+    for n in (0, 5, -1):
+        assert lib.mx8_quantize_batch(m.FMT_MXFP8, ctypes.cast(items, ctypes.c_void_p), n, m.ROWWISE, None, 0,
+                                      None) == m.ERR_INVALID_ARG
+    assert lib.mx8_quantize_batch(m.FMT_NVFP4, ctypes.cast(items, ctypes.c_void_p), 1, m.ROWWISE, None, 0,
+                                  None) == m.ERR_INVALID_ARG
+    # one item with cols % 32 != 0 fails the whole call before any launch
+    items[0] = m.QuantizeItem(16, 64, 48, 48, 16, 16, None, None)
+    assert lib.mx8_quantize_batch(m.FMT_MXFP8, ctypes.cast(items, ctypes.c_void_p), 1, m.ROWWISE, None, 0,
+                                  None) == m.ERR_INVALID_ARG
