@@ -1282,6 +1282,41 @@ def run_reference(args):
     ranks.emit(out)
 
 
+def run_profile(args):
+    """For ncu: every launch of the step and of the parts timed beside it
+    (not the DeepSeek-V3 layer or the sweep, whose kernels are the step's at
+    other shapes), once as warm-up and once more to be captured
+    (`ncu --launch-skip` = the launches of the first pass).  Prints the labels
+    in launch order with their kernel counts."""
+    import torch
+    import __graft_entry__
+    import moe_mx8_quantize_gb300 as mx
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    step = Step(dev)
+    parts = [("step", step, step.launches(), Step.KERNELS_PER_LABEL),
+             ("mxfp4_linear", None, None, {}), ("dequantized_backward", None, None, {}),
+             ("nvfp4_recipe_linear", None, None, Nvfp4RecipeLinear.KERNELS), ("moe_gate_up_quant_h", None, None, {})]
+    objs = {"mxfp4_linear": Mxfp4Linear, "dequantized_backward": DequantBackward,
+            "nvfp4_recipe_linear": Nvfp4RecipeLinear, "moe_gate_up_quant_h": FusedQuantH}
+    seq = []
+    for name, obj, fl, kern in parts:
+        if obj is None:
+            obj = objs[name](step)
+            fl = obj.launches()
+        seq += [(f"{name}: {lab}", fn, kern.get(lab, 1)) for lab, fn in fl]
+    for _ in range(2):
+        for _, fn, _ in seq:
+            fn()
+        torch.cuda.synchronize()
+    for ws in step.workspaces():
+        if mx.check_device_error(ws) != mx.OK:
+            raise RuntimeError("device error in the profile pass")
+    print(json.dumps({"kernels_per_pass": sum(k for _, _, k in seq),
+                      "launches": [[lab, k] for lab, _, k in seq]}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1291,9 +1326,12 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-extra", action="store_true", help="skip the MXFP4 linear-layer measurement")
+    ap.add_argument("--no-extra", action="store_true", help="skip the measurements beside the step")
+    ap.add_argument("--profile", action="store_true", help="run every launch twice for ncu and exit")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.profile:
+        run_profile(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)
