@@ -289,8 +289,13 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
   constexpr bool kGather = (kMode & kModeGather) != 0;
   constexpr bool kSwiGLU = (kMode & kModeSwiGLU) != 0;
   constexpr bool kQuantH = (kMode & kModeQuantH) != 0;
-  // scales moved into tensor memory by the epilogue warps (else tcgen05.cp)
+  // scales moved into tensor memory by the epilogue warps (single GEMMs), by
+  // the producer warps and the MMA warp (grouped GEMMs: their epilogue warps
+  // are busy; with BN = 256 those four warps cover the four lane quarters),
+  // else by the MMA thread with tcgen05.cp (gathered A)
   constexpr bool kWarpScales = F::kSfTiles > 0 && !kGrouped;
+  constexpr bool kProdScales = F::kSfTiles > 0 && kGrouped && !kGather && kBN == 256;
+  constexpr bool kSepScales = kWarpScales || kProdScales;   // scale tiles land on their own barrier
   static_assert(kGather <= kGrouped && kSwiGLU <= kGrouped, "fused modes are grouped only");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -309,7 +314,7 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
       mbar_init(smem_u32(&sm.full[s]), L::kProducers);
       mbar_init(smem_u32(&sm.empty[s]), 1);
       mbar_init(smem_u32(&sm.sf_full[s]), 1 + L::kBRow128);
-      mbar_init(smem_u32(&sm.sf_ready[s]), L::kEpiWarps);
+      mbar_init(smem_u32(&sm.sf_ready[s]), kProdScales ? 4 : L::kEpiWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sm.acc_full[i]), 1);
@@ -381,6 +386,98 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
     return F::kSfTiles == 0 ? 0 : static_cast<int>(sf_kt - sf0 < F::kSfTiles ? sf_kt - sf0 : F::kSfTiles);
   };
 
+  // Scale staging (kSepScales).  Each 512-byte scale tile is 32 rows of 16
+  // bytes; every lane quarter of tensor memory gets the same 32 x 16 bytes,
+  // row i in lane i of the quarter, over the tile's 4 columns (the layout the
+  // block-scaled MMA reads).  A staging warp moves its quarter of every stage,
+  // in order, as soon as the stage's scale tiles have landed, then arrives on
+  // the stage's "scales ready" barrier.  Single GEMMs: the epilogue warps
+  // (A's tiles by the first four, B's by the last four).  Grouped GEMMs with
+  // BN = 256: the A producer, the MMA warp and the two B producers (warps 0,
+  // 1, 10, 11: one per quarter), A's and B's tiles each, between their own
+  // waits.  A stage can only be refilled after its MMAs, which wait for its
+  // scales, so a stage's barriers are never more than one phase ahead and its
+  // shared-memory tiles and tensor-memory columns are never overwritten while
+  // in use.
+  const int cta_units = unit0 < nunits ? static_cast<int>((nunits - 1 - unit0) / ustep + 1) : 0;
+  const int stage_total = kSepScales ? cta_units * ktiles : 0;
+  const int squarter = warp & 3;
+  const bool epi_warp = warp >= 2 && warp < 2 + L::kEpiWarps;
+  const bool stager = kWarpScales ? epi_warp : (kProdScales && !epi_warp);
+  const bool stage_a = kProdScales || (warp - 2) / 4 == 0;
+  const bool stage_b = kProdScales || (warp - 2) / 4 == L::kBRow128 - 1;
+  int staged = 0;
+  auto stage_scales = [&](int j) {
+    const int ss = j % L::kStages;
+    const uint32_t tq = tmem + (static_cast<uint32_t>(squarter * 32) << 16) + L::kAccCols +
+                        static_cast<uint32_t>(ss) * L::kSfColsPerStage;
+    if (stage_a) {
+#pragma unroll
+      for (int jj = 0; jj < F::kSfTiles; ++jj)
+        tmem_st_32x32b_x4(tq + 4 * jj, *reinterpret_cast<const uint4*>(sm.sfa[ss] + 512 * jj + 16 * lane));
+    }
+    if (stage_b) {
+#pragma unroll
+      for (int jj = 0; jj < F::kSfTiles; ++jj)
+#pragma unroll
+        for (int h = 0; h < L::kBRow128; ++h)
+          tmem_st_32x32b_x4(tq + L::kSfaCols + (jj * L::kBRow128 + h) * 4,
+                            *reinterpret_cast<const uint4*>(sm.sfb[ss] + (h * F::kSfTiles + jj) * 512 + 16 * lane));
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&sm.sf_ready[ss]));
+  };
+  // Stages every landed stage below `limit` (warp-uniform, never blocks).
+  auto stage_landed = [&](int limit) -> bool {
+    bool any = false;
+    if (kSepScales && stager) {
+      const int lim = limit < stage_total ? limit : stage_total;
+      while (staged < lim && __all_sync(0xffffffffu, mbar_test_wait(smem_u32(&sm.sf_full[staged % L::kStages]),
+                                                                    (staged / L::kStages) & 1))) {
+        stage_scales(staged++);
+        any = true;
+      }
+    }
+    return any;
+  };
+  // Warp-uniform bounded wait for the phase `parity` of barrier `bar`, staging
+  // landed scales below `limit` meanwhile.  The producer and MMA warps sleep
+  // in mbarrier.try_wait (first on the oldest stage they still have to move:
+  // its scales land before the operands and before the stage is released, so
+  // it is the next event; then on `bar`); the epilogue warps of single GEMMs
+  // poll, as they have their own work between the tests.
+  auto wait_staging = [&](uint32_t bar, uint32_t parity, int limit, int code) -> bool {
+    const int lim = limit < stage_total ? limit : stage_total;
+    uint64_t t0 = 0;
+    while (true) {
+      if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
+      if (stager && staged < lim) {
+        const uint32_t sb = smem_u32(&sm.sf_full[staged % L::kStages]);
+        const uint32_t sp = (staged / L::kStages) & 1;
+        if (__all_sync(0xffffffffu, kProdScales ? mbar_try_wait(sb, sp) : mbar_test_wait(sb, sp))) {
+          stage_scales(staged++);
+          t0 = 0;
+          continue;
+        }
+      } else if (kProdScales) {
+        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+      }
+      if (__any_sync(0xffffffffu, *reinterpret_cast<volatile int*>(&sm.abort) != 0)) return false;
+      const uint64_t now = __shfl_sync(0xffffffffu, globaltimer(), 0);
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitLimitNs) {
+        if (lane == 0) {
+          atomicCAS(err, 0, code);
+          sm.abort = 1;
+        }
+        return false;
+      }
+    }
+  };
+
   if (prod >= 0) {
     // ------------------------------------------------------------ producers
     if (kGather && prod == 0) {
@@ -447,7 +544,8 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
           mbar_wait(smem_u32(&sm.full[j % L::kStages]), (j / L::kStages) & 1, err, kErrWaitTeardown,
                     nullptr, 100000000ull);
       }
-    } else if (lane == 0) {
+    } else if (kProdScales || lane == 0) {
+      // (with producer staging the whole warp runs the loop; lane 0 issues)
       int it = 0;
       bool ok = true;
       for (int64_t u = unit0; ok && u < nunits; u += ustep) {
@@ -458,7 +556,14 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
         for (int kt = 0; kt < ktiles; ++kt, ++it) {
           const int s = it % L::kStages;
           const uint32_t ph = (it / L::kStages) & 1;
-          if (!mbar_wait(smem_u32(&sm.empty[s]), ph ^ 1, err, kErrWaitProducer, &sm.abort)) {
+          if constexpr (kProdScales) {
+            const uint32_t eb = smem_u32(&sm.empty[s]);
+            if (!wait_staging(eb, ph ^ 1, it, kErrWaitProducer)) {
+              ok = false;
+              break;
+            }
+            if (lane != 0) continue;
+          } else if (!mbar_wait(smem_u32(&sm.empty[s]), ph ^ 1, err, kErrWaitProducer, &sm.abort)) {
             ok = false;
             break;
           }
@@ -472,8 +577,8 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
           if constexpr (F::kSfTiles > 0) {
             int64_t sf0;
             const int nsf = scale_tiles_of_stage(kt, sf0);
-            const uint32_t sbar = kWarpScales ? smem_u32(&sm.sf_full[s]) : full;
-            if (kWarpScales) {
+            const uint32_t sbar = kSepScales ? smem_u32(&sm.sf_full[s]) : full;
+            if (kSepScales) {
               mbar_arrive_expect_tx(sbar, nsf * 512);
               mbar_arrive_expect_tx(full, op_bytes);
             } else {
@@ -503,12 +608,24 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
           }
         }
       }
-      if (!ok) {
+      if constexpr (kProdScales) {
+        // the stages this warp has not moved yet (the MMAs wait for them)
+        if (ok) {
+          const int last = stage_total;
+          while (ok && staged < last) {
+            const uint32_t fb = smem_u32(&sm.sf_full[staged % L::kStages]);
+            const uint32_t fp = (staged / L::kStages) & 1;
+            ok = wait_staging(fb, fp, staged, kErrWaitScales);
+            if (ok) stage_scales(staged++);
+          }
+        }
+      }
+      if (!ok && lane == 0) {
         // let the copies already issued land before the block exits
         for (int j = (it > L::kStages ? it - L::kStages : 0); j < it; ++j) {
           mbar_wait(smem_u32(&sm.full[j % L::kStages]), (j / L::kStages) & 1, err, kErrWaitTeardown,
                     nullptr, 100000000ull);
-          if (kWarpScales)
+          if (kSepScales)
             mbar_wait(smem_u32(&sm.sf_full[j % L::kStages]), (j / L::kStages) & 1, err, kErrWaitTeardown,
                       nullptr, 100000000ull);
         }
@@ -516,14 +633,22 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // (with producer staging the whole warp runs the loop, moving its lane
+    // quarter of each stage's scales while it waits; lane 0 issues)
+    if (kProdScales || lane == 0) {
       int it = 0, tcount = 0;
       bool ok = true;
       const uint32_t sf_base = tmem + L::kAccCols;
       for (int64_t u = unit0; ok && u < nunits; u += ustep, ++tcount) {
         const int as = tcount % L::kAccBufs;
         const uint32_t aph = (tcount / L::kAccBufs) & 1;
-        if (!mbar_wait(smem_u32(&sm.acc_empty[as]), aph ^ 1, err, kErrWaitAccum, &sm.abort)) {
+        if constexpr (kProdScales) {
+          const uint32_t eb = smem_u32(&sm.acc_empty[as]);
+          if (!wait_staging(eb, aph ^ 1, it + 1, kErrWaitAccum)) {
+            ok = false;
+            break;
+          }
+        } else if (!mbar_wait(smem_u32(&sm.acc_empty[as]), aph ^ 1, err, kErrWaitAccum, &sm.abort)) {
           ok = false;
           break;
         }
@@ -532,14 +657,24 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
         for (int kt = 0; kt < ktiles; ++kt, ++it) {
           const int s = it % L::kStages;
           const uint32_t ph = (it / L::kStages) & 1;
-          if (!mbar_wait(smem_u32(&sm.full[s]), ph, err, kErrWaitConsumer, &sm.abort)) {
-            ok = false;
-            break;
-          }
-          if constexpr (kWarpScales) {
-            if (!mbar_wait(smem_u32(&sm.sf_ready[s]), ph, err, kErrWaitScales, &sm.abort)) {
+          if constexpr (kProdScales) {
+            // this warp's own quarter first (the scales land before the operands)
+            const uint32_t fb = smem_u32(&sm.full[s]), rb = smem_u32(&sm.sf_ready[s]);
+            if (!wait_staging(fb, ph, it + 1, kErrWaitConsumer) || !wait_staging(rb, ph, it + 1, kErrWaitScales)) {
               ok = false;
               break;
+            }
+            if (lane != 0) continue;
+          } else {
+            if (!mbar_wait(smem_u32(&sm.full[s]), ph, err, kErrWaitConsumer, &sm.abort)) {
+              ok = false;
+              break;
+            }
+            if constexpr (kWarpScales) {
+              if (!mbar_wait(smem_u32(&sm.sf_ready[s]), ph, err, kErrWaitScales, &sm.abort)) {
+                ok = false;
+                break;
+              }
             }
           }
           tc_fence_after();
@@ -549,7 +684,7 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
           // blocks adjacent
           const uint32_t tsfa = sf_base + s * L::kSfColsPerStage;
           const uint32_t tsfb = tsfa + L::kSfaCols;
-          if constexpr (F::kSfTiles > 0 && !kWarpScales) {
+          if constexpr (F::kSfTiles > 0 && !kSepScales) {
             int64_t sf0;
             const int nsf = scale_tiles_of_stage(kt, sf0);
             for (int j = 0; j < nsf; ++j) {
@@ -587,11 +722,13 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
           tc_commit(smem_u32(&sm.empty[s]));   // stage free once these MMAs finish
         }
         if (!ok) break;
-        tc_commit(smem_u32(&sm.acc_full[as]));  // accumulator ready for the epilogue
+        if (lane == 0) tc_commit(smem_u32(&sm.acc_full[as]));  // accumulator ready for the epilogue
       }
       // no MMA may be in flight when tensor memory is released
-      tc_commit(smem_u32(&sm.drain));
-      mbar_wait(smem_u32(&sm.drain), 0, err, kErrWaitTeardown, nullptr, 100000000ull);
+      if (lane == 0) {
+        tc_commit(smem_u32(&sm.drain));
+        mbar_wait(smem_u32(&sm.drain), 0, err, kErrWaitTeardown, nullptr, 100000000ull);
+      }
     }
   } else {
     // ------------------------------------------------------------ epilogue (warps 2 .. 1 + kEpiWarps)
@@ -599,78 +736,15 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
     const int quarter = warp & 3;              // tcgen05.ld lane quarter of this warp
     const int col0 = (ew / 4) * 128;           // this warp's 128 accumulator columns
     const int r_in_tile = quarter * 32 + lane;
-    // Scale staging.  Each 512-byte scale tile is 32 rows of 16 bytes; every
-    // lane quarter of tensor memory gets the same 32 x 16 bytes, row i in
-    // lane i of the quarter, over the tile's 4 columns (the layout the
-    // block-scaled MMA reads).  Stages are staged in order as their scale
-    // tiles land: a stage can only be refilled after its MMAs, which wait for
-    // its scales, so a stage's barriers are never more than one phase ahead.
-    const int cta_tiles = unit0 < nunits ? static_cast<int>((nunits - 1 - unit0) / ustep + 1) : 0;
-    const int total_stages = kWarpScales ? cta_tiles * ktiles : 0;
-    const bool stage_a = ew / 4 == 0, stage_b = ew / 4 == L::kBRow128 - 1;
-    int staged = 0;
-    auto stage_scales = [&](int it) {
-      const int s = it % L::kStages;
-      const uint32_t tq = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + L::kAccCols +
-                          static_cast<uint32_t>(s) * L::kSfColsPerStage;
-      if (stage_a) {
-#pragma unroll
-        for (int j = 0; j < F::kSfTiles; ++j)
-          tmem_st_32x32b_x4(tq + 4 * j, *reinterpret_cast<const uint4*>(sm.sfa[s] + 512 * j + 16 * lane));
-      }
-      if (stage_b) {
-#pragma unroll
-        for (int j = 0; j < F::kSfTiles; ++j)
-#pragma unroll
-          for (int h = 0; h < L::kBRow128; ++h)
-            tmem_st_32x32b_x4(tq + L::kSfaCols + (j * L::kBRow128 + h) * 4,
-                              *reinterpret_cast<const uint4*>(sm.sfb[s] + (h * F::kSfTiles + j) * 512 + 16 * lane));
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm.sf_ready[s]));
-    };
-    // Stages every stage whose scale tiles have landed (warp-uniform, never
-    // blocks); called between the pieces of the epilogue's own work too, so
-    // the MMAs of the next tile keep their scales while a tile is stored.
-    auto stage_landed = [&]() -> bool {
-      bool any = false;
-      if constexpr (kWarpScales) {
-        while (staged < total_stages &&
-               __all_sync(0xffffffffu, mbar_test_wait(smem_u32(&sm.sf_full[staged % L::kStages]),
-                                                      (staged / L::kStages) & 1))) {
-          stage_scales(staged++);
-          any = true;
-        }
-      }
-      return any;
-    };
     // Waits (warp-uniformly, bounded) for accumulator `as` to fill, staging
-    // every stage that lands meanwhile.
+    // (single GEMMs) every stage that lands meanwhile.
     auto wait_accumulator = [&](int as, uint32_t aph) -> bool {
       if constexpr (!kWarpScales) {
         return __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.acc_full[as]), aph, err, kErrWaitEpilogue, &sm.abort));
       } else {
-        uint64_t t0 = 0;
-        while (true) {
-          if (__all_sync(0xffffffffu, mbar_test_wait(smem_u32(&sm.acc_full[as]), aph))) return true;
-          if (stage_landed()) {
-            t0 = 0;
-            continue;
-          }
-          if (__any_sync(0xffffffffu, *reinterpret_cast<volatile int*>(&sm.abort) != 0)) return false;
-          const uint64_t now = __shfl_sync(0xffffffffu, globaltimer(), 0);
-          if (t0 == 0) {
-            t0 = now;
-          } else if (now - t0 > kWaitLimitNs) {
-            if (lane == 0) {
-              atomicCAS(err, 0, staged < total_stages ? kErrWaitScales : kErrWaitEpilogue);
-              sm.abort = 1;
-            }
-            return false;
-          }
-        }
+        const uint32_t fb = smem_u32(&sm.acc_full[as]);
+        return wait_staging(fb, aph, stage_total,
+                            staged < stage_total ? kErrWaitScales : kErrWaitEpilogue);
       }
     };
     int tcount = 0;
@@ -692,7 +766,7 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.acc_empty[as]));   // accumulator drained into registers
-      stage_landed();
+      if constexpr (kWarpScales) stage_landed(stage_total);
 
       const TileCoord tc = tile_of(u);
       const bool row_ok = r_in_tile < tc.rows;
@@ -825,7 +899,7 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
         const int32_t y = static_cast<int32_t>(tc.a_row0 + quarter * 32);
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
-          if (ch > 0) stage_landed();
+          if (kWarpScales && ch > 0) stage_landed(stage_total);
           const int64_t n0 = tc.n0 + col0 + ch * 32;
           if (n0 >= N) break;
           float v[32];
