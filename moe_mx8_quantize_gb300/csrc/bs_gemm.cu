@@ -146,9 +146,13 @@ struct Layout {
   static constexpr int kSfaBytes = Cfg<kFmt>::kSfTiles > 0 ? Cfg<kFmt>::kSfTiles * 512 : 16;
   static constexpr int kSfbBytes = Cfg<kFmt>::kSfTiles > 0 ? Cfg<kFmt>::kSfTiles * 512 * kBRow128 : 16;
   static constexpr int kStageBytes = kTileABytes + kTileBBytes + kSfaBytes + kSfbBytes;
-  static constexpr int kEpiStageBytes = 2048;                         // 32 rows x 64 B per epilogue warp
+  // 32 rows x 64 B per epilogue warp for the bulk stores (the SwiGLU
+  // epilogue stores h directly; with h quantization the area holds the row
+  // maxima)
+  static constexpr int kEpiStageBytes = (kMode & kModeSwiGLU) && !(kMode & kModeQuantH) ? 16 : 2048;
   static constexpr int kFixed = 256 + (kBN / 32) * kEpiStageBytes + ((kMode & kModeQuantH) ? 1024 + 32 : 0) +
-                                (kGrouped ? static_cast<int>(sizeof(GroupSmem)) : 0);
+                                ((kMode & kModeGather) ? 4 * BM : 0) +
+                                (kGrouped ? static_cast<int>(sizeof(GroupTiles)) : 0);
   static constexpr int kStagesFit = (kSmemBudget - kFixed) / kStageBytes;
   static constexpr int kStages = kStagesFit > 10 ? 10 : kStagesFit;
   static constexpr int kAccBufs = kBN == 128 ? 2 : 1;
@@ -190,7 +194,7 @@ struct __align__(1024) GemmSmem {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-  int32_t gtok[BM];                                   // gathered mode: source rows of the tile
+  int32_t gtok[(kMode & kModeGather) ? BM : 1];       // gathered mode: source rows of the tile
   uint64_t hmax_full[2];                              // h quantization: a band's row maxima are all in
   float2 tab[(kMode & kModeQuantH) ? 128 : 1];        // h quantization: {E4M3 value, RN(1/value)}
 };
@@ -236,7 +240,7 @@ struct TileCoord {
 
 template <bool kGrouped, int kNT>
 __device__ __forceinline__ TileCoord decode_tile(int64_t t, int64_t tiles_n, int64_t M,
-                                                 const GroupSmem* gs, int G) {
+                                                 const GroupTiles* gs, int G) {
   TileCoord c;
   if (!kGrouped) {
     const int64_t tm = (M + BM - 1) / BM;
@@ -249,9 +253,9 @@ __device__ __forceinline__ TileCoord decode_tile(int64_t t, int64_t tiles_n, int
     return c;
   }
   const int64_t gmt = t / tiles_n;                   // global m-tile band
-  const int g = upper_group(gs->pref, G, gmt * BM);
-  const int64_t mt0 = gs->pref[g] / BM;
-  const int64_t mtiles = gs->pref[g + 1] / BM - mt0;
+  const int g = upper_group(gs->tpref, G, gmt);
+  const int64_t mt0 = gs->tpref[g];
+  const int64_t mtiles = gs->tpref[g + 1] - mt0;
   const int64_t local = t - mt0 * tiles_n;
   const int64_t mt = local % mtiles, nt = local / mtiles;
   const int64_t ng = gs->offs[g + 1] - gs->offs[g];
@@ -265,10 +269,10 @@ __device__ __forceinline__ TileCoord decode_tile(int64_t t, int64_t tiles_n, int
 
 // Grouped band gmt (a 128-row tile of the padded grouped layout) and h tile
 // nt of the cluster mode.
-__device__ __forceinline__ TileCoord decode_band(int64_t gmt, int nt, const GroupSmem* gs, int G) {
+__device__ __forceinline__ TileCoord decode_band(int64_t gmt, int nt, const GroupTiles* gs, int G) {
   TileCoord c;
-  const int g = upper_group(gs->pref, G, gmt * BM);
-  const int64_t mt = gmt - gs->pref[g] / BM;
+  const int g = upper_group(gs->tpref, G, gmt);
+  const int64_t mt = gmt - gs->tpref[g];
   const int64_t ng = gs->offs[g + 1] - gs->offs[g];
   c.g = g;
   c.a_row0 = gs->offs[g] + mt * BM;
@@ -300,7 +304,7 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   Smem& sm = *reinterpret_cast<Smem*>(base);
-  GroupSmem* gs = reinterpret_cast<GroupSmem*>(base + sizeof(Smem));
+  GroupTiles* gs = reinterpret_cast<GroupTiles*>(base + sizeof(Smem));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int* err = args.err;
@@ -335,7 +339,7 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
     tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
     tmem_relinquish();
   }
-  if (kGrouped) load_group_prefix(*gs, args.offs, args.G);   // contains __syncthreads
+  if (kGrouped) load_group_tiles(*gs, args.offs, args.G);   // contains __syncthreads
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -351,7 +355,7 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
   const int64_t n_out = kSwiGLU ? F_ : N;
   const int64_t tiles_n = (n_out + kNT - 1) / kNT;
   const int64_t n_rt = (N + 127) / 128;                   // 128-row scale tiles of B (per group)
-  const int64_t tiles_m = kGrouped ? gs->pref[args.G] / BM : (M + BM - 1) / BM;
+  const int64_t tiles_m = kGrouped ? gs->tpref[args.G] : (M + BM - 1) / BM;
   // output tiles strided over the CTAs; with h quantization, 128-row bands
   // strided over the clusters, CTA rank r of a cluster taking h tile r
   const int64_t nunits = kQuantH ? tiles_m : tiles_m * tiles_n;
@@ -1008,7 +1012,7 @@ cudaError_t launch_variant(const GemmArgs& a, const CUtensorMap& tmap_a, const C
   const unsigned grid = static_cast<unsigned>(ntiles < sm_count ? ntiles : sm_count);
   if (grid == 0) return cudaSuccess;
   auto k = bs_gemm_kernel<kFmt, kGrouped, kBN, kMode>;
-  constexpr size_t smem = sizeof(GemmSmem<kFmt, kGrouped, kBN, kMode>) + (kGrouped ? sizeof(GroupSmem) : 0) + 1024;
+  constexpr size_t smem = sizeof(GemmSmem<kFmt, kGrouped, kBN, kMode>) + (kGrouped ? sizeof(GroupTiles) : 0) + 1024;
   static_assert(smem <= 227 * 1024, "shared memory over the per-block limit");
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -1026,7 +1030,7 @@ cudaError_t launch_quant_h(const GemmArgs& a, const CUtensorMap& tmap_a, const C
   const int cs = static_cast<int>(a.ffn / 128);
   if (cs < 1 || cs > kMaxClusterTiles || a.ffn % 128 != 0) return cudaErrorInvalidValue;
   auto k = bs_gemm_kernel<1, true, 256, kMode>;
-  constexpr size_t smem = sizeof(GemmSmem<1, true, 256, kMode>) + sizeof(GroupSmem) + 1024;
+  constexpr size_t smem = sizeof(GemmSmem<1, true, 256, kMode>) + sizeof(GroupTiles) + 1024;
   static_assert(smem <= 227 * 1024, "shared memory over the per-block limit");
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
