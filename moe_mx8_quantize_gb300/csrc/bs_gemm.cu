@@ -46,11 +46,16 @@
 //     so the tensor pipe runs MMAs only.  A tcgen05.cp of a 512-byte scale
 //     tile costs the in-order tensor pipe about 45 ns; NVFP4 copies 12 per
 //     stage, which was 40% of the Fprop GEMM (39 -> 31 us on 2048x2048->8192);
-//   - grouped GEMM: the MMA thread copies them (tcgen05.cp) right before the
-//     stage's MMAs.  The MoE GEMMs have short K per tile (3 stages for the
-//     768-wide down projection) and, for gate|up, a SwiGLU epilogue, and the
-//     epilogue warps then could not keep the MMAs fed (gate|up 154-214 us
-//     against 115 us with the copies).
+//   - grouped GEMM (BN = 256): the three producer warps, each right after
+//     issuing its loads, and one more warp (epilogue warp 5 in the SwiGLU
+//     GEMM, between its own work; the MMA warp in the others) move one lane
+//     quarter each.  The MoE GEMMs have short K per tile (3 stages for the
+//     768-wide down projection) and, for gate|up, a SwiGLU epilogue: the
+//     epilogue warps alone could not keep the MMAs fed (gate|up 154-214 us
+//     against 115 us with tcgen05.cp in the MMA thread); with the producers
+//     staging, the DeepSeek-V3-shaped gate|up runs in 2139 us against 3019;
+//   - grouped GEMM with gathered A: the MMA thread copies them with
+//     tcgen05.cp right before the stage's MMAs.
 // BN = 128 keeps two accumulators (epilogue fully overlapped); BN = 256 moves
 // half the operand bytes per FLOP of BN = 128 and keeps one accumulator (the
 // 512 tensor-memory columns hold 256 accumulator columns plus the scales).
@@ -300,6 +305,16 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
   constexpr bool kWarpScales = F::kSfTiles > 0 && !kGrouped;
   constexpr bool kProdScales = F::kSfTiles > 0 && kGrouped && !kGather && kBN == 256;
   constexpr bool kSepScales = kWarpScales || kProdScales;   // scale tiles land on their own barrier
+  // Lane quarter 1 of the producer staging: epilogue warp 5 in the SwiGLU
+  // GEMM (it stages while it waits for an accumulator and half-way through
+  // each tile's SwiGLU); the MMA warp in the other modes, whose epilogues
+  // stage badly (long bulk stores, cluster exchanges).  A tcgen05.st /
+  // wait::st in the warp that issues the MMAs waits for its MMAs in flight
+  // and so serialises them with the staging.
+  // (Measured: gate|up 2569 -> 2139 us on the DeepSeek-V3 shape; warp 5
+  // staging in the down projection made it 71.6 -> 79.8 us on Qwen3.)
+  constexpr bool kEpiStager = kProdScales && kSwiGLU && !kQuantH;
+  constexpr bool kMmaStages = kProdScales && !kEpiStager;
   static_assert(kGather <= kGrouped && kSwiGLU <= kGrouped, "fused modes are grouped only");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -407,7 +422,9 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
   const int stage_total = kSepScales ? cta_units * ktiles : 0;
   const int squarter = warp & 3;
   const bool epi_warp = warp >= 2 && warp < 2 + L::kEpiWarps;
-  const bool stager = kWarpScales ? epi_warp : (kProdScales && !epi_warp);
+  // (grouped: warps 0, 10, 11 and 5 or 1, see kEpiStager)
+  const bool stager = kWarpScales ? epi_warp
+                                  : (kProdScales && (warp == 0 || warp >= 2 + L::kEpiWarps || warp == (kEpiStager ? 5 : 1)));
   const bool stage_a = kProdScales || (warp - 2) / 4 == 0;
   const bool stage_b = kProdScales || (warp - 2) / 4 == L::kBRow128 - 1;
   int staged = 0;
@@ -637,18 +654,17 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // (with producer staging the whole warp runs the loop, moving its lane
-    // quarter of each stage's scales while it waits; lane 0 issues)
-    if (kProdScales || lane == 0) {
+    // (when it stages a lane quarter the whole warp runs the loop; lane 0
+    // issues)
+    if (kMmaStages || lane == 0) {
       int it = 0, tcount = 0;
       bool ok = true;
       const uint32_t sf_base = tmem + L::kAccCols;
       for (int64_t u = unit0; ok && u < nunits; u += ustep, ++tcount) {
         const int as = tcount % L::kAccBufs;
         const uint32_t aph = (tcount / L::kAccBufs) & 1;
-        if constexpr (kProdScales) {
-          const uint32_t eb = smem_u32(&sm.acc_empty[as]);
-          if (!wait_staging(eb, aph ^ 1, it + 1, kErrWaitAccum)) {
+        if constexpr (kMmaStages) {
+          if (!wait_staging(smem_u32(&sm.acc_empty[as]), aph ^ 1, it + 1, kErrWaitAccum)) {
             ok = false;
             break;
           }
@@ -661,10 +677,10 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
         for (int kt = 0; kt < ktiles; ++kt, ++it) {
           const int s = it % L::kStages;
           const uint32_t ph = (it / L::kStages) & 1;
-          if constexpr (kProdScales) {
+          if constexpr (kMmaStages) {
             // this warp's own quarter first (the scales land before the operands)
-            const uint32_t fb = smem_u32(&sm.full[s]), rb = smem_u32(&sm.sf_ready[s]);
-            if (!wait_staging(fb, ph, it + 1, kErrWaitConsumer) || !wait_staging(rb, ph, it + 1, kErrWaitScales)) {
+            if (!wait_staging(smem_u32(&sm.full[s]), ph, it + 1, kErrWaitConsumer) ||
+                !wait_staging(smem_u32(&sm.sf_ready[s]), ph, it + 1, kErrWaitScales)) {
               ok = false;
               break;
             }
@@ -674,7 +690,7 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
               ok = false;
               break;
             }
-            if constexpr (kWarpScales) {
+            if constexpr (kSepScales) {
               if (!mbar_wait(smem_u32(&sm.sf_ready[s]), ph, err, kErrWaitScales, &sm.abort)) {
                 ok = false;
                 break;
@@ -741,15 +757,15 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
     const int col0 = (ew / 4) * 128;           // this warp's 128 accumulator columns
     const int r_in_tile = quarter * 32 + lane;
     // Waits (warp-uniformly, bounded) for accumulator `as` to fill, staging
-    // (single GEMMs) every stage that lands meanwhile.
+    // (single GEMMs; warp 5 of the SwiGLU GEMM) every stage that lands
+    // meanwhile.
     auto wait_accumulator = [&](int as, uint32_t aph) -> bool {
-      if constexpr (!kWarpScales) {
-        return __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.acc_full[as]), aph, err, kErrWaitEpilogue, &sm.abort));
-      } else {
-        const uint32_t fb = smem_u32(&sm.acc_full[as]);
-        return wait_staging(fb, aph, stage_total,
-                            staged < stage_total ? kErrWaitScales : kErrWaitEpilogue);
+      const uint32_t fb = smem_u32(&sm.acc_full[as]);
+      if constexpr (kWarpScales || kEpiStager) {
+        if (stager)
+          return wait_staging(fb, aph, stage_total, staged < stage_total ? kErrWaitScales : kErrWaitEpilogue);
       }
+      return __all_sync(0xffffffffu, mbar_wait(fb, aph, err, kErrWaitEpilogue, &sm.abort));
     };
     int tcount = 0;
     for (int64_t u = unit0; u < nunits; u += ustep, ++tcount) {
@@ -770,7 +786,7 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.acc_empty[as]));   // accumulator drained into registers
-      if constexpr (kWarpScales) stage_landed(stage_total);
+      if constexpr (kWarpScales || kEpiStager) stage_landed(stage_total);
 
       const TileCoord tc = tile_of(u);
       const bool row_ok = r_in_tile < tc.rows;
@@ -796,11 +812,13 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
       const float s_ab = __fmul_rn(sa, sg);
       if constexpr (kSwiGLU && !kQuantH) {
         // g and u rounded to bf16 exactly as the unfused gate|up output would
-        // be, then h = RN_bf16(silu(g) * u): 64 columns, 128 contiguous bytes
-        if (!row_ok) continue;
+        // be, then h = RN_bf16(silu(g) * u): 64 columns, 128 contiguous bytes.
+        // Every lane runs the loop (rows past the tile's end store nothing),
+        // so the warp can stage scales half-way through.
         uint4* hrow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(args.C) + m * args.ldc + tc.n0 + 64 * half);
 #pragma unroll
         for (int q8 = 0; q8 < 8; ++q8) {
+          if (kEpiStager && q8 == 4) stage_landed(stage_total);   // (warp-uniform here)
           uint32_t p[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -814,7 +832,7 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
             }
             p[j] = pack_bf16x2(hv[0], hv[1]);
           }
-          hrow[q8] = make_uint4(p[0], p[1], p[2], p[3]);
+          if (row_ok) hrow[q8] = make_uint4(p[0], p[1], p[2], p[3]);
         }
         continue;
       }
@@ -903,7 +921,7 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
         const int32_t y = static_cast<int32_t>(tc.a_row0 + quarter * 32);
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
-          if (kWarpScales && ch > 0) stage_landed(stage_total);
+          if ((kWarpScales || kEpiStager) && ch > 0) stage_landed(stage_total);
           const int64_t n0 = tc.n0 + col0 + ch * 32;
           if (n0 >= N) break;
           float v[32];
