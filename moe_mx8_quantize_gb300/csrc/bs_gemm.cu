@@ -771,6 +771,47 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
     for (int64_t u = unit0; u < nunits; u += ustep, ++tcount) {
       const int as = tcount % L::kAccBufs;
       const uint32_t aph = (tcount / L::kAccBufs) & 1;
+      // Grouped GEMMs read the tile's FP32 decode scales before the wait, so
+      // the loads complete while the accumulator fills (not with h
+      // quantization, nor in single GEMMs: their epilogues have no registers
+      // to spare; measured slower).
+      constexpr bool kEarlyScales = kGrouped && !kQuantH;
+      TileCoord tc;
+      bool row_ok = false;
+      int64_t m = 0;
+      auto load_coords = [&]() {
+        tc = tile_of(u);
+        row_ok = r_in_tile < tc.rows;
+        m = tc.a_row0 + r_in_tile;
+      };
+      auto load_sa = [&]() -> float {
+        float v = 1.f;
+        if (row_ok) {
+          if (args.a32_mode == 1) {
+            int64_t src = m;
+            if (kGather) {
+              src = args.a_rows[m];
+              src = src < 0 ? 0 : (src >= args.a_src_rows ? args.a_src_rows - 1 : src);
+            }
+            v = args.A32[src];
+          } else if (args.a32_mode == 2) {
+            v = args.A32[0];
+          }
+        }
+        return v;
+      };
+      auto load_sg = [&]() -> float {
+        if (kGrouped && args.B32 != nullptr) return args.B32[tc.g];
+        if (!kGrouped && args.b32_mode == 2) return args.B32[0];
+        return 1.f;
+      };
+      float sa = 1.f, sg = 1.f;
+      if constexpr (kEarlyScales) {
+        load_coords();
+        sa = load_sa();
+        sg = load_sg();
+      }
+      const bool b_row = !kGrouped && args.b32_mode == 1;
       if (!wait_accumulator(as, aph)) break;
       tc_fence_after();
       uint32_t r[4][32];
@@ -787,26 +828,11 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.acc_empty[as]));   // accumulator drained into registers
       if constexpr (kWarpScales || kEpiStager) stage_landed(stage_total);
-
-      const TileCoord tc = tile_of(u);
-      const bool row_ok = r_in_tile < tc.rows;
-      const int64_t m = tc.a_row0 + r_in_tile;
-      float sa = 1.f;
-      if (row_ok) {
-        if (args.a32_mode == 1) {
-          int64_t src = m;
-          if (kGather) {
-            src = args.a_rows[m];
-            src = src < 0 ? 0 : (src >= args.a_src_rows ? args.a_src_rows - 1 : src);
-          }
-          sa = args.A32[src];
-        }
-        else if (args.a32_mode == 2) sa = args.A32[0];
+      if constexpr (!kEarlyScales) {
+        load_coords();
+        sa = load_sa();
+        sg = load_sg();
       }
-      float sg = 1.f;
-      if (kGrouped && args.B32 != nullptr) sg = args.B32[tc.g];
-      else if (!kGrouped && args.b32_mode == 2) sg = args.B32[0];
-      const bool b_row = !kGrouped && args.b32_mode == 1;
       // the two FP32 decode scales are combined first: acc * A32 alone can
       // overflow for tokens whose amax is near the bf16 maximum
       const float s_ab = __fmul_rn(sa, sg);
