@@ -194,6 +194,16 @@ def test_nvfp4_group_scope_ragged_groups_resident():
     _nv_check(xb[:300], mx.SCOPE_TENSOR)
 
 
+@pytest.mark.parametrize("cols", [2560, 7168, 9216])
+def test_nvfp4_group_scope_long_rows(cols):
+    """Rows longer than 2048 values (the DeepSeek-V3 hidden size among them)
+    are streamed four 512-value chunks at a time: ragged groups, a tail chunk
+    shorter than 512, empty groups and tensor scope, bit-exact."""
+    xb = inputs.bits(inputs.sweep(260, cols, seed=cols))
+    _nv_check(xb, mx.SCOPE_GROUP, [0, 1, 1, 129, 200, 260])
+    _nv_check(xb, mx.SCOPE_TENSOR)
+
+
 def test_nvfp4_tensor_scope_large():
     g = torch.Generator(device="cuda").manual_seed(18)
     W = inputs.normal_bf16((8192, 2048), 0.02, g, "cuda")
