@@ -51,7 +51,8 @@
 //
 // Group / tensor scope (one FP32 scale per expert weight or per tensor) needs
 // the scope amax before any element is encoded.  A single kernel takes work
-// items from an ordered ticket counter: "amax" items (16 rows, 32 for paired rows: fold their
+// items from an ordered ticket counter: "amax" items (16 rows; 32 for paired
+// rows, 8 for rows over 2048 values: fold their
 // maximum into the group's word, then count themselves done) and "encode"
 // items (16 scale rows of the group: wait until all of the group's amax items
 // are done, then encode).  Tickets hand out a lead of amax items first (about
@@ -74,13 +75,16 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 // Rows (or scale rows) per work item of the scoped kernel: two per data warp
-// (two pairs for the paired-row shapes).  Smaller items keep the data that
-// the blocks hold between an amax item and its encode item -- about two
-// items per block -- well inside L2 (measured: 16-row items read less from
-// DRAM than 32-row ones; 8-row items cost more in ticket traffic).
+// (two pairs for the paired-row shapes; one for rows over 2048 values).
+// Smaller items keep the data that the blocks hold between an amax item and
+// its encode item -- about two items per block -- well inside L2 (measured:
+// 16-row items read less from DRAM than 32-row ones; 8-row items cost more in
+// ticket traffic.  For the 7168-wide DeepSeek-V3 gate|up expert weights, 8-row
+// items (115 KB) read 1.72x the input from DRAM against 1.94x for 16 rows,
+// 4958 -> 4286 us; 4-row items read 1.50x but cost more in tickets).
 template <int kCh>
 struct ScopedItem {
-  static constexpr int kRows = kCh < 0 ? 32 : 16;
+  static constexpr int kRows = kCh < 0 ? 32 : (kCh == 0 ? 8 : 16);
 };
 constexpr int64_t kL2LeadBytes = 32ll << 20;  // input bytes between a group's amax and encode items
 
@@ -649,7 +653,11 @@ __global__ void __launch_bounds__(kScopedThreads, kCh >= 8 ? 1 : (kCh < 0 ? 3 : 
       if (cum[mid] <= k) lo = mid; else hi = mid - 1;
     }
     const int g = lo;
-    const int64_t item = k - cum[g];
+    // A group's encode items run in the reverse order of its amax items: the
+    // rows read last for the amax are read again first, while still in L2
+    // (a group larger than L2 -- 58.7 MB for a DeepSeek-V3 gate|up expert --
+    // otherwise misses L2 on every row of its second read).
+    const int64_t item = enc ? (cum[g + 1] - cum[g]) - 1 - (k - cum[g]) : k - cum[g];
     sm.tg[slot] = g;
     sm.tenc[slot] = enc;
     sm.titem[slot] = item;
