@@ -1317,6 +1317,58 @@ def run_profile(args):
                       "launches": [[lab, k] for lab, _, k in seq]}))
 
 
+def run_profile_case(args):
+    """For ncu: one launch of the DeepSeek-V3-shaped kernels on synthetic
+    operands, sized for a capture --
+      dsv3_gemms: the gate|up (SwiGLU) and down grouped NVFP4 GEMMs at the
+        full layer shape (131072 dispatched rows, Zipf(1.1) routing over 256
+        experts, hidden 7168, FFN 2048), random E2M1 codes and E4M3 block
+        scales of 1.0 (about 9 GB on the device);
+      dsv3_wgu: group-scope NVFP4 quantization of 24 experts' gate|up weights
+        ([4096, 7168] bf16 each, 1.4 GB)."""
+    import torch
+    import __graft_entry__
+    import moe_mx8_quantize_gb300 as mx
+    from moe_mx8_quantize_gb300 import inputs
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    q = inputs.DSV3_SHAPE
+    T, H, E, F, k = q["tokens"], q["hidden"], q["experts"], q["ffn"], q["topk"]
+    if args.profile_case == "dsv3_gemms":
+        ids = inputs.route_zipf(T, E, k, 1.1, torch.Generator(device="cpu").manual_seed(3), "cpu")
+        offs = inputs.dispatch(ids, E).offsets.to(dev)
+        R = T * k
+        u8 = lambda n: torch.randint(0, 256, (n,), dtype=torch.uint8, device=dev)
+        sc = lambda n: torch.full((n,), 0x38, dtype=torch.uint8, device=dev)
+        A4, SA4 = u8(R * H // 2).view(R, H // 2), sc(mx.scale_bytes_grouped(mx.FMT_NVFP4, R, E, H))
+        W4, SW4 = u8(E * 2 * F * H // 2).view(E, 2 * F, H // 2), sc(mx.scale_bytes(mx.FMT_NVFP4, E * 2 * F, H))
+        H4, SH4 = u8(R * F // 2).view(R, F // 2), sc(mx.scale_bytes_grouped(mx.FMT_NVFP4, R, E, F))
+        Wd4, SWd4 = u8(E * H * F // 2).view(E, H, F // 2), sc(mx.scale_bytes(mx.FMT_NVFP4, E * H, F))
+        A32, W32 = torch.full((R,), 0.01, device=dev), torch.full((E,), 0.01, device=dev)
+        hs = torch.empty((R, F), dtype=torch.bfloat16, device=dev)
+        out = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
+        ws = mx.new_workspace(E, dev)
+        mx.bs_grouped_gemm_fused_into(mx.FMT_NVFP4, offs, R, A4, SA4, W4, SW4, H, hs, A32, W32, None,
+                                      mx.EPI_SWIGLU, ws)
+        mx.bs_grouped_gemm_into(mx.FMT_NVFP4, offs, H4, SH4, Wd4, SWd4, F, out, A32, W32, ws)
+    elif args.profile_case == "dsv3_wgu":
+        n = 24
+        W = inputs.normal_bf16((n * 2 * F, H), 0.02, torch.Generator(device="cuda").manual_seed(5), "cuda")
+        offs = torch.arange(n + 1, device=dev, dtype=torch.int64) * (2 * F)
+        qw = torch.empty((n * 2 * F, H // 2), dtype=torch.uint8, device=dev)
+        sw = torch.empty(mx.scale_bytes(mx.FMT_NVFP4, n * 2 * F, H), dtype=torch.uint8, device=dev)
+        s32 = torch.empty(n, dtype=torch.float32, device=dev)
+        ws = mx.new_workspace(n, dev)
+        mx.nvfp4_quantize_into(W, qw, sw, s32, mx.SCOPE_GROUP, offs, ws)
+    else:
+        raise SystemExit(f"unknown profile case {args.profile_case}")
+    torch.cuda.synchronize()
+    if mx.check_device_error(ws) != mx.OK:
+        raise RuntimeError("device error in the profile case")
+    print(json.dumps({"case": args.profile_case, "device_gb": round(torch.cuda.memory_allocated() / 1e9, 2)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1328,8 +1380,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the measurements beside the step")
     ap.add_argument("--profile", action="store_true", help="run every launch twice for ncu and exit")
+    ap.add_argument("--profile-case", choices=["dsv3_gemms", "dsv3_wgu"],
+                    help="run one DeepSeek-V3-shaped kernel case once for ncu and exit")
     args = ap.parse_args()
-    if args.profile:
+    if args.profile_case:
+        run_profile_case(args)
+    elif args.profile:
         run_profile(args)
     elif args.impl == "reference":
         run_reference(args)
