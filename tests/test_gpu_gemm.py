@@ -181,6 +181,28 @@ def test_nvfp4_grouped_small(T, H, E, N, topk, zipf):
     _check(y.ravel(), ref, absref, K=H)
 
 
+@pytest.mark.parametrize("T,H,E,N,topk,zipf", [(64, 256, 5, 256, 2, False), (300, 512, 16, 384, 4, True),
+                                               (40, 96, 7, 136, 1, False)])
+def test_mxfp8_grouped(T, H, E, N, topk, zipf):
+    """MXFP8 MoE grouped GEMM (one 512-byte scale tile per 128-element stage,
+    staged into tensor memory by the producer warps and the MMA warp):
+    routed token rows in the grouped scale layout times per-expert weights,
+    ragged and Zipf-skewed groups, a K that ends inside a stage."""
+    d = inputs.moe(T, "cpu", T, H, E, N // 2, topk, routing="zipf" if zipf else "uniform", with_weights=True)
+    disp = inputs.dispatch(d["topk_ids"], E)
+    offs = disp.offsets.numpy()
+    A, SA = oracle.mxfp8_quantize_rowwise(inputs.bits(d["X"][disp.token_of_row]))
+    B, SB = oracle.mxfp8_quantize_rowwise(inputs.bits(d["W_gu"]).reshape(E * N, H))
+    go = torch.tensor(offs, dtype=torch.int64, device="cuda")
+    y = host(mx.bs_grouped_gemm(mx.FMT_MXFP8, go, dev(A), dev(oracle.swizzle_scales(SA, offs)),
+                                dev(B.reshape(E, N, H)), dev(oracle.swizzle_scales(SB, np.arange(E + 1) * N)), H,
+                                out_dtype=torch.float32))
+    rows = A.shape[0]
+    pairs = np.array([(m, n) for m in range(rows) for n in range(N)])
+    ref, absref = oracle.grouped_gemm_ref(0, offs, A, SA, B.reshape(E, N, H), SB, H, pairs=pairs)
+    _check(y.ravel(), ref, absref, K=H)
+
+
 def test_nvfp4_grouped_empty_and_single_row_groups():
     H, N, E = 256, 128, 6
     rng = np.random.default_rng(3)
