@@ -299,9 +299,9 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
   constexpr bool kSwiGLU = (kMode & kModeSwiGLU) != 0;
   constexpr bool kQuantH = (kMode & kModeQuantH) != 0;
   // scales moved into tensor memory by the epilogue warps (single GEMMs), by
-  // the producer warps and the MMA warp (grouped GEMMs: their epilogue warps
-  // are busy; with BN = 256 those four warps cover the four lane quarters),
-  // else by the MMA thread with tcgen05.cp (gathered A)
+  // the three producer warps and one more warp per lane quarter (grouped
+  // GEMMs with BN = 256: see kEpiStager), else by the MMA thread with
+  // tcgen05.cp (gathered A)
   constexpr bool kWarpScales = F::kSfTiles > 0 && !kGrouped;
   constexpr bool kProdScales = F::kSfTiles > 0 && kGrouped && !kGather && kBN == 256;
   constexpr bool kSepScales = kWarpScales || kProdScales;   // scale tiles land on their own barrier
@@ -412,9 +412,9 @@ __global__ void __launch_bounds__(Layout<kFmt, kGrouped, kBN, kMode>::kThreads, 
   // in order, as soon as the stage's scale tiles have landed, then arrives on
   // the stage's "scales ready" barrier.  Single GEMMs: the epilogue warps
   // (A's tiles by the first four, B's by the last four).  Grouped GEMMs with
-  // BN = 256: the A producer, the MMA warp and the two B producers (warps 0,
-  // 1, 10, 11: one per quarter), A's and B's tiles each, between their own
-  // waits.  A stage can only be refilled after its MMAs, which wait for its
+  // BN = 256: the A producer and the two B producers (warps 0, 10, 11) and,
+  // for lane quarter 1, epilogue warp 5 or the MMA warp (kEpiStager), A's and
+  // B's tiles each, between their own waits.  A stage can only be refilled after its MMAs, which wait for its
   // scales, so a stage's barriers are never more than one phase ahead and its
   // shared-memory tiles and tensor-memory columns are never overwritten while
   // in use.
