@@ -155,3 +155,40 @@ def test_quantize_batch_rejects_bad_counts(lib):
     items[0] = m.QuantizeItem(16, 64, 48, 48, 16, 16, None, None)
     assert lib.mx8_quantize_batch(m.FMT_MXFP8, ctypes.cast(items, ctypes.c_void_p), 1, m.ROWWISE, None, 0,
                                   None) == m.ERR_INVALID_ARG
+
+
+def test_fused_swiglu_noalloc_and_selftest_arguments_rejected_on_host(lib):
+    """The entries the other host checks do not reach: argument errors come
+    back before any device work (no GPU in this process)."""
+    import moe_mx8_quantize_gb300 as m
+    p = ctypes.c_void_p(16)      # never dereferenced
+    odd = ctypes.c_void_p(18)    # not 4-byte aligned
+    # SwiGLU: ffn % 8, ld_gate_up < 2 ffn, ld_h < ffn, misaligned, empty
+    assert lib.mx8_swiglu(p, 4, 12, 24, p, 12, None) == m.ERR_INVALID_ARG
+    assert lib.mx8_swiglu(p, 4, 64, 96, p, 64, None) == m.ERR_INVALID_ARG
+    assert lib.mx8_swiglu(p, 4, 64, 128, p, 32, None) == m.ERR_INVALID_ARG
+    assert lib.mx8_swiglu(odd, 4, 64, 128, p, 64, None) == m.ERR_ALIGNMENT
+    assert lib.mx8_swiglu(None, 0, 64, 128, None, 64, None) == m.OK
+    # gate|up GEMM with h quantized: group count, N % 256, F / 128 above the
+    # cluster limit, K % 32, missing outputs, misaligned S_dec, no workspace
+    args = lambda G, N, K, qh=p, s32=p, ws=p, wsb=1 << 20: (G, p, 256, N, K, p, p, None, p, p, None, qh, p, s32,
+                                                            None, 0, ws, wsb, None)
+    assert lib.bs_grouped_gemm_swiglu_nvfp4(*args(0, 512, 64)) == m.ERR_INVALID_ARG
+    assert lib.bs_grouped_gemm_swiglu_nvfp4(*args(2, 384, 64)) == m.ERR_INVALID_ARG
+    assert lib.bs_grouped_gemm_swiglu_nvfp4(*args(2, 2304, 64)) == m.ERR_UNSUPPORTED
+    assert lib.bs_grouped_gemm_swiglu_nvfp4(*args(2, 512, 48)) == m.ERR_INVALID_ARG
+    assert lib.bs_grouped_gemm_swiglu_nvfp4(*args(2, 512, 64, qh=None)) == m.ERR_INVALID_ARG
+    assert lib.bs_grouped_gemm_swiglu_nvfp4(*args(2, 512, 64, s32=odd)) == m.ERR_ALIGNMENT
+    assert lib.bs_grouped_gemm_swiglu_nvfp4(*args(2, 512, 64, ws=None, wsb=0)) == m.ERR_WORKSPACE
+    # the no-allocation quantizer: scope, cols % 16, group scope without
+    # offsets, group count, misaligned, empty
+    assert lib.nvfp4_quantize_per_token_noalloc(p, 4, 32, 32, 7, None, 0, p, p, p, None) == m.ERR_INVALID_ARG
+    assert lib.nvfp4_quantize_per_token_noalloc(p, 4, 24, 24, 0, None, 0, p, p, p, None) == m.ERR_INVALID_ARG
+    assert lib.nvfp4_quantize_per_token_noalloc(p, 4, 32, 32, 1, None, 0, p, p, p, None) == m.ERR_INVALID_ARG
+    assert lib.nvfp4_quantize_per_token_noalloc(p, 4, 32, 32, 1, p, 0, p, p, p, None) == m.ERR_INVALID_ARG
+    assert lib.nvfp4_quantize_per_token_noalloc(odd, 4, 32, 32, 0, None, 0, p, p, p, None) == m.ERR_ALIGNMENT
+    assert lib.nvfp4_quantize_per_token_noalloc(None, 0, 0, 0, 0, None, 0, None, None, None, None) == m.OK
+    # the bounded-wait self test: workspace, wait limit
+    assert lib.mx8_selftest_bounded_wait(None, 1000, None) == m.ERR_WORKSPACE
+    assert lib.mx8_selftest_bounded_wait(p, 0, None) == m.ERR_INVALID_ARG
+    assert lib.mx8_selftest_bounded_wait(p, 3000000000, None) == m.ERR_INVALID_ARG
