@@ -92,7 +92,7 @@ def _L():
         lib.or_rht16.argtypes = [_p, ctypes.c_uint, _p]
         lib.or_nvfp4_quantize_rht_colwise.argtypes = [_p, _i64, _i64, _i64, ctypes.c_uint, ctypes.c_int,
                                                       ctypes.c_uint64, _p, _p, _p]
-        lib.or_philox4x64_10.argtypes = [_p, _p, _p]
+        lib.or_philox4x32_10.argtypes = [_p, _p, _p]
         lib.or_sr_bits.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
         lib.or_sr_bits.restype = ctypes.c_uint32
         lib.or_e2m1_sr.argtypes = [ctypes.c_float, ctypes.c_uint32]
@@ -290,12 +290,12 @@ def nvfp4_quantize_rht_colwise(x_bits, sign_mask, stochastic=False, seed=0):
     return qT, sT, s32
 
 
-def philox4x64_10(counter, key):
-    """Philox4x64-10 block: 4 x uint64 counter, 2 x uint64 key -> 4 x uint64."""
-    c = np.ascontiguousarray(np.asarray(counter, np.uint64).reshape(4))
-    k = np.ascontiguousarray(np.asarray(key, np.uint64).reshape(2))
-    out = np.empty(4, np.uint64)
-    _L().or_philox4x64_10(_ptr(c), _ptr(k), _ptr(out))
+def philox4x32_10(counter, key):
+    """Philox4x32-10 block: 4 x uint32 counter, 2 x uint32 key -> 4 x uint32."""
+    c = np.ascontiguousarray(np.asarray(counter, np.uint32).reshape(4))
+    k = np.ascontiguousarray(np.asarray(key, np.uint32).reshape(2))
+    out = np.empty(4, np.uint32)
+    _L().or_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
     return out
 
 

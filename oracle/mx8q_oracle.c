@@ -475,40 +475,40 @@ void or_nvfp4_quantize_2d(const uint16_t *x, i64 R, i64 C, i64 ld,
  * probability given by the distance to each, which removes the bias; it is
  * applied to gradients only).
  *
- * Random bits: the counter-based generator Philox4x64-10 (Salmon, Moraes,
+ * Random bits: the counter-based generator Philox4x32-10 (Salmon, Moraes,
  * Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011): ten
- * rounds of two 64x64->128-bit multiplications with the round constants
- * M0 = 0xD2E7470EE14C6C93, M1 = 0xCA5A826395121157 and Weyl key increments
- * W0 = 0x9E3779B97F4A7C15, W1 = 0xBB67AE8584CAA73B:
+ * rounds of two 32x32->64-bit multiplications with the round constants
+ * M0 = 0xD2511F53, M1 = 0xCD9E8D57 and Weyl key increments
+ * W0 = 0x9E3779B9, W1 = 0xBB67AE85:
  *   (hi0, lo0) = M0 * c0, (hi1, lo1) = M1 * c2,
  *   c = (hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0);  k += (W0, W1) between rounds. */
-void or_philox4x64_10(const uint64_t *ctr_in, const uint64_t *key_in, uint64_t *out)
+void or_philox4x32_10(const uint32_t *ctr_in, const uint32_t *key_in, uint32_t *out)
 {
-    const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
-    const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
-    uint64_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
-    uint64_t k0 = key_in[0], k1 = key_in[1];
+    const uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+    const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+    uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+    uint32_t k0 = key_in[0], k1 = key_in[1];
     for (int round = 0; round < 10; round++) {
         if (round > 0) { k0 += W0; k1 += W1; }
-        unsigned __int128 p0 = (unsigned __int128)M0 * c0, p1 = (unsigned __int128)M1 * c2;
-        uint64_t hi0 = (uint64_t)(p0 >> 64), lo0 = (uint64_t)p0;
-        uint64_t hi1 = (uint64_t)(p1 >> 64), lo1 = (uint64_t)p1;
-        uint64_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        uint64_t p0 = (uint64_t)M0 * c0, p1 = (uint64_t)M1 * c2;
+        uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+        uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+        uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
         c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
     }
     out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
 }
 
 /* The 32 random bits of element e of a quantized tensor under seed: one
- * Philox block (counter (e / 8, 0, 0, 0), key (seed, 0)) gives 8 words of 32
- * bits; element e takes word e % 8 (the low half of 64-bit output (e % 8) / 2
- * for even e, the high half for odd e). */
+ * Philox block, counter (e / 4 mod 2^32, e / 4 div 2^32, 0, 0) and key
+ * (seed mod 2^32, seed div 2^32), gives 4 words of 32 bits; element e takes
+ * word e % 4. */
 uint32_t or_sr_bits(uint64_t seed, uint64_t e)
 {
-    uint64_t ctr[4] = {e >> 3, 0, 0, 0}, key[2] = {seed, 0}, out[4];
-    or_philox4x64_10(ctr, key, out);
-    uint64_t w = out[(e & 7) >> 1];
-    return (e & 1) ? (uint32_t)(w >> 32) : (uint32_t)w;
+    uint32_t ctr[4] = {(uint32_t)(e >> 2), (uint32_t)(e >> 34), 0, 0};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)}, out[4];
+    or_philox4x32_10(ctr, key, out);
+    return out[e & 3];
 }
 
 /* E2M1 code of v by stochastic rounding with 32 random bits:

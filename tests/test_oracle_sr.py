@@ -2,9 +2,9 @@
 metodologia de preentrenamiento de 4 bits utilizando NVFP4", section "La
 metodologia de formacion de cuatro partes": round up or down with
 probabilities given by the distances to the two nearest representable
-values).  The counter-based generator is checked against NumPy's Philox
-bit generator (Philox4x64-10); the rounding against its thresholds and its
-expectation."""
+values).  The counter-based generator (Philox4x32-10) is checked against
+the known-answer vectors published with it; the rounding against its
+thresholds and its expectation."""
 import numpy as np
 import pytest
 
@@ -13,16 +13,31 @@ import oracle
 E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
 
 
-@pytest.mark.parametrize("n,key", [(1, (0, 0)), (7, (0x1234, 0)), (2 ** 40 + 3, (0xDEADBEEFCAFEF00D, 0x55)),
-                                   (2 ** 64 - 1, (1, 2))])
-def test_philox_matches_numpy(n, key):
-    """NumPy's Philox increments its counter before each block: counter n - 1
-    yields the block of counter n."""
-    bg = np.random.Philox(key=np.array(key, dtype=np.uint64),
-                          counter=np.array([(n - 1) % 2 ** 64, 0, 0, 0], dtype=np.uint64))
-    want = bg.random_raw(4)
-    got = oracle.philox4x64_10([n, 0, 0, 0], key)
-    assert np.array_equal(got, want)
+# Known-answer vectors of Philox4x32-10 distributed with the generator
+# (Random123 "kat_vectors": counter words, key words -> output words).
+PHILOX4X32_KAT = [
+    ((0x00000000, 0x00000000, 0x00000000, 0x00000000), (0x00000000, 0x00000000),
+     (0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8)),
+    ((0xFFFFFFFF, 0xFFFFFFFF, 0xFFFFFFFF, 0xFFFFFFFF), (0xFFFFFFFF, 0xFFFFFFFF),
+     (0x408F276D, 0x41C83B0E, 0xA20BC7C6, 0x6D5451FD)),
+    ((0x243F6A88, 0x85A308D3, 0x13198A2E, 0x03707344), (0xA4093822, 0x299F31D0),
+     (0xD16CFE09, 0x94FDCCEB, 0x5001E420, 0x24126EA1)),
+]
+
+
+@pytest.mark.parametrize("ctr,key,want", PHILOX4X32_KAT)
+def test_philox_known_answers(ctr, key, want):
+    assert [int(w) for w in oracle.philox4x32_10(ctr, key)] == list(want)
+
+
+def test_sr_bits_word_layout():
+    """Element e takes word e % 4 of the block with counter (e / 4 split in
+    two 32-bit words, 0, 0) and key (seed split in two 32-bit words)."""
+    for seed, e in ((0, 0), (5, 7), (0x243F6A8885A308D3, 2 ** 35 + 6), (2 ** 64 - 1, 2 ** 64 - 1)):
+        blk = oracle.philox4x32_10([(e >> 2) & 0xFFFFFFFF, e >> 34, 0, 0], [seed & 0xFFFFFFFF, seed >> 32])
+        assert oracle.sr_bits(seed, e) == int(blk[e % 4])
+    # the first KAT vector is element 0..3 of seed 0
+    assert [oracle.sr_bits(0, e) for e in range(4)] == list(PHILOX4X32_KAT[0][2])
 
 
 def test_sr_bits_are_uniform():
