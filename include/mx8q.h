@@ -283,9 +283,9 @@ mx8_status nvfp4_quantize_rht_colwise(const void *x, int64_t rows, int64_t cols,
  * the block scales as nvfp4_quantize_per_token() with NVFP4_SCOPE_TOKEN; each
  * code is the E2M1 value below or above RN(x * r), chosen with 32 random
  * bits b: above when (b >> 8) < p * 2^24, p the distance to the value below
- * over the grid spacing; b = Philox4x64-10 (counter (e / 8, 0, 0, 0), key
- * (seed, 0)), 32-bit word e % 8 of its four 64-bit outputs (low half first),
- * e = row * cols + column.  Same layouts and requirements as the token scope
+ * over the grid spacing; b = Philox4x32-10 (Salmon et al., SC 2011) with
+ * counter (e / 4 split into two 32-bit words, 0, 0) and key (seed split into
+ * two 32-bit words), word e % 4 of its four outputs, e = row * cols + column.  Same layouts and requirements as the token scope
  * of nvfp4_quantize_per_token() (plain scale layout, padding rows zero).
  */
 mx8_status nvfp4_quantize_per_token_sr(const void *x, int64_t rows, int64_t cols, int64_t ld,

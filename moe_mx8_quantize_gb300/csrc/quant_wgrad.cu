@@ -19,10 +19,11 @@
 // Gradients (same section: round-to-nearest-even biases gradients; stochastic
 // rounding, gradients only) take stochastically rounded codes: the block
 // scales stay round-to-nearest, and element e of the output (its index in the
-// quantized matrix) rounds with the 32 bits of Philox4x64-10 block e / 8 under
+// quantized matrix) rounds with word e % 4 of Philox4x32-10 block e / 4 under
 // the caller's seed.  nvfp4_sr_token_kernel is the per-token quantizer of a
-// gradient (the Dgrad operand) with stochastic codes: one warp per row, the
-// row read once for its amax and once more (from L2) for the encode.
+// gradient (the Dgrad operand) with stochastic codes: a team of up to 256
+// threads per row, which holds rows of up to 16384 values in registers (one
+// HBM read) and reduces the row's amax over the team.
 #include "device.cuh"
 #include "kernels.h"
 
@@ -32,6 +33,86 @@ namespace {
 
 constexpr int kTile = 128;
 constexpr int kWThreads = 256;
+
+// ---------------------------------------------------------------- stochastic rounding
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
+// easy as 1, 2, 3", SC 2011) on four counters at once: ten rounds of two
+// 32x32->64-bit products with the round constants M0, M1, and the Weyl key
+// increments W0, W1 between rounds; the four blocks share the key schedule
+// and give the scheduler four independent chains.
+__device__ __forceinline__ void philox4x32_10_x4(uint32_t (&c)[4][4], uint32_t k0, uint32_t k1) {
+  constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+  constexpr uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) {
+      k0 += W0;
+      k1 += W1;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint64_t p0 = static_cast<uint64_t>(M0) * c[j][0];
+      const uint64_t p1 = static_cast<uint64_t>(M1) * c[j][2];
+      const uint32_t n0 = static_cast<uint32_t>(p1 >> 32) ^ c[j][1] ^ k0;
+      const uint32_t n2 = static_cast<uint32_t>(p0 >> 32) ^ c[j][3] ^ k1;
+      c[j][0] = n0;
+      c[j][1] = static_cast<uint32_t>(p1);
+      c[j][2] = n2;
+      c[j][3] = static_cast<uint32_t>(p0);
+    }
+  }
+}
+
+// The 32 random bits of elements e0 .. e0 + 15 (e0 % 4 == 0) under seed:
+// element e takes word e % 4 of the block with counter (e / 4 split into two
+// 32-bit words, 0, 0) and key (seed split into two 32-bit words).
+__device__ __forceinline__ void sr_bits16(uint64_t seed, uint64_t e0, uint32_t (&bits)[16]) {
+  uint32_t c[4][4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint64_t n = (e0 >> 2) + static_cast<uint64_t>(j);
+    c[j][0] = static_cast<uint32_t>(n);
+    c[j][1] = static_cast<uint32_t>(n >> 32);
+    c[j][2] = 0;
+    c[j][3] = 0;
+  }
+  philox4x32_10_x4(c, static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) bits[i] = c[i >> 2][i & 3];
+}
+
+// E2M1 code of v by stochastic rounding with 32 random bits b: |v| >= 6
+// gives 6; otherwise |v| lies in [lo, hi) of the grid {0, .5, 1, 1.5, 2, 3,
+// 4, 6} and rounds up to hi when (b >> 8) < p * 2^24, p = (|v| - lo) / (hi -
+// lo); the sign is kept and NaN gives a zero code.  Read off the binary32
+// fields of a = |v| (s = its exponent and top mantissa bit): for a >= 0.5
+// the code of lo is max(s, 253) - 252 (from 1 for [0.5, 1) to 6 for [4, 6),
+// 7 and up from 6 on, capped at 7), and p * 2^24 is 4 times the 22 mantissa
+// bits below the top one (a >= 1) or 2 times the 23 mantissa bits ([0.5,
+// 1)), so the test is b < (a << 10) or b < (a << 9) as 32-bit integers (the
+// exponent bits shift out).  For a < 0.5, lo = 0 and p * 2^24 = a * 2^25,
+// exact in binary32, compared with the 24 bits as a float.
+__device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t bits) {
+  const uint32_t ub = __float_as_uint(v);
+  const uint32_t ab = ub & 0x7FFFFFFFu;
+  const uint32_t t = ab >= 0x3F800000u ? ab << 10 : ab << 9;
+  uint32_t code = min(max(ab >> 22, 253u) - 252u + (bits < t ? 1u : 0u), 7u);
+  if (ab < 0x3F000000u) code = __uint2float_rn(bits >> 8) < __fmul_rn(__uint_as_float(ab), 33554432.0f) ? 1u : 0u;
+  if (ab > 0x7F800000u) code = 0u;
+  return code | ((ub >> 28) & 8u);
+}
+
+// Sixteen values -> sixteen stochastically rounded E2M1 nibbles (element 0
+// in the low nibble of codes.x).
+__device__ __forceinline__ uint2 e2m1x16_sr(const float (&v)[16], const uint32_t (&bits)[16]) {
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    lo |= e2m1_sr(v[i], bits[i]) << (4 * i);
+    hi |= e2m1_sr(v[8 + i], bits[8 + i]) << (4 * i);
+  }
+  return make_uint2(lo, hi);
+}
 
 __device__ __forceinline__ void rht16(float (&v)[16], uint32_t mask) {
 #pragma unroll
@@ -58,7 +139,7 @@ __device__ __forceinline__ int tile_byte(int row, int k) {
 // kEncode = false: atomicMax of max |y| into amax_bits; true: encode (kSR:
 // stochastically rounded codes).
 template <bool kEncode, bool kSR>
-__global__ void __launch_bounds__(kWThreads) rht_colwise_kernel(
+__global__ void __launch_bounds__(kWThreads, 4) rht_colwise_kernel(
     const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ld, uint32_t mask, uint64_t seed,
     uint32_t* __restrict__ amax_bits, uint8_t* __restrict__ qT, uint8_t* __restrict__ sT,
     float* __restrict__ s32) {
@@ -107,21 +188,23 @@ __global__ void __launch_bounds__(kWThreads) rht_colwise_kernel(
       }
       const uint32_t sb = cvt_e4m3x2(__fmul_rn(__fdiv_rn(bmax, 6.0f), senc), 0.0f) & 0xFFu;
       const float r = sb ? fminf(__fdiv_rn(senc, e4m3_to_f32(sb)), FLT_MAX) : 0.f;
-      float a[8], b[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        a[i] = __fmul_rn(v[i], r);
-        b[i] = __fmul_rn(v[8 + i], r);
-      }
       uint2 packed;
       if (kSR) {
+        float y[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(v[i], r);
         // element index in the transposed copy: row c0 + c, column r0 + 16 k
         const uint64_t e0 = static_cast<uint64_t>(c0 + c) * static_cast<uint64_t>(R) + static_cast<uint64_t>(r0 + 16 * k);
-        uint32_t ba[8], bb[8];
-        sr_bits8(seed, e0, ba);
-        sr_bits8(seed, e0 + 8, bb);
-        packed = make_uint2(e2m1x8_sr(a, ba), e2m1x8_sr(b, bb));
+        uint32_t bits[16];
+        sr_bits16(seed, e0, bits);
+        packed = e2m1x16_sr(y, bits);
       } else {
+        float a[8], b[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          a[i] = __fmul_rn(v[i], r);
+          b[i] = __fmul_rn(v[8 + i], r);
+        }
         packed = make_uint2(cvt_e2m1x8(a), cvt_e2m1x8(b));
       }
       *reinterpret_cast<uint2*>(&codes[c][8 * k]) = packed;
@@ -159,65 +242,129 @@ __global__ void __launch_bounds__(kWThreads) rht_colwise_kernel(
 
 // Per-token NVFP4 of a gradient with stochastically rounded codes (block
 // scales and S_dec as the round-to-nearest quantizer); scale rows past R
-// (padding of the last 128-row tile) are written as zero.
+// (padding of the last 128-row tile) are written as zero.  A team of kTeam
+// threads (a power of two, 32 .. 256) quantizes one row: thread t of the team
+// takes the row's 16-element blocks t, t + kTeam, ..., holds them in
+// registers (kNB of them; kNB = 0 for longer rows, which are read twice, the
+// second time from L2), and the team reduces the row's amax with shuffles
+// and, across its warps, through shared memory (two buffers, one barrier a
+// row).
+template <int kTeam, int kNB>
 __global__ void __launch_bounds__(kWThreads) nvfp4_sr_token_kernel(
     const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ld, uint64_t seed, uint8_t* __restrict__ q,
     uint8_t* __restrict__ sblk, float* __restrict__ s32) {
-  const int lane = threadIdx.x & 31;
-  const int64_t kt = (C / 16 + 3) / 4;
+  constexpr int kRowsPerCta = kWThreads / kTeam;
+  constexpr int kTeamWarps = kTeam / 32;
+  __shared__ float2 tab[128];
+  __shared__ float red[2][kWThreads / 32];
+  nvfp4_init_scale_table(tab);
+  __syncthreads();
+  const int tt = threadIdx.x % kTeam;
+  const int team = threadIdx.x / kTeam;
+  const int64_t nb = C / 16;
+  const int64_t kt = (nb + 3) / 4;
   const int64_t RP = (R + 127) / 128 * 128;
-  const int64_t nw = static_cast<int64_t>(gridDim.x) * (kWThreads / 32);
-  for (int64_t row = static_cast<int64_t>(blockIdx.x) * (kWThreads / 32) + (threadIdx.x >> 5); row < RP; row += nw) {
-    uint8_t* srow = sblk + (row >> 7) * kt * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4;
-    if (row >= R) {                                        // padding scale row
-      for (int64_t b = lane; b < kt * 4; b += 32) srow[(b >> 2) * 512 + (b & 3)] = 0;
+  const int64_t groups = (RP + kRowsPerCta - 1) / kRowsPerCta;
+  int par = 0;
+  for (int64_t g = blockIdx.x; g < groups; g += gridDim.x, par ^= 1) {
+    const int64_t row = g * kRowsPerCta + team;
+    const bool live = row < R;
+    const uint16_t* xr = x + (live ? row : 0) * ld;
+    uint4 w[kNB > 0 ? kNB : 1][2];
+    uint32_t m = 0;
+    if (live) {
+      if constexpr (kNB > 0) {
+#pragma unroll
+        for (int j = 0; j < kNB; ++j) {
+          const int64_t b = tt + static_cast<int64_t>(j) * kTeam;
+          if (b < nb) {
+            w[j][0] = __ldg(reinterpret_cast<const uint4*>(xr + 16 * b));
+            w[j][1] = __ldg(reinterpret_cast<const uint4*>(xr + 16 * b + 8));
+            m = amax2(m, absmax16(w[j][0], w[j][1]));
+          }
+        }
+      } else {
+        for (int64_t b = tt; b < nb; b += kTeam)
+          m = amax2(m, absmax16(__ldg(reinterpret_cast<const uint4*>(xr + 16 * b)),
+                                __ldg(reinterpret_cast<const uint4*>(xr + 16 * b + 8))));
+      }
+    }
+    float amax = warp_max(abs_halves_max(m));
+    if constexpr (kTeamWarps > 1) {
+      if ((threadIdx.x & 31) == 0) red[par][threadIdx.x >> 5] = amax;
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < kTeamWarps; ++i) amax = fmaxf(amax, red[par][team * kTeamWarps + i]);
+    }
+    if (row >= RP) continue;
+    uint8_t* srow = sblk + sf_row_base(row, kt);
+    if (!live) {                                           // padding scale row
+      for (int64_t b = tt; b < kt * 4; b += kTeam) srow[(b >> 2) * 512 + (b & 3)] = 0;
       continue;
     }
-    const uint16_t* xr = x + row * ld;
-    uint32_t m = 0;
-    for (int64_t c = 8 * lane; c < C; c += 256) {
-      const uint4 w = __ldg(reinterpret_cast<const uint4*>(xr + c));
-      m = amax2(m, amax2(amax2(w.x, w.y), amax2(w.z, w.w)));
-    }
     float senc, sdec;
-    nvfp4_scales(warp_max(abs_halves_max(m)), senc, sdec);
-    if (lane == 0) s32[row] = sdec;
-    for (int64_t b = lane; b < C / 16; b += 32) {          // 16-element block b of the row
-      const uint4 w0 = __ldg(reinterpret_cast<const uint4*>(xr + 16 * b));
-      const uint4 w1 = __ldg(reinterpret_cast<const uint4*>(xr + 16 * b + 8));
-      const float bmax = abs_halves_max(absmax16(w0, w1));
-      const uint32_t sb = cvt_e4m3x2(__fmul_rn(__fdiv_rn(bmax, 6.0f), senc), 0.0f) & 0xFFu;
-      const float r = sb ? fminf(__fdiv_rn(senc, e4m3_to_f32(sb)), FLT_MAX) : 0.f;
+    nvfp4_scales(amax, senc, sdec);
+    if (tt == 0) s32[row] = sdec;
+    auto encode = [&](const uint4& w0, const uint4& w1, int64_t b) {
+      float r;
+      const uint32_t sb = nvfp4_block_scale(abs_halves_max(absmax16(w0, w1)), senc, tab, r);
+      const uint64_t rr = f32x2_splat(r);
       const uint32_t ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-      float a[8], bv[8];
+      float v[16];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        a[2 * i] = __fmul_rn(bf16_lo(ws[i]), r);
-        a[2 * i + 1] = __fmul_rn(bf16_hi(ws[i]), r);
-        bv[2 * i] = __fmul_rn(bf16_lo(ws[4 + i]), r);
-        bv[2 * i + 1] = __fmul_rn(bf16_hi(ws[4 + i]), r);
-      }
-      const uint64_t e0 = static_cast<uint64_t>(row) * static_cast<uint64_t>(C) + static_cast<uint64_t>(16 * b);
-      uint32_t ba[8], bb[8];
-      sr_bits8(seed, e0, ba);
-      sr_bits8(seed, e0 + 8, bb);
-      *reinterpret_cast<uint2*>(q + row * (C / 2) + 8 * b) = make_uint2(e2m1x8_sr(a, ba), e2m1x8_sr(bv, bb));
+      for (int i = 0; i < 8; ++i) mul_bf16x2(ws[i], rr, v[2 * i], v[2 * i + 1]);
+      uint32_t bits[16];
+      sr_bits16(seed, static_cast<uint64_t>(row) * static_cast<uint64_t>(C) + static_cast<uint64_t>(16 * b), bits);
+      *reinterpret_cast<uint2*>(q + row * (C / 2) + 8 * b) = e2m1x16_sr(v, bits);
       srow[(b >> 2) * 512 + (b & 3)] = static_cast<uint8_t>(sb);
+    };
+    if constexpr (kNB > 0) {
+#pragma unroll
+      for (int j = 0; j < kNB; ++j) {
+        const int64_t b = tt + static_cast<int64_t>(j) * kTeam;
+        if (b < nb) encode(w[j][0], w[j][1], b);
+      }
+    } else {
+      for (int64_t b = tt; b < nb; b += kTeam)
+        encode(__ldg(reinterpret_cast<const uint4*>(xr + 16 * b)), __ldg(reinterpret_cast<const uint4*>(xr + 16 * b + 8)),
+               b);
     }
     // padding scale columns of the row's last 4-block group are zero
-    for (int64_t b = C / 16 + lane; b < kt * 4; b += 32) srow[(b >> 2) * 512 + (b & 3)] = 0;
+    for (int64_t b = nb + tt; b < kt * 4; b += kTeam) srow[(b >> 2) * 512 + (b & 3)] = 0;
   }
+}
+
+template <int kTeam, int kNB>
+void launch_sr_token(const uint16_t* x, int64_t R, int64_t C, int64_t ld, uint64_t seed, uint8_t* q, uint8_t* sblk,
+                     float* s32, int sm_count, cudaStream_t stream) {
+  const int64_t groups = ((R + 127) / 128 * 128 + kWThreads / kTeam - 1) / (kWThreads / kTeam);
+  const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+  nvfp4_sr_token_kernel<kTeam, kNB><<<static_cast<unsigned>(groups < cap ? groups : cap), kWThreads, 0, stream>>>(
+      x, R, C, ld, seed, q, sblk, s32);
 }
 
 }  // namespace
 
 cudaError_t launch_nvfp4_sr_token(const uint16_t* x, int64_t R, int64_t C, int64_t ld, uint64_t seed, uint8_t* q,
                                   uint8_t* sblk, float* s32, int sm_count, cudaStream_t stream) {
-  const int64_t rows = (R + 127) / 128 * 128;
-  const int64_t want = (rows + kWThreads / 32 - 1) / (kWThreads / 32);
-  const int64_t cap = static_cast<int64_t>(sm_count) * 8;
-  nvfp4_sr_token_kernel<<<static_cast<unsigned>(want < cap ? want : cap), kWThreads, 0, stream>>>(x, R, C, ld, seed,
-                                                                                                 q, sblk, s32);
+  // the smallest team that covers the row's 16-element blocks once (32 ..
+  // 256 threads); wider rows take 2 or 4 blocks a thread, past 16384 values
+  // the two-read path
+  const int64_t nb = C / 16;
+  if (nb <= 32)
+    launch_sr_token<32, 1>(x, R, C, ld, seed, q, sblk, s32, sm_count, stream);
+  else if (nb <= 64)
+    launch_sr_token<64, 1>(x, R, C, ld, seed, q, sblk, s32, sm_count, stream);
+  else if (nb <= 128)
+    launch_sr_token<128, 1>(x, R, C, ld, seed, q, sblk, s32, sm_count, stream);
+  else if (nb <= 256)
+    launch_sr_token<256, 1>(x, R, C, ld, seed, q, sblk, s32, sm_count, stream);
+  else if (nb <= 512)
+    launch_sr_token<256, 2>(x, R, C, ld, seed, q, sblk, s32, sm_count, stream);
+  else if (nb <= 1024)
+    launch_sr_token<256, 4>(x, R, C, ld, seed, q, sblk, s32, sm_count, stream);
+  else
+    launch_sr_token<256, 0>(x, R, C, ld, seed, q, sblk, s32, sm_count, stream);
   return cudaGetLastError();
 }
 

@@ -54,10 +54,13 @@ def test_rht_colwise_stochastic(seed):
     assert np.array_equal(host(s)[: sw.size], sw)
 
 
-@pytest.mark.parametrize("shape", [(5, 16), (130, 96), (2048, 8192), (33, 4096)])
+@pytest.mark.parametrize("shape", [(5, 16), (130, 96), (3, 1008), (70, 1536), (33, 4096), (2048, 8192),
+                                   (40, 12288), (9, 20480)])
 def test_per_token_stochastic(shape):
     """Per-token NVFP4 of a gradient with stochastic codes, bit-exact against
-    the oracle (codes, scale tiles with padding, S_dec)."""
+    the oracle (codes, scale tiles with padding, S_dec); the widths take every
+    team size of the kernel (32 .. 256 threads a row), 1, 2 and 4 blocks a
+    thread, and the two-read path of rows over 16384 values."""
     xb = inputs.bits(inputs.normal_bf16(shape, 1e-3, torch.Generator().manual_seed(shape[0]), "cpu", 0.01, 30))
     q, s, s32 = mx.nvfp4_quantize_per_token_sr(dev(xb), 1234567 + shape[0])
     oq, os_, o32 = oracle.nvfp4_quantize_sr(xb, 1234567 + shape[0])
