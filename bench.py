@@ -791,7 +791,8 @@ def time_each(launches, K2, stream):
 
 
 # Nominal dense tensor rates per GPU (TFLOP/s) quoted as context: 4.5 PF FP8 and
-# 9 PF FP4 (the targets the GEMMs are judged against), 2.25 PF BF16.
+# 9 PF FP4 (the dense FP8 / FP4 peaks the GEMM fractions are also given
+# against), 2.25 PF BF16.
 NOMINAL_TFLOPS = {"bf16": 2250.0, "fp8": 4500.0, "fp4": 9000.0}
 
 
